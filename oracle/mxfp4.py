@@ -1,0 +1,116 @@
+"""MXFP4 quantization and its exact three-way error decomposition
+(test infrastructure only).
+
+Source: "Decomposing MXFP4 quantization error ..." (arXiv 2605.20402v2),
+abstract.  MXFP4 block scales are powers of two; the quantization error is
+proved to split exactly into three additive components: scale bias (from
+rounding the scale to a power of two), deadzone truncation (small values
+zeroed) and grid noise (rounding to the nearest 4-bit grid point).  The
+abstract gives names and exactness but no formulas.
+
+Readings:
+
+* Format (OCP MX): 32-element blocks along K, E2M1 elements, one E8M0
+  scale 2**e per block with e = floor(log2 a) - 2 (a = max |x|, 2 = the
+  exponent of E2M1's largest power of two), clamped to [-127, 127]; a == 0
+  gives e = -127.  code_i = E2M1(x_i * 2**-e) (fp32 multiply, RNE,
+  satfinite so 6 < |y| < 8 saturates to 6, sign kept).  Scale byte = e + 127.
+* Decomposition, telescoping through the ideal real scale s* = a / 6 (the
+  scale that puts the block maximum exactly on the grid's top level):
+      Q_s(x)  = 2**e * E2M1(x / 2**e)         (what MXFP4 stores)
+      Q*(x)   = s*   * E2M1(x / s*)           (same grid, ideal scale)
+      E = Q_s - x                              total error
+      B = Q_s - Q*                             scale bias
+      D = (Q* - x) where E2M1(x / s*) == 0     deadzone truncation
+      G = (Q* - x) where E2M1(x / s*) != 0     grid noise
+  so E = B + D + G exactly.  s* and x / s* are computed in fp32 (the
+  precision of the kernel) so both sides take the same rounding decisions;
+  the four components are then formed in fp64, where they are exact.
+  A block with a == 0 has every component 0.
+* Per-block statistics: [|B|^2, |D|^2, |G|^2, |E|^2] summed over the block,
+  and the deadzone count = #{i : E2M1(x_i / s*) == 0 and x_i != 0}.
+"""
+
+import numpy as np
+
+from .formats import e2m1_encode, e2m1_value
+from .nvfp4 import pack
+
+BLOCK = 32
+
+
+def block_exponent(a):
+    """e = floor(log2 a) - 2 clamped to [-127, 127]; a == 0 -> -127.
+    floor(log2 a) is read exactly from frexp (a = m * 2**q, 0.5 <= m < 1)."""
+    a = np.asarray(a, dtype=np.float64)
+    _, q = np.frexp(a)
+    e = np.where(a > 0, q - 1 - 2, -127)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def quantize(x):
+    """MXFP4-quantize float32 values of bf16 numbers ``x`` [M, K], K % 32 == 0.
+
+    Returns dict(codes [M,K] uint8, packed [M,K/2], scale [M,K/32] uint8 E8M0,
+    e [M,K/32] int64).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, K = x.shape
+    if K % BLOCK:
+        raise ValueError("K must be a multiple of 32")
+    xb = x.reshape(M, K // BLOCK, BLOCK)
+    a = np.max(np.abs(xb), axis=2)
+    e = block_exponent(a)
+    inv = np.power(2.0, -e).astype(np.float32)          # exact power of two
+    y = (xb * inv[:, :, None]).astype(np.float32)
+    codes = e2m1_encode(y).reshape(M, K)
+    return dict(codes=codes, packed=pack(codes), scale=(e + 127).astype(np.uint8), e=e)
+
+
+def dequantize(codes, scale):
+    M, K = codes.shape
+    v = e2m1_value(codes).reshape(M, K // BLOCK, BLOCK)
+    return (v * np.power(2.0, scale.astype(np.float64) - 127.0)[:, :, None]).reshape(M, K)
+
+
+def decompose(x):
+    """Elementwise decomposition of the MXFP4 error of ``x`` [M, K].
+
+    Returns dict(E, B, D, G) as float64 [M, K], ``dead`` bool [M, K] (the
+    deadzone mask) and the quantize() outputs."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, K = x.shape
+    q = quantize(x)
+    xb = x.reshape(M, K // BLOCK, BLOCK)
+    a = np.max(np.abs(xb), axis=2)
+    Qs = dequantize(q["codes"], q["scale"]).reshape(M, K // BLOCK, BLOCK)
+    nz = a > 0
+    s_star = np.where(nz, a / np.float32(6.0), np.float32(1.0)).astype(np.float32)
+    y_star = (xb / s_star[:, :, None]).astype(np.float32)
+    c_star = e2m1_encode(y_star)
+    Qstar = e2m1_value(c_star) * s_star.astype(np.float64)[:, :, None]
+    x64 = xb.astype(np.float64)
+    dead = ((c_star & 0x7) == 0)
+    E = Qs - x64
+    B = Qs - Qstar
+    D = np.where(dead, Qstar - x64, 0.0)
+    G = np.where(dead, 0.0, Qstar - x64)
+    zero_blk = ~nz[:, :, None]
+    B = np.where(zero_blk, 0.0, B)
+    D = np.where(zero_blk, 0.0, D)
+    G = np.where(zero_blk, 0.0, G)
+    E = np.where(zero_blk, 0.0, E)
+    deadzone = dead & (x64 != 0) & ~zero_blk
+    r = lambda t: t.reshape(M, K)
+    return dict(E=r(E), B=r(B), D=r(D), G=r(G), dead=r(deadzone), **q)
+
+
+def block_stats(x):
+    """Per-block statistics [M, K/32, 4] = (|B|^2, |D|^2, |G|^2, |E|^2) in
+    fp64 and the deadzone count [M, K/32] (uint8)."""
+    d = decompose(x)
+    M, K = d["E"].shape
+    sq = lambda t: np.sum(t.reshape(M, K // BLOCK, BLOCK) ** 2, axis=2)
+    stats = np.stack([sq(d["B"]), sq(d["D"]), sq(d["G"]), sq(d["E"])], axis=-1)
+    cnt = np.sum(d["dead"].reshape(M, K // BLOCK, BLOCK), axis=2).astype(np.uint8)
+    return stats, cnt, d

@@ -1,0 +1,102 @@
+"""Pins of the oracle's MXFP4 quantizer and error decomposition (CPU only)."""
+
+import json
+import os
+
+import numpy as np
+
+from oracle import mxfp4, formats as F
+from nvfp4_w4a4_gemm_gb300 import workloads as W
+
+
+def test_worked_example(golden_dir):
+    with open(os.path.join(golden_dir, "mxfp4_worked.json")) as f:
+        ex = json.load(f)
+    x = np.zeros((1, ex["block_len"]), np.float32)
+    x[0, :4] = ex["x_head"]
+    d = mxfp4.decompose(x)
+    assert d["scale"][0, 0] == ex["scale_byte"]
+    assert list(d["codes"][0, :4]) == ex["codes_head"]
+    assert np.all(d["codes"][0, 4:] == 0)
+    for key in "EBDG":
+        np.testing.assert_allclose(d[key][0, :4], ex[key + "_head"], rtol=0, atol=1e-12)
+        assert np.all(d[key][0, 4:] == 0)
+    assert d["dead"].sum() == ex["deadzone_count"]
+
+
+def test_scales_are_powers_of_two_and_cover_the_block():
+    # Decomposing MXFP4 error abstract: scales come from power-of-two rounding.
+    x = W.activations(32, 512, 6, "t3x20", 4, 4).float().numpy()
+    q = mxfp4.quantize(x)
+    s = F.e8m0_value(q["scale"])
+    assert np.all(np.log2(s) == np.round(np.log2(s)))
+    a = np.abs(x).reshape(32, 16, 32).max(-1)
+    ratio = a / s
+    assert np.all((ratio >= 4) & (ratio < 8))       # e = floor(log2 a) - 2
+
+
+def test_roundtrip_of_grid_representable_blocks():
+    rng = np.random.default_rng(2)
+    M, nb = 6, 8
+    e = rng.integers(-20, 20, size=(M, nb))
+    c = rng.integers(0, 16, size=(M, nb, 32))
+    c[:, :, 0] = np.where(rng.random((M, nb)) < 0.5, 6, 7)   # max |c| in {4, 6}
+    # keep the block max at index 0: cap other magnitudes at the chosen max
+    top = F.e2m1_value(c[:, :, 0])
+    others = np.minimum(np.abs(F.e2m1_value(c[:, :, 1:])), top[:, :, None])
+    sign = np.where(c[:, :, 1:] & 8, -1.0, 1.0)
+    x = np.concatenate([top[:, :, None], others * sign], axis=2)
+    x = (x * np.power(2.0, e)[:, :, None]).reshape(M, nb * 32).astype(np.float32)
+    q = mxfp4.quantize(x)
+    assert np.array_equal(q["e"], e)
+    assert np.array_equal(mxfp4.dequantize(q["codes"], q["scale"]), x.astype(np.float64))
+
+
+def test_decomposition_is_exact_and_additive():
+    x = W.activations(64, 1024, 10, "t3x20", 5, 5).float().numpy()
+    d = mxfp4.decompose(x)
+    # E = B + D + G holds exactly (every term is exact in fp64)
+    assert np.array_equal(d["B"] + d["D"] + d["G"], d["E"])
+    assert np.array_equal(d["E"], mxfp4.dequantize(d["codes"], d["scale"]) - x)
+    # D and G have disjoint supports
+    assert not np.any((d["D"] != 0) & (d["G"] != 0))
+    # deadzone entries are exactly those zeroed at the ideal scale: D = -x
+    assert np.array_equal(d["D"][d["dead"]], -x[d["dead"]].astype(np.float64))
+
+
+def test_no_scale_bias_when_block_max_is_six_times_power_of_two():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 64)).astype(np.float32)
+    x = F.bf16_round(x)
+    x = np.clip(x, -2.9, 2.9)
+    x[:, 0] = 6.0 * 0.5     # a = 3 = 6 * 2^-1 -> s* = s = 2^-1
+    x[:, 32] = -6.0 * 2.0 ** 3
+    d = mxfp4.decompose(x)
+    assert np.all(d["B"] == 0)
+
+
+def test_no_grid_noise_or_deadzone_on_grid_at_ideal_scale():
+    s = 2.0 ** -2
+    c = np.array([6, -4, 3, 0.5, -1.5, 2, 1, 0] * 4, np.float64)
+    x = (c * s).astype(np.float32)[None, :]
+    d = mxfp4.decompose(x)
+    assert np.all(d["D"] == 0) and np.all(d["G"] == 0)
+
+
+def test_deadzone_special_case():
+    # every |x| <= a/24 except the max -> those entries are all deadzone
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 24.0
+    x[0, 1:] = F.bf16_round(np.linspace(-0.99, 0.99, 31).astype(np.float32))
+    d = mxfp4.decompose(x)
+    nz = x[0, 1:] != 0
+    assert np.all(d["dead"][0, 1:][nz])
+    assert np.array_equal(d["D"][0, 1:], -x[0, 1:].astype(np.float64))
+
+
+def test_block_stats_consistent():
+    x = W.activations(16, 256, 3, "t3x20", 6, 6).float().numpy()
+    st, cnt, d = mxfp4.block_stats(x)
+    assert st.shape == (16, 8, 4) and cnt.shape == (16, 8)
+    np.testing.assert_allclose(st[..., 3], (d["E"] ** 2).reshape(16, 8, 32).sum(-1))
+    assert np.array_equal(cnt, d["dead"].reshape(16, 8, 32).sum(-1))

@@ -1,0 +1,126 @@
+"""Pins of the oracle's NVFP4 quantizer (CPU only)."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import nvfp4, formats as F
+from nvfp4_w4a4_gemm_gb300 import workloads as W
+
+
+def _golden(golden_dir):
+    with open(os.path.join(golden_dir, "nvfp4_worked.json")) as f:
+        return json.load(f)["examples"]
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_worked_examples(golden_dir, idx):
+    ex = _golden(golden_dir)[idx]
+    x = np.array(ex["x"], np.float32)[None, :]
+    assert np.array_equal(F.bf16_round(x), x), "fixture values must be bf16-exact"
+    q = nvfp4.quantize(x, chan=np.array(ex["chan"]))
+    assert q["g"] == np.float32(ex["g"])
+    assert list(q["sigma"][0]) == ex["sigma"]
+    assert list(q["codes"][0]) == ex["codes"]
+    assert np.array_equal(q["resid"][0], np.array(ex["resid"], np.float32))
+    if "packed_block1" in ex:
+        assert list(q["packed"][0, 8:16]) == ex["packed_block1"]
+
+
+def test_roundtrip_of_grid_representable_blocks():
+    # g = 2^j; block 0 carries sigma = 448 and a +-6 code so that
+    # amax = 2688 g exactly; other blocks any E4M3 sigma_b with a +-6 code.
+    rng = np.random.default_rng(1)
+    for j in (-8, -3, 0, 2):
+        g = 2.0 ** j
+        M, nb = 8, 12
+        sig = rng.integers(0x08, 0x7F, size=(M, nb))  # normal E4M3 scales
+        sig[0, 0] = 0x7E
+        c = rng.integers(0, 16, size=(M, nb, 16))
+        c[:, :, 3] = 7  # +6 in every block so sigma_b is recovered exactly
+        x = F.e2m1_value(c) * F.e4m3_decode(sig)[:, :, None] * g
+        x = x.reshape(M, nb * 16).astype(np.float32)
+        assert np.array_equal(F.bf16_round(x), x)
+        q = nvfp4.quantize(x)
+        assert q["g"] == np.float32(g)
+        assert np.array_equal(q["sigma"], sig.astype(np.uint8))
+        deq = nvfp4.dequantize(q["codes"], q["sigma"], q["g"])
+        # exact values (negative zero codes compare equal to 0)
+        assert np.array_equal(deq, x.astype(np.float64))
+        assert np.all(q["resid_f32"] == 0)
+
+
+def test_zero_tensor_and_zero_blocks():
+    x = np.zeros((3, 32), np.float32)
+    q = nvfp4.quantize(x, chan=np.array([0, 31]))
+    assert q["g"] == 1.0
+    assert np.all(q["sigma"] == 0) and np.all(q["codes"] == 0)
+    assert np.all(q["resid"] == 0)
+
+
+def test_scale_is_max_over_block_and_bounded():
+    # invariants on heavy-tailed data: sigma*g*6 >= a up to E4M3 rounding
+    # (< 2^-4 relative for normals), codes within the grid, |y| <= 6.
+    x = W.activations(64, 512, 8, "t3x20", 3, 3).float().numpy()
+    q = nvfp4.quantize(x)
+    a = np.abs(x).reshape(64, 32, 16).max(-1)
+    s = F.e4m3_decode(q["sigma"]) * q["g"]
+    nz = q["sigma"] >= 8
+    assert np.all(np.abs(s[nz] * 6 - a[nz]) <= a[nz] * 2.0 ** -4 + 1e-30)
+    # the block maximum lands on a top code (6 or 4 after rounding)
+    deq = nvfp4.dequantize(q["codes"], q["sigma"], q["g"])
+    err = np.abs(deq - x).reshape(64, 32, 16).max(-1)
+    assert np.all(err <= s * 1.0 + 1e-30)     # at most half the coarsest step (2) times d
+
+
+def test_tile_layout_positions():
+    # byte offset of (row, scale index) in the 128x4 tile layout
+    off = nvfp4.scale_tile_offsets(256, 8)  # 2 row tiles x 2 column tiles
+    assert off[0, 0] == 0 and off[0, 1] == 1 and off[0, 3] == 3
+    assert off[1, 0] == 16 and off[31, 0] == 496
+    assert off[32, 0] == 4 and off[64, 0] == 8 and off[96, 3] == 15
+    assert off[0, 4] == 512 and off[128, 0] == 1024 and off[128, 4] == 1536
+    assert len(np.unique(off)) == off.size == nvfp4.scale_bytes(256, 128)
+
+
+def test_tile_layout_ragged_padding():
+    assert nvfp4.scale_bytes(1, 16) == 128 * 4
+    assert nvfp4.scale_bytes(130, 80) == 256 * 8
+    off = nvfp4.scale_tile_offsets(130, 5)
+    assert off.max() < nvfp4.scale_bytes(130, 80) and len(np.unique(off)) == off.size
+
+
+def test_grouped_row_map():
+    offs = np.array([0, 3, 3, 200, 201])
+    prow = nvfp4.grouped_row_map(offs)
+    assert list(prow[:3]) == [0, 1, 2]
+    assert prow[3] == 128 and prow[199] == 128 + 196 and prow[200] == 384
+    assert prow.max() < (2 + 4) * 128  # within the stated upper bound
+
+
+def test_grouped_residual_uses_each_experts_channels():
+    x = W.random_bf16((10, 64), 5).float().numpy()
+    offs = np.array([0, 4, 10])
+    chan = np.array([[0, 5], [7, 63]])
+    q = nvfp4.quantize_grouped(x, offs, chan)
+    assert np.array_equal(q["resid"][:4], F.bf16_round(q["resid_f32"][:4][:, [0, 5]]))
+    assert np.array_equal(q["resid"][4:], F.bf16_round(q["resid_f32"][4:][:, [7, 63]]))
+
+
+def test_pack_unpack():
+    c = np.random.default_rng(0).integers(0, 16, (3, 32)).astype(np.uint8)
+    p = nvfp4.pack(c)
+    assert p.shape == (3, 16) and p[0, 0] == (c[0, 0] | (c[0, 1] << 4))
+    assert np.array_equal(nvfp4.unpack(p), c)
+
+
+def test_comp_weights_exact_in_bf16():
+    wt = W.weights_t(32, 128, 9).float().numpy()
+    q = nvfp4.quantize(wt)
+    chan = np.array([1, 17, 64, 127])
+    ws = nvfp4.comp_weights(q["codes"], q["sigma"], chan)
+    assert np.array_equal(F.bf16_round(ws.astype(np.float32)).astype(np.float64), ws)
+    deq = nvfp4.dequantize(q["codes"], q["sigma"], q["g"])
+    assert np.array_equal(ws * np.float64(q["g"]), deq[:, chan])
