@@ -1,0 +1,244 @@
+/*
+ * nvfp4w4a4.h -- C ABI of the GB300 (sm_103a) NVFP4 / MXFP4 W4A4 linear
+ * layer with Residual Activation Compensation.
+ *
+ * What the library computes (sources are named per entry point):
+ *
+ *   Y = deq(q(X)) . deq(q(W^T))^T + R_S . W_S^T
+ *
+ * X [M, K] bf16 activations, quantized online to NVFP4; W^T [N, K] the
+ * pre-quantized weights; R_S = bf16(X - deq(q(X))) on a fixed set S of k
+ * high-error channels; W_S [N, k] the matching weight columns.
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 tensors are passed as uint16_t bit patterns; every tensor is
+ *     row-major with the stated leading dimension.
+ *   - All data pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing and keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it and never synchronize (except nvfp4_check_status).
+ *   - Return value: NVFP4_OK or an NVFP4_ERR_* code.  Argument errors are
+ *     detected on the host before anything is launched; a launch failure is
+ *     NVFP4_ERR_CUDA; errors detected inside kernels (a bounded wait that
+ *     gave up, an out-of-range channel index) are latched on the device and
+ *     reported by nvfp4_check_status.
+ *   - No C++ exception crosses this interface.
+ *
+ * Block-scale layout ("tiled"): the E4M3 (NVFP4) or E8M0 (MXFP4) block
+ * scales of an [R, K] operand are stored as 512-byte tiles of 128 rows x 4
+ * scale columns; tile (r/128, s/4) is at ((r/128) * ceil(ns/4) + s/4) * 512
+ * (ns = scales per row) and the byte of (r, s) inside it is at
+ * (r%32)*16 + ((r%128)/32)*4 + s%4.  This is the tile the block-scaled
+ * tensor-core MMA reads.  Rows are padded to a multiple of 128; padding
+ * bytes are unspecified, except that a row's last partial group of 4 is
+ * zero-filled.
+ *
+ * FP4 codes: E2M1, two per byte, element 2j in bits 0..3 and 2j+1 in 4..7.
+ */
+#ifndef NVFP4W4A4_H
+#define NVFP4W4A4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad flag */
+  NVFP4_ERR_UNSUPPORTED = 2, /* shape or device not handled (needs sm_103) */
+  NVFP4_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  NVFP4_ERR_TIMEOUT = 4,     /* a kernel's bounded wait gave up (check_status) */
+  NVFP4_ERR_WORKSPACE = 5    /* workspace missing or too small */
+};
+
+enum { NVFP4_FMT_NVFP4 = 0, NVFP4_FMT_MXFP4 = 1 };
+
+/* Compensation weight rows: the dequantized NVFP4 weight columns (default;
+ * the correction then uses the same weights as the W4A4 product), or the
+ * original bf16 weight columns. */
+enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1 };
+
+/* Library version (major*10000 + minor*100 + patch). */
+int nvfp4_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* nvfp4_status_string(int status);
+
+/* NVFP4_OK if `device` is a compute capability 10.3 GPU (the only target
+ * this library is built for), else NVFP4_ERR_UNSUPPORTED / _CUDA. */
+int nvfp4_device_supported(int device);
+
+/* Bytes of the tiled block-scale buffer of an [rows, K] operand. */
+size_t nvfp4_scale_bytes(int64_t rows, int64_t K);  /* 16-element blocks */
+size_t mxfp4_scale_bytes(int64_t rows, int64_t K);  /* 32-element blocks */
+/* Upper bound for an expert-sorted [M_total, K] operand of E experts, where
+ * each expert's rows start a new 128-row tile (any routing fits). */
+size_t nvfp4_grouped_scale_bytes(int64_t M_total, int64_t K, int32_t E);
+
+/* Workspace for the dynamic tensor scale of nvfp4_quantize(_grouped). */
+size_t nvfp4_quantize_workspace_bytes(void);
+
+/*
+ * nvfp4_quantize -- online NVFP4 activation quantization plus the
+ * compensation residual slice.  One pass over X (two when the tensor scale
+ * is dynamic: an amax pre-pass, then the quantizer).
+ *
+ * Source: QUADS (arXiv 2607.15810) abstract (NVFP4 fine-grained scaling,
+ * activations re-quantized online on the coarse E2M1 grid); gist.science
+ * explainer of QUADS, Technisches Resuemee 2.2 B (residual term Delta X_q on
+ * the high-residual channels); FourSight (arXiv 2611.04887) abstract
+ * (those channels kept in BF16).
+ *
+ * Arithmetic per 16-element block of a row (fp32, IEEE RNE, no FMA):
+ *   g      = *g_in, or amax|X| / 2688 (1 if X == 0) when g_in == NULL
+ *   sigma  = E4M3_rn_satfinite((max|x_i| / 6) / g)           -> scales
+ *   d      = sigma * g;  codes = 0 if d == 0, else
+ *   code_i = E2M1_rn_satfinite(x_i * (1 / d))  (sign kept)  -> codes
+ *   resid[m, i] = bf16(x[m, chan[i]] - E2M1(code) * d)      -> resid
+ *
+ * x      [M, K] bf16, row stride ldx elements (16-byte aligned, ldx % 8 == 0)
+ * K      multiple of 16;  M >= 0
+ * g_in   device float or NULL (dynamic scale; needs workspace)
+ * g_out  device float or NULL: receives the tensor scale used
+ * codes  [M, K/2] bytes (4-byte aligned)
+ * scales nvfp4_scale_bytes(M, K) bytes, tiled layout (16-byte aligned)
+ * chan   device int32 [k], sorted ascending, unique, in [0, K); NULL if k == 0
+ * resid  [M, k] bf16; NULL if k == 0
+ * workspace / ws_bytes: >= nvfp4_quantize_workspace_bytes() when g_in == NULL
+ */
+int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
+                   uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid,
+                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * nvfp4_quantize_grouped -- nvfp4_quantize over expert-sorted MoE rows.
+ * Row r belongs to the expert e with offsets[e] <= r < offsets[e+1] and takes
+ * its residual slice on that expert's channels chan[e*k .. e*k+k).  One
+ * tensor scale covers all rows.  Scales use the grouped tiled layout: expert
+ * e's rows start at tile row sum_{e'<e} ceil(M_e'/128)*128, so each 128-row
+ * GEMM tile of one expert reads whole scale tiles.
+ * Source: QUADS abstract (MoE rollout), as nvfp4_quantize.
+ * offsets  device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = M_total
+ * scales   nvfp4_grouped_scale_bytes(M_total, K, E) bytes
+ * chan     device int32 [E, k];  resid [M_total, k]
+ */
+int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
+                           const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * mxfp4_quantize -- MXFP4 quantization (32-element blocks, power-of-two
+ * E8M0 scale 2^e with e = floor(log2 max|x|) - 2 clamped to [-127, 127],
+ * codes E2M1_rn_satfinite(x * 2^-e)), optionally with the per-block
+ * three-way error decomposition.
+ * Source: "Decomposing MXFP4 quantization error" (arXiv 2605.20402v2),
+ * abstract: error = scale bias (power-of-two rounding) + deadzone truncation
+ * (small values zeroed) + grid noise (nearest-grid rounding), exactly.
+ * Decomposition through the ideal scale s* = max|x| / 6 (fp32):
+ *   Q_s = 2^e E2M1(x/2^e), Q* = s* E2M1(x/s*), E = Q_s - x, B = Q_s - Q*,
+ *   D = Q* - x where E2M1(x/s*) == 0, G = Q* - x elsewhere (E = B + D + G).
+ * x      [M, K] bf16 (K % 32 == 0), codes [M, K/2], scales mxfp4_scale_bytes(M, K)
+ * stats  NULL or float [M*K/32][4] = (|B|^2, |D|^2, |G|^2, |E|^2) per block
+ *        (16-byte aligned), block b of row m at index m*(K/32) + b
+ * deadzone NULL or uint8 [M*K/32]: #{x != 0 zeroed at the ideal scale}
+ */
+int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* scales,
+                   float* stats, uint8_t* deadzone, void* stream);
+
+/*
+ * nvfp4_prepare_comp_weights -- the compensation weight columns W_S, once,
+ * offline.  Source: gist.science explainer of QUADS, 2.2 B (the residual term
+ * is multiplied into the output); FourSight abstract (BF16 channels).
+ * flags = NVFP4_COMP_W_DEQ: w_sel[e, n, i] = E2M1(code[e, n, S_i]) *
+ *         sigma[e, n, S_i/16] (exact in bf16; the tensor scale g_w is applied
+ *         in the GEMM epilogue);  b_codes/b_scales required, wt_bf16 ignored.
+ * flags = NVFP4_COMP_W_BF16: w_sel[e, n, i] = wt_bf16[e, n, S_i].
+ * b_codes [E, N, K/2]; b_scales E consecutive nvfp4_scale_bytes(N, K) tiles;
+ * wt_bf16 [E, N, K]; chan [E, k]; w_sel [E, N, k] bf16.
+ * A channel index outside [0, K) writes 0 and latches NVFP4_ERR_INVALID_ARG
+ * for nvfp4_check_status.
+ */
+int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b_codes, const uint8_t* b_scales,
+                               const uint16_t* wt_bf16, const int32_t* chan, int32_t k, int flags,
+                               uint16_t* w_sel, void* stream);
+
+/*
+ * nvfp4_calibrate_channels -- choose the k compensated channels from a
+ * calibration batch: per-channel population variance of the fp32 NVFP4
+ * residual x - deq(q(x)) (dynamic tensor scale of the batch), top k, ties to
+ * the lower index, sorted ascending.  Grouped (offsets != NULL): per expert
+ * over its rows; an expert with fewer than 2 rows uses all rows.
+ * Source: FourSight abstract ("top-variance channels"); gist.science
+ * explainer of QUADS 2.2 B (binary channel mask of high-residual channels).
+ * chan_out device int32 [E, k] (E = 1 when offsets == NULL).
+ * workspace >= nvfp4_calibrate_workspace_bytes(K, E).
+ */
+size_t nvfp4_calibrate_workspace_bytes(int64_t K, int32_t E);
+int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_t ldx, int32_t E,
+                             const int32_t* offsets, int32_t k, int32_t* chan_out, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/*
+ * w4a4_gemm_comp -- dense block-scaled W4A4 GEMM with the compensation term
+ * fused into the epilogue, on the tcgen05 FP4 tensor cores.
+ * Source: QUADS abstract (native W4A4 FP4 GEMMs kept; Residual Activation
+ * Compensation corrects high-error channels); gist.science explainer of
+ * QUADS 2.2 B (the residual term is added to the quantized output);
+ * FourSight abstract (BF16 channels alongside native NVFP4).
+ *
+ *   acc  = sum_K (sa*qa)(sb*qb)            (FP4 MMA, fp32 accumulate)
+ *   accc = resid . w_sel^T                 (BF16 MMA, fp32 accumulate)
+ *   y    = bf16_rn(ga*gb*acc + c*accc),  c = gb (COMP_W_DEQ) or 1 (COMP_W_BF16)
+ *
+ * fmt     NVFP4_FMT_NVFP4 (E4M3 scales, 16-blocks) or NVFP4_FMT_MXFP4 (E8M0
+ *         scales, 32-blocks; ga, gb ignored, k must be 0)
+ * M >= 0, N % 128 == 0, K % 64 == 0 (K % 128 for MXFP4)
+ * a_codes [M, K/2], a_scales tiled [M, K] (16-byte aligned)
+ * b_codes [N, K/2] (= W^T), b_scales tiled [N, K]
+ * g_a, g_b device floats (NVFP4), or NULL for 1
+ * resid [M, k] bf16, w_sel [N, k] bf16 (k % 16 == 0; NULL if k == 0)
+ * y [M, N] bf16 (16-byte aligned)
+ * workspace / ws_bytes: >= w4a4_gemm_workspace_bytes(M, N, K) (may be 0)
+ */
+size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_codes, const uint8_t* a_scales,
+                   const float* g_a, const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                   const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
+                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * w4a4_grouped_gemm_comp -- MoE grouped version: for each expert e, rows
+ * [offsets[e], offsets[e+1]) of A times expert e's weights, with that
+ * expert's compensation columns.  Persistent tiles over (expert, m, n).
+ * Source: QUADS abstract (MoE rollout on native W4A4 GEMMs), as above.
+ * offsets  device int32 [E+1] (same as nvfp4_quantize_grouped)
+ * a_scales grouped tiled layout (nvfp4_quantize_grouped)
+ * g_a      device float [1];  g_b device float [E]
+ * b_codes [E, N, K/2]; b_scales E consecutive nvfp4_scale_bytes(N, K) tiles
+ * resid [M_total, k]; w_sel [E, N, k]; y [M_total, N]
+ */
+size_t w4a4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K);
+int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                           const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                           const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                           const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Reads (and with clear != 0 resets) the device-side error latch of every
+ * kernel family on the current device.  Synchronizes the device.  Returns
+ * NVFP4_OK, NVFP4_ERR_TIMEOUT or NVFP4_ERR_INVALID_ARG; *detail (may be NULL)
+ * receives which wait gave up. */
+int nvfp4_check_status(int clear, uint32_t* detail);
+
+/* Upper bound in nanoseconds of every device-side wait (default 2 s). */
+int nvfp4_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4W4A4_H */

@@ -1,0 +1,263 @@
+"""Thin ctypes binding of ``libnvfp4w4a4.so`` (the C ABI in include/nvfp4w4a4.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtype/device/contiguity, allocates the outputs with torch (device memory is
+the caller's plumbing), and calls the C entry point of the same name on the
+current torch stream.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback path: if the library is missing or the
+device is not sm_103, calls raise.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4w4a4.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
+FMT_NVFP4, FMT_MXFP4 = 0, 1
+COMP_W_DEQ, COMP_W_BF16 = 0, 1
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "nvfp4_version": ([], ctypes.c_int),
+    "nvfp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "nvfp4_device_supported": ([ctypes.c_int], ctypes.c_int),
+    "nvfp4_scale_bytes": ([_I64, _I64], _SZ),
+    "mxfp4_scale_bytes": ([_I64, _I64], _SZ),
+    "nvfp4_grouped_scale_bytes": ([_I64, _I64, _I32], _SZ),
+    "nvfp4_quantize_workspace_bytes": ([], _SZ),
+    "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P], ctypes.c_int),
+    "nvfp4_quantize_grouped": ([_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
+                               ctypes.c_int),
+    "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "nvfp4_prepare_comp_weights": ([_I32, _I64, _I64, _P, _P, _P, _P, _I32, ctypes.c_int, _P, _P], ctypes.c_int),
+    "nvfp4_calibrate_workspace_bytes": ([_I64, _I32], _SZ),
+    "nvfp4_calibrate_channels": ([_P, _I64, _I64, _I64, _I32, _P, _I32, _P, _P, _SZ, _P], ctypes.c_int),
+    "w4a4_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
+    "w4a4_gemm_comp": ([ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32, ctypes.c_int, _P,
+                        _P, _SZ, _P], ctypes.c_int),
+    "w4a4_grouped_gemm_workspace_bytes": ([_I32, _I64, _I64, _I64], _SZ),
+    "w4a4_grouped_gemm_comp": ([ctypes.c_int, _I32, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
+                                ctypes.c_int, _P, _P, _SZ, _P], ctypes.c_int),
+    "nvfp4_check_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+    "nvfp4_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
+}
+
+EXPORTED = tuple(_SIGS)
+
+
+class NvfpError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+
+
+def load(path=None):
+    """Load (once) and return the ctypes library; raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} (run `python -m nvfp4_w4a4_gemm_gb300.build`)")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in _SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().nvfp4_status_string(status).decode()
+
+
+def _check(fn, status):
+    if status != OK:
+        raise NvfpError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
+
+
+def scale_bytes(rows, K):
+    return load().nvfp4_scale_bytes(rows, K)
+
+
+def mx_scale_bytes(rows, K):
+    return load().mxfp4_scale_bytes(rows, K)
+
+
+def grouped_scale_bytes(M_total, K, E):
+    return load().nvfp4_grouped_scale_bytes(M_total, K, E)
+
+
+def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None):
+    """x bf16 [M, K] -> dict(codes u8 [M, K/2], scales u8 tiled, g f32 [1],
+    resid bf16 [M, k]).  g: None (dynamic) or device float32 [1]."""
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    dev = x.device
+    k = 0 if chan is None else int(chan.numel())
+    if chan is not None:
+        _need(chan, torch.int32, "chan")
+    if g is not None:
+        _need(g, torch.float32, "g")
+    o = out or {}
+    codes = o.get("codes") if o.get("codes") is not None else torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    scales = o.get("scales") if o.get("scales") is not None else torch.empty(
+        lib.nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    resid = o.get("resid") if o.get("resid") is not None else torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    if g_out is None:
+        g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = o.get("ws")
+    if ws is None and g is None:
+        ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    st = lib.nvfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(g), _ptr(g_out), _ptr(codes), _ptr(scales),
+                            _ptr(chan) if k else None, k, _ptr(resid) if k else None, _ptr(ws),
+                            0 if ws is None else ws.numel(), _stream())
+    _check("nvfp4_quantize", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+
+
+def nvfp4_quantize_grouped(x, offsets, chan, g=None, g_out=None):
+    """Expert-sorted rows x [M_total, K], offsets int32 [E+1], chan int32 [E, k]."""
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    _need(offsets, torch.int32, "offsets")
+    _need(chan, torch.int32, "chan")
+    M, K = x.shape
+    E = offsets.numel() - 1
+    k = chan.shape[1] if chan.dim() == 2 else 0
+    dev = x.device
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(lib.nvfp4_grouped_scale_bytes(M, K, E), dtype=torch.uint8, device=dev)
+    resid = torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    if g_out is None:
+        g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    st = lib.nvfp4_quantize_grouped(_ptr(x), M, K, x.stride(0), E, _ptr(offsets), _ptr(g), _ptr(g_out),
+                                    _ptr(codes), _ptr(scales), _ptr(chan) if k else None, k,
+                                    _ptr(resid) if k else None, _ptr(ws), ws.numel(), _stream())
+    _check("nvfp4_quantize_grouped", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+
+
+def mxfp4_quantize(x, stats=False):
+    """x bf16 [M, K] (K % 32 == 0) -> dict(codes, scales, stats f32 [M*K/32, 4], dead u8 [M*K/32])."""
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    dev = x.device
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(lib.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    st_t = torch.empty((M * K // 32, 4), dtype=torch.float32, device=dev) if stats else None
+    dead = torch.empty(M * K // 32, dtype=torch.uint8, device=dev) if stats else None
+    st = lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales), _ptr(st_t), _ptr(dead), _stream())
+    _check("mxfp4_quantize", st)
+    return dict(codes=codes, scales=scales, stats=st_t, dead=dead)
+
+
+def nvfp4_prepare_comp_weights(b_codes, b_scales, chan, flags=COMP_W_DEQ, wt=None, E=1):
+    """Compensation weight columns w_sel [E, N, k] (or [N, k] when E == 1)."""
+    lib = load()
+    _need(chan, torch.int32, "chan")
+    k = chan.shape[-1]
+    if b_codes.dim() == 2:
+        N, Kh = b_codes.shape
+    else:
+        E, N, Kh = b_codes.shape
+    K = Kh * 2
+    dev = b_codes.device
+    w_sel = torch.empty((E, N, k), dtype=torch.bfloat16, device=dev)
+    st = lib.nvfp4_prepare_comp_weights(E, N, K, _ptr(b_codes), _ptr(b_scales), _ptr(wt), _ptr(chan), k, flags,
+                                        _ptr(w_sel), _stream())
+    _check("nvfp4_prepare_comp_weights", st)
+    return w_sel[0] if E == 1 and b_codes.dim() == 2 else w_sel
+
+
+def nvfp4_calibrate_channels(x_cal, k, offsets=None):
+    """Channel sets int32 [k] (dense) or [E, k] (grouped by offsets)."""
+    lib = load()
+    _need(x_cal, torch.bfloat16, "x_cal")
+    M, K = x_cal.shape
+    E = 1 if offsets is None else offsets.numel() - 1
+    ws = torch.empty(lib.nvfp4_calibrate_workspace_bytes(K, E), dtype=torch.uint8, device=x_cal.device)
+    out = torch.empty((E, k), dtype=torch.int32, device=x_cal.device)
+    st = lib.nvfp4_calibrate_channels(_ptr(x_cal), M, K, x_cal.stride(0), E, _ptr(offsets), k, _ptr(out),
+                                      _ptr(ws), ws.numel(), _stream())
+    _check("nvfp4_calibrate_channels", st)
+    return out[0] if offsets is None else out
+
+
+def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_NVFP4, y=None, ws=None):
+    """y [M, N] bf16 = block-scaled W4A4 product (+ compensation).  qa / qb
+    are the dicts returned by the quantizers (qb for W^T [N, K])."""
+    lib = load()
+    a_codes, b_codes = qa["codes"], qb["codes"]
+    M, Kh = a_codes.shape
+    K = Kh * 2
+    k = 0 if resid is None else resid.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    need = lib.w4a4_gemm_workspace_bytes(M, N, K)
+    if need and ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=a_codes.device)
+    st = lib.w4a4_gemm_comp(fmt, M, N, K, _ptr(a_codes), _ptr(qa["scales"]), _ptr(qa.get("g")),
+                            _ptr(b_codes), _ptr(qb["scales"]), _ptr(qb.get("g")),
+                            _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags, _ptr(y),
+                            _ptr(ws), 0 if ws is None else ws.numel(), _stream())
+    _check("w4a4_gemm_comp", st)
+    return y
+
+
+def w4a4_grouped_gemm_comp(qa, offsets, b_codes, b_scales, g_b, N, resid=None, w_sel=None, flags=COMP_W_DEQ,
+                           y=None):
+    """MoE: y [M_total, N] bf16; b_codes [E, N, K/2], b_scales E tiles, g_b [E]."""
+    lib = load()
+    a_codes = qa["codes"]
+    M, Kh = a_codes.shape
+    K = Kh * 2
+    E = offsets.numel() - 1
+    k = 0 if resid is None else resid.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    st = lib.w4a4_grouped_gemm_comp(FMT_NVFP4, E, _ptr(offsets), M, N, K, _ptr(a_codes), _ptr(qa["scales"]),
+                                    _ptr(qa.get("g")), _ptr(b_codes), _ptr(b_scales), _ptr(g_b),
+                                    _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags, _ptr(y),
+                                    None, 0, _stream())
+    _check("w4a4_grouped_gemm_comp", st)
+    return y
+
+
+def check_status(clear=True):
+    """Synchronizes and returns (status, detail) of the device error latch."""
+    d = ctypes.c_uint32(0)
+    st = load().nvfp4_check_status(1 if clear else 0, ctypes.byref(d))
+    return st, d.value
+
+
+def set_wait_limit_ns(ns):
+    _check("nvfp4_set_wait_limit_ns", load().nvfp4_set_wait_limit_ns(int(ns)))

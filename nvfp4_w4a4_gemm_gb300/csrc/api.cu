@@ -1,0 +1,302 @@
+// C ABI of the library: argument validation on the host, then the kernel
+// launches on the caller's stream.  Declarations and their documentation are
+// in include/nvfp4w4a4.h.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/nvfp4w4a4.h"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  cudaError_t err = cudaSuccess;
+};
+
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+const DeviceInfo* device_info(int* dev_out = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_once[dev], [dev] {
+    DeviceInfo& d = g_info[dev];
+    d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+  });
+  if (dev_out) *dev_out = dev;
+  return &g_info[dev];
+}
+
+// Resolves the current device and checks it is the sm_103 this library is
+// built for.
+int current_device(const DeviceInfo** out) {
+  const DeviceInfo* d = device_info();
+  if (d == nullptr || d->err != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (!(d->cc_major == 10 && d->cc_minor == 3)) return NVFP4_ERR_UNSUPPORTED;
+  *out = d;
+  return NVFP4_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+const __nv_bfloat16* bf(const uint16_t* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
+__nv_bfloat16* bf(uint16_t* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
+
+constexpr size_t kQuantWs = sizeof(float) * nv4::kMaxAmaxPartials;
+
+int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* scales,
+                     const int32_t* chan, int32_t k, uint16_t* resid, int block) {
+  if (M < 0 || K <= 0 || K % block != 0 || ldx < K || ldx % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (K > (int64_t)1 << 30 || M > (int64_t)1 << 40) return NVFP4_ERR_UNSUPPORTED;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) || !aligned(scales, 16))
+    return NVFP4_ERR_INVALID_ARG;
+  if (k < 0 || k > K) return NVFP4_ERR_INVALID_ARG;
+  if (k > 0 && (!chan || !resid || !aligned(chan, 4) || !aligned(resid, 2))) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_version(void) { return 10000; }
+
+const char* nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_UNSUPPORTED: return "unsupported shape or device (needs sm_103)";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    case NVFP4_ERR_TIMEOUT: return "device wait timed out";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int nvfp4_device_supported(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return (major == 10 && minor == 3) ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
+size_t nvfp4_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return (size_t)(round_up(rows, 128) * round_up(K / 16, 4));
+}
+
+size_t mxfp4_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return (size_t)(round_up(rows, 128) * round_up(K / 32, 4));
+}
+
+size_t nvfp4_grouped_scale_bytes(int64_t M_total, int64_t K, int32_t E) {
+  if (M_total < 0 || K < 0 || E < 0) return 0;
+  return (size_t)((round_up(M_total, 128) + (int64_t)E * 128) * round_up(K / 16, 4));
+}
+
+size_t nvfp4_quantize_workspace_bytes(void) { return kQuantWs; }
+
+int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
+                   uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid,
+                   void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_quant_args(x, M, K, ldx, codes, scales, chan, k, resid, 16);
+  if (st != NVFP4_OK) return st;
+  if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
+    return NVFP4_ERR_WORKSPACE;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if (M == 0 && g_in != nullptr) return NVFP4_OK;
+  return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M, K, ldx, g_in, g_out, codes, scales, chan, k, bf(resid),
+                                              nullptr, 1, static_cast<float*>(workspace), d->num_sms,
+                                              as_stream(stream)));
+}
+
+int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
+                           const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  int st = check_quant_args(x, M_total, K, ldx, codes, scales, chan, k, resid, 16);
+  if (st != NVFP4_OK) return st;
+  if (E <= 0 || E > 4096 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
+  if ((int64_t)E * k + 2 * E + 1 > (200 * 1024) / 4) return NVFP4_ERR_UNSUPPORTED;  // smem copy of chan
+  if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
+    return NVFP4_ERR_WORKSPACE;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
+  return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
+                                              bf(resid), offsets, E, static_cast<float*>(workspace), d->num_sms,
+                                              as_stream(stream)));
+}
+
+int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* scales,
+                   float* stats, uint8_t* deadzone, void* stream) {
+  int st = check_quant_args(x, M, K, ldx, codes, scales, nullptr, 0, nullptr, 32);
+  if (st != NVFP4_OK) return st;
+  if (stats != nullptr && !aligned(stats, 16)) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  return from_cuda(nv4::launch_mxfp4_quantize(bf(x), M, K, ldx, codes, scales, stats, deadzone, d->num_sms,
+                                              as_stream(stream)));
+}
+
+int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b_codes, const uint8_t* b_scales,
+                               const uint16_t* wt_bf16, const int32_t* chan, int32_t k, int flags,
+                               uint16_t* w_sel, void* stream) {
+  if (E <= 0 || N < 0 || K <= 0 || K % 16 != 0 || k < 0 || k > K) return NVFP4_ERR_INVALID_ARG;
+  if (flags != NVFP4_COMP_W_DEQ && flags != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
+  if (k == 0 || N == 0) return NVFP4_OK;
+  if (!chan || !w_sel) return NVFP4_ERR_INVALID_ARG;
+  if (flags == NVFP4_COMP_W_DEQ && (!b_codes || !b_scales)) return NVFP4_ERR_INVALID_ARG;
+  if (flags == NVFP4_COMP_W_BF16 && !wt_bf16) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  int st;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  return from_cuda(nv4::launch_comp_weights(b_codes, b_scales, flags == NVFP4_COMP_W_BF16 ? bf(wt_bf16) : nullptr,
+                                            N, K, chan, k, E, nvfp4_scale_bytes(N, K), bf(w_sel), d->num_sms,
+                                            as_stream(stream)));
+}
+
+size_t nvfp4_calibrate_workspace_bytes(int64_t K, int32_t E) {
+  if (K < 0 || E < 0) return 0;
+  return 256 + kQuantWs + sizeof(double) * 2 * (size_t)K * (size_t)(E + 1);
+}
+
+int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_t ldx, int32_t E,
+                             const int32_t* offsets, int32_t k, int32_t* chan_out, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  if (M <= 0 || K <= 0 || K % 16 != 0 || ldx < K || ldx % 8 != 0 || k < 0 || k > K) return NVFP4_ERR_INVALID_ARG;
+  if (!x_cal || !aligned(x_cal, 16) || (k > 0 && !chan_out)) return NVFP4_ERR_INVALID_ARG;
+  if (offsets != nullptr && (E <= 0 || !aligned(offsets, 4))) return NVFP4_ERR_INVALID_ARG;
+  if (offsets == nullptr) E = 1;
+  if (K > 16384) return NVFP4_ERR_UNSUPPORTED;  // selection keeps K variances in shared memory
+  if (k == 0) return NVFP4_OK;
+  if (!workspace || ws_bytes < nvfp4_calibrate_workspace_bytes(K, E) || !aligned(workspace, 16))
+    return NVFP4_ERR_WORKSPACE;
+  const DeviceInfo* d = nullptr;
+  int st;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  char* w = static_cast<char*>(workspace);
+  float* g = reinterpret_cast<float*>(w);
+  float* partials = reinterpret_cast<float*>(w + 256);
+  double* sums = reinterpret_cast<double*>(w + 256 + kQuantWs);
+  const size_t per = (size_t)K * (size_t)E;
+  double* sum = sums;
+  double* sumsq = sums + per;
+  double* sum_all = sums + 2 * per;
+  double* sumsq_all = sum_all + K;
+  cudaError_t e = nv4::launch_tensor_scale(bf(x_cal), M, K, ldx, partials, g, d->num_sms, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(sums, 0, sizeof(double) * 2 * (size_t)K * (size_t)(E + 1), s);
+  if (e == cudaSuccess) e = nv4::launch_channel_stats(bf(x_cal), M, K, ldx, g, offsets, E, sum, sumsq, d->num_sms, s);
+  if (e == cudaSuccess && offsets != nullptr)
+    e = nv4::launch_channel_stats(bf(x_cal), M, K, ldx, g, nullptr, 1, sum_all, sumsq_all, d->num_sms, s);
+  if (e == cudaSuccess)
+    e = nv4::launch_select_channels(sum, sumsq, offsets, E, M, sum_all, sumsq_all, K, k, chan_out, s);
+  return from_cuda(e);
+}
+
+static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
+                             const uint8_t* a_scales, const uint8_t* b_codes, const uint8_t* b_scales,
+                             const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y) {
+  if (fmt != NVFP4_FMT_NVFP4 && fmt != NVFP4_FMT_MXFP4) return NVFP4_ERR_INVALID_ARG;
+  if (flags != NVFP4_COMP_W_DEQ && flags != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
+  if (M < 0 || N <= 0 || K <= 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % (fmt == NVFP4_FMT_MXFP4 ? 128 : 64) != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (M > ((int64_t)1 << 31) - 256 || N > ((int64_t)1 << 31) - 256 || K > ((int64_t)1 << 30)) return NVFP4_ERR_UNSUPPORTED;
+  if (fmt == NVFP4_FMT_MXFP4 && k != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (k % 8 != 0 || k > K) return NVFP4_ERR_UNSUPPORTED;
+  if (M == 0) return NVFP4_OK;
+  if (!a_codes || !a_scales || !b_codes || !b_scales || !y) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(a_scales, 16) || !aligned(b_scales, 16) ||
+      !aligned(y, 16))
+    return NVFP4_ERR_INVALID_ARG;
+  if (k > 0 && (!resid || !w_sel || !aligned(resid, 16) || !aligned(w_sel, 16))) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const DeviceInfo* d = device_info();
+  const int sms = (d && d->err == cudaSuccess && d->num_sms > 0) ? d->num_sms : 152;
+  return nv4::gemm_workspace_bytes(M, N, K, sms);
+}
+
+int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_codes, const uint8_t* a_scales,
+                   const float* g_a, const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                   const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
+                   void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_gemm_common(fmt, M, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k, flags, y);
+  if (st != NVFP4_OK || M == 0) return st;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  const size_t need = nv4::gemm_workspace_bytes(M, N, K, d->num_sms);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need || !aligned(workspace, 16))) return NVFP4_ERR_WORKSPACE;
+  nv4::GemmProblem p;
+  p.fmt = fmt; p.M = M; p.N = N; p.K = K;
+  p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
+  p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
+  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.flags = flags; p.y = bf(y);
+  p.ws = workspace; p.ws_bytes = ws_bytes;
+  return from_cuda(nv4::launch_gemm(p, d->num_sms, as_stream(stream)));
+}
+
+size_t w4a4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K) {
+  (void)E; (void)M_total; (void)N; (void)K;
+  return 0;
+}
+
+int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                           const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                           const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                           const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_gemm_common(fmt, M_total, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k, flags, y);
+  if (st != NVFP4_OK) return st;
+  if (E <= 0 || E > 65536 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  if (fmt != NVFP4_FMT_NVFP4) return NVFP4_ERR_UNSUPPORTED;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  nv4::GemmProblem p;
+  p.fmt = fmt; p.M = M_total; p.N = N; p.K = K;
+  p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
+  p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
+  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.flags = flags; p.y = bf(y);
+  p.E = E; p.offsets = offsets; p.ws = workspace; p.ws_bytes = ws_bytes;
+  return from_cuda(nv4::launch_grouped_gemm(p, d->num_sms, as_stream(stream)));
+}
+
+int nvfp4_check_status(int clear, uint32_t* detail) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+  uint32_t q[2] = {0, 0}, g[2] = {0, 0};
+  if (nv4::quant_status(q, clear != 0) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (nv4::gemm_status(g, clear != 0) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const uint32_t* hit = g[0] ? g : q;
+  if (detail) *detail = hit[1];
+  return hit[0] == 0 ? NVFP4_OK : (int)hit[0];
+}
+
+int nvfp4_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) return NVFP4_ERR_INVALID_ARG;
+  return from_cuda(nv4::gemm_set_wait_limit(ns));
+}
+
+}  // extern "C"

@@ -1,0 +1,531 @@
+// Block-scaled W4A4 GEMM with the residual-compensation term fused into the
+// epilogue, on the 5th-generation (tcgen05) tensor cores of sm_103a.
+//
+//   acc  = sum_K (sa qa)(sb qb)      kind::mxf4nvf4 (NVFP4, E4M3 scales) or
+//                                    kind::mxf4 (MXFP4, E8M0 scales), fp32 in TMEM
+//   accc = R_S . W_S^T               kind::f16 (BF16), fp32 in TMEM
+//   y    = bf16(alpha * acc + beta * accc)
+//
+// Sources: QUADS (arXiv 2607.15810) abstract -- native W4A4 FP4 GEMMs are
+// kept while Residual Activation Compensation corrects the high-error
+// activation channels; gist.science explainer of QUADS, Technisches
+// Resuemee 2.2 B -- the residual term is added to the quantized output;
+// FourSight (arXiv 2611.04887) abstract -- the compensated channels stay in
+// BF16 alongside native NVFP4.
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: A/B code tiles (128 x 128 B, 128-byte swizzle)
+//               and their block-scale tiles (2 KB bulk copies) into a ring of
+//               smem stages; after the FP4 k-tiles of an output tile it
+//               streams the compensation operands R_S / W_S through the same
+//               ring as 128 x 64 bf16 tiles.
+//   warp 1      allocates TMEM, copies the block scales smem -> TMEM
+//               (tcgen05.cp) and issues the MMAs from one thread; completion
+//               is signalled with tcgen05.commit on mbarriers.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulators, the scale-and-add,
+//               bf16 conversion and stores; warp w reads TMEM lanes
+//               32*(w%4) .. 32*(w%4)+31.
+// TMEM (512 columns): two 128-column FP4 accumulators (so the epilogue of
+// one tile overlaps the main loop of the next), one 128-column compensation
+// accumulator, and two 32-column scale-factor slots (A 16 + B 16) used by
+// alternate k-tiles.
+// Every mbarrier wait is bounded; a wait that gives up latches an error for
+// nvfp4_check_status and the CTA winds down.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace nv4 {
+namespace {
+
+constexpr int BM = 128;               // output rows per tile (MMA M)
+constexpr int BN = 128;               // output columns per tile (MMA N)
+constexpr int BKB = 128;              // bytes of K per k-tile row: 256 FP4 or 64 bf16
+constexpr int kStages = 5;
+constexpr int kTileBytes = BM * BKB;  // 16 KB (A); B the same since BN == BM
+constexpr int kSfBytes = 2048;        // 4 scale chunks of 128 rows x 4 scales
+constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfBytes;  // 36 KB
+constexpr int kThreads = 192;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColComp = 256, kColSf = 384;  // SF: 2 x (16 A + 16 B)
+
+enum WaitSite : uint32_t {
+  kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6
+};
+
+struct GemmParams {
+  CUtensorMap tm_a;  // A codes [rows, K/2] u8
+  CUtensorMap tm_b;  // B codes [N, K/2] u8, or [E, N, K/2]
+  CUtensorMap tm_r;  // R_S [rows, k] bf16
+  CUtensorMap tm_w;  // W_S [N, k] bf16, or [E, N, k]
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  uint64_t b_sf_expert_stride;
+  const float* g_a;
+  const float* g_b;
+  __nv_bfloat16* y;
+  int64_t M, N, K;
+  int k;
+  int flags;
+  int fmt;
+  int E;
+  const int32_t* offsets;
+  int grouped;
+};
+
+struct Tile {
+  int e;          // expert (0 for dense)
+  int64_t row0;   // first row of A / Y
+  int rows;       // valid rows (<= 128)
+  int64_t sf_rt;  // 128-row tile index in A's scale layout
+  int n0;         // first output column
+};
+
+// Grouped schedule tables in shared memory (after the stage ring).
+struct SchedSmem {
+  int32_t* off;         // [E+1] row offsets
+  int32_t* tile_start;  // [E+1] prefix of per-expert tile counts
+  int32_t* pbase;       // [E] scale-layout tile row of each expert
+};
+
+__device__ __forceinline__ bool tile_of(const GemmParams& p, const SchedSmem& s, int64_t t, int n_tiles_n, Tile& out) {
+  if (!p.grouped) {
+    const int64_t mt = t / n_tiles_n;
+    const int nt = (int)(t - mt * n_tiles_n);
+    out.e = 0;
+    out.row0 = mt * BM;
+    const int64_t rem = p.M - out.row0;
+    out.rows = rem < BM ? (int)rem : BM;
+    out.sf_rt = mt;
+    out.n0 = nt * BN;
+    return true;
+  }
+  // expert e: last with tile_start[e] <= t
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int64_t local = t - s.tile_start[e];
+  const int64_t mt = local / n_tiles_n;
+  const int nt = (int)(local - mt * n_tiles_n);
+  out.e = e;
+  out.row0 = (int64_t)s.off[e] + mt * BM;
+  const int64_t rem = (int64_t)s.off[e + 1] - out.row0;
+  out.rows = rem < BM ? (int)rem : BM;
+  out.sf_rt = (int64_t)(s.pbase[e] >> 7) + mt;
+  out.n0 = nt * BN;
+  return true;
+}
+
+__device__ __forceinline__ uint32_t idesc_fp4(int fmt, uint32_t sf_id) {
+  // a/b format E2M1 (=1) at bits 7 and 10, N>>3 at 17, scale type at 23
+  // (0 = UE4M3, 1 = UE8M0), M>>4 at 24, scale-factor ids at 29 (A) / 4 (B).
+  uint32_t d = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  if (fmt == 1) d |= (1u << 23) | (sf_id << 29) | (sf_id << 4);
+  return d;
+}
+
+__device__ __forceinline__ uint32_t idesc_bf16() {
+  // D f32 (=1) at bit 4, A/B bf16 (=1) at bits 7 / 10, K-major both.
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// 128-byte swizzled, K-major operand tile: 8-row atoms of 1024 bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
+// Scale chunk for tcgen05.cp: 32 rows x 16 bytes, no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
+
+__global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base for the swizzled stages
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* comp_empty = acc_empty + 2;
+  uint64_t* drain = comp_empty + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  SchedSmem sched{};
+  int64_t num_tiles;
+  const int n_tiles_n = (int)(p.N / BN);
+  if (p.grouped) {
+    sched.off = s_sched;
+    sched.tile_start = s_sched + (p.E + 1);
+    sched.pbase = s_sched + 2 * (p.E + 1);
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sched.off[i] = p.offsets[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t ts = 0, pb = 0;
+      for (int e = 0; e < p.E; ++e) {
+        const int32_t me = sched.off[e + 1] - sched.off[e];
+        const int32_t mt = (me + BM - 1) / BM;
+        sched.tile_start[e] = ts;
+        sched.pbase[e] = pb;
+        ts += mt * n_tiles_n;
+        pb += mt * BM;
+      }
+      sched.tile_start[p.E] = ts;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(comp_empty, 4);
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  num_tiles = p.grouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BM - 1) / BM) * (int64_t)n_tiles_n;
+
+  const int sf_chunks_per_kt = p.fmt == 1 ? 2 : 4;  // 512-byte chunks per 256-element k-tile
+  const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
+  const int n_kt = (int)((p.K + 255) / 256);
+  const int n_ct = (p.k + 63) / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_a);
+      tma_prefetch_desc(&p.tm_b);
+      if (n_ct > 0) {
+        tma_prefetch_desc(&p.tm_r);
+        tma_prefetch_desc(&p.tm_w);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        Tile tl;
+        tile_of(p, sched, t, n_tiles_n, tl);
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+          uint8_t* sa = stages + stage * kStageBytes;
+          uint8_t* sb = sa + kTileBytes;
+          uint8_t* sfa = sb + kTileBytes;
+          uint8_t* sfb = sfa + kSfBytes;
+          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+          const uint32_t sf_bytes = (uint32_t)nch * 512u;
+          mbar_arrive_expect_tx(&full[stage], 2u * kTileBytes + 2u * sf_bytes);
+          tma_load_2d(sa, &p.tm_a, &full[stage], kt * BKB, (int32_t)tl.row0);
+          if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0, tl.e);
+          else tma_load_2d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0);
+          bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
+          bulk_load(sfb, p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride + ((uint64_t)(tl.n0 / BN) * n_cg + cg0) * 512u,
+                    sf_bytes, &full[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        for (int ct = 0; ct < n_ct && ok; ++ct) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+          uint8_t* sa = stages + stage * kStageBytes;
+          uint8_t* sb = sa + kTileBytes;
+          mbar_arrive_expect_tx(&full[stage], 2u * kTileBytes);
+          tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
+          if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
+          else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // wind down: let copies already issued land before the CTA exits
+        for (int i = 0; i < kStages; ++i) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&full[i], 0) && !mbar_try_wait(&full[i], 1)) {
+            if (globaltimer() - t0 > 1000000ull) break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      uint32_t comp_phase = 0;
+      bool ok = true;
+      uint32_t kt_global = 0;  // alternates the scale-factor TMEM slot
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + stage * kStageBytes);
+          const uint32_t sb = sa + kTileBytes;
+          const uint32_t sfa = sb + kTileBytes;
+          const uint32_t sfb = sfa + kSfBytes;
+          const uint32_t col_sf = kColSf + (kt_global & 1u) * 32u;
+          const uint32_t t_sfa = tmem + col_sf, t_sfb = tmem + col_sf + 16u;
+          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+          for (int c = 0; c < nch; ++c) {
+            tmem_cp_32x128b_x4(t_sfa + 4u * c, desc_sf(sfa + 512u * c));
+            tmem_cp_32x128b_x4(t_sfb + 4u * c, desc_sf(sfb + 512u * c));
+          }
+          const int64_t krem = p.K - (int64_t)kt * 256;
+          const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
+          for (int j = 0; j < n_mma; ++j) {
+            const uint64_t adesc = desc_sw128(sa + 32u * j);
+            const uint64_t bdesc = desc_sw128(sb + 32u * j);
+            const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
+            if (p.fmt == 1) {
+              mma_mxf4_2x(d_acc, adesc, bdesc, idesc_fp4(1, (uint32_t)(j & 1) * 2u), t_sfa + 4u * (j >> 1),
+                          t_sfb + 4u * (j >> 1), accum);
+            } else {
+              mma_nvf4_4x(d_acc, adesc, bdesc, idesc_fp4(0, 0), t_sfa + 4u * j, t_sfb + 4u * j, accum);
+            }
+          }
+          tc_commit(&empty[stage]);
+          ++kt_global;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (n_ct > 0 && ok) {
+          if (!mbar_wait(comp_empty, comp_phase ^ 1u, kWaitCompEmpty, s_abort)) { ok = false; break; }
+          comp_phase ^= 1u;
+          tc_fence_after();
+          for (int ct = 0; ct < n_ct && ok; ++ct) {
+            if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(stages + stage * kStageBytes);
+            const uint32_t sb = sa + kTileBytes;
+            const int krem = p.k - ct * 64;
+            const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
+            for (int j = 0; j < n_mma; ++j) {
+              mma_bf16(tmem + kColComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
+                       (ct > 0 || j > 0) ? 1u : 0u);
+            }
+            tc_commit(&empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, kWaitDrain, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------ epilogue ----
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      Tile tl;
+      tile_of(p, sched, t, n_tiles_n, tl);
+      if (!mbar_wait(&acc_full[acc], acc_phase, kWaitAccFull, s_abort)) break;
+      tc_fence_after();
+      float alpha = 1.f, beta = 0.f;
+      if (p.fmt == 0) {
+        const float ga = p.g_a ? *p.g_a : 1.f;
+        const float gb = p.g_b ? p.g_b[tl.e] : 1.f;
+        alpha = ga * gb;
+        beta = (p.flags == 1) ? 1.f : gb;
+      }
+      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kColAcc1 : kColAcc0);
+      const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kColComp;
+      const bool row_ok = r < tl.rows;
+      __nv_bfloat16* yrow = p.y + (tl.row0 + r) * p.N + tl.n0;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t v[16], w[16];
+        tmem_ld_32x32b_x16(t_acc + c, v);
+        if (n_ct > 0) tmem_ld_32x32b_x16(t_cmp + c, w);
+        tmem_ld_wait();
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float y0 = alpha * __uint_as_float(v[2 * i]);
+          float y1 = alpha * __uint_as_float(v[2 * i + 1]);
+          if (n_ct > 0) {
+            y0 = fmaf(beta, __uint_as_float(w[2 * i]), y0);
+            y1 = fmaf(beta, __uint_as_float(w[2 * i + 1]), y1);
+          }
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&acc_empty[acc]);
+        if (n_ct > 0) mbar_arrive(comp_empty);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- host side ---
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+// rank-2 or rank-3 row-major tensor: dims innermost first
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, int rank,
+              const uint64_t* dims, uint32_t box0, uint32_t box1) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t gdim[3], gstr[2];
+  cuuint32_t box[3] = {box0, box1, 1}, estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+  gstr[0] = dims[0] * esize;
+  if (rank == 3) gstr[1] = dims[0] * dims[1] * esize;
+  return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+
+cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int E = grouped ? pr.E : 1;
+  const uint64_t rows = (uint64_t)pr.M;
+  const uint64_t kb = (uint64_t)(pr.K / 2);
+  {
+    const uint64_t d[2] = {kb, rows};
+    if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
+  }
+  if (grouped) {
+    const uint64_t d[3] = {kb, (uint64_t)pr.N, (uint64_t)E};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 3, d, BKB, BN)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t d[2] = {kb, (uint64_t)pr.N};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BN)) return cudaErrorInvalidValue;
+  }
+  if (pr.k > 0) {
+    const uint64_t dr[2] = {(uint64_t)pr.k, rows};
+    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
+    if (grouped) {
+      const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BN))
+        return cudaErrorInvalidValue;
+    } else {
+      const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BN))
+        return cudaErrorInvalidValue;
+    }
+  }
+  p.a_sf = pr.a_scales;
+  p.b_sf = pr.b_scales;
+  const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
+  p.b_sf_expert_stride = (uint64_t)(((pr.N + 127) / 128) * 128) * (uint64_t)n_sf_cols;
+  p.g_a = pr.g_a;
+  p.g_b = pr.g_b;
+  p.y = pr.y;
+  p.M = pr.M;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.k = pr.k;
+  p.flags = pr.flags;
+  p.fmt = pr.fmt;
+  p.E = E;
+  p.offsets = pr.offsets;
+  p.grouped = grouped ? 1 : 0;
+
+  const int n_tiles_n = (int)(pr.N / BN);
+  int64_t tiles;
+  if (grouped) tiles = ((pr.M + BM - 1) / BM + E) * (int64_t)n_tiles_n;  // upper bound
+  else tiles = ((pr.M + BM - 1) / BM) * (int64_t)n_tiles_n;
+  int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  if (grid < 1) grid = 1;
+  const size_t smem = kSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
+  cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  w4a4_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int) { return 0; }
+
+cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {
+  return launch(p, false, num_sms, stream);
+}
+
+cudaError_t launch_grouped_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {
+  if ((size_t)p.E * 12 + 8 > 227 * 1024 - kSmemBytes) return cudaErrorInvalidValue;
+  return launch(p, true, num_sms, stream);
+}
+
+cudaError_t gemm_status(uint32_t* out2, bool clear) {
+  cudaError_t err = cudaMemcpyFromSymbol(out2, g_dev_status, sizeof(uint32_t) * 2);
+  if (err == cudaSuccess && clear) {
+    const uint32_t z[2] = {0u, 0u};
+    err = cudaMemcpyToSymbol(g_dev_status, z, sizeof(z));
+  }
+  return err;
+}
+
+cudaError_t gemm_set_wait_limit(uint64_t ns) { return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns)); }
+
+}  // namespace nv4

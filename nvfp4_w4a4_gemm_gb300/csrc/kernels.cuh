@@ -1,0 +1,65 @@
+// Launchers of the library's kernels (internal; the C ABI is in api.cu).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace nv4 {
+
+constexpr int kMaxAmaxPartials = 1024;
+
+int amax_partials_count(int64_t M, int64_t K, int num_sms);
+
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
+                                  float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
+                                  __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
+                                  int num_sms, cudaStream_t stream);
+
+cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
+                                int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
+                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_channel_stats(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g,
+                                 const int32_t* offsets, int E, double* sum, double* sumsq, int num_sms,
+                                 cudaStream_t stream);
+
+cudaError_t launch_select_channels(const double* sum, const double* sumsq, const int32_t* offsets, int E,
+                                   int64_t M_all, const double* sum_all, const double* sumsq_all, int64_t K, int k,
+                                   int32_t* chan_out, cudaStream_t stream);
+
+cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* partials,
+                                float* g_out, int num_sms, cudaStream_t stream);
+
+cudaError_t quant_status(uint32_t* out2, bool clear);
+
+// ----------------------------------------------------------------- GEMM ----
+struct GemmProblem {
+  int fmt = 0;  // 0 NVFP4, 1 MXFP4
+  int64_t M = 0, N = 0, K = 0;
+  const uint8_t* a_codes = nullptr;
+  const uint8_t* a_scales = nullptr;
+  const float* g_a = nullptr;
+  const uint8_t* b_codes = nullptr;
+  const uint8_t* b_scales = nullptr;
+  const float* g_b = nullptr;
+  const __nv_bfloat16* resid = nullptr;
+  const __nv_bfloat16* w_sel = nullptr;
+  int k = 0;
+  int flags = 0;
+  __nv_bfloat16* y = nullptr;
+  int E = 1;                        // grouped: number of experts
+  const int32_t* offsets = nullptr; // grouped: [E+1]
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream);
+cudaError_t gemm_status(uint32_t* out2, bool clear);
+cudaError_t gemm_set_wait_limit(uint64_t ns);
+
+}  // namespace nv4

@@ -1,0 +1,661 @@
+// Online activation quantizers (HBM-bound, one pass over X):
+//   * NVFP4: 16-element blocks, E4M3 block scale under an FP32 tensor scale,
+//     E2M1 codes (RNE, satfinite) packed two per byte, the block scales
+//     written straight into the 128x4 tile layout the block-scaled MMA reads,
+//     and the BF16 compensation residual x - deq(q(x)) on the channel set S.
+//   * MXFP4: 32-element blocks with power-of-two (E8M0) scales, optionally
+//     with the per-block three-way error decomposition statistics.
+//   * helpers: tensor amax pre-pass, compensation weight rows, calibration
+//     statistics and top-k channel selection.
+//
+// Sources: QUADS (arXiv 2607.15810) abstract -- activations are quantized
+// online and their error comes from the coarse E2M1 grid; gist.science
+// explainer of QUADS, Technisches Resuemee 2.2 B -- residual term on the
+// high-residual channels; FourSight (arXiv 2611.04887) abstract -- those
+// channels kept in BF16, chosen by variance; "Decomposing MXFP4 quantization
+// error" (arXiv 2605.20402v2) abstract -- scale bias + deadzone truncation +
+// grid noise.
+//
+// Thread mapping (NVFP4): one thread owns 8 consecutive bf16 of a row (one
+// 16-byte load), two adjacent lanes own one 16-element block and combine
+// their absmax with one shuffle; a warp covers a 256-element row segment and
+// writes 128 contiguous code bytes.  Each warp keeps several segments' loads
+// in flight before doing any arithmetic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace nv4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;            // row segments in flight per warp
+constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Byte offset of the 4-scale group (row, scale column group cg) in the
+// 128x4 tile layout: tile (row/128, cg) of 512 bytes, then (row%32)*16 +
+// ((row%128)/32)*4 inside it.
+__device__ __forceinline__ uint64_t tile_group_offset(int64_t row, int64_t cg, int64_t n_cg) {
+  return ((uint64_t)(row >> 7) * n_cg + cg) * 512u + (uint64_t)(row & 31) * 16u + (uint64_t)((row >> 5) & 3) * 4u;
+}
+
+// Reduce the amax pre-pass partials to the tensor decode scale.
+__device__ float tensor_scale_from_partials(const float* partials, int n) {
+  __shared__ float red[kThreads / 32];
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partials[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  __syncthreads();
+  return m > 0.f ? __fdiv_rn(m, kAmaxToScale) : 1.0f;
+}
+
+// First index i in sorted s[0..n) with s[i] >= v.
+__device__ __forceinline__ int lower_bound_i32(const int32_t* s, int n, int32_t v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s[mid] < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// ------------------------------------------------------------- amax -------
+__global__ void __launch_bounds__(kThreads) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
+                                                        int64_t ldx, float* __restrict__ partials) {
+  const int64_t vec_per_row = K / 8;
+  const int64_t total = M * vec_per_row;
+  float m = 0.f;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / vec_per_row, c = (v - r * vec_per_row) * 8;
+    float f[8];
+    unpack8(ldg_stream(x + r * ldx + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  }
+  __shared__ float red[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.f;
+    for (int i = 0; i < kThreads / 32; ++i) b = fmaxf(b, red[i]);
+    partials[blockIdx.x] = b;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) scale_from_partials_kernel(const float* __restrict__ partials, int n,
+                                                                      float* __restrict__ g_out) {
+  const float g = tensor_scale_from_partials(partials, n);
+  if (threadIdx.x == 0) *g_out = g;
+}
+
+// ------------------------------------------------------------ NVFP4 -------
+struct QuantArgs {
+  const __nv_bfloat16* x;
+  int64_t M, K, ldx;
+  const float* g_in;        // static tensor scale, or nullptr
+  const float* partials;    // dynamic: amax partials
+  int n_partials;
+  float* g_out;             // may be nullptr
+  uint8_t* codes;           // [M, K/2]
+  uint8_t* scales;          // tiled
+  const int32_t* chan;      // [E, k] sorted per expert (E = 1 for dense)
+  int k;
+  __nv_bfloat16* resid;     // [M, k]
+  const int32_t* offsets;   // grouped: [E+1] device, else nullptr
+  int E;
+};
+
+template <bool kGrouped>
+__global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
+  extern __shared__ int32_t smem_i32[];
+  // smem: chan [E*k] | offsets [E+1] | padded bases [E]
+  int32_t* s_chan = smem_i32;
+  int32_t* s_off = s_chan + a.E * a.k;
+  int32_t* s_pbase = s_off + (a.E + 1);
+  const int nchan = a.E * a.k;
+  for (int i = threadIdx.x; i < nchan; i += blockDim.x) s_chan[i] = a.chan[i];
+  if (kGrouped) {
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t base = 0;
+      for (int e = 0; e < a.E; ++e) {
+        s_pbase[e] = base;
+        base += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
+      }
+    }
+  }
+  float g;
+  if (a.g_in != nullptr) {
+    g = *a.g_in;
+    __syncthreads();
+  } else {
+    g = tensor_scale_from_partials(a.partials, a.n_partials);  // contains __syncthreads
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.g_out != nullptr) *a.g_out = g;
+
+  const int lane = threadIdx.x & 31;
+  const int64_t seg_per_row = (a.K + 255) / 256;
+  const int64_t n_seg = a.M * seg_per_row;
+  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n_cg = (a.K / 16 + 3) / 4;
+
+  for (int64_t s0 = warp_global * kUnroll; s0 < n_seg; s0 += n_warps * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t s = s0 + u;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (s < n_seg) {
+        const int64_t r = s / seg_per_row;
+        const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
+        if (c < a.K) v[u] = ldg_stream(a.x + r * a.ldx + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t s = s0 + u;
+      if (s >= n_seg) break;  // warp-uniform
+      const int64_t r = s / seg_per_row;
+      const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
+      const bool valid = c < a.K;
+      float f[8];
+      unpack8(v[u], f);
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
+      const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
+      const uint32_t sig = cvt_e4m3(t);
+      const float d = __fmul_rn(e4m3_to_f32(sig), g);
+      uint32_t packed = 0;
+      float deq[8];
+      if (d != 0.f) {
+        const float rcp = __fdiv_rn(1.0f, d);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t b = cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp));
+          packed |= b << (8 * i);
+          const uint32_t h2 = cvt_e2m1x2_to_f16x2(b);
+          deq[2 * i] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
+          deq[2 * i + 1] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), d);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) deq[i] = 0.f;
+      }
+      // row of the scale tile layout (grouped: each expert starts a tile)
+      int64_t srow = r;
+      int e = 0;
+      if (kGrouped) {
+        // expert of row r: last e with offsets[e] <= r
+        int lo = 0, hi = a.E;  // find e in [0, E)
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_off[mid] <= r) lo = mid; else hi = mid;
+        }
+        e = lo;
+        srow = (int64_t)s_pbase[e] + (r - s_off[e]);
+      }
+      if (valid) {
+        *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
+      }
+      // gather the 4 block scales of a 64-element group into lane%8 == 0
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 2);
+      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 4);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 6);
+      if ((lane & 7) == 0 && valid) {
+        const int64_t blk = c / 16;  // multiple of 4
+        const int64_t nb = a.K / 16;
+        uint32_t word = sig;
+        if (blk + 1 < nb) word |= s1 << 8;
+        if (blk + 2 < nb) word |= s2 << 16;
+        if (blk + 3 < nb) word |= s3 << 24;
+        *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
+      }
+      // compensation residual on the channels of S that fall in [c, c+8)
+      if (valid && a.k > 0) {
+        const int32_t* S = s_chan + e * a.k;
+        int i = lower_bound_i32(S, a.k, (int32_t)c);
+        for (; i < a.k && S[i] < c + 8; ++i) {
+          const int j = S[i] - (int)c;
+          float xf = f[0], dq = deq[0];
+#pragma unroll
+          for (int q = 1; q < 8; ++q) if (j == q) { xf = f[q]; dq = deq[q]; }
+          a.resid[r * a.k + i] = __float2bfloat16_rn(__fsub_rn(xf, dq));
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ MXFP4 -------
+struct MxArgs {
+  const __nv_bfloat16* x;
+  int64_t M, K, ldx;
+  uint8_t* codes;
+  uint8_t* scales;     // tiled, K/32 scales per row
+  float* stats;        // [M*K/32][4] or nullptr
+  uint8_t* dead;       // [M*K/32] or nullptr
+};
+
+// floor(log2 a) - 2 clamped to [-127, 127], from the fp32 bit pattern.
+__device__ __forceinline__ int mx_exponent(float a) {
+  if (!(a > 0.f)) return -127;
+  const uint32_t b = __float_as_uint(a);
+  int ex = (int)((b >> 23) & 0xFF);
+  int fl;
+  if (ex == 0) {
+    fl = 31 - __clz(b & 0x7FFFFFu) - 149;  // subnormal: value = m * 2^-149
+  } else {
+    fl = ex - 127;
+  }
+  int e = fl - 2;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // exact 2^e for e in [-149, 127]
+  if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+  return __uint_as_float(1u << (e + 149));
+}
+
+__device__ __forceinline__ float e2m1_mag(uint32_t code) {
+  const uint32_t h2 = cvt_e2m1x2_to_f16x2(code & 0x7u);
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+__global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(MxArgs a) {
+  // one thread = 8 elements, 4 lanes = one 32-element block
+  const int lane = threadIdx.x & 31;
+  const int64_t seg_per_row = (a.K + 255) / 256;
+  const int64_t n_seg = a.M * seg_per_row;
+  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t nblk = a.K / 32;
+  const int64_t n_cg = (nblk + 3) / 4;
+  for (int64_t s0 = warp_global * kUnroll; s0 < n_seg; s0 += n_warps * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t s = s0 + u;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (s < n_seg) {
+        const int64_t r = s / seg_per_row;
+        const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
+        if (c < a.K) v[u] = ldg_stream(a.x + r * a.ldx + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t s = s0 + u;
+      if (s >= n_seg) break;
+      const int64_t r = s / seg_per_row;
+      const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
+      const bool valid = c < a.K;
+      float f[8];
+      unpack8(v[u], f);
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      const int e = mx_exponent(am);
+      const float inv = pow2f(-e);
+      uint32_t packed = 0;
+      uint32_t cds[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t b = cvt_e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
+        packed |= b << (8 * i);
+        cds[2 * i] = b & 0xF;
+        cds[2 * i + 1] = b >> 4;
+      }
+      if (valid) *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
+      const uint32_t sb = (uint32_t)(e + 127);
+      // 4 blocks of 32 per 128 elements = 16 lanes; gather into lane%16 == 0
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 4);
+      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 8);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 12);
+      if ((lane & 15) == 0 && valid) {
+        const int64_t blk = c / 32;
+        uint32_t word = sb;
+        if (blk + 1 < nblk) word |= s1 << 8;
+        if (blk + 2 < nblk) word |= s2 << 16;
+        if (blk + 3 < nblk) word |= s3 << 24;
+        *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(r, blk / 4, n_cg)) = word;
+      }
+      if (a.stats != nullptr || a.dead != nullptr) {
+        // decomposition through the ideal scale s* = a / 6 (fp32)
+        float eb = 0.f, ed = 0.f, eg = 0.f, ee = 0.f;
+        uint32_t nd = 0;
+        if (am > 0.f) {
+          const float ss = __fdiv_rn(am, 6.0f);
+          const float sc = pow2f(e);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t bs = cvt_e2m1x2(__fdiv_rn(f[2 * i], ss), __fdiv_rn(f[2 * i + 1], ss));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float xv = f[2 * i + h];
+              const uint32_t cs = (bs >> (4 * h)) & 0xF;
+              const uint32_t cq = cds[2 * i + h];
+              const float qs = copysignf(__fmul_rn(e2m1_mag(cq), sc), (cq & 8) ? -1.f : 1.f);
+              const float qst = copysignf(__fmul_rn(e2m1_mag(cs), ss), (cs & 8) ? -1.f : 1.f);
+              const float E = __fsub_rn(qs, xv);
+              const float B = __fsub_rn(qs, qst);
+              const float R = __fsub_rn(qst, xv);
+              ee = __fmaf_rn(E, E, ee);
+              eb = __fmaf_rn(B, B, eb);
+              if ((cs & 7u) == 0u) {
+                ed = __fmaf_rn(R, R, ed);
+                nd += (xv != 0.f) ? 1u : 0u;
+              } else {
+                eg = __fmaf_rn(R, R, eg);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          eb += __shfl_xor_sync(0xffffffffu, eb, o);
+          ed += __shfl_xor_sync(0xffffffffu, ed, o);
+          eg += __shfl_xor_sync(0xffffffffu, eg, o);
+          ee += __shfl_xor_sync(0xffffffffu, ee, o);
+          nd += __shfl_xor_sync(0xffffffffu, nd, o);
+        }
+        if ((lane & 3) == 0 && valid) {
+          const int64_t bidx = r * nblk + c / 32;
+          if (a.stats != nullptr)
+            *reinterpret_cast<float4*>(a.stats + bidx * 4) = make_float4(eb, ed, eg, ee);
+          if (a.dead != nullptr) a.dead[bidx] = (uint8_t)nd;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------ compensation weights -----
+// w_sel[e][n][i] = E2M1(code[e][n][S_e[i]]) * sigma[e][n][S_e[i]/16] (exact in
+// bf16), or the original bf16 W^T[e][n][S_e[i]] when `wt` is given.
+__global__ void comp_weights_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                    const __nv_bfloat16* __restrict__ wt, int64_t N, int64_t K,
+                                    const int32_t* __restrict__ chan, int k, int E, uint64_t scale_stride,
+                                    __nv_bfloat16* __restrict__ w_sel) {
+  const int64_t total = (int64_t)E * N * k;
+  const int64_t n_cg = (K / 16 + 3) / 4;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int i = (int)(t % k);
+    const int64_t n = (t / k) % N;
+    const int e = (int)(t / ((int64_t)k * N));
+    const int64_t j = chan[(int64_t)e * k + i];
+    if (j < 0 || j >= K) {
+      report_error(kDevErrInvalidArg, 0x100u);
+      w_sel[t] = __float2bfloat16_rn(0.f);
+      continue;
+    }
+    if (wt != nullptr) {
+      w_sel[t] = wt[((int64_t)e * N + n) * K + j];
+      continue;
+    }
+    const uint8_t byte = codes[((int64_t)e * N + n) * (K / 2) + j / 2];
+    const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 0xF);
+    const int64_t blk = j / 16;
+    const uint8_t sig = scales[(uint64_t)e * scale_stride + tile_group_offset(n, blk / 4, n_cg) + (blk & 3)];
+    float v = __fmul_rn(e2m1_mag(code), e4m3_to_f32(sig));
+    if (code & 8u) v = -v;
+    w_sel[t] = __float2bfloat16_rn(v);
+  }
+}
+
+// ------------------------------------------------------- calibration ------
+// Per-channel sum and sum of squares (fp64) of the fp32 residual
+// x - deq(q(x)) over rows; grouped: per expert (stats [E][K]).
+__global__ void __launch_bounds__(kThreads) channel_stats_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
+                                                                 int64_t K, int64_t ldx, const float* __restrict__ g_ptr,
+                                                                 const int32_t* __restrict__ offsets, int E,
+                                                                 double* __restrict__ sum, double* __restrict__ sumsq) {
+  // grid: x = 16-column groups (blocks), y = row chunks; each thread one
+  // block of 16 channels of one row at a time, accumulating locally over
+  // rows of one expert before flushing with fp64 atomics.
+  const float g = *g_ptr;
+  const int64_t nblk = K / 16;
+  const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= nblk) return;
+  const int64_t rows_per = (M + gridDim.y - 1) / gridDim.y;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per;
+  const int64_t r1 = r0 + rows_per < M ? r0 + rows_per : M;
+  double s[16], q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = q[i] = 0.0;
+  int cur_e = -1;
+  auto flush = [&](int e) {
+    if (e < 0) return;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      atomicAdd(sum + (int64_t)e * K + blk * 16 + i, s[i]);
+      atomicAdd(sumsq + (int64_t)e * K + blk * 16 + i, q[i]);
+      s[i] = q[i] = 0.0;
+    }
+  };
+  for (int64_t r = r0; r < r1; ++r) {
+    int e = 0;
+    if (offsets != nullptr) {
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= r) lo = mid; else hi = mid;
+      }
+      e = lo;
+    }
+    if (e != cur_e) { flush(cur_e); cur_e = e; }
+    float f[16];
+    unpack8(*reinterpret_cast<const uint4*>(x + r * ldx + blk * 16), *reinterpret_cast<float(*)[8]>(f));
+    unpack8(*reinterpret_cast<const uint4*>(x + r * ldx + blk * 16 + 8), *reinterpret_cast<float(*)[8]>(f + 8));
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
+    const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
+    const float d = __fmul_rn(e4m3_to_f32(cvt_e4m3(t)), g);
+    const float rcp = d != 0.f ? __fdiv_rn(1.0f, d) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float d0 = 0.f, d1 = 0.f;
+      if (d != 0.f) {
+        const uint32_t b = cvt_e2m1x2(__fmul_rn(f[i], rcp), __fmul_rn(f[i + 1], rcp));
+        const uint32_t h2 = cvt_e2m1x2_to_f16x2(b);
+        d0 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
+        d1 = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), d);
+      }
+      const double r0d = (double)__fsub_rn(f[i], d0), r1d = (double)__fsub_rn(f[i + 1], d1);
+      s[i] += r0d; q[i] += r0d * r0d;
+      s[i + 1] += r1d; q[i + 1] += r1d * r1d;
+    }
+  }
+  flush(cur_e);
+}
+
+// Top-k channels by population variance (ties -> lower index), sorted
+// ascending.  One CTA per expert; rank of channel j = number of channels
+// that beat it.  Experts with fewer than 2 rows use the all-row statistics
+// (sum_all / sumsq_all over M_all rows).
+__global__ void __launch_bounds__(1024) select_channels_kernel(const double* __restrict__ sum,
+                                                               const double* __restrict__ sumsq,
+                                                               const int32_t* __restrict__ offsets, int64_t M_all,
+                                                               const double* __restrict__ sum_all,
+                                                               const double* __restrict__ sumsq_all, int64_t K, int k,
+                                                               int32_t* __restrict__ chan_out) {
+  extern __shared__ double s_var[];
+  int* s_flag = reinterpret_cast<int*>(s_var + K);
+  const int e = blockIdx.x;
+  int64_t rows = M_all;
+  const double* S = sum + (int64_t)e * K;
+  const double* Q = sumsq + (int64_t)e * K;
+  if (offsets != nullptr) {
+    rows = offsets[e + 1] - offsets[e];
+    if (rows < 2) { S = sum_all; Q = sumsq_all; rows = M_all; }
+  }
+  const double inv = rows > 0 ? 1.0 / (double)rows : 0.0;
+  for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
+    const double mu = S[j] * inv;
+    const double v = Q[j] * inv - mu * mu;
+    s_var[j] = v > 0.0 ? v : 0.0;
+  }
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
+    const double vj = s_var[j];
+    int64_t rank = 0;
+    for (int64_t i = 0; i < K; ++i) {
+      const double vi = s_var[i];
+      rank += (vi > vj) || (vi == vj && i < j);
+    }
+    s_flag[j] = rank < k ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // compaction in index order (K small)
+    int n = 0;
+    for (int64_t j = 0; j < K && n < k; ++j)
+      if (s_flag[j]) chan_out[(int64_t)e * k + n++] = (int32_t)j;
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers ---
+cudaError_t quant_status(uint32_t* out2, bool clear) {
+  cudaError_t err = cudaMemcpyFromSymbol(out2, g_dev_status, sizeof(uint32_t) * 2);
+  if (err == cudaSuccess && clear) {
+    const uint32_t z[2] = {0u, 0u};
+    err = cudaMemcpyToSymbol(g_dev_status, z, sizeof(z));
+  }
+  return err;
+}
+
+cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* partials,
+                                float* g_out, int num_sms, cudaStream_t stream) {
+  const int p = amax_partials_count(M, K, num_sms);
+  amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
+  scale_from_partials_kernel<<<1, kThreads, 0, stream>>>(partials, p, g_out);
+  return cudaGetLastError();
+}
+
+int amax_partials_count(int64_t M, int64_t K, int num_sms) {
+  int64_t vecs = M * (K / 8);
+  int64_t want = (vecs + kThreads - 1) / kThreads;
+  int64_t cap = (int64_t)num_sms * 4;
+  if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
+  if (want < 1) want = 1;
+  return (int)(want < cap ? want : cap);
+}
+
+cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
+                                  float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
+                                  __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
+                                  int num_sms, cudaStream_t stream) {
+  if (M == 0) { k = 0; chan = nullptr; resid = nullptr; }
+  QuantArgs a{};
+  a.x = x; a.M = M; a.K = K; a.ldx = ldx;
+  a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
+  a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
+  if (g_in == nullptr) {
+    const int p = amax_partials_count(M, K, num_sms);
+    amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
+    a.partials = partials;
+    a.n_partials = p;
+  }
+  const int64_t n_seg = M * ((K + 255) / 256);
+  const int64_t warps_needed = (n_seg + kUnroll - 1) / kUnroll;
+  int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
+  const int64_t cap = (int64_t)num_sms * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const size_t smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
+  if (offsets != nullptr) {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(nvfp4_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    nvfp4_quant_kernel<true><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
+  } else {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(nvfp4_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    nvfp4_quant_kernel<false><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  MxArgs a{x, M, K, ldx, codes, scales, stats, dead};
+  const int64_t n_seg = M * ((K + 255) / 256);
+  int64_t blocks = ((n_seg + kUnroll - 1) / kUnroll + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  mxfp4_quant_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
+                                int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
+                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream) {
+  const int64_t total = (int64_t)E * N * k;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+  comp_weights_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, wt, N, K, chan, k, E, scale_stride, w_sel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_channel_stats(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g,
+                                 const int32_t* offsets, int E, double* sum, double* sumsq, int num_sms,
+                                 cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  const int64_t nblk = K / 16;
+  const unsigned bx = (unsigned)((nblk + kThreads - 1) / kThreads);
+  int64_t by = ((int64_t)num_sms * 4 + bx - 1) / bx;
+  if (by > M) by = M;
+  if (by < 1) by = 1;
+  channel_stats_kernel<<<dim3(bx, (unsigned)by), kThreads, 0, stream>>>(x, M, K, ldx, g, offsets, E, sum, sumsq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_channels(const double* sum, const double* sumsq, const int32_t* offsets, int E,
+                                   int64_t M_all, const double* sum_all, const double* sumsq_all, int64_t K, int k,
+                                   int32_t* chan_out, cudaStream_t stream) {
+  const size_t smem = (size_t)K * (sizeof(double) + sizeof(int));
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(select_channels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  select_channels_kernel<<<E, 1024, smem, stream>>>(sum, sumsq, offsets, M_all, sum_all, sumsq_all, K, k, chan_out);
+  return cudaGetLastError();
+}
+
+}  // namespace nv4

@@ -1,0 +1,101 @@
+"""C-ABI surface checks that need no GPU: the library loads, exports every
+symbol include/nvfp4w4a4.h declares, the size helpers agree with the oracle's
+layout, and argument errors are reported before anything touches a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import nvfp4 as onv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4w4a4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_w4a4_gemm_gb300 import binding
+    if not os.path.exists(binding.LIB_PATH):
+        from nvfp4_w4a4_gemm_gb300 import build
+        build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("nvfp4_quantize", "mxfp4_quantize", "w4a4_gemm_comp", "w4a4_grouped_gemm_comp"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from nvfp4_w4a4_gemm_gb300 import binding
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.EXPORTED)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.nvfp4_version() >= 10000
+    assert lib.nvfp4_status_string(0) == b"ok"
+    assert b"argument" in lib.nvfp4_status_string(1)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (64, 256), (130, 80), (8192, 4096), (16, 4096)])
+def test_scale_bytes_match_oracle_layout(lib, M, K):
+    assert lib.nvfp4_scale_bytes(M, K) == onv.scale_bytes(M, K)
+    off = onv.scale_tile_offsets(M, K // 16)
+    assert off.max() < lib.nvfp4_scale_bytes(M, K)
+
+
+def test_grouped_scale_bytes_bound(lib):
+    assert lib.nvfp4_grouped_scale_bytes(32768, 2048, 128) == onv.grouped_scale_bytes(32768, 2048, 128)
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: validation fails first
+    # K not a multiple of 16
+    assert lib.nvfp4_quantize(fake, 4, 24, 24, None, None, fake, fake, None, 0, None, None, 0, None) == 1
+    # misaligned x
+    assert lib.nvfp4_quantize(P((1 << 20) + 2), 4, 32, 32, fake, None, fake, fake, None, 0, None, None, 0,
+                              None) == 1
+    # ldx < K
+    assert lib.nvfp4_quantize(fake, 4, 32, 16, fake, None, fake, fake, None, 0, None, None, 0, None) == 1
+    # k > 0 without channel list
+    assert lib.nvfp4_quantize(fake, 4, 32, 32, fake, None, fake, fake, None, 4, fake, None, 0, None) == 1
+    # MXFP4 needs K % 32
+    assert lib.mxfp4_quantize(fake, 4, 48, 48, fake, fake, None, None, None) == 1
+    # GEMM: bad format / flag / N not a multiple of 128
+    assert lib.w4a4_gemm_comp(7, 4, 128, 64, fake, fake, None, fake, fake, None, None, None, 0, 0, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_gemm_comp(0, 4, 128, 64, fake, fake, None, fake, fake, None, None, None, 0, 9, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_gemm_comp(0, 4, 100, 64, fake, fake, None, fake, fake, None, None, None, 0, 0, fake,
+                              None, 0, None) == 2
+    # MXFP4 with compensation is not part of the method
+    assert lib.w4a4_gemm_comp(1, 4, 128, 128, fake, fake, None, fake, fake, None, fake, fake, 16, 0, fake,
+                              None, 0, None) == 2
+    # grouped: missing offsets
+    assert lib.w4a4_grouped_gemm_comp(0, 4, None, 8, 128, 64, fake, fake, None, fake, fake, None, None, None,
+                                      0, 0, fake, None, 0, None) == 1
+    # dynamic tensor scale without workspace
+    assert lib.nvfp4_quantize(fake, 4, 32, 32, None, None, fake, fake, None, 0, None, None, 0, None) == 5
+
+
+def test_empty_problem_is_a_no_op(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    # M == 0 with a static scale launches nothing and needs no device
+    assert lib.w4a4_gemm_comp(0, 0, 128, 64, None, None, None, None, None, None, None, None, 0, 0, None,
+                              None, 0, None) == 0
+    assert lib.nvfp4_prepare_comp_weights(1, 128, 64, fake, fake, None, fake, 0, 0, fake, None) == 0

@@ -1,0 +1,129 @@
+"""GPU parity of the W4A4 GEMM with compensation against the fp64 oracle.
+Tolerance (problem statement): |y - y_ref| <= 4e-3 |y_ref| + 1e-3 rms(Y_ref)
+elementwise, y_ref the fp64 product of the same dequantized operands."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm as og, mxfp4 as omx, nvfp4 as onv
+from nvfp4_w4a4_gemm_gb300 import workloads as W
+from tests.helpers import f32, gemm_within_tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_w4a4_gemm_gb300 import binding
+    binding.load()
+    return binding
+
+
+def _dense_case(nv, x, wt, chan, flags=0):
+    """Run quantize(X) + quantize(W^T) + comp weights + GEMM on the GPU and
+    the oracle on the same inputs; returns (y_gpu fp64, y_ref fp64)."""
+    N = wt.shape[0]
+    ch = torch.as_tensor(np.asarray(chan), dtype=torch.int32).cuda() if len(chan) else None
+    qx = nv.nvfp4_quantize(x.cuda(), chan=ch)
+    qw = nv.nvfp4_quantize(wt.cuda())
+    ws = None
+    if len(chan):
+        ws = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], ch, flags=flags,
+                                           wt=wt.cuda() if flags else None)
+    y = nv.w4a4_gemm_comp(qx, qw, N, resid=qx["resid"] if len(chan) else None, w_sel=ws, flags=flags)
+    torch.cuda.synchronize()
+    st, _ = nv.check_status()
+    assert st == 0, f"device status {st}"
+    y_ref, _, _ = og.linear_comp(f32(x), f32(wt), np.asarray(chan, np.int64), bf16_weights=bool(flags))
+    return f32(y).astype(np.float64), y_ref
+
+
+def _assert_close(y, y_ref):
+    ok, ratio, rms = gemm_within_tol(y, y_ref)
+    assert ok, f"max err/allowance = {ratio:.3f} (rms {rms:.4g})"
+
+
+def test_tiny_workload(nv):
+    from oracle import calib
+    d = W.dense_inputs("tiny")
+    chan = calib.calibrate(W.dense_inputs("tiny", True, False)["x"].float().numpy(), 8)
+    y, y_ref = _dense_case(nv, d["x"], d["wt"], chan)
+    _assert_close(y, y_ref)
+
+
+@pytest.mark.parametrize("M,N,K,k", [(128, 128, 256, 0), (300, 384, 1024, 64), (77, 256, 320, 72),
+                                     (1, 128, 64, 8), (513, 128, 2048, 128), (16, 640, 4096, 64)])
+def test_shapes(nv, M, N, K, k):
+    x = W.activations(M, K, max(1, K // 100), "t3x20", K + 1, M + 2)
+    wt = W.weights_t(N, K, N + K)
+    rng = np.random.default_rng(M + N + K)
+    chan = np.sort(rng.choice(K, size=k, replace=False))
+    y, y_ref = _dense_case(nv, x, wt, chan)
+    _assert_close(y, y_ref)
+
+
+def test_bf16_weight_flag(nv):
+    x = W.activations(200, 512, 5, "t3x20", 9, 9)
+    wt = W.weights_t(256, 512, 10)
+    chan = np.arange(0, 512, 8)
+    y, y_ref = _dense_case(nv, x, wt, chan, flags=1)
+    _assert_close(y, y_ref)
+
+
+def test_full_compensation_k_equals_K(nv):
+    x = W.activations(64, 256, 4, "x50", 1, 1)
+    wt = W.weights_t(128, 256, 2)
+    y, y_ref = _dense_case(nv, x, wt, np.arange(256))
+    _assert_close(y, y_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 384, 640), (8192 // 16, 5120 // 10, 5120)])
+def test_mxfp4_gemm(nv, M, N, K):
+    N = (N + 127) // 128 * 128
+    x = W.activations(M, K, max(1, K // 100), "t3x20", 5, M)
+    wt = W.weights_t(N, K, 6)
+    qx = nv.mxfp4_quantize(x.cuda())
+    qw = nv.mxfp4_quantize(wt.cuda())
+    y = nv.w4a4_gemm_comp(dict(codes=qx["codes"], scales=qx["scales"]), dict(codes=qw["codes"], scales=qw["scales"]),
+                          N, fmt=nv.FMT_MXFP4)
+    torch.cuda.synchronize()
+    ax = omx.quantize(f32(x))
+    aw = omx.quantize(f32(wt))
+    y_ref = og.reference(omx.dequantize(ax["codes"], ax["scale"]), omx.dequantize(aw["codes"], aw["scale"]))
+    _assert_close(f32(y), y_ref)
+
+
+def test_grouped_gemm_small(nv):
+    # 6 experts with ragged (and one empty) row counts
+    counts = [0, 5, 130, 1, 256, 77]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, K, N, k = int(offs[-1]), 512, 256, 32
+    E = len(counts)
+    x = W.activations(M, K, 5, "t3x20", 3, 4)
+    wt = W.weights_t(N, K, 7, experts=E)
+    rng = np.random.default_rng(1)
+    chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
+    offs_t = torch.from_numpy(offs).cuda()
+    chan_t = torch.from_numpy(chan).cuda()
+    qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t)
+    # per-expert weight quantization (each expert its own tensor scale)
+    codes, scales, gs = [], [], []
+    for e in range(E):
+        q = nv.nvfp4_quantize(wt[e].cuda())
+        codes.append(q["codes"]); scales.append(q["scales"]); gs.append(q["g"])
+    b_codes = torch.stack(codes)
+    b_scales = torch.cat(scales)
+    g_b = torch.cat(gs)
+    w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan_t, E=E)
+    y = nv.w4a4_grouped_gemm_comp(qx, offs_t, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel)
+    torch.cuda.synchronize()
+    st, _ = nv.check_status()
+    assert st == 0
+    rq = onv.quantize_grouped(f32(x), offs, chan)
+    a = onv.dequantize(rq["codes"], rq["sigma"], rq["g"])
+    bq = [onv.quantize(f32(wt[e])) for e in range(E)]
+    b = np.stack([onv.dequantize(q["codes"], q["sigma"], q["g"]) for q in bq])
+    ws = np.stack([og.comp_weight_rows(bq[e], chan[e]) for e in range(E)])
+    y_ref = og.grouped_reference(a, offs, b, rq["resid"], ws)
+    _assert_close(f32(y), y_ref)

@@ -1,0 +1,183 @@
+"""GPU parity of the quantizers against the oracle: codes, scale bytes and the
+bf16 residual must be bit-exact; MXFP4 decomposition statistics within
+fp32-vs-fp64 rounding, deadzone counts exact."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import calib, mxfp4 as omx, nvfp4 as onv, formats as F
+from nvfp4_w4a4_gemm_gb300 import workloads as W
+from tests.helpers import bf16_bits_of, f32, gather_scales, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_w4a4_gemm_gb300 import binding
+    binding.load()
+    return binding
+
+
+def _check_nvfp4(nv, x_cpu, chan=None, g=None):
+    x = x_cpu.cuda()
+    ch = None if chan is None else torch.as_tensor(chan, dtype=torch.int32).cuda()
+    gt = None if g is None else torch.tensor([g], dtype=torch.float32).cuda()
+    q = nv.nvfp4_quantize(x, g=gt, chan=ch)
+    torch.cuda.synchronize()
+    ref = onv.quantize(f32(x_cpu), g=g, chan=chan)
+    M, K = x_cpu.shape
+    assert f32(q["g"])[0] == ref["g"]
+    assert np.array_equal(u8(q["codes"]), ref["packed"]), "codes differ"
+    sc = gather_scales(q["scales"], onv.scale_tile_offsets(M, K // 16))
+    assert np.array_equal(sc, ref["sigma"]), "scale bytes differ"
+    if chan is not None and len(chan):
+        want = F.bf16_bits(ref["resid_f32"][:, np.asarray(chan)])
+        assert np.array_equal(bf16_bits_of(q["resid"]), want), "residual differs"
+    return q, ref
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_worked_examples(nv, golden_dir, idx):
+    with open(os.path.join(golden_dir, "nvfp4_worked.json")) as f:
+        ex = json.load(f)["examples"][idx]
+    x = torch.tensor([ex["x"]], dtype=torch.float32).to(torch.bfloat16)
+    q, _ = _check_nvfp4(nv, x, chan=ex["chan"])
+    assert list(u8(q["codes"])[0][: len(ex["codes"]) // 2]) == list(onv.pack(np.array(ex["codes"])))
+    np.testing.assert_array_equal(f32(q["resid"])[0], np.array(ex["resid"], np.float32))
+
+
+def test_tiny_workload(nv):
+    d = W.dense_inputs("tiny")
+    chan = calib.calibrate(W.dense_inputs("tiny", True, False)["x"].float().numpy(), 8)
+    _check_nvfp4(nv, d["x"], chan=chan)
+    _check_nvfp4(nv, d["wt"])
+
+
+@pytest.mark.parametrize("M,K,k", [(1, 16, 1), (3, 48, 5), (130, 80, 7), (257, 1040, 33), (64, 4096, 128),
+                                   (517, 2064, 64)])
+def test_ragged_shapes(nv, M, K, k):
+    x = W.activations(M, K, max(1, K // 100), "t3x20", M + K, M * 7 + 1)
+    rng = np.random.default_rng(M * 31 + K)
+    chan = np.sort(rng.choice(K, size=k, replace=False))
+    _check_nvfp4(nv, x, chan=chan)
+
+
+def test_static_scale_and_g_out(nv):
+    x = W.random_bf16((40, 96), 3, scale=2.0)
+    _check_nvfp4(nv, x, chan=[0, 95], g=0.0123)
+
+
+def test_edge_blocks(nv):
+    # zero blocks, all-equal blocks, +-6 saturation, subnormal-scale and
+    # zero-scale blocks, negative values rounding to zero.
+    rows = []
+    rows.append([0.0] * 64)
+    rows.append([1.5] * 64)
+    rows.append([2688.0] + [-2688.0] * 15 + [3.0] * 16 + [1e-3] * 16 + [-1e-6, 1e-6] * 8)
+    rows.append([1e-5 * (i - 32) for i in range(64)])
+    rows.append([-0.01] * 16 + [600.0] + [0.0] * 15 + [7.9] * 16 + [-100.0] + [0.1] * 15)
+    x = torch.tensor(rows, dtype=torch.float32).to(torch.bfloat16)
+    _check_nvfp4(nv, x, chan=list(range(0, 64, 3)))
+
+
+def test_exhaustive_e2m1_rounding_of_bf16(nv):
+    # With g = 1 and one 6.0 per block, sigma = 1 and d = 1, so code = E2M1(x)
+    # exactly: every bf16 value in [-6, 6] goes through the GPU conversion.
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = F.bf16_from_bits(bits)
+    v = v[np.isfinite(v) & (np.abs(v) <= 6.0)]
+    per = 15
+    nb = -(-len(v) // per)
+    flat = np.zeros(nb * per, np.float32)
+    flat[: len(v)] = v
+    body = np.zeros((nb, 16), np.float32)
+    body[:, 0] = 6.0
+    body[:, 1:] = flat.reshape(nb, per)
+    head = np.zeros((1, 16), np.float32)
+    head[0, 0] = 2688.0                      # tensor amax -> g = 1
+    pad = np.zeros(((-(nb + 1)) % 16, 16), np.float32)
+    pad[:, 0] = 6.0
+    x = np.concatenate([head, body, pad]).reshape(-1, 256)
+    _check_nvfp4(nv, torch.from_numpy(x).to(torch.bfloat16))
+
+
+def test_exhaustive_e4m3_block_scales_of_bf16(nv):
+    # every positive bf16 block maximum up to 2688 with g = 1
+    bits = np.arange(1, 0x7F80, dtype=np.uint32).astype(np.uint16)
+    a = F.bf16_from_bits(bits)
+    a = a[(a > 0) & (a <= 2688.0)]
+    n = -(-len(a) // 16) * 16
+    col = np.zeros(n, np.float32)
+    col[: len(a)] = a
+    col[0] = 2688.0
+    x = np.zeros((n, 16), np.float32)
+    x[:, 0] = col
+    x[:, 1] = col * np.float32(0.37)
+    _check_nvfp4(nv, torch.from_numpy(F.bf16_round(x.reshape(-1, 64))).to(torch.bfloat16))
+
+
+def test_grouped_quantize(nv):
+    d = W.moe_inputs(with_weights=False, which=("gate_up",))
+    offs = d["offsets"].numpy()
+    E = int(np.searchsorted(offs, 3000, side="right")) - 1   # experts fully below row 3000
+    offs_c = offs[: E + 1].astype(np.int32)
+    x = d["x_gate_up"][: int(offs_c[-1])]
+    rng = np.random.default_rng(0)
+    chan = np.stack([np.sort(rng.choice(2048, 32, replace=False)) for _ in range(E)]).astype(np.int32)
+    q = nv.nvfp4_quantize_grouped(x.cuda(), torch.from_numpy(offs_c).cuda(), torch.from_numpy(chan).cuda())
+    torch.cuda.synchronize()
+    ref = onv.quantize_grouped(f32(x), offs_c, chan)
+    assert f32(q["g"])[0] == ref["g"]
+    assert np.array_equal(u8(q["codes"]), ref["packed"])
+    sc = gather_scales(q["scales"], onv.grouped_scale_tile_offsets(offs_c, 2048 // 16))
+    assert np.array_equal(sc, ref["sigma"])
+    assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(ref["resid"]))
+
+
+@pytest.mark.parametrize("M,K", [(64, 256), (33, 160), (256, 5120)])
+def test_mxfp4_quantize_and_decomposition(nv, M, K):
+    x = W.activations(M, K, max(1, K // 100), "t3x20", K, M + 3)
+    q = nv.mxfp4_quantize(x.cuda(), stats=True)
+    torch.cuda.synchronize()
+    st, cnt, d = omx.block_stats(f32(x))
+    assert np.array_equal(u8(q["codes"]), d["packed"])
+    sc = gather_scales(q["scales"], onv.scale_tile_offsets(M, K // 32))
+    assert np.array_equal(sc, d["scale"])
+    assert np.array_equal(u8(q["dead"]).reshape(M, K // 32), cnt)
+    g = f32(q["stats"]).reshape(M, K // 32, 4).astype(np.float64)
+    # fp32 kernel vs fp64 oracle: per-block relative 1e-5 of the block's
+    # total error energy (the components' products of s* round in fp32)
+    tol = 1e-5 * (st[..., 3:4] + st.sum(-1, keepdims=True)) + 1e-30
+    assert np.all(np.abs(g - st) <= tol)
+
+
+def test_comp_weights_both_modes(nv):
+    wt = W.weights_t(256, 512, 11)
+    qw = nv.nvfp4_quantize(wt.cuda())
+    chan = torch.tensor([0, 15, 16, 100, 511], dtype=torch.int32).cuda()
+    ws = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan)
+    wb = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan, flags=nv.COMP_W_BF16, wt=wt.cuda())
+    torch.cuda.synchronize()
+    ref = onv.quantize(f32(wt))
+    want = onv.comp_weights(ref["codes"], ref["sigma"], chan.cpu().numpy())
+    assert np.array_equal(f32(ws).astype(np.float64), want)
+    assert np.array_equal(f32(wb), f32(wt)[:, chan.cpu().numpy()])
+
+
+def test_calibration_selects_like_oracle(nv):
+    for name in ("tiny", "decode"):
+        xc = W.dense_inputs(name, calibration=True, with_weights=False)["x"]
+        k = W.SPECS[name].k
+        got = nv.nvfp4_calibrate_channels(xc.cuda(), k).cpu().numpy()
+        want = calib.calibrate(f32(xc), k)
+        if not np.array_equal(np.sort(got), want):
+            # only near-ties at the boundary may differ (fp64 summation order)
+            var = calib.channel_variance(onv.quantize(f32(xc))["resid_f32"])
+            diff = set(got.tolist()) ^ set(want.tolist())
+            kth = np.sort(var)[::-1][k - 1]
+            assert all(abs(var[j] - kth) <= 1e-9 * kth for j in diff)
