@@ -1,0 +1,384 @@
+"""Benchmark of the NVFP4 W4A4 linear layer with residual compensation.
+
+One step = the whole hot path on one batch of the prefill-shape dense
+workload (X [8192, 4096] bf16 with 41 Student-t outlier channels, W [4096,
+4096], k = 128 compensated channels):
+  1. online NVFP4 quantization of X with a dynamic tensor scale (amax
+     pre-pass + one-pass quantizer that also writes the bf16 residual slice),
+  2. the block-scaled W4A4 GEMM on tcgen05 with the compensation term fused
+     into the epilogue, bf16 output.
+Weight quantization, the compensation weight columns and the channel
+calibration are offline (done once, untimed), as in a rollout engine.
+
+Timing: CUDA events on the launching stream around each kernel of every
+step; 4 rotating (X, W) sets of 74 MB each (296 MB > the 129 MB L2) so every
+step reads its inputs from HBM.  `value` is the layer's throughput
+2*M*N*K / (quantize + GEMM time) in TFLOP/s; the GEMM kernel alone is
+reported in `roofline` against the FP4 tensor peak and the quantizer in
+`components` against HBM bandwidth.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+layer shards by rows with no exchange step), the step time is the max over
+ranks and `value` the sum of all ranks' work over that time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from nvfp4_w4a4_gemm_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD = "prefill"
+N_SETS = 4
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio on GB300
+FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+# ------------------------------------------------------------ helpers ----
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        def pick(*keys):
+            for k in keys:
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k])
+            return None
+        hbm = pick("hbm_gbs", "hbm_GBs", "copy_gbs")
+        bf = pick("bf16_tflops", "bf16_tflops_burst")
+        bfs = pick("bf16_tflops_sustained")
+        if hbm and bf:
+            return dict(hbm_gbs=hbm, bf16_tflops=bf, bf16_tflops_sustained=bfs or bf, source="measured")
+    return dict(FALLBACK, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.rows = []
+        self.proc = None
+        self.dev = device
+
+    def start(self):
+        sel = []
+        try:
+            bus = torch.cuda.get_device_properties(self.dev).pci_bus_id
+            sel = ["-i", f"{bus}"] if bus else []
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                     reasons=sorted(reasons), samples=len(sm))
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist, rank, ws
+    return None, 0, 1
+
+
+def max_over_ranks(dist, value, device):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------- our arm -----
+def prepare(nv, rank):
+    """Offline part: inputs, weight quantization, calibration, comp weights."""
+    s = W.SPECS[WORKLOAD]
+    dev = torch.device("cuda")
+    xc = W.activations(s.M, s.K, s.n_out, s.outlier, s.seed, s.seed + 1000).to(dev)
+    chan = nv.nvfp4_calibrate_channels(xc, s.k)
+    del xc
+    sets = []
+    for i in range(N_SETS):
+        x = W.activations(s.M, s.K, s.n_out, s.outlier, s.seed, s.seed + 17 * i + 101 * rank).to(dev)
+        wt = W.weights_t(s.N, s.K, s.seed + 500 + i + 101 * rank).to(dev)
+        qw = nv.nvfp4_quantize(wt)
+        w_sel = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan)
+        del wt
+        sets.append(dict(x=x, qw=qw, w_sel=w_sel))
+    M, K, N, k = s.M, s.K, s.N, s.k
+    out = dict(codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+               scales=torch.empty(nv.scale_bytes(M, K), dtype=torch.uint8, device=dev),
+               resid=torch.empty((M, k), dtype=torch.bfloat16, device=dev),
+               ws=torch.empty(nv.load().nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev))
+    g_x = torch.empty(1, dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    return s, chan, sets, out, g_x, y
+
+
+def step(nv, s, chan, st, out, g_x, y, ev=None):
+    if ev is not None:
+        ev[0].record()
+    qx = nv.nvfp4_quantize(st["x"], chan=chan, out=out, g_out=g_x)
+    if ev is not None:
+        ev[1].record()
+    nv.w4a4_gemm_comp(qx, st["qw"], s.N, resid=qx["resid"], w_sel=st["w_sel"], y=y)
+    if ev is not None:
+        ev[2].record()
+
+
+def run_ours(args):
+    from nvfp4_w4a4_gemm_gb300 import binding as nv
+    dist, rank, ws = dist_setup()
+    nv.load()
+    dev = torch.device("cuda")
+    s, chan, sets, out, g_x, y = prepare(nv, rank)
+    flops = 2.0 * s.M * s.N * s.K
+    for i in range(args.warmup):
+        step(nv, s, chan, sets[i % N_SETS], out, g_x, y)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(nv, s, chan, sets[i % N_SETS], out, g_x, y, evs[i])
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = clk.stop()
+    st, _ = nv.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+    t_q = [e[0].elapsed_time(e[1]) for e in evs]
+    t_g = [e[1].elapsed_time(e[2]) for e in evs]
+    ms_step = statistics.mean(a + b for a, b in zip(t_q, t_g))
+    ms_step = max_over_ranks(dist, ms_step, dev)
+    ms_gemm = max_over_ranks(dist, statistics.mean(t_g), dev)
+    ms_quant = max_over_ranks(dist, statistics.mean(t_q), dev)
+
+    # ---- e2e: host buffers through the same public calls ----
+    x_host = sets[0]["x"].cpu().pin_memory()
+    y_host = torch.empty((s.M, s.N), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(sets[0]["x"])
+    st_e2e = dict(sets[0])
+    st_e2e["x"] = x_dev
+    e2e_steps = max(3, args.steps // 2)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(nv, s, chan, st_e2e, out, g_x, y)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(nv, s, chan, st_e2e, out, g_x, y)
+        y_host.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
+    q_bytes = s.M * s.K * 2 + s.M * s.K // 2 + nv.scale_bytes(s.M, s.K) + s.M * s.k * 2
+    quant_gbs = q_bytes / (ms_quant * 1e-3) / 1e9
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get("w4a4_gemm_kernel", {}).get(WORKLOAD)
+    res = {
+        "metric": "W4A4+comp GEMM TFLOPS (% FP4 peak); NVFP4 quantize GB/s (% HBM)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4-e2m1 x e4m3 block scales, fp32 accumulate, bf16 compensation/output",
+        "data": "synthetic (seeded; N(0,1) activations with 1% Student-t(3)x20 outlier channels, N(0,0.02^2) weights)",
+        "config": {"workload": "prefill-shape dense linear: X[8192,4096] bf16, W[4096,4096] NVFP4, k=128 "
+                               "compensated channels; dynamic-scale NVFP4 quantize + W4A4 GEMM + fused compensation",
+                   "M": s.M, "N": s.N, "K": s.K, "k": s.k,
+                   "l2": f"inputs rotate over {N_SETS} (X, W) sets = "
+                         f"{N_SETS * (s.M * s.K * 2 + s.N * s.K // 2) / 1e6:.0f} MB > L2 129 MB",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"kernel": "w4a4_gemm_kernel", "bound": "tensor", "achieved": round(gemm_tflops, 1),
+                     "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{pk['source']}: bf16 {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4/BF16)",
+                     "algorithmic": "2*M*N*K per launch (compensation FLOPs excluded, its time included)"},
+        "components": {
+            "gemm_ms": round(ms_gemm, 4), "gemm_tflops": round(gemm_tflops, 1),
+            "quantize_ms": round(ms_quant, 4), "quantize_gbs": round(quant_gbs, 1),
+            "quantize_frac_hbm": round(quant_gbs / pk["hbm_gbs"], 4),
+            "quantize_bytes": q_bytes, "hbm_peak_gbs": pk["hbm_gbs"],
+            "quantize_note": "dynamic tensor scale: amax pre-pass + quantizer (both timed); bytes = X read once + "
+                             "codes + scales + residual",
+        },
+        "e2e": {"value": round(ws * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": s.M * s.K * 2, "d2h_bytes_per_step": s.M * s.N * 2,
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(s, sample_rows=args.cpu_rows or 4096, steps=2)
+    print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ the oracle arm ----
+def cpu_baseline(s, sample_rows=4096, steps=2):
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload:
+    the per-batch part (quantize `sample_rows` rows of X with the residual
+    slice + the fp64 reference GEMM with compensation against all N outputs);
+    weight quantization is offline on both arms and not timed."""
+    from oracle import calib, gemm as og, nvfp4 as onv
+    x = W.activations(sample_rows, s.K, s.n_out, s.outlier, s.seed, s.seed + 2000).float().numpy()
+    xc = W.activations(min(s.M, 2048), s.K, s.n_out, s.outlier, s.seed, s.seed + 1000).float().numpy()
+    chan = calib.calibrate(xc, s.k).astype(np.int64)
+    wt = W.weights_t(s.N, s.K, s.seed + 500).float().numpy()
+    qw = onv.quantize(wt)
+    b = onv.dequantize(qw["codes"], qw["sigma"], qw["g"])
+    w_sel = og.comp_weight_rows(qw, chan)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        qx = onv.quantize(x, chan=chan)
+        a = onv.dequantize(qx["codes"], qx["sigma"], qx["g"])
+        og.reference(a, b, qx["resid"], w_sel)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    flops = 2.0 * sample_rows * s.N * s.K
+    try:
+        threads = len(os.sched_getaffinity(0))
+    except AttributeError:
+        threads = os.cpu_count()
+    return {"value": round(flops / t / 1e12, 5), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{sample_rows} of {s.M} rows of the prefill workload: NVFP4 quantize with residual slice "
+                      f"+ fp64 reference GEMM with compensation vs all {s.N} outputs (numpy; BLAS threads = "
+                      f"host cores); weight quantization offline", "seconds": round(t, 3)}
+
+
+def run_reference(args):
+    dist, rank, ws = dist_setup()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    s = W.SPECS[WORKLOAD]
+    rows = args.cpu_rows or 2048
+    # the oracle keeps no state between steps, so warm-up steps are not run;
+    # every timed step is one bounded sample of the batch
+    cb = cpu_baseline(s, sample_rows=rows, steps=max(1, args.steps))
+    ms = s.M / rows * cb["seconds"] * 1e3   # full-batch step time, scaled from the sample
+    res = {
+        "impl": "reference",
+        "metric": "W4A4+comp GEMM TFLOPS (% FP4 peak); NVFP4 quantize GB/s (% HBM)",
+        "value": cb["value"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+        "config": {"workload": "prefill-shape dense linear: X[8192,4096] bf16, W[4096,4096] NVFP4, k=128 "
+                               "compensated channels", "sample_rows_per_step": rows},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="oracle sample rows (default 4096 for cpu_baseline, 2048 per reference step)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

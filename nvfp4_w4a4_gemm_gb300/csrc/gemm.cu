@@ -13,22 +13,25 @@
 // FourSight (arXiv 2611.04887) abstract -- the compensated channels stay in
 // BF16 alongside native NVFP4.
 //
-// Design (one persistent CTA per SM, 192 threads):
+// Design (one persistent CTA per SM, 224 threads):
 //   warp 0      TMA producer: A/B code tiles (128 x 128 B, 128-byte swizzle)
 //               and their block-scale tiles (2 KB bulk copies) into a ring of
 //               smem stages; after the FP4 k-tiles of an output tile it
 //               streams the compensation operands R_S / W_S through the same
 //               ring as 128 x 64 bf16 tiles.
-//   warp 1      allocates TMEM, copies the block scales smem -> TMEM
-//               (tcgen05.cp) and issues the MMAs from one thread; completion
-//               is signalled with tcgen05.commit on mbarriers.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulators, the scale-and-add,
+//   warp 1      allocates TMEM and issues the MMAs from one thread;
+//               completion is signalled with tcgen05.commit on mbarriers.
+//   warp 2      copies each stage's block scales smem -> TMEM (tcgen05.cp)
+//               into that stage's own TMEM slot.  Measured on GB300, a
+//               32x128b.warpx4 copy costs about as much as a 128x128x64 FP4
+//               MMA and copies from a second warp overlap the MMAs, while
+//               copies issued by the MMA thread serialize with them.
+//   warps 3..6  epilogue: tcgen05.ld of the accumulators, the scale-and-add,
 //               bf16 conversion and stores; warp w reads TMEM lanes
 //               32*(w%4) .. 32*(w%4)+31.
 // TMEM (512 columns): two 128-column FP4 accumulators (so the epilogue of
 // one tile overlaps the main loop of the next), one 128-column compensation
-// accumulator, and two 32-column scale-factor slots (A 16 + B 16) used by
-// alternate k-tiles.
+// accumulator, and one 32-column scale-factor slot (A 16 + B 16) per stage.
 // Every mbarrier wait is bounded; a wait that gives up latches an error for
 // nvfp4_check_status and the CTA winds down.
 #include <cuda.h>
@@ -48,17 +51,19 @@ namespace {
 constexpr int BM = 128;               // output rows per tile (MMA M)
 constexpr int BN = 128;               // output columns per tile (MMA N)
 constexpr int BKB = 128;              // bytes of K per k-tile row: 256 FP4 or 64 bf16
-constexpr int kStages = 5;
+constexpr int kStages = 4;             // = number of TMEM scale slots
 constexpr int kTileBytes = BM * BKB;  // 16 KB (A); B the same since BN == BM
 constexpr int kSfBytes = 2048;        // 4 scale chunks of 128 rows x 4 scales
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfBytes;  // 36 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColComp = 256, kColSf = 384;  // SF: 2 x (16 A + 16 B)
+constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColComp = 256, kColSf = 384;  // SF: kStages x (16 A + 16 B)
+static_assert(kColSf + 32 * kStages <= kTmemCols, "TMEM budget");
 
 enum WaitSite : uint32_t {
-  kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6
+  kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6,
+  kWaitSfFull = 7, kWaitSfDrain = 8
 };
 
 struct GemmParams {
@@ -157,7 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* comp_empty = acc_empty + 2;
   uint64_t* drain = comp_empty + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_full = drain + 1;
+  uint64_t* sf_drain = sf_full + kStages;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
@@ -197,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     }
     mbar_init(comp_empty, 4);
     mbar_init(drain, 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&sf_full[i], 1);
+    mbar_init(sf_drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -278,26 +287,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       uint32_t acc_phase = 0;
       uint32_t comp_phase = 0;
       bool ok = true;
-      uint32_t kt_global = 0;  // alternates the scale-factor TMEM slot
       for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
         for (int kt = 0; kt < n_kt && ok; ++kt) {
-          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+          if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stages + stage * kStageBytes);
           const uint32_t sb = sa + kTileBytes;
-          const uint32_t sfa = sb + kTileBytes;
-          const uint32_t sfb = sfa + kSfBytes;
-          const uint32_t col_sf = kColSf + (kt_global & 1u) * 32u;
+          const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
           const uint32_t t_sfa = tmem + col_sf, t_sfb = tmem + col_sf + 16u;
-          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
-          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
-          for (int c = 0; c < nch; ++c) {
-            tmem_cp_32x128b_x4(t_sfa + 4u * c, desc_sf(sfa + 512u * c));
-            tmem_cp_32x128b_x4(t_sfb + 4u * c, desc_sf(sfb + 512u * c));
-          }
           const int64_t krem = p.K - (int64_t)kt * 256;
           const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
           for (int j = 0; j < n_mma; ++j) {
@@ -312,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
             }
           }
           tc_commit(&empty[stage]);
-          ++kt_global;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (n_ct > 0 && ok) {
@@ -320,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           comp_phase ^= 1u;
           tc_fence_after();
           for (int ct = 0; ct < n_ct && ok; ++ct) {
-            if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+            if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(stages + stage * kStageBytes);
             const uint32_t sb = sa + kTileBytes;
@@ -342,6 +341,36 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       // all MMAs issued by this thread complete before TMEM is released
       tc_commit(drain);
       mbar_wait(drain, 0, kWaitDrain, nullptr);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- scale copies ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
+          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+          if (kt < n_kt) {
+            tc_fence_after();
+            const uint32_t sfa = smem_u32(stages + stage * kStageBytes) + 2u * kTileBytes;
+            const uint32_t sfb = sfa + kSfBytes;
+            const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
+            const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+            const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+            for (int c = 0; c < nch; ++c) {
+              tmem_cp_32x128b_x4(tmem + col_sf + 4u * c, desc_sf(sfa + 512u * c));
+              tmem_cp_32x128b_x4(tmem + col_sf + 16u + 4u * c, desc_sf(sfb + 512u * c));
+            }
+            tc_commit(&sf_full[stage]);
+          } else {
+            mbar_arrive(&sf_full[stage]);  // compensation k-tile: nothing to copy
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, kWaitSfDrain, nullptr);
     }
   } else {
     // ------------------------------------------------------ epilogue ----

@@ -33,7 +33,8 @@ namespace nv4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;            // row segments in flight per warp
+constexpr int kUnroll = 4;            // row segments in flight per warp (MXFP4)
+constexpr int64_t kMaxMapK = 65536;   // dense channel map in shared memory up to this K
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -86,17 +87,33 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* s, int n, int32_t 
 }
 
 // ------------------------------------------------------------- amax -------
+// Work unit = one row x 1024 columns (4 x 16 bytes per lane); one 32-bit
+// division per unit; the next unit's loads are issued before the current
+// one is reduced.
 __global__ void __launch_bounds__(kThreads) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, float* __restrict__ partials) {
-  const int64_t vec_per_row = K / 8;
-  const int64_t total = M * vec_per_row;
+  const int lane = threadIdx.x & 31;
+  const uint32_t gpr = (uint32_t)((K + 1023) / 1024);
+  const uint32_t n_units = (uint32_t)(M * gpr);
+  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
   float m = 0.f;
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = v / vec_per_row, c = (v - r * vec_per_row) * 8;
-    float f[8];
-    unpack8(ldg_stream(x + r * ldx + c), f);
+  for (uint32_t u = warp_global; u < n_units; u += n_warps) {
+    const uint32_t r = u / gpr, g = u - r * gpr;
+    const __nv_bfloat16* row = x + (int64_t)r * ldx;
+    uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int i = 0; i < 4; ++i) {
+      const int64_t c = (int64_t)g * 1024 + i * 256 + lane * 8;
+      v[i] = c < K ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float f[8];
+      unpack8(v[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    }
   }
   __shared__ float red[kThreads / 32];
 #pragma unroll
@@ -131,17 +148,107 @@ struct QuantArgs {
   __nv_bfloat16* resid;     // [M, k]
   const int32_t* offsets;   // grouped: [E+1] device, else nullptr
   int E;
+  int use_map;              // dense: channel -> slot map in shared memory
 };
+
+// Quantize one 8-element piece (half a 16-block; the partner lane holds the
+// other half) and emit codes, scales and residuals.
+template <bool kGrouped>
+__device__ __forceinline__ void quant_piece(const QuantArgs& a, const uint4& raw, int64_t r, int64_t c, int lane,
+                                            float g, int64_t n_cg, const int16_t* s_map, const int32_t* s_chan,
+                                            const int32_t* s_off, const int32_t* s_pbase) {
+  const bool valid = c < a.K;
+  float f[8];
+  unpack8(raw, f);
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
+  const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
+  const uint32_t sig = cvt_e4m3(t);
+  const float d = __fmul_rn(e4m3_to_f32(sig), g);
+  uint32_t packed = 0;
+  if (d != 0.f) {
+    const float rcp = __fdiv_rn(1.0f, d);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      packed |= cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp)) << (8 * i);
+  }
+  int64_t srow = r;
+  int e = 0;
+  if (kGrouped) {
+    int lo = 0, hi = a.E;  // expert of row r: last e with offsets[e] <= r
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= r) lo = mid; else hi = mid;
+    }
+    e = lo;
+    srow = (int64_t)s_pbase[e] + (r - s_off[e]);
+  }
+  if (valid) *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
+  // gather the 4 block scales of a 64-element group into lane % 8 == 0
+  const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 2);
+  const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 4);
+  const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 6);
+  if ((lane & 7) == 0 && valid) {
+    const int64_t blk = c / 16;  // multiple of 4
+    const int64_t nb = a.K / 16;
+    uint32_t word = sig;
+    if (blk + 1 < nb) word |= s1 << 8;
+    if (blk + 2 < nb) word |= s2 << 16;
+    if (blk + 3 < nb) word |= s3 << 24;
+    *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
+  }
+  if (!valid || a.k == 0) return;
+  // compensation residual x - E2M1(code) * d on the channels of S in [c, c+8)
+  auto resid_at = [&](int j, int slot) {
+    float dq = 0.f;
+    if (d != 0.f) {
+      const uint32_t h2 = cvt_e2m1x2_to_f16x2((packed >> (8 * (j >> 1))) & 0xFFu);
+      const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
+      dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
+    }
+    float xf = f[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) if (j == q) xf = f[q];
+    a.resid[r * a.k + slot] = __float2bfloat16_rn(__fsub_rn(xf, dq));
+  };
+  if (!kGrouped && a.use_map) {
+    const uint4 mw = *reinterpret_cast<const uint4*>(s_map + c);
+    const uint32_t w[4] = {mw.x, mw.y, mw.z, mw.w};
+    if (((w[0] & w[1] & w[2] & w[3]) & 0x80008000u) == 0x80008000u) return;  // no channel of S here
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int slot = (int)(int16_t)((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      if (slot >= 0) resid_at(j, slot);
+    }
+  } else {
+    const int32_t* S = s_chan + e * a.k;
+    int i = lower_bound_i32(S, a.k, (int32_t)c);
+    for (; i < a.k && S[i] < c + 8; ++i) resid_at(S[i] - (int)c, i);
+  }
+}
 
 template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
-  extern __shared__ int32_t smem_i32[];
-  // smem: chan [E*k] | offsets [E+1] | padded bases [E]
+  extern __shared__ __align__(16) int32_t smem_i32[];
+  // dense + map: int16 slot map [K] | grouped: chan [E*k] | offsets [E+1] | padded bases [E]
+  int16_t* s_map = reinterpret_cast<int16_t*>(smem_i32);
   int32_t* s_chan = smem_i32;
   int32_t* s_off = s_chan + a.E * a.k;
   int32_t* s_pbase = s_off + (a.E + 1);
-  const int nchan = a.E * a.k;
-  for (int i = threadIdx.x; i < nchan; i += blockDim.x) s_chan[i] = a.chan[i];
+  if (!kGrouped && a.use_map) {
+    for (int64_t i = threadIdx.x; i < a.K; i += blockDim.x) s_map[i] = -1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.k; i += blockDim.x) {
+      const int32_t j = a.chan[i];
+      if (j >= 0 && j < a.K) s_map[j] = (int16_t)i;
+    }
+  } else {
+    const int nchan = a.E * a.k;
+    for (int i = threadIdx.x; i < nchan; i += blockDim.x) s_chan[i] = a.chan[i];
+  }
   if (kGrouped) {
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
     __syncthreads();
@@ -163,99 +270,38 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.g_out != nullptr) *a.g_out = g;
 
   const int lane = threadIdx.x & 31;
-  const int64_t seg_per_row = (a.K + 255) / 256;
-  const int64_t n_seg = a.M * seg_per_row;
-  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t gpr = (uint32_t)((a.K + 1023) / 1024);   // 1024-column groups per row
+  const uint32_t n_units = (uint32_t)(a.M * gpr);
+  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
   const int64_t n_cg = (a.K / 16 + 3) / 4;
 
-  for (int64_t s0 = warp_global * kUnroll; s0 < n_seg; s0 += n_warps * kUnroll) {
-    uint4 v[kUnroll];
+  uint32_t u = warp_global;
+  uint4 cur[4];
+  auto load_unit = [&](uint32_t uu, uint4 (&v)[4]) {
+    const uint32_t r = uu / gpr, gi = uu - r * gpr;
+    const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t s = s0 + u;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (s < n_seg) {
-        const int64_t r = s / seg_per_row;
-        const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
-        if (c < a.K) v[u] = ldg_stream(a.x + r * a.ldx + c);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int64_t c = (int64_t)gi * 1024 + i * 256 + lane * 8;
+      v[i] = c < a.K ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (u < n_units) load_unit(u, cur);
+  while (u < n_units) {
+    const uint32_t nu = u + n_warps;
+    uint4 nxt[4];
+    if (nu < n_units) load_unit(nu, nxt);
+    const uint32_t r = u / gpr, gi = u - r * gpr;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t c = (int64_t)gi * 1024 + i * 256 + lane * 8;
+      if ((int64_t)gi * 1024 + i * 256 >= a.K) break;  // warp-uniform
+      quant_piece<kGrouped>(a, cur[i], r, c, lane, g, n_cg, s_map, s_chan, s_off, s_pbase);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t s = s0 + u;
-      if (s >= n_seg) break;  // warp-uniform
-      const int64_t r = s / seg_per_row;
-      const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
-      const bool valid = c < a.K;
-      float f[8];
-      unpack8(v[u], f);
-      float am = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
-      const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
-      const uint32_t sig = cvt_e4m3(t);
-      const float d = __fmul_rn(e4m3_to_f32(sig), g);
-      uint32_t packed = 0;
-      float deq[8];
-      if (d != 0.f) {
-        const float rcp = __fdiv_rn(1.0f, d);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t b = cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp));
-          packed |= b << (8 * i);
-          const uint32_t h2 = cvt_e2m1x2_to_f16x2(b);
-          deq[2 * i] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
-          deq[2 * i + 1] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), d);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) deq[i] = 0.f;
-      }
-      // row of the scale tile layout (grouped: each expert starts a tile)
-      int64_t srow = r;
-      int e = 0;
-      if (kGrouped) {
-        // expert of row r: last e with offsets[e] <= r
-        int lo = 0, hi = a.E;  // find e in [0, E)
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (s_off[mid] <= r) lo = mid; else hi = mid;
-        }
-        e = lo;
-        srow = (int64_t)s_pbase[e] + (r - s_off[e]);
-      }
-      if (valid) {
-        *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
-      }
-      // gather the 4 block scales of a 64-element group into lane%8 == 0
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 2);
-      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 4);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 6);
-      if ((lane & 7) == 0 && valid) {
-        const int64_t blk = c / 16;  // multiple of 4
-        const int64_t nb = a.K / 16;
-        uint32_t word = sig;
-        if (blk + 1 < nb) word |= s1 << 8;
-        if (blk + 2 < nb) word |= s2 << 16;
-        if (blk + 3 < nb) word |= s3 << 24;
-        *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
-      }
-      // compensation residual on the channels of S that fall in [c, c+8)
-      if (valid && a.k > 0) {
-        const int32_t* S = s_chan + e * a.k;
-        int i = lower_bound_i32(S, a.k, (int32_t)c);
-        for (; i < a.k && S[i] < c + 8; ++i) {
-          const int j = S[i] - (int)c;
-          float xf = f[0], dq = deq[0];
-#pragma unroll
-          for (int q = 1; q < 8; ++q) if (j == q) { xf = f[q]; dq = deq[q]; }
-          a.resid[r * a.k + i] = __float2bfloat16_rn(__fsub_rn(xf, dq));
-        }
-      }
-    }
+    for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    u = nu;
   }
 }
 
@@ -586,19 +632,21 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
+  a.use_map = (offsets == nullptr && k > 0 && K <= kMaxMapK) ? 1 : 0;
   if (g_in == nullptr) {
     const int p = amax_partials_count(M, K, num_sms);
     amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
     a.partials = partials;
     a.n_partials = p;
   }
-  const int64_t n_seg = M * ((K + 255) / 256);
-  const int64_t warps_needed = (n_seg + kUnroll - 1) / kUnroll;
-  int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
+  const int64_t n_units = M * ((K + 1023) / 1024);
+  int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
   const int64_t cap = (int64_t)num_sms * 4;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const size_t smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
+  size_t smem;
+  if (a.use_map) smem = sizeof(int16_t) * (size_t)((K + 7) / 8 * 8);
+  else smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
   if (offsets != nullptr) {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(nvfp4_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
