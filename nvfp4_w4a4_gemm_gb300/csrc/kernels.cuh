@@ -6,7 +6,7 @@
 
 namespace nv4 {
 
-constexpr int kMaxAmaxPartials = 1024;
+constexpr int kMaxAmaxPartials = 2048;
 
 int amax_partials_count(int64_t M, int64_t K, int num_sms);
 

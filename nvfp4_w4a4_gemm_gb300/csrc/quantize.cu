@@ -151,47 +151,50 @@ struct QuantArgs {
   int use_map;              // dense: channel -> slot map in shared memory
 };
 
-// Quantize one 8-element piece (half a 16-block; the partner lane holds the
-// other half) and emit codes, scales and residuals.
+// Quantize one 16-element block owned by this thread (x[c .. c+16) of row r)
+// and emit its 8 code bytes, its scale byte (4 lanes' scales are gathered
+// into one 32-bit tile-layout store) and its residuals.
 template <bool kGrouped>
-__device__ __forceinline__ void quant_piece(const QuantArgs& a, const uint4& raw, int64_t r, int64_t c, int lane,
-                                            float g, int64_t n_cg, const int16_t* s_map, const int32_t* s_chan,
-                                            const int32_t* s_off, const int32_t* s_pbase) {
+__device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw0, const uint4& raw1, int64_t r,
+                                            int64_t c, int lane, float g, int64_t n_cg, const int16_t* s_map,
+                                            const int32_t* s_chan, const int32_t* s_off, const int32_t* s_pbase) {
   const bool valid = c < a.K;
-  float f[8];
-  unpack8(raw, f);
+  float f[16];
+  unpack8(raw0, *reinterpret_cast<float(*)[8]>(f));
+  unpack8(raw1, *reinterpret_cast<float(*)[8]>(f + 8));
   float am = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
   // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
   const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
   const uint32_t sig = cvt_e4m3(t);
   const float d = __fmul_rn(e4m3_to_f32(sig), g);
-  uint32_t packed = 0;
+  uint32_t lo = 0, hi = 0;
   if (d != 0.f) {
     const float rcp = __fdiv_rn(1.0f, d);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      packed |= cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp)) << (8 * i);
+    for (int i = 0; i < 4; ++i) {
+      lo |= cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp)) << (8 * i);
+      hi |= cvt_e2m1x2(__fmul_rn(f[8 + 2 * i], rcp), __fmul_rn(f[8 + 2 * i + 1], rcp)) << (8 * i);
+    }
   }
   int64_t srow = r;
   int e = 0;
   if (kGrouped) {
-    int lo = 0, hi = a.E;  // expert of row r: last e with offsets[e] <= r
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_off[mid] <= r) lo = mid; else hi = mid;
+    int l = 0, h = a.E;  // expert of row r: last e with offsets[e] <= r
+    while (h - l > 1) {
+      const int mid = (l + h) >> 1;
+      if (s_off[mid] <= r) l = mid; else h = mid;
     }
-    e = lo;
+    e = l;
     srow = (int64_t)s_pbase[e] + (r - s_off[e]);
   }
-  if (valid) *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
-  // gather the 4 block scales of a 64-element group into lane % 8 == 0
-  const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 2);
-  const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 4);
-  const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 6);
-  if ((lane & 7) == 0 && valid) {
+  if (valid) *reinterpret_cast<uint2*>(a.codes + r * (a.K / 2) + c / 2) = make_uint2(lo, hi);
+  // gather the 4 block scales of a 64-element group into lane % 4 == 0
+  const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 1);
+  const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 2);
+  const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 3);
+  if ((lane & 3) == 0 && valid) {
     const int64_t blk = c / 16;  // multiple of 4
     const int64_t nb = a.K / 16;
     uint32_t word = sig;
@@ -201,39 +204,44 @@ __device__ __forceinline__ void quant_piece(const QuantArgs& a, const uint4& raw
     *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
   }
   if (!valid || a.k == 0) return;
-  // compensation residual x - E2M1(code) * d on the channels of S in [c, c+8)
+  // compensation residual x - E2M1(code) * d on the channels of S in [c, c+16)
   auto resid_at = [&](int j, int slot) {
     float dq = 0.f;
     if (d != 0.f) {
-      const uint32_t h2 = cvt_e2m1x2_to_f16x2((packed >> (8 * (j >> 1))) & 0xFFu);
+      const uint32_t word = j < 8 ? lo : hi;
+      const uint32_t h2 = cvt_e2m1x2_to_f16x2((word >> (8 * ((j & 7) >> 1))) & 0xFFu);
       const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
       dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
     }
     float xf = f[0];
 #pragma unroll
-    for (int q = 1; q < 8; ++q) if (j == q) xf = f[q];
+    for (int q = 1; q < 16; ++q) if (j == q) xf = f[q];
     a.resid[r * a.k + slot] = __float2bfloat16_rn(__fsub_rn(xf, dq));
   };
   if (!kGrouped && a.use_map) {
-    const uint4 mw = *reinterpret_cast<const uint4*>(s_map + c);
-    const uint32_t w[4] = {mw.x, mw.y, mw.z, mw.w};
-    if (((w[0] & w[1] & w[2] & w[3]) & 0x80008000u) == 0x80008000u) return;  // no channel of S here
+    const uint4 m0 = *reinterpret_cast<const uint4*>(s_map + c);
+    const uint4 m1 = *reinterpret_cast<const uint4*>(s_map + c + 8);
+    const uint32_t w[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    uint32_t all = 0xFFFFFFFFu;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int i = 0; i < 8; ++i) all &= w[i];
+    if ((all & 0x80008000u) == 0x80008000u) return;  // no channel of S in this block
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
       const int slot = (int)(int16_t)((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
       if (slot >= 0) resid_at(j, slot);
     }
   } else {
     const int32_t* S = s_chan + e * a.k;
     int i = lower_bound_i32(S, a.k, (int32_t)c);
-    for (; i < a.k && S[i] < c + 8; ++i) resid_at(S[i] - (int)c, i);
+    for (; i < a.k && S[i] < c + 16; ++i) resid_at(S[i] - (int)c, i);
   }
 }
 
 template <bool kGrouped>
-__global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
   extern __shared__ __align__(16) int32_t smem_i32[];
-  // dense + map: int16 slot map [K] | grouped: chan [E*k] | offsets [E+1] | padded bases [E]
+  // dense + map: int16 slot map [K] | otherwise: chan [E*k] | offsets [E+1] | padded bases [E]
   int16_t* s_map = reinterpret_cast<int16_t*>(smem_i32);
   int32_t* s_chan = smem_i32;
   int32_t* s_off = s_chan + a.E * a.k;
@@ -269,24 +277,27 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
   }
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.g_out != nullptr) *a.g_out = g;
 
+  // work unit = one row x 1024 columns: each lane owns 2 blocks of 16
   const int lane = threadIdx.x & 31;
-  const uint32_t gpr = (uint32_t)((a.K + 1023) / 1024);   // 1024-column groups per row
+  const uint32_t gpr = (uint32_t)((a.K + 1023) / 1024);
   const uint32_t n_units = (uint32_t)(a.M * gpr);
   const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
   const int64_t n_cg = (a.K / 16 + 3) / 4;
 
-  uint32_t u = warp_global;
-  uint4 cur[4];
   auto load_unit = [&](uint32_t uu, uint4 (&v)[4]) {
     const uint32_t r = uu / gpr, gi = uu - r * gpr;
     const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t c = (int64_t)gi * 1024 + i * 256 + lane * 8;
-      v[i] = c < a.K ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
+    for (int h = 0; h < 2; ++h) {
+      const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
+      const bool ok = c < a.K;
+      v[2 * h] = ok ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
+      v[2 * h + 1] = ok ? ldg_stream(row + c + 8) : make_uint4(0, 0, 0, 0);
     }
   };
+  uint32_t u = warp_global;
+  uint4 cur[4];
   if (u < n_units) load_unit(u, cur);
   while (u < n_units) {
     const uint32_t nu = u + n_warps;
@@ -294,10 +305,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(QuantArgs a) {
     if (nu < n_units) load_unit(nu, nxt);
     const uint32_t r = u / gpr, gi = u - r * gpr;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t c = (int64_t)gi * 1024 + i * 256 + lane * 8;
-      if ((int64_t)gi * 1024 + i * 256 >= a.K) break;  // warp-uniform
-      quant_piece<kGrouped>(a, cur[i], r, c, lane, g, n_cg, s_map, s_chan, s_off, s_pbase);
+    for (int h = 0; h < 2; ++h) {
+      if ((int64_t)gi * 1024 + h * 512 >= a.K) break;  // warp-uniform
+      const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
+      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, s_map, s_chan, s_off, s_pbase);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
@@ -617,7 +628,7 @@ cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, in
 int amax_partials_count(int64_t M, int64_t K, int num_sms) {
   int64_t vecs = M * (K / 8);
   int64_t want = (vecs + kThreads - 1) / kThreads;
-  int64_t cap = (int64_t)num_sms * 4;
+  int64_t cap = (int64_t)num_sms * 8;
   if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
   if (want < 1) want = 1;
   return (int)(want < cap ? want : cap);
@@ -641,7 +652,12 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   }
   const int64_t n_units = M * ((K + 1023) / 1024);
   int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
-  const int64_t cap = (int64_t)num_sms * 4;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, offsets ? (const void*)nvfp4_quant_kernel<true>
+                                                                     : (const void*)nvfp4_quant_kernel<false>,
+                                                    kThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   size_t smem;
