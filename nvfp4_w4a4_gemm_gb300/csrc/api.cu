@@ -64,6 +64,8 @@ int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8
                      const int32_t* chan, int32_t k, uint16_t* resid, int block) {
   if (M < 0 || K <= 0 || K % block != 0 || ldx < K || ldx % 8 != 0) return NVFP4_ERR_INVALID_ARG;
   if (K > (int64_t)1 << 30 || M > (int64_t)1 << 40) return NVFP4_ERR_UNSUPPORTED;
+  // the quantizers index (row, 1024-column group) work units with 32 bits
+  if (M * ((K + 1023) / 1024) >= ((int64_t)1 << 32)) return NVFP4_ERR_UNSUPPORTED;
   if (M == 0) return NVFP4_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) || !aligned(scales, 16))
     return NVFP4_ERR_INVALID_ARG;
