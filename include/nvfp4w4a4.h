@@ -131,6 +131,31 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
                            size_t ws_bytes, void* stream);
 
 /*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize with the dynamic tensor scale,
+ * for callers that cannot allocate device memory: code running where
+ * cudaMalloc is off limits (an engine that owns all device memory through
+ * its own allocator, a hot path that must never allocate) has no way to
+ * provide nvfp4_quantize's workspace.  This entry point needs none: the amax
+ * pre-pass keeps its per-block partial maxima in a scratch array owned by
+ * the library, a file-scope device array of 2048 floats (8 KB) that every
+ * GPU which loads the library holds until the process exits.  It allocates
+ * nothing and calls no allocating routine.
+ * The paper has no counterpart of this entry point; it exists only for such
+ * callers.  Arguments and results are those of nvfp4_quantize with
+ * g_in == NULL (g_out may be NULL).
+ * - The first call on a device resolves the scratch array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ * - Every call shares the one array: calls that overlap on the GPU (issued
+ *   on different streams without ordering) race and may give wrong scales.
+ *   Nothing in the array needs clearing between calls.
+ * - Returns NVFP4_ERR_UNSUPPORTED if the pre-pass would need more than the
+ *   array's 2048 partials (it uses min(8 x SM count, 2048), so any shape the
+ *   quantizer accepts fits).
+ */
+int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* g_out, uint8_t* codes,
+                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* stream);
+
+/*
  * mxfp4_quantize -- MXFP4 quantization (32-element blocks, power-of-two
  * E8M0 scale 2^e with e = floor(log2 max|x|) - 2 clamped to [-127, 127],
  * codes E2M1_rn_satfinite(x * 2^-e)), optionally with the per-block

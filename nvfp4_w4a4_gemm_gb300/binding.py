@@ -38,6 +38,7 @@ _SIGS = {
     "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_quantize_grouped": ([_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
                                ctypes.c_int),
+    "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
     "nvfp4_prepare_comp_weights": ([_I32, _I64, _I64, _P, _P, _P, _P, _I32, ctypes.c_int, _P, _P], ctypes.c_int),
     "nvfp4_calibrate_workspace_bytes": ([_I64, _I32], _SZ),
@@ -139,6 +140,30 @@ def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None):
                             _ptr(chan) if k else None, k, _ptr(resid) if k else None, _ptr(ws),
                             0 if ws is None else ws.numel(), _stream())
     _check("nvfp4_quantize", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+
+
+def nvfp4_quantize_noalloc(x, chan=None, out=None, g_out=None):
+    """nvfp4_quantize with a dynamic tensor scale and no workspace: for
+    callers that cannot allocate device memory (the library keeps the
+    scratch).  Outputs are allocated here unless given in ``out``."""
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    dev = x.device
+    k = 0 if chan is None else int(chan.numel())
+    if chan is not None:
+        _need(chan, torch.int32, "chan")
+    o = out or {}
+    codes = o.get("codes") if o.get("codes") is not None else torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    scales = o.get("scales") if o.get("scales") is not None else torch.empty(
+        lib.nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    resid = o.get("resid") if o.get("resid") is not None else torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    if g_out is None:
+        g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    st = lib.nvfp4_quantize_noalloc(_ptr(x), M, K, x.stride(0), _ptr(g_out), _ptr(codes), _ptr(scales),
+                                    _ptr(chan) if k else None, k, _ptr(resid) if k else None, _stream())
+    _check("nvfp4_quantize_noalloc", st)
     return dict(codes=codes, scales=scales, g=g_out, resid=resid)
 
 

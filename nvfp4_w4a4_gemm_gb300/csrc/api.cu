@@ -149,6 +149,18 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
                                               as_stream(stream)));
 }
 
+int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* g_out, uint8_t* codes,
+                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* stream) {
+  int st = check_quant_args(x, M, K, ldx, codes, scales, chan, k, resid, 16);
+  if (st != NVFP4_OK) return st;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if (nv4::amax_partials_count(M, K, d->num_sms) > nv4::noalloc_partials_capacity()) return NVFP4_ERR_UNSUPPORTED;
+  const cudaError_t e = nv4::launch_nvfp4_quantize_noalloc(bf(x), M, K, ldx, g_out, codes, scales, chan, k, bf(resid),
+                                                           d->num_sms, as_stream(stream));
+  return e == cudaErrorInvalidValue ? NVFP4_ERR_UNSUPPORTED : from_cuda(e);
+}
+
 int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* scales,
                    float* stats, uint8_t* deadzone, void* stream) {
   int st = check_quant_args(x, M, K, ldx, codes, scales, nullptr, 0, nullptr, 32);

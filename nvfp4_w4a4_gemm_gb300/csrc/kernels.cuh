@@ -35,6 +35,13 @@ cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, in
 
 cudaError_t quant_status(uint32_t* out2, bool clear);
 
+// Dynamic-scale NVFP4 quantize with its amax scratch in a library-owned
+// device array (no caller workspace, no allocation).
+int noalloc_partials_capacity();
+cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* g_out,
+                                          uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
+                                          __nv_bfloat16* resid, int num_sms, cudaStream_t stream);
+
 // ----------------------------------------------------------------- GEMM ----
 struct GemmProblem {
   int fmt = 0;  // 0 NVFP4, 1 MXFP4

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <mutex>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -720,6 +721,55 @@ cudaError_t launch_select_channels(const double* sum, const double* sumsq, const
     cudaFuncSetAttribute(select_channels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   select_channels_kernel<<<E, 1024, smem, stream>>>(sum, sumsq, offsets, M_all, sum_all, sumsq_all, K, k, chan_out);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------- allocation-free path ----
+// Scratch of the dynamic-scale quantizer for callers that cannot allocate
+// device memory (an engine whose allocator is closed to kernels' helpers, or
+// code that must not call cudaMalloc on its hot path).  The amax pre-pass
+// writes one partial maximum per CTA here instead of into a caller
+// workspace.  Every CTA writes its own slot before the quantizer reads it, so
+// nothing needs clearing between calls; calls that overlap on the GPU (on
+// different streams) share this array and race.  Each GPU that loads the
+// library keeps these 8 KB until the process exits.
+static __device__ __align__(256) float g_noalloc_partials[kMaxAmaxPartials];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device.  The first call
+// on a device resolves it with cudaGetSymbolAddress (host code cannot use the
+// array's name as a device address).
+static cudaError_t noalloc_partials(float** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_noalloc_partials);
+    if (err != cudaSuccess) return err;
+    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+int noalloc_partials_capacity() { return kMaxAmaxPartials; }
+
+cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* g_out,
+                                          uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
+                                          __nv_bfloat16* resid, int num_sms, cudaStream_t stream) {
+  if (amax_partials_count(M, K, num_sms) > kMaxAmaxPartials) return cudaErrorInvalidValue;
+  float* partials = nullptr;
+  const cudaError_t err = noalloc_partials(&partials);
+  if (err != cudaSuccess) return err;
+  return launch_nvfp4_quantize(x, M, K, ldx, nullptr, g_out, codes, scales, chan, k, resid, nullptr, 1, partials,
+                               num_sms, stream);
 }
 
 }  // namespace nv4
