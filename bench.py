@@ -125,6 +125,29 @@ class ClockSampler:
                      reasons=sorted(reasons), samples=len(sm))
 
 
+def git_blob_hash(path):
+    """git's blob id of a file (sha1 of 'blob <size>\\0' + content), computed
+    without git so it works where the repository has no .git."""
+    import hashlib
+    with open(path, "rb") as f:
+        data = f.read()
+    return hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
+
+
+def gemm_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu capture, or None when
+    the kernel source changed since the counters were taken."""
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tr_path):
+        return None
+    with open(tr_path) as f:
+        rec = json.load(f).get("w4a4_gemm_kernel", {}).get(WORKLOAD)
+    src = os.path.join(ROOT, "nvfp4_w4a4_gemm_gb300", "csrc", "gemm.cu")
+    if not rec or git_blob_hash(src) != rec.get("gemm_cu_blob"):
+        return None
+    return rec["bytes"]
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
@@ -253,11 +276,7 @@ def run_ours(args):
     q_bytes = s.M * s.K * 2 + s.M * s.K // 2 + nv.scale_bytes(s.M, s.K) + s.M * s.k * 2
     quant_gbs = q_bytes / (ms_quant * 1e-3) / 1e9
     value = ws * flops / (ms_step * 1e-3) / 1e12
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            traffic = json.load(f).get("w4a4_gemm_kernel", {}).get(WORKLOAD)
+    traffic = gemm_traffic()
     res = {
         "metric": "W4A4+comp GEMM TFLOPS (% FP4 peak); NVFP4 quantize GB/s (% HBM)",
         "value": round(value, 2),
