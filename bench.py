@@ -307,7 +307,8 @@ def run_ours(args):
             "quantize_frac_hbm": round(quant_gbs / pk["hbm_gbs"], 4),
             "quantize_bytes": q_bytes, "hbm_peak_gbs": pk["hbm_gbs"],
             "quantize_note": "dynamic tensor scale: amax pre-pass + quantizer (both timed); bytes = X read once + "
-                             "codes + scales + residual",
+                             "codes + scales + residual; inside the step the quantizer also absorbs the write-back of "
+                             "the previous GEMM's 64 MB bf16 output from L2",
         },
         "e2e": {"value": round(ws * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": s.M * s.K * 2, "d2h_bytes_per_step": s.M * s.N * 2,
@@ -316,11 +317,126 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
     }
+    if not args.no_workloads:
+        res["workloads"] = other_workloads(nv, pk)
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(s, sample_rows=args.cpu_rows or 4096, steps=2)
     print(json.dumps(res))
     if dist is not None:
         dist.destroy_process_group()
+
+
+# ------------------------------------------- the other four workloads ----
+def _time_steps(fn, steps, flush):
+    """Mean device time (ms) of `fn` over `steps` runs; the L2 is flushed by
+    writing a buffer larger than it between runs (outside the timed window)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        e0.record()
+        fn()
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+
+def other_workloads(nv, pk, steps=10):
+    """Decode, MoE and MXFP4 workloads: one step each = the kernels of that
+    path on one batch (dynamic-scale quantize + GEMM)."""
+    dev = torch.device("cuda")
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+
+    # decode: X[16,4096] x W[4096,14336], k=64 (HBM-bound on the weights)
+    s = W.SPECS["decode"]
+    d = W.dense_inputs("decode")
+    x, wt = d["x"].to(dev), d["wt"].to(dev)
+    chan = nv.nvfp4_calibrate_channels(W.dense_inputs("decode", True, False)["x"].to(dev), s.k)
+    qw = nv.nvfp4_quantize(wt)
+    ws = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan)
+    del wt
+    y = torch.empty((s.M, s.N), dtype=torch.bfloat16, device=dev)
+
+    def dec():
+        qx = nv.nvfp4_quantize(x, chan=chan)
+        nv.w4a4_gemm_comp(qx, qw, s.N, resid=qx["resid"], w_sel=ws, y=y)
+    ms = _time_steps(dec, steps, flush)
+    byts = qw["codes"].numel() + qw["scales"].numel() + ws.numel() * 2 + x.numel() * 2 + y.numel() * 2
+    out["decode"] = {"shape": "X[16,4096] x W[4096,14336], k=64", "ms_per_step": round(ms, 4),
+                     "tflops": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12, 2),
+                     "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                     "bytes_per_step": byts, "bound": "hbm",
+                     "note": "dynamic-scale quantize of X + GEMM (generic 128x128-tile path, no split-K yet)"}
+    del qw, ws, x, y
+
+    # MoE: 4096 tokens top-8 of 128 experts; gate/up [2048->1536] and down [768->2048], k=32 per expert
+    s = W.SPECS["moe"]
+    dm = W.moe_inputs()
+    offs = dm["offsets"].to(dev)
+    E = s.experts
+    res = {}
+    tot_ms, tot_flops, tot_bytes = 0.0, 0.0, 0
+    for which, xk, wk in (("gate_up", "x_gate_up", "wt_gate_up"), ("down", "x_down", "wt_down")):
+        xg = dm[xk].to(dev)
+        K = xg.shape[1]
+        gen = torch.Generator().manual_seed(7)
+        chan = torch.stack([torch.sort(torch.randperm(K, generator=gen)[: s.k]).values for _ in range(E)])
+        chan = chan.to(torch.int32).to(dev)
+        codes, scales, gs = [], [], []
+        for e in range(E):
+            q = nv.nvfp4_quantize(dm[wk][e].to(dev))
+            codes.append(q["codes"]); scales.append(q["scales"]); gs.append(q["g"])
+        b_codes, b_scales, g_b = torch.stack(codes), torch.cat(scales), torch.cat(gs)
+        del codes, scales
+        N = b_codes.shape[1]
+        w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan, E=E)
+        yg = torch.empty((xg.shape[0], N), dtype=torch.bfloat16, device=dev)
+
+        def moe():
+            qx = nv.nvfp4_quantize_grouped(xg, offs, chan)
+            nv.w4a4_grouped_gemm_comp(qx, offs, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel, y=yg)
+        ms = _time_steps(moe, steps, flush)
+        flops = 2.0 * xg.shape[0] * N * K
+        byts = (b_codes.numel() + b_scales.numel() + w_sel.numel() * 2 + xg.numel() * 2 + yg.numel() * 2)
+        res[which] = {"ms_per_step": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                      "gbs": round(byts / (ms * 1e-3) / 1e9, 1)}
+        tot_ms += ms; tot_flops += flops; tot_bytes += byts
+        del xg, b_codes, b_scales, g_b, w_sel, yg
+    out["moe"] = {"shape": "4096 tokens x top-8 of 128 experts, hidden 2048, gate/up 1536, down 2048, k=32/expert",
+                  "ms_per_step": round(tot_ms, 4), "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 1),
+                  "frac_fp4_peak": round(tot_flops / (tot_ms * 1e-3) / 1e12 / fp4_peak, 4),
+                  "gbs": round(tot_bytes / (tot_ms * 1e-3) / 1e9, 1),
+                  "frac_hbm": round(tot_bytes / (tot_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                  "bytes_per_step": tot_bytes, "per_projection": res,
+                  "note": "each projection: grouped dynamic-scale quantize + grouped GEMM with compensation"}
+    del dm
+
+    # MXFP4: X[8192,5120] x W[5120,5120], 32-blocks, decomposition statistics
+    s = W.SPECS["mxfp4"]
+    d = W.dense_inputs("mxfp4")
+    x, wt = d["x"].to(dev), d["wt"].to(dev)
+    qw = nv.mxfp4_quantize(wt)
+    del wt
+    y = torch.empty((s.M, s.N), dtype=torch.bfloat16, device=dev)
+    box = {}
+
+    def mx():
+        qx = nv.mxfp4_quantize(x, stats=True)
+        box["q"] = qx
+        nv.w4a4_gemm_comp(dict(codes=qx["codes"], scales=qx["scales"]), dict(codes=qw["codes"], scales=qw["scales"]),
+                          s.N, fmt=nv.FMT_MXFP4, y=y)
+    ms = _time_steps(mx, steps, flush)
+    out["mxfp4"] = {"shape": "X[8192,5120] x W[5120,5120], MXFP4 + per-block decomposition", "ms_per_step": round(ms, 4),
+                    "tflops": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12, 1),
+                    "frac_fp4_peak": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12 / fp4_peak, 4)}
+    return out
 
 
 # ------------------------------------------------------ the oracle arm ----
@@ -393,6 +509,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=None,
                     help="oracle sample rows (default 4096 for cpu_baseline, 2048 per reference step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the decode / MoE / MXFP4 measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

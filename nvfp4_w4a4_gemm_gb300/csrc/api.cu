@@ -191,7 +191,7 @@ int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b
 
 size_t nvfp4_calibrate_workspace_bytes(int64_t K, int32_t E) {
   if (K < 0 || E < 0) return 0;
-  return 256 + kQuantWs + sizeof(double) * 2 * (size_t)K * (size_t)(E + 1);
+  return 256 + kQuantWs + sizeof(double) * 2 * (size_t)K * (size_t)(E + 1) + sizeof(int32_t) * (size_t)K * E;
 }
 
 int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_t ldx, int32_t E,
@@ -201,7 +201,6 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
   if (!x_cal || !aligned(x_cal, 16) || (k > 0 && !chan_out)) return NVFP4_ERR_INVALID_ARG;
   if (offsets != nullptr && (E <= 0 || !aligned(offsets, 4))) return NVFP4_ERR_INVALID_ARG;
   if (offsets == nullptr) E = 1;
-  if (K > 16384) return NVFP4_ERR_UNSUPPORTED;  // selection keeps K variances in shared memory
   if (k == 0) return NVFP4_OK;
   if (!workspace || ws_bytes < nvfp4_calibrate_workspace_bytes(K, E) || !aligned(workspace, 16))
     return NVFP4_ERR_WORKSPACE;
@@ -223,8 +222,9 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
   if (e == cudaSuccess) e = nv4::launch_channel_stats(bf(x_cal), M, K, ldx, g, offsets, E, sum, sumsq, d->num_sms, s);
   if (e == cudaSuccess && offsets != nullptr)
     e = nv4::launch_channel_stats(bf(x_cal), M, K, ldx, g, nullptr, 1, sum_all, sumsq_all, d->num_sms, s);
+  int32_t* flags = reinterpret_cast<int32_t*>(sums + 2 * (size_t)K * (size_t)(E + 1));
   if (e == cudaSuccess)
-    e = nv4::launch_select_channels(sum, sumsq, offsets, E, M, sum_all, sumsq_all, K, k, chan_out, s);
+    e = nv4::launch_select_channels(sum, sumsq, offsets, E, M, sum_all, sumsq_all, K, k, flags, chan_out, s);
   return from_cuda(e);
 }
 

@@ -26,9 +26,11 @@ cudaError_t launch_channel_stats(const __nv_bfloat16* x, int64_t M, int64_t K, i
                                  const int32_t* offsets, int E, double* sum, double* sumsq, int num_sms,
                                  cudaStream_t stream);
 
-cudaError_t launch_select_channels(const double* sum, const double* sumsq, const int32_t* offsets, int E,
+// Top-k channel selection; `sumsq` is overwritten with the variances and
+// `flag_ws` (int32 [E, K]) is scratch.
+cudaError_t launch_select_channels(const double* sum, double* sumsq, const int32_t* offsets, int E,
                                    int64_t M_all, const double* sum_all, const double* sumsq_all, int64_t K, int k,
-                                   int32_t* chan_out, cudaStream_t stream);
+                                   int32_t* flag_ws, int32_t* chan_out, cudaStream_t stream);
 
 cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* partials,
                                 float* g_out, int num_sms, cudaStream_t stream);

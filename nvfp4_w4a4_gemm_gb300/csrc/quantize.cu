@@ -35,7 +35,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;            // row segments in flight per warp (MXFP4)
-constexpr int64_t kMaxMapK = 65536;   // dense channel map in shared memory up to this K
+constexpr int64_t kMaxMapK = 262144;  // dense per-block channel table in shared memory up to this K
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -157,15 +157,15 @@ struct QuantArgs {
 // into one 32-bit tile-layout store) and its residuals.
 template <bool kGrouped>
 __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw0, const uint4& raw1, int64_t r,
-                                            int64_t c, int lane, float g, int64_t n_cg, const int16_t* s_map,
+                                            int64_t c, int lane, float g, int64_t n_cg, const uint32_t* s_tab,
                                             const int32_t* s_chan, const int32_t* s_off, const int32_t* s_pbase) {
   const bool valid = c < a.K;
-  float f[16];
-  unpack8(raw0, *reinterpret_cast<float(*)[8]>(f));
-  unpack8(raw1, *reinterpret_cast<float(*)[8]>(f + 8));
-  float am = 0.f;
+  // block absmax on packed bf16 pairs (exact: a max of bf16 values)
+  const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+  __nv_bfloat162 m2 = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
+  for (int i = 1; i < 8; ++i) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+  const float am = fmaxf(__low2float(m2), __high2float(m2));
   // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
   const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
   const uint32_t sig = cvt_e4m3(t);
@@ -175,8 +175,11 @@ __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw
     const float rcp = __fdiv_rn(1.0f, d);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      lo |= cvt_e2m1x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp)) << (8 * i);
-      hi |= cvt_e2m1x2(__fmul_rn(f[8 + 2 * i], rcp), __fmul_rn(f[8 + 2 * i + 1], rcp)) << (8 * i);
+      lo |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w[i] << 16), rcp), __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), rcp))
+            << (8 * i);
+      hi |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w[4 + i] << 16), rcp),
+                       __fmul_rn(__uint_as_float(w[4 + i] & 0xFFFF0000u), rcp))
+            << (8 * i);
     }
   }
   int64_t srow = r;
@@ -214,23 +217,22 @@ __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw
       const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
       dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
     }
-    float xf = f[0];
+    uint32_t wj = w[0];
 #pragma unroll
-    for (int q = 1; q < 16; ++q) if (j == q) xf = f[q];
+    for (int q = 1; q < 8; ++q) if ((j >> 1) == q) wj = w[q];
+    const float xf = __uint_as_float((j & 1) ? (wj & 0xFFFF0000u) : (wj << 16));
     a.resid[r * a.k + slot] = __float2bfloat16_rn(__fsub_rn(xf, dq));
   };
   if (!kGrouped && a.use_map) {
-    const uint4 m0 = *reinterpret_cast<const uint4*>(s_map + c);
-    const uint4 m1 = *reinterpret_cast<const uint4*>(s_map + c + 8);
-    const uint32_t w[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    uint32_t all = 0xFFFFFFFFu;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) all &= w[i];
-    if ((all & 0x80008000u) == 0x80008000u) return;  // no channel of S in this block
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int slot = (int)(int16_t)((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-      if (slot >= 0) resid_at(j, slot);
+    // per-block entry: bits 16..31 = which of the 16 channels are in S,
+    // bits 0..15 = slot of the block's first channel of S
+    const uint32_t ent = s_tab[c >> 4];
+    uint32_t mask = ent >> 16;
+    int slot = (int)(ent & 0xFFFFu);
+    while (mask) {
+      const int j = __ffs(mask) - 1;
+      resid_at(j, slot++);
+      mask &= mask - 1;
     }
   } else {
     const int32_t* S = s_chan + e * a.k;
@@ -242,21 +244,25 @@ __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw
 template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
   extern __shared__ __align__(16) int32_t smem_i32[];
-  // dense + map: int16 slot map [K] | otherwise: chan [E*k] | offsets [E+1] | padded bases [E]
-  int16_t* s_map = reinterpret_cast<int16_t*>(smem_i32);
+  // chan [E*k] | dense + map: per-block table [K/16] | grouped: offsets [E+1] | padded bases [E]
   int32_t* s_chan = smem_i32;
+  uint32_t* s_tab = reinterpret_cast<uint32_t*>(s_chan + a.E * a.k);
   int32_t* s_off = s_chan + a.E * a.k;
   int32_t* s_pbase = s_off + (a.E + 1);
-  if (!kGrouped && a.use_map) {
-    for (int64_t i = threadIdx.x; i < a.K; i += blockDim.x) s_map[i] = -1;
-    __syncthreads();
-    for (int i = threadIdx.x; i < a.k; i += blockDim.x) {
-      const int32_t j = a.chan[i];
-      if (j >= 0 && j < a.K) s_map[j] = (int16_t)i;
-    }
-  } else {
+  {
     const int nchan = a.E * a.k;
     for (int i = threadIdx.x; i < nchan; i += blockDim.x) s_chan[i] = a.chan[i];
+  }
+  if (!kGrouped && a.use_map) {
+    __syncthreads();
+    const int64_t nb = a.K / 16;
+    for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
+      int i = lower_bound_i32(s_chan, a.k, (int32_t)(b * 16));
+      const uint32_t first = (uint32_t)i;
+      uint32_t mask = 0;
+      for (; i < a.k && s_chan[i] < b * 16 + 16; ++i) mask |= 1u << (s_chan[i] - (int32_t)(b * 16));
+      s_tab[b] = (mask << 16) | (first & 0xFFFFu);
+    }
   }
   if (kGrouped) {
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
     for (int h = 0; h < 2; ++h) {
       if ((int64_t)gi * 1024 + h * 512 >= a.K) break;  // warp-uniform
       const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
-      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, s_map, s_chan, s_off, s_pbase);
+      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, s_tab, s_chan, s_off, s_pbase);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
@@ -563,46 +569,84 @@ __global__ void __launch_bounds__(kThreads) channel_stats_kernel(const __nv_bflo
 }
 
 // Top-k channels by population variance (ties -> lower index), sorted
-// ascending.  One CTA per expert; rank of channel j = number of channels
-// that beat it.  Experts with fewer than 2 rows use the all-row statistics
-// (sum_all / sumsq_all over M_all rows).
-__global__ void __launch_bounds__(1024) select_channels_kernel(const double* __restrict__ sum,
-                                                               const double* __restrict__ sumsq,
-                                                               const int32_t* __restrict__ offsets, int64_t M_all,
-                                                               const double* __restrict__ sum_all,
-                                                               const double* __restrict__ sumsq_all, int64_t K, int k,
-                                                               int32_t* __restrict__ chan_out) {
-  extern __shared__ double s_var[];
-  int* s_flag = reinterpret_cast<int*>(s_var + K);
-  const int e = blockIdx.x;
+// ascending, in three small kernels: per-channel variance (in place over the
+// sum-of-squares array), rank of every channel among its expert's channels
+// (rank < k selects it), and an order-preserving compaction.  Experts with
+// fewer than 2 rows use the all-row statistics.
+__global__ void __launch_bounds__(256) channel_var_kernel(const double* __restrict__ sum, double* __restrict__ sumsq,
+                                                          const int32_t* __restrict__ offsets, int64_t M_all,
+                                                          const double* __restrict__ sum_all,
+                                                          const double* __restrict__ sumsq_all, int64_t K) {
+  const int e = blockIdx.y;
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= K) return;
   int64_t rows = M_all;
-  const double* S = sum + (int64_t)e * K;
-  const double* Q = sumsq + (int64_t)e * K;
+  double s1 = sum[(int64_t)e * K + j], s2 = sumsq[(int64_t)e * K + j];
   if (offsets != nullptr) {
     rows = offsets[e + 1] - offsets[e];
-    if (rows < 2) { S = sum_all; Q = sumsq_all; rows = M_all; }
+    if (rows < 2) { s1 = sum_all[j]; s2 = sumsq_all[j]; rows = M_all; }
   }
   const double inv = rows > 0 ? 1.0 / (double)rows : 0.0;
-  for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
-    const double mu = S[j] * inv;
-    const double v = Q[j] * inv - mu * mu;
-    s_var[j] = v > 0.0 ? v : 0.0;
-  }
-  __syncthreads();
-  for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
-    const double vj = s_var[j];
-    int64_t rank = 0;
-    for (int64_t i = 0; i < K; ++i) {
-      const double vi = s_var[i];
-      rank += (vi > vj) || (vi == vj && i < j);
+  const double mu = s1 * inv;
+  const double v = s2 * inv - mu * mu;
+  sumsq[(int64_t)e * K + j] = v > 0.0 ? v : 0.0;
+}
+
+__global__ void __launch_bounds__(256) channel_rank_kernel(const double* __restrict__ var, int64_t K, int k,
+                                                           int32_t* __restrict__ flag) {
+  __shared__ double s_v[1024];
+  const int e = blockIdx.y;
+  const double* V = var + (int64_t)e * K;
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const double vj = j < K ? V[j] : 0.0;
+  int64_t rank = 0;
+  for (int64_t i0 = 0; i0 < K; i0 += 1024) {
+    const int n = (int)((K - i0) < 1024 ? (K - i0) : 1024);
+    __syncthreads();
+    for (int t = threadIdx.x; t < n; t += blockDim.x) s_v[t] = V[i0 + t];
+    __syncthreads();
+    for (int t = 0; t < n; ++t) {
+      const double vi = s_v[t];
+      rank += (vi > vj) || (vi == vj && i0 + t < j);
     }
-    s_flag[j] = rank < k ? 1 : 0;
   }
+  if (j < K) flag[(int64_t)e * K + j] = rank < k ? 1 : 0;
+}
+
+__global__ void __launch_bounds__(1024) channel_compact_kernel(const int32_t* __restrict__ flag, int64_t K, int k,
+                                                               int32_t* __restrict__ chan_out) {
+  __shared__ int s_warp[32];
+  __shared__ int s_base;
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) s_base = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {  // compaction in index order (K small)
-    int n = 0;
-    for (int64_t j = 0; j < K && n < k; ++j)
-      if (s_flag[j]) chan_out[(int64_t)e * k + n++] = (int32_t)j;
+  for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+    const int64_t j = j0 + threadIdx.x;
+    const int f = j < K ? flag[(int64_t)e * K + j] : 0;
+    int incl = f;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int v = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      s_warp[lane] = v;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int before = s_base + (warp > 0 ? s_warp[warp - 1] : 0) + incl - f;
+    if (f && before < k) chan_out[(int64_t)e * k + before] = (int32_t)j;
+    __syncthreads();
+    if (threadIdx.x == 0) s_base += s_warp[(blockDim.x >> 5) - 1];
+    __syncthreads();
   }
 }
 
@@ -644,7 +688,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
-  a.use_map = (offsets == nullptr && k > 0 && K <= kMaxMapK) ? 1 : 0;
+  a.use_map = (offsets == nullptr && k > 0 && k < 65536 && K <= kMaxMapK) ? 1 : 0;
   if (g_in == nullptr) {
     const int p = amax_partials_count(M, K, num_sms);
     amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
@@ -661,9 +705,8 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  size_t smem;
-  if (a.use_map) smem = sizeof(int16_t) * (size_t)((K + 7) / 8 * 8);
-  else smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
+  size_t smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
+  if (a.use_map) smem += sizeof(uint32_t) * (size_t)(K / 16);
   if (offsets != nullptr) {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(nvfp4_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -713,13 +756,13 @@ cudaError_t launch_channel_stats(const __nv_bfloat16* x, int64_t M, int64_t K, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_select_channels(const double* sum, const double* sumsq, const int32_t* offsets, int E,
+cudaError_t launch_select_channels(const double* sum, double* sumsq, const int32_t* offsets, int E,
                                    int64_t M_all, const double* sum_all, const double* sumsq_all, int64_t K, int k,
-                                   int32_t* chan_out, cudaStream_t stream) {
-  const size_t smem = (size_t)K * (sizeof(double) + sizeof(int));
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(select_channels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  select_channels_kernel<<<E, 1024, smem, stream>>>(sum, sumsq, offsets, M_all, sum_all, sumsq_all, K, k, chan_out);
+                                   int32_t* flag_ws, int32_t* chan_out, cudaStream_t stream) {
+  const dim3 grid((unsigned)((K + 255) / 256), (unsigned)E);
+  channel_var_kernel<<<grid, 256, 0, stream>>>(sum, sumsq, offsets, M_all, sum_all, sumsq_all, K);
+  channel_rank_kernel<<<grid, 256, 0, stream>>>(sumsq, K, k, flag_ws);
+  channel_compact_kernel<<<E, 1024, 0, stream>>>(flag_ws, K, k, chan_out);
   return cudaGetLastError();
 }
 
