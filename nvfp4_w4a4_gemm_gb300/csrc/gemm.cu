@@ -92,6 +92,8 @@ struct Tile {
   int rows;       // valid rows (<= 128)
   int64_t sf_rt;  // 128-row tile index in A's scale layout
   int n0;         // first output column
+  bool m_valid;   // wide tiles: A rows exist
+  bool n_valid;   // wide tiles: the second 128-row half of B exists
 };
 
 // Grouped schedule tables in shared memory (after the stage ring).
@@ -437,6 +439,371 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   }
 }
 
+// ===================================================== wide-tile kernel ====
+// 128 x 256 output tiles with N = 256 MMAs: per unit of MMA work this halves
+// the block-scale copies into TMEM for the B operand's rows relative to two
+// 128 x 128 tiles (copies and MMAs share the tensor pipe).  TMEM holds one
+// 256-column accumulator and 4 scale slots of 48 columns (A 16 + B 32), so
+// the compensation term accumulates into the main accumulator: its residual
+// tile is pre-scaled in shared memory by c = 1/g_a (1/(g_a g_b) with BF16
+// weight columns) by a transform warp, and the epilogue applies g_a g_b once.
+// Eight epilogue warps drain the accumulator quickly (two per TMEM lane
+// quarter, 128 columns each) and release it before storing.
+//   warp 0 TMA | warp 1 MMA | warp 2 scale copies | warp 3 residual scaling |
+//   warps 4..11 epilogue
+constexpr int BNW = 256;
+constexpr int kWStages = 4;
+constexpr int kWTileA = BM * BKB;               // 16 KB
+constexpr int kWTileB = BNW * BKB;              // 32 KB
+constexpr int kWSfA = 2048, kWSfB = 4096;
+constexpr int kWStageBytes = kWTileA + kWTileB + kWSfA + kWSfB;  // 54 KB
+constexpr int kWThreads = 384;
+constexpr uint32_t kWColSf = 256;               // slots of 48 columns after the accumulator
+static_assert(kWColSf + 48 * kWStages <= kTmemCols, "TMEM budget");
+constexpr size_t kWSmemBytes = 1024 + (size_t)kWStages * kWStageBytes + 512;
+
+__device__ __forceinline__ uint32_t idesc_fp4_n(int fmt, uint32_t sf_id, int n) {
+  uint32_t d = (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  if (fmt == 1) d |= (1u << 23) | (sf_id << 29) | (sf_id << 4);
+  return d;
+}
+__device__ __forceinline__ uint32_t idesc_bf16_n(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tile_of_w(const GemmParams& p, const SchedSmem& s, int64_t t, int n_tiles_n,
+                                          Tile& out) {
+  int64_t local = t, row_end;
+  int e = 0;
+  if (p.grouped) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    e = lo;
+    local = t - s.tile_start[e];
+  }
+  const int64_t mt = local / n_tiles_n;
+  const int nt = (int)(local - mt * n_tiles_n);
+  out.e = e;
+  out.n0 = nt * BNW;
+  if (p.grouped) {
+    out.row0 = (int64_t)s.off[e] + mt * BM;
+    row_end = s.off[e + 1];
+    out.sf_rt = (int64_t)(s.pbase[e] >> 7) + mt;
+  } else {
+    out.row0 = mt * BM;
+    row_end = p.M;
+    out.sf_rt = mt;
+  }
+  const int64_t rem = row_end - out.row0;
+  out.rows = rem < BM ? (int)rem : BM;
+  out.m_valid = true;
+  out.n_valid = out.n0 + 128 < p.N;  // second 128-row half of B exists
+}
+
+__global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWStages * kWStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kWStages;
+  uint64_t* sf_full = empty + kWStages;
+  uint64_t* comp_ready = sf_full + kWStages;
+  uint64_t* acc_full = comp_ready + kWStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint64_t* sf_drain = drain + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  SchedSmem sched{};
+  const int n_tiles_n = (int)((p.N + BNW - 1) / BNW);
+  if (p.grouped) {
+    sched.off = s_sched;
+    sched.tile_start = s_sched + (p.E + 1);
+    sched.pbase = s_sched + 2 * (p.E + 1);
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sched.off[i] = p.offsets[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t ts = 0, pb = 0;
+      for (int e = 0; e < p.E; ++e) {
+        const int32_t mt = (sched.off[e + 1] - sched.off[e] + BM - 1) / BM;
+        sched.tile_start[e] = ts;
+        sched.pbase[e] = pb;
+        ts += mt * n_tiles_n;
+        pb += mt * BM;
+      }
+      sched.tile_start[p.E] = ts;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&sf_full[i], 1);
+      mbar_init(&comp_ready[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 8);
+    mbar_init(drain, 1);
+    mbar_init(sf_drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int64_t num_tiles = p.grouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BM - 1) / BM) * (int64_t)n_tiles_n;
+  const int sf_chunks_per_kt = p.fmt == 1 ? 2 : 4;
+  const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;
+  const int n_kt = (int)((p.K + 255) / 256);
+  const int n_ct = (p.k + 63) / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_a);
+      tma_prefetch_desc(&p.tm_b);
+      if (n_ct > 0) {
+        tma_prefetch_desc(&p.tm_r);
+        tma_prefetch_desc(&p.tm_w);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        Tile tl;
+        tile_of_w(p, sched, t, n_tiles_n, tl);
+        const uint8_t* sfb_src0 = p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride;
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+          uint8_t* sa = stages + stage * kWStageBytes;
+          uint8_t* sb = sa + kWTileA;
+          uint8_t* sfa = sb + kWTileB;
+          uint8_t* sfb = sfa + kWSfA;
+          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+          const uint32_t sf_bytes = (uint32_t)nch * 512u;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWTileA + kWTileB) + sf_bytes * (tl.n_valid ? 3u : 2u));
+          tma_load_2d(sa, &p.tm_a, &full[stage], kt * BKB, (int32_t)tl.row0);
+          if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0, tl.e);
+          else tma_load_2d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0);
+          bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
+          const uint64_t bt = (uint64_t)(tl.n0 / 128);
+          bulk_load(sfb, sfb_src0 + (bt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
+          if (tl.n_valid) bulk_load(sfb + 2048, sfb_src0 + ((bt + 1) * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+        for (int ct = 0; ct < n_ct && ok; ++ct) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+          uint8_t* sa = stages + stage * kWStageBytes;
+          uint8_t* sb = sa + kWTileA;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWTileA + kWTileB));
+          tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
+          if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
+          else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t idesc_main = idesc_fp4_n(p.fmt, 0, BNW);
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+        acc_phase ^= 1u;
+        tc_fence_after();
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+          if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
+          const uint32_t sb = sa + kWTileA;
+          const uint32_t t_sfa = tmem + kWColSf + (uint32_t)stage * 48u;
+          const uint32_t t_sfb = t_sfa + 16u;
+          const int64_t krem = p.K - (int64_t)kt * 256;
+          const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
+          for (int j = 0; j < n_mma; ++j) {
+            const uint64_t adesc = desc_sw128(sa + 32u * j);
+            const uint64_t bdesc = desc_sw128(sb + 32u * j);
+            const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
+            if (p.fmt == 1) {
+              mma_mxf4_2x(tmem, adesc, bdesc, idesc_fp4_n(1, (uint32_t)(j & 1) * 2u, BNW), t_sfa + 4u * (j >> 1),
+                          t_sfb + 8u * (j >> 1), accum);
+            } else {
+              mma_nvf4_4x(tmem, adesc, bdesc, idesc_main, t_sfa + 4u * j, t_sfb + 8u * j, accum);
+            }
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+        for (int ct = 0; ct < n_ct && ok; ++ct) {
+          if (!mbar_wait(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
+          const uint32_t sb = sa + kWTileA;
+          const int krem = p.k - ct * 64;
+          const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
+          for (int j = 0; j < n_mma; ++j)
+            mma_bf16(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16_n(BNW), 1u);
+          tc_commit(&empty[stage]);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, kWaitDrain, nullptr);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- scale copies ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        // every stage use completes one phase of sf_full[stage] (a plain arrive
+        // for compensation k-tiles), so its parity tracks the stage's
+        for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
+          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+          if (kt >= n_kt) {
+            mbar_arrive(&sf_full[stage]);
+          } else {
+            tc_fence_after();
+            const uint32_t sfa = smem_u32(stages + stage * kWStageBytes) + (uint32_t)(kWTileA + kWTileB);
+            const uint32_t sfb = sfa + kWSfA;
+            const uint32_t t_sfa = tmem + kWColSf + (uint32_t)stage * 48u;
+            const uint32_t t_sfb = t_sfa + 16u;
+            const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+            const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+            for (int c = 0; c < nch; ++c) {
+              tmem_cp_32x128b_x4(t_sfa + 4u * c, desc_sf(sfa + 512u * c));
+              tmem_cp_32x128b_x4(t_sfb + 8u * c, desc_sf(sfb + 512u * c));
+              tmem_cp_32x128b_x4(t_sfb + 8u * c + 4u, desc_sf(sfb + 2048u + 512u * c));
+            }
+            tc_commit(&sf_full[stage]);
+          }
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, kWaitSfDrain, nullptr);
+    }
+  } else if (warp == 3) {
+    // ----------------------------------------- residual pre-scaling ----
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const float ga = p.g_a ? *p.g_a : 1.f;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok && n_ct > 0; t += gridDim.x) {
+      int e = 0;
+      if (p.grouped) {
+        Tile tl;
+        tile_of_w(p, sched, t, n_tiles_n, tl);
+        e = tl.e;
+      }
+      float c = __fdiv_rn(1.0f, ga);
+      if (p.flags == 1) c = __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[e] : 1.f));
+      // every stage use completes one phase of comp_ready[stage] (a plain
+      // arrive for FP4 k-tiles), so its parity tracks the stage's
+      for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
+        if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+        if (kt < n_kt) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comp_ready[stage]);
+        } else {
+          uint4* ra = reinterpret_cast<uint4*>(stages + stage * kWStageBytes);
+#pragma unroll 4
+          for (int i = lane; i < kWTileA / 16; i += 32) {
+            uint4 v = ra[i];
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(w[q] << 16) * c,
+                                                              __uint_as_float(w[q] & 0xFFFF0000u) * c);
+              w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            ra[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comp_ready[stage]);
+        }
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue ----
+    const int q = warp & 3;            // TMEM lane quarter
+    const int h = (warp - 4) >> 2;     // column half
+    const int r = q * 32 + lane;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      Tile tl;
+      tile_of_w(p, sched, t, n_tiles_n, tl);
+      if (!mbar_wait(acc_full, acc_phase, kWaitAccFull, s_abort)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      float alpha = 1.f;
+      if (p.fmt == 0) alpha = (p.g_a ? *p.g_a : 1.f) * (p.g_b ? p.g_b[tl.e] : 1.f);
+      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+      uint32_t packed[64];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(t_acc + (uint32_t)(b * 64 + c * 16), v[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(alpha * __uint_as_float(v[c][2 * i]),
+                                                            alpha * __uint_as_float(v[c][2 * i + 1]));
+            packed[b * 32 + c * 8 + i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);   // accumulator free: the next tile's MMAs may start
+      const int64_t col0 = tl.n0 + h * 128;
+      if (r < tl.rows && col0 < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(p.y + (tl.row0 + r) * p.N + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------- host side ---
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -473,7 +840,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
-cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
+cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   const int E = grouped ? pr.E : 1;
@@ -533,6 +900,70 @@ cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_
   return cudaGetLastError();
 }
 
+
+cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int E = grouped ? pr.E : 1;
+  const uint64_t rows = (uint64_t)pr.M;
+  const uint64_t kb = (uint64_t)(pr.K / 2);
+  {
+    const uint64_t d[2] = {kb, rows};
+    if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
+  }
+  if (grouped) {
+    const uint64_t d[3] = {kb, (uint64_t)pr.N, (uint64_t)E};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 3, d, BKB, BNW)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t d[2] = {kb, (uint64_t)pr.N};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BNW)) return cudaErrorInvalidValue;
+  }
+  if (pr.k > 0) {
+    const uint64_t dr[2] = {(uint64_t)pr.k, rows};
+    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
+    if (grouped) {
+      const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BNW))
+        return cudaErrorInvalidValue;
+    } else {
+      const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BNW))
+        return cudaErrorInvalidValue;
+    }
+  }
+  p.a_sf = pr.a_scales;
+  p.b_sf = pr.b_scales;
+  const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
+  p.b_sf_expert_stride = (uint64_t)(((pr.N + 127) / 128) * 128) * (uint64_t)n_sf_cols;
+  p.g_a = pr.g_a;
+  p.g_b = pr.g_b;
+  p.y = pr.y;
+  p.M = pr.M;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.k = pr.k;
+  p.flags = pr.flags;
+  p.fmt = pr.fmt;
+  p.E = E;
+  p.offsets = pr.offsets;
+  p.grouped = grouped ? 1 : 0;
+  const int64_t n_tiles_n = (pr.N + BNW - 1) / BNW;
+  const int64_t tiles = grouped ? ((pr.M + BM - 1) / BM + E) * n_tiles_n : ((pr.M + BM - 1) / BM) * n_tiles_n;
+  int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  if (grid < 1) grid = 1;
+  const size_t smem = kWSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
+  cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  w4a4_gemm_wide_kernel<<<grid, kWThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
+  // few rows: 128 x 128 tiles keep more SMs busy; otherwise 128 x 256 tiles
+  if (!grouped && pr.M <= 2 * BM) return launch_narrow(pr, grouped, num_sms, stream);
+  return launch_wide(pr, grouped, num_sms, stream);
+}
+
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int) { return 0; }
@@ -542,7 +973,7 @@ cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) 
 }
 
 cudaError_t launch_grouped_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {
-  if ((size_t)p.E * 12 + 8 > 227 * 1024 - kSmemBytes) return cudaErrorInvalidValue;
+  if ((size_t)p.E * 12 + 8 > 227 * 1024 - kWSmemBytes) return cudaErrorInvalidValue;
   return launch(p, true, num_sms, stream);
 }
 
