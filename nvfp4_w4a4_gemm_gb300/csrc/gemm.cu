@@ -84,6 +84,8 @@ struct GemmParams {
   int E;
   const int32_t* offsets;
   int grouped;
+  int split;        // narrow kernel: K splits per tile (1 = none)
+  float* partial;   // split > 1: fp32 partial sums [split][M][N]
 };
 
 struct Tile {
@@ -220,11 +222,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   num_tiles = p.grouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BM - 1) / BM) * (int64_t)n_tiles_n;
+  // work units: (tile, K split); unit u covers FP4 k-tiles [kt_lo(u), kt_hi(u))
+  // and carries the compensation k-tiles only for split 0
+  const int split = p.split > 1 ? p.split : 1;
+  const int64_t num_units = num_tiles * split;
 
   const int sf_chunks_per_kt = p.fmt == 1 ? 2 : 4;  // 512-byte chunks per 256-element k-tile
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
   const int n_kt = (int)((p.K + 255) / 256);
   const int n_ct = (p.k + 63) / 64;
+  auto kt_lo = [&](int64_t u) { return (int)((u % split) * n_kt / split); };
+  auto kt_hi = [&](int64_t u) { return (int)((u % split + 1) * n_kt / split); };
+  auto ct_of = [&](int64_t u) { return (u % split) == 0 ? n_ct : 0; };
 
   if (warp == 0) {
     // ------------------------------------------------------ producer ----
@@ -238,10 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
         Tile tl;
-        tile_of(p, sched, t, n_tiles_n, tl);
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
+        tile_of(p, sched, u / split, n_tiles_n, tl);
+        const int kt1 = kt_hi(u), n_ct_u = ct_of(u);
+        for (int kt = kt_lo(u); kt < kt1 && ok; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
           uint8_t* sa = stages + stage * kStageBytes;
           uint8_t* sb = sa + kTileBytes;
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
                     sf_bytes, &full[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        for (int ct = 0; ct < n_ct && ok; ++ct) {
+        for (int ct = 0; ct < n_ct_u && ok; ++ct) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
           uint8_t* sa = stages + stage * kStageBytes;
           uint8_t* sb = sa + kTileBytes;
@@ -289,11 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       uint32_t acc_phase = 0;
       uint32_t comp_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
+        for (int kt = kt0; kt < kt1 && ok; ++kt) {
           if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stages + stage * kStageBytes);
@@ -305,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           for (int j = 0; j < n_mma; ++j) {
             const uint64_t adesc = desc_sw128(sa + 32u * j);
             const uint64_t bdesc = desc_sw128(sb + 32u * j);
-            const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
+            const uint32_t accum = (kt > kt0 || j > 0) ? 1u : 0u;
             if (p.fmt == 1) {
               mma_mxf4_2x(d_acc, adesc, bdesc, idesc_fp4(1, (uint32_t)(j & 1) * 2u), t_sfa + 4u * (j >> 1),
                           t_sfb + 4u * (j >> 1), accum);
@@ -316,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           tc_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (n_ct > 0 && ok) {
+        if (n_ct_u > 0 && ok) {
           if (!mbar_wait(comp_empty, comp_phase ^ 1u, kWaitCompEmpty, s_abort)) { ok = false; break; }
           comp_phase ^= 1u;
           tc_fence_after();
-          for (int ct = 0; ct < n_ct && ok; ++ct) {
+          for (int ct = 0; ct < n_ct_u && ok; ++ct) {
             if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(stages + stage * kStageBytes);
@@ -350,10 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
+      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
+        for (int kt = kt0; kt < kt1 + n_ct_u && ok; ++kt) {
           if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
-          if (kt < n_kt) {
+          if (kt < kt1) {
             tc_fence_after();
             const uint32_t sfa = smem_u32(stages + stage * kStageBytes) + 2u * kTileBytes;
             const uint32_t sfb = sfa + kSfBytes;
@@ -380,9 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x) {
       Tile tl;
-      tile_of(p, sched, t, n_tiles_n, tl);
+      tile_of(p, sched, u / split, n_tiles_n, tl);
+      const int n_ct_u = ct_of(u);
       if (!mbar_wait(&acc_full[acc], acc_phase, kWaitAccFull, s_abort)) break;
       tc_fence_after();
       float alpha = 1.f, beta = 0.f;
@@ -400,18 +413,26 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       for (int c = 0; c < BN; c += 16) {
         uint32_t v[16], w[16];
         tmem_ld_32x32b_x16(t_acc + c, v);
-        if (n_ct > 0) tmem_ld_32x32b_x16(t_cmp + c, w);
+        if (n_ct_u > 0) tmem_ld_32x32b_x16(t_cmp + c, w);
         tmem_ld_wait();
+        float yv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          yv[i] = alpha * __uint_as_float(v[i]);
+          if (n_ct_u > 0) yv[i] = fmaf(beta, __uint_as_float(w[i]), yv[i]);
+        }
+        if (split > 1) {  // fp32 partial sums, reduced in split order by the finalize kernel
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(p.partial + ((u % split) * p.M + tl.row0 + r) * p.N + tl.n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
+          }
+          continue;
+        }
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float y0 = alpha * __uint_as_float(v[2 * i]);
-          float y1 = alpha * __uint_as_float(v[2 * i + 1]);
-          if (n_ct > 0) {
-            y0 = fmaf(beta, __uint_as_float(w[2 * i]), y0);
-            y1 = fmaf(beta, __uint_as_float(w[2 * i + 1]), y1);
-          }
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(yv[2 * i], yv[2 * i + 1]);
           packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
         if (row_ok) {
@@ -424,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&acc_empty[acc]);
-        if (n_ct > 0) mbar_arrive(comp_empty);
+        if (n_ct_u > 0) mbar_arrive(comp_empty);
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -436,6 +457,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Sum of the split-K partials in split order (deterministic), bf16 output.
+__global__ void __launch_bounds__(256) splitk_finalize_kernel(const float* __restrict__ partial, int split, int64_t M,
+                                                              int64_t N, __nv_bfloat16* __restrict__ y) {
+  const int64_t total = M * N / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(partial)[i];
+    for (int s = 1; s < split; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(partial + (int64_t)s * M * N)[i];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+    reinterpret_cast<uint2*>(y)[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
   }
 }
 
@@ -840,6 +876,20 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
+// K splits for the narrow kernel: when its tiles cannot fill the SMs (few
+// rows, e.g. decode), each tile's K range is split so the units cover about
+// three waves; the partials go to the caller's workspace.
+int narrow_split(int64_t M, int64_t N, int64_t K, int num_sms) {
+  if (M > 2 * BM) return 1;
+  const int64_t tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int64_t n_kt = (K + 255) / 256;
+  if (tiles >= num_sms || n_kt < 2) return 1;
+  int64_t s = (3 * (int64_t)num_sms + tiles - 1) / tiles;
+  if (s > n_kt) s = n_kt;
+  if (s > 16) s = 16;
+  return (int)(s < 1 ? 1 : s);
+}
+
 cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -891,12 +941,24 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   int64_t tiles;
   if (grouped) tiles = ((pr.M + BM - 1) / BM + E) * (int64_t)n_tiles_n;  // upper bound
   else tiles = ((pr.M + BM - 1) / BM) * (int64_t)n_tiles_n;
-  int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  p.split = grouped ? 1 : narrow_split(pr.M, pr.N, pr.K, num_sms);
+  p.partial = static_cast<float*>(pr.ws);
+  if (p.split > 1 && (pr.ws == nullptr || pr.ws_bytes < (size_t)p.split * pr.M * pr.N * sizeof(float)))
+    return cudaErrorInvalidValue;
+  const int64_t units = tiles * p.split;
+  int grid = (int)(units < num_sms ? units : num_sms);
   if (grid < 1) grid = 1;
   const size_t smem = kSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
   cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   w4a4_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
+  if (p.split > 1) {
+    const int64_t n4 = pr.M * pr.N / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    splitk_finalize_kernel<<<(unsigned)(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(p.partial, p.split, pr.M, pr.N,
+                                                                                    pr.y);
+  }
   return cudaGetLastError();
 }
 
@@ -966,7 +1028,10 @@ cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_
 
 }  // namespace
 
-size_t gemm_workspace_bytes(int64_t, int64_t, int64_t, int) { return 0; }
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
+  const int split = narrow_split(M, N, K, num_sms);
+  return split > 1 ? (size_t)split * (size_t)M * (size_t)N * sizeof(float) : 0;
+}
 
 cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {
   return launch(p, false, num_sms, stream);

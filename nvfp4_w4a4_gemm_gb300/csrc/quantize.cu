@@ -35,7 +35,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;            // row segments in flight per warp (MXFP4)
-constexpr int64_t kMaxMapK = 262144;  // dense per-block channel table in shared memory up to this K
+constexpr size_t kMaxTableBytes = 64 * 1024;  // channel bitmaps + prefixes kept in shared memory up to this size
+constexpr int kResStage = 256;                 // residual values staged per warp and row unit
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -152,19 +153,51 @@ struct QuantArgs {
   int use_map;              // dense: channel -> slot map in shared memory
 };
 
+// bf16 element j (0..15) of the 8 packed words of a block.
+__device__ __forceinline__ float bf16_elem(const uint4& r0, const uint4& r1, int j) {
+  const int q = j >> 1;
+  uint32_t wq = r0.x;
+  wq = q == 1 ? r0.y : wq;
+  wq = q == 2 ? r0.z : wq;
+  wq = q == 3 ? r0.w : wq;
+  wq = q == 4 ? r1.x : wq;
+  wq = q == 5 ? r1.y : wq;
+  wq = q == 6 ? r1.z : wq;
+  wq = q == 7 ? r1.w : wq;
+  return __uint_as_float((j & 1) ? (wq & 0xFFFF0000u) : (wq << 16));
+}
+
+// Residual x_j - E2M1(code_j) * d of element j of a quantized block.
+__device__ __forceinline__ __nv_bfloat16 block_residual(const uint4& r0, const uint4& r1, uint32_t lo, uint32_t hi,
+                                                        float d, int j) {
+  float dq = 0.f;
+  if (d != 0.f) {
+    const uint32_t word = j < 8 ? lo : hi;
+    const uint32_t h2 = cvt_e2m1x2_to_f16x2((word >> (8 * ((j & 7) >> 1))) & 0xFFu);
+    const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
+    dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
+  }
+  return __float2bfloat16_rn(__fsub_rn(bf16_elem(r0, r1, j), dq));
+}
+
 // Quantize one 16-element block owned by this thread (x[c .. c+16) of row r)
 // and emit its 8 code bytes, its scale byte (4 lanes' scales are gathered
 // into one 32-bit tile-layout store) and its residuals.
 template <bool kGrouped>
 __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw0, const uint4& raw1, int64_t r,
-                                            int64_t c, int lane, float g, int64_t n_cg, const uint32_t* s_tab,
-                                            const int32_t* s_chan, const int32_t* s_off, const int32_t* s_pbase) {
+                                            int64_t c, int lane, float g, int64_t n_cg, int64_t srow, int e,
+                                            const uint32_t* s_bits, const uint16_t* s_pref, int n_words,
+                                            const int32_t* s_chan, __nv_bfloat16* s_res, int res_base) {
   const bool valid = c < a.K;
   // block absmax on packed bf16 pairs (exact: a max of bf16 values)
-  const uint32_t w[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
-  __nv_bfloat162 m2 = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
-#pragma unroll
-  for (int i = 1; i < 8; ++i) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+  __nv_bfloat162 m2 = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.x));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.y)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.z)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.w)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.x)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.y)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.z)));
+  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.w)));
   const float am = fmaxf(__low2float(m2), __high2float(m2));
   // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
   const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
@@ -172,26 +205,15 @@ __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw
   const float d = __fmul_rn(e4m3_to_f32(sig), g);
   uint32_t lo = 0, hi = 0;
   if (d != 0.f) {
-    const float rcp = __fdiv_rn(1.0f, d);
+    const float rcp = __frcp_rn(d);
+    const uint32_t w0[4] = {raw0.x, raw0.y, raw0.z, raw0.w}, w1[4] = {raw1.x, raw1.y, raw1.z, raw1.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      lo |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w[i] << 16), rcp), __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), rcp))
+      lo |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w0[i] << 16), rcp), __fmul_rn(__uint_as_float(w0[i] & 0xFFFF0000u), rcp))
             << (8 * i);
-      hi |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w[4 + i] << 16), rcp),
-                       __fmul_rn(__uint_as_float(w[4 + i] & 0xFFFF0000u), rcp))
+      hi |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w1[i] << 16), rcp), __fmul_rn(__uint_as_float(w1[i] & 0xFFFF0000u), rcp))
             << (8 * i);
     }
-  }
-  int64_t srow = r;
-  int e = 0;
-  if (kGrouped) {
-    int l = 0, h = a.E;  // expert of row r: last e with offsets[e] <= r
-    while (h - l > 1) {
-      const int mid = (l + h) >> 1;
-      if (s_off[mid] <= r) l = mid; else h = mid;
-    }
-    e = l;
-    srow = (int64_t)s_pbase[e] + (r - s_off[e]);
   }
   if (valid) *reinterpret_cast<uint2*>(a.codes + r * (a.K / 2) + c / 2) = make_uint2(lo, hi);
   // gather the 4 block scales of a 64-element group into lane % 4 == 0
@@ -208,71 +230,89 @@ __device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw
     *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
   }
   if (!valid || a.k == 0) return;
-  // compensation residual x - E2M1(code) * d on the channels of S in [c, c+16)
-  auto resid_at = [&](int j, int slot) {
-    float dq = 0.f;
-    if (d != 0.f) {
-      const uint32_t word = j < 8 ? lo : hi;
-      const uint32_t h2 = cvt_e2m1x2_to_f16x2((word >> (8 * ((j & 7) >> 1))) & 0xFFu);
-      const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
-      dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
-    }
-    uint32_t wj = w[0];
-#pragma unroll
-    for (int q = 1; q < 8; ++q) if ((j >> 1) == q) wj = w[q];
-    const float xf = __uint_as_float((j & 1) ? (wj & 0xFFFF0000u) : (wj << 16));
-    a.resid[r * a.k + slot] = __float2bfloat16_rn(__fsub_rn(xf, dq));
-  };
-  if (!kGrouped && a.use_map) {
-    // per-block entry: bits 16..31 = which of the 16 channels are in S,
-    // bits 0..15 = slot of the block's first channel of S
-    const uint32_t ent = s_tab[c >> 4];
-    uint32_t mask = ent >> 16;
-    int slot = (int)(ent & 0xFFFFu);
+  // compensation residual on the channels of S in [c, c+16)
+  if (a.use_map) {
+    // the expert's channel bitmap: bit j%32 of word j/32 is set for j in S;
+    // slot of channel j = set bits before it (prefix count + popcount)
+    const int w = (int)(c >> 5);
+    const uint32_t bits = s_bits[e * n_words + w];
+    const int sh = (int)(c & 31);  // 0 or 16
+    uint32_t mask = (bits >> sh) & 0xFFFFu;
+    int slot = (int)s_pref[e * n_words + w] + (sh ? __popc(bits & 0xFFFFu) : 0);
     while (mask) {
       const int j = __ffs(mask) - 1;
-      resid_at(j, slot++);
+      const __nv_bfloat16 v = block_residual(raw0, raw1, lo, hi, d, j);
+      if (s_res != nullptr) s_res[slot - res_base] = v;  // staged; written out coalesced per row unit
+      else a.resid[r * a.k + slot] = v;
+      ++slot;
       mask &= mask - 1;
     }
   } else {
     const int32_t* S = s_chan + e * a.k;
     int i = lower_bound_i32(S, a.k, (int32_t)c);
-    for (; i < a.k && S[i] < c + 16; ++i) resid_at(S[i] - (int)c, i);
+    for (; i < a.k && S[i] < c + 16; ++i) a.resid[r * a.k + i] = block_residual(raw0, raw1, lo, hi, d, S[i] - (int)c);
   }
 }
 
 template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
   extern __shared__ __align__(16) int32_t smem_i32[];
-  // chan [E*k] | dense + map: per-block table [K/16] | grouped: offsets [E+1] | padded bases [E]
-  int32_t* s_chan = smem_i32;
-  uint32_t* s_tab = reinterpret_cast<uint32_t*>(s_chan + a.E * a.k);
-  int32_t* s_off = s_chan + a.E * a.k;
+  // offsets [E+1] | padded bases [E] | chan [E*k] (fallback only) |
+  // bitmap words [E][n_words] | prefix counts [E][n_words] (uint16)
+  const int n_words = (int)((a.K + 31) / 32);
+  int32_t* s_off = smem_i32;
   int32_t* s_pbase = s_off + (a.E + 1);
-  {
-    const int nchan = a.E * a.k;
-    for (int i = threadIdx.x; i < nchan; i += blockDim.x) s_chan[i] = a.chan[i];
-  }
-  if (!kGrouped && a.use_map) {
-    __syncthreads();
-    const int64_t nb = a.K / 16;
-    for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) {
-      int i = lower_bound_i32(s_chan, a.k, (int32_t)(b * 16));
-      const uint32_t first = (uint32_t)i;
-      uint32_t mask = 0;
-      for (; i < a.k && s_chan[i] < b * 16 + 16; ++i) mask |= 1u << (s_chan[i] - (int32_t)(b * 16));
-      s_tab[b] = (mask << 16) | (first & 0xFFFFu);
-    }
-  }
-  if (kGrouped) {
+  int32_t* s_chan = s_pbase + a.E;
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_chan + (a.use_map ? 0 : a.E * a.k));
+  uint16_t* s_pref = reinterpret_cast<uint16_t*>(s_bits + (a.use_map ? a.E * n_words : 0));
+  __nv_bfloat16* s_res_all = reinterpret_cast<__nv_bfloat16*>(
+      reinterpret_cast<uintptr_t>(s_pref + (a.use_map ? a.E * n_words : 0)) + 15 & ~uintptr_t(15));
+  if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int32_t base = 0;
-      for (int e = 0; e < a.E; ++e) {
-        s_pbase[e] = base;
-        base += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
+  if (a.use_map) {
+    // one warp per expert: clear its bitmap, set the bits of its channels,
+    // then prefix counts by a warp scan over per-lane word ranges
+    const int warp_id = threadIdx.x >> 5, ln = threadIdx.x & 31, n_wp = blockDim.x >> 5;
+    const int per = (n_words + 31) / 32;
+    for (int e = warp_id; e < a.E; e += n_wp) {
+      uint32_t* bits = s_bits + e * n_words;
+      for (int w = ln; w < n_words; w += 32) bits[w] = 0u;
+      __syncwarp();
+      for (int i = ln; i < a.k; i += 32) {
+        const int32_t j = a.chan[e * a.k + i];
+        if (j >= 0 && j < a.K) atomicOr(&bits[j >> 5], 1u << (j & 31));
       }
+      __syncwarp();
+      uint32_t cnt = 0;
+      for (int q = 0; q < per; ++q) {
+        const int w = ln * per + q;
+        if (w < n_words) cnt += __popc(bits[w]);
+      }
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (ln >= o) incl += v;
+      }
+      uint32_t run = incl - cnt;
+      for (int q = 0; q < per; ++q) {
+        const int w = ln * per + q;
+        if (w < n_words) {
+          s_pref[e * n_words + w] = (uint16_t)run;
+          run += __popc(bits[w]);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    for (int i = threadIdx.x; i < a.E * a.k; i += blockDim.x) s_chan[i] = a.chan[i];
+  }
+  __syncthreads();
+  if (kGrouped && threadIdx.x == 0) {
+    int32_t base = 0;
+    for (int e = 0; e < a.E; ++e) {
+      s_pbase[e] = base;
+      base += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
     }
   }
   float g;
@@ -311,11 +351,39 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
     uint4 nxt[4];
     if (nu < n_units) load_unit(nu, nxt);
     const uint32_t r = u / gpr, gi = u - r * gpr;
+    int64_t srow = r;
+    int e = 0;
+    if (kGrouped) {  // expert of row r: last e with offsets[e] <= r
+      int l = 0, hh = a.E;
+      while (hh - l > 1) {
+        const int mid = (l + hh) >> 1;
+        if (s_off[mid] <= (int32_t)r) l = mid; else hh = mid;
+      }
+      e = l;
+      srow = (int64_t)s_pbase[e] + ((int64_t)r - s_off[e]);
+    }
+    // residual slots of this row unit form one contiguous range [rb, re)
+    // (S is sorted): stage them per warp, then write the range coalesced
+    __nv_bfloat16* stage_buf = nullptr;
+    int rb = 0, re = 0;
+    if (a.use_map) {
+      const int w0 = (int)(gi * 32);
+      rb = s_pref[e * n_words + w0];
+      re = (w0 + 32 < n_words) ? (int)s_pref[e * n_words + w0 + 32] : a.k;
+      if (re - rb <= kResStage) stage_buf = s_res_all + (threadIdx.x >> 5) * kResStage;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if ((int64_t)gi * 1024 + h * 512 >= a.K) break;  // warp-uniform
       const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
-      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, s_tab, s_chan, s_off, s_pbase);
+      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, srow, e, s_bits, s_pref, n_words,
+                            s_chan, stage_buf, rb);
+    }
+    if (stage_buf != nullptr && re > rb) {
+      __syncwarp();
+      __nv_bfloat16* dst = a.resid + (int64_t)r * a.k;
+      for (int i = rb + lane; i < re; i += 32) dst[i] = stage_buf[i - rb];
+      __syncwarp();
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
@@ -688,34 +756,34 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
-  a.use_map = (offsets == nullptr && k > 0 && k < 65536 && K <= kMaxMapK) ? 1 : 0;
+  {
+    const size_t words = (size_t)((K + 31) / 32);
+    const size_t tab = (size_t)a.E * words * (sizeof(uint32_t) + sizeof(uint16_t));
+    a.use_map = (k > 0 && k < 65536 && tab <= kMaxTableBytes) ? 1 : 0;
+  }
   if (g_in == nullptr) {
     const int p = amax_partials_count(M, K, num_sms);
     amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
     a.partials = partials;
     a.n_partials = p;
   }
+  size_t smem = sizeof(int32_t) * (2 * (size_t)a.E + 1);
+  if (a.use_map)
+    smem += (size_t)a.E * (size_t)((K + 31) / 32) * (sizeof(uint32_t) + sizeof(uint16_t)) + 16 +
+            (size_t)(kThreads / 32) * kResStage * sizeof(__nv_bfloat16);
+  else smem += sizeof(int32_t) * (size_t)a.E * k;
+  const void* kern = offsets ? (const void*)nvfp4_quant_kernel<true> : (const void*)nvfp4_quant_kernel<false>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int64_t n_units = M * ((K + 1023) / 1024);
   int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, offsets ? (const void*)nvfp4_quant_kernel<true>
-                                                                     : (const void*)nvfp4_quant_kernel<false>,
-                                                    kThreads, 0) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  size_t smem = sizeof(int32_t) * ((size_t)a.E * k + (offsets ? 2 * a.E + 1 : 0));
-  if (a.use_map) smem += sizeof(uint32_t) * (size_t)(K / 16);
-  if (offsets != nullptr) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(nvfp4_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    nvfp4_quant_kernel<true><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
-  } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(nvfp4_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    nvfp4_quant_kernel<false><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
-  }
+  if (offsets != nullptr) nvfp4_quant_kernel<true><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
+  else nvfp4_quant_kernel<false><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
