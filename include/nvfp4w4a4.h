@@ -83,8 +83,11 @@ size_t nvfp4_quantize_workspace_bytes(void);
 
 /*
  * nvfp4_quantize -- online NVFP4 activation quantization plus the
- * compensation residual slice.  One pass over X (two when the tensor scale
- * is dynamic: an amax pre-pass, then the quantizer).
+ * compensation residual slice.  One pass over X with a static tensor scale.
+ * With a dynamic scale it is one cooperative launch that reads X twice: an
+ * amax phase, a grid-wide barrier, then the quantize phase (whose reads
+ * mostly hit L2).  The barrier wait is bounded; a CTA that gives up records
+ * a timeout (nvfp4_check_status) and writes nothing.
  *
  * Source: QUADS (arXiv 2607.15810) abstract (NVFP4 fine-grained scaling,
  * activations re-quantized online on the coarse E2M1 grid); gist.science
@@ -107,7 +110,11 @@ size_t nvfp4_quantize_workspace_bytes(void);
  * scales nvfp4_scale_bytes(M, K) bytes, tiled layout (16-byte aligned)
  * chan   device int32 [k], sorted ascending, unique, in [0, K); NULL if k == 0
  * resid  [M, k] bf16; NULL if k == 0
- * workspace / ws_bytes: >= nvfp4_quantize_workspace_bytes() when g_in == NULL
+ * workspace / ws_bytes: >= nvfp4_quantize_workspace_bytes() when g_in == NULL;
+ *        holds the amax partials and the grid barrier, so calls that may run
+ *        concurrently on the GPU need separate workspaces
+ * Errors: NVFP4_ERR_CUDA when the cooperative launch is refused (e.g. the
+ *        device cannot keep every CTA resident).
  */
 int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
                    uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid,

@@ -58,14 +58,20 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 const __nv_bfloat16* bf(const uint16_t* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 __nv_bfloat16* bf(uint16_t* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 
-constexpr size_t kQuantWs = sizeof(float) * nv4::kMaxAmaxPartials;
+constexpr size_t kQuantWs = nv4::kQuantWorkspaceBytes;
+
+unsigned int* quant_barrier(void* workspace) {
+  return workspace == nullptr
+             ? nullptr
+             : reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + nv4::kQuantBarrierOffset);
+}
 
 int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, uint8_t* scales,
                      const int32_t* chan, int32_t k, uint16_t* resid, int block) {
   if (M < 0 || K <= 0 || K % block != 0 || ldx < K || ldx % 8 != 0) return NVFP4_ERR_INVALID_ARG;
   if (K > (int64_t)1 << 30 || M > (int64_t)1 << 40) return NVFP4_ERR_UNSUPPORTED;
   // the quantizers index (row, 1024-column group) work units with 32 bits
-  if (M * ((K + 1023) / 1024) >= ((int64_t)1 << 32)) return NVFP4_ERR_UNSUPPORTED;
+  if (M * ((K + 1023) / 1024) >= ((int64_t)1 << 31)) return NVFP4_ERR_UNSUPPORTED;
   if (M == 0) return NVFP4_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) || !aligned(scales, 16))
     return NVFP4_ERR_INVALID_ARG;
@@ -127,8 +133,8 @@ int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const f
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   if (M == 0 && g_in != nullptr) return NVFP4_OK;
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M, K, ldx, g_in, g_out, codes, scales, chan, k, bf(resid),
-                                              nullptr, 1, static_cast<float*>(workspace), d->num_sms,
-                                              as_stream(stream)));
+                                              nullptr, 1, static_cast<float*>(workspace), quant_barrier(workspace),
+                                              d->num_sms, as_stream(stream)));
 }
 
 int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
@@ -145,8 +151,8 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
-                                              bf(resid), offsets, E, static_cast<float*>(workspace), d->num_sms,
-                                              as_stream(stream)));
+                                              bf(resid), offsets, E, static_cast<float*>(workspace),
+                                              quant_barrier(workspace), d->num_sms, as_stream(stream)));
 }
 
 int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* g_out, uint8_t* codes,

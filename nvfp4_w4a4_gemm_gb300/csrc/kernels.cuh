@@ -7,13 +7,17 @@
 namespace nv4 {
 
 constexpr int kMaxAmaxPartials = 2048;
+// Dynamic-scale quantizer scratch: amax partials, then the fused pass's grid
+// barrier words at this byte offset.
+constexpr size_t kQuantBarrierOffset = sizeof(float) * kMaxAmaxPartials;
+constexpr size_t kQuantWorkspaceBytes = kQuantBarrierOffset + 256;
 
 int amax_partials_count(int64_t M, int64_t K, int num_sms);
 
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  int num_sms, cudaStream_t stream);
+                                  unsigned int* bar, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);

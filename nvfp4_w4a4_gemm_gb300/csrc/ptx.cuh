@@ -250,6 +250,36 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
       : "f"(hi), "f"(lo));
   return out;
 }
+// 8 bf16 (4 packed words) times s2 = {s, s}: f32x2 multiplies, each product
+// rounded to nearest fp32, then E2M1 codes (RNE, satfinite) packed into one
+// word, element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t bf16x8_mul_e2m1(const uint4& w, uint64_t s2) {
+  uint32_t out;
+#define NV4_E2M1_PAIR(W, T)                                                   \
+  "shl.b32 lo, " W ", 16;\n\tand.b32 hi, " W ", 0xFFFF0000;\n\t"             \
+  "mov.b64 x, {lo, hi};\n\tmul.rn.f32x2 p, x, %5;\n\tmov.b64 {lo, hi}, p;\n\t" \
+  "cvt.rn.satfinite.e2m1x2.f32 " T ", hi, lo;\n\t"
+  asm("{\n\t.reg .b64 x, p;\n\t.reg .b32 lo, hi;\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      NV4_E2M1_PAIR("%1", "t0") NV4_E2M1_PAIR("%2", "t1") NV4_E2M1_PAIR("%3", "t2") NV4_E2M1_PAIR("%4", "t3")
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(out)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "l"(s2));
+#undef NV4_E2M1_PAIR
+  return out;
+}
+// Per-half max of magnitudes of two bf16 pairs (max.xorsign.abs: the result's
+// sign bits carry no meaning, its magnitudes are max(|a|, |b|)).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// 32-byte streaming global load (256-bit; the address must be 32-byte aligned).
+__device__ __forceinline__ void ldg_stream32(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
 // One byte of two E2M1 codes -> two exact halves (low nibble -> .x).
 __device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t out;

@@ -36,7 +36,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;            // row segments in flight per warp (MXFP4)
 constexpr size_t kMaxTableBytes = 64 * 1024;  // channel bitmaps + prefixes kept in shared memory up to this size
-constexpr int kResStage = 256;                 // residual values staged per warp and row unit
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -67,7 +66,7 @@ __device__ __forceinline__ uint64_t tile_group_offset(int64_t row, int64_t cg, i
 __device__ float tensor_scale_from_partials(const float* partials, int n) {
   __shared__ float red[kThreads / 32];
   float m = 0.f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partials[i]);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, __ldcg(partials + i));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -140,8 +139,9 @@ struct QuantArgs {
   const __nv_bfloat16* x;
   int64_t M, K, ldx;
   const float* g_in;        // static tensor scale, or nullptr
-  const float* partials;    // dynamic: amax partials
-  int n_partials;
+  float* partials;          // dynamic: pre-pass partials, or one slot per CTA (fused)
+  int n_partials;           // pre-pass partial count
+  unsigned int* bar;        // fused: grid barrier {arrivals (zero at launch), generation}
   float* g_out;             // may be nullptr
   uint8_t* codes;           // [M, K/2]
   uint8_t* scales;          // tiled
@@ -150,113 +150,292 @@ struct QuantArgs {
   __nv_bfloat16* resid;     // [M, k]
   const int32_t* offsets;   // grouped: [E+1] device, else nullptr
   int E;
-  int use_map;              // dense: channel -> slot map in shared memory
+  int use_map;              // channel bitmaps + prefix counts in shared memory
+  int vec32;                // rows start on 32-byte boundaries: 256-bit loads
 };
 
-// bf16 element j (0..15) of the 8 packed words of a block.
-__device__ __forceinline__ float bf16_elem(const uint4& r0, const uint4& r1, int j) {
-  const int q = j >> 1;
-  uint32_t wq = r0.x;
-  wq = q == 1 ? r0.y : wq;
-  wq = q == 2 ? r0.z : wq;
-  wq = q == 3 ? r0.w : wq;
-  wq = q == 4 ? r1.x : wq;
-  wq = q == 5 ? r1.y : wq;
-  wq = q == 6 ? r1.z : wq;
-  wq = q == 7 ? r1.w : wq;
-  return __uint_as_float((j & 1) ? (wq & 0xFFFF0000u) : (wq << 16));
+constexpr float kRcp6 = 0x1.555556p-3f;  // 1/6 rounded to nearest fp32
+
+// x / 6 rounded to nearest fp32 for a bf16 value x >= 2^-100: a product with
+// RN(1/6) and one fma correction step (Markstein's division refinement).
+// Exact for every bf16 significand (all 128 checked exhaustively against the
+// rational quotient).
+__device__ __forceinline__ float div6_rn(float x) {
+  const float q0 = __fmul_rn(x, kRcp6);
+  const float r = __fmaf_rn(-q0, 6.0f, x);
+  return __fmaf_rn(r, kRcp6, q0);
 }
 
-// Residual x_j - E2M1(code_j) * d of element j of a quantized block.
-__device__ __forceinline__ __nv_bfloat16 block_residual(const uint4& r0, const uint4& r1, uint32_t lo, uint32_t hi,
-                                                        float d, int j) {
-  float dq = 0.f;
-  if (d != 0.f) {
-    const uint32_t word = j < 8 ? lo : hi;
-    const uint32_t h2 = cvt_e2m1x2_to_f16x2((word >> (8 * ((j & 7) >> 1))) & 0xFFu);
-    const unsigned short h = (j & 1) ? (unsigned short)(h2 >> 16) : (unsigned short)(h2 & 0xFFFFu);
-    dq = __fmul_rn(__half2float(__ushort_as_half(h)), d);
-  }
-  return __float2bfloat16_rn(__fsub_rn(bf16_elem(r0, r1, j), dq));
+// E4M3 block-scale byte of a block with absmax am: E4M3((am / 6) / g) with
+// both divisions rounded to nearest in fp32, then RNE + satfinite.  The fast
+// path multiplies by yg = RN(1/g) instead of dividing; that product is within
+// 3 fp32 ulps of RN(q/g), so it selects the same E4M3 value unless it lies
+// within a few ulps of an E4M3 rounding midpoint (normal E4M3 range: fp32
+// patterns whose low 20 bits are 0x80000) or outside [2^-6, 2^20).  Those
+// blocks, and tensor scales outside [2^-100, 2^100], take the two IEEE
+// divisions.
+__device__ __noinline__ float scale_quotient_ieee(float am, float g) { return __fdiv_rn(__fdiv_rn(am, 6.0f), g); }
+
+__device__ __forceinline__ uint32_t block_scale_byte(float am, float g, float yg, bool fast) {
+  float t = __fmul_rn(div6_rn(am), yg);
+  const int dist = (int)(__float_as_uint(t) & 0xFFFFFu) - 0x80000;
+  const bool ok = fast && (am == 0.f || (am >= 0x1p-100f && t >= 0x1p-6f && t < 0x1p20f && abs(dist) > 8));
+  if (!ok) t = scale_quotient_ieee(am, g);
+  return cvt_e4m3(t);
 }
 
-// Quantize one 16-element block owned by this thread (x[c .. c+16) of row r)
-// and emit its 8 code bytes, its scale byte (4 lanes' scales are gathered
-// into one 32-bit tile-layout store) and its residuals.
-template <bool kGrouped>
-__device__ __forceinline__ void quant_block(const QuantArgs& a, const uint4& raw0, const uint4& raw1, int64_t r,
-                                            int64_t c, int lane, float g, int64_t n_cg, int64_t srow, int e,
-                                            const uint32_t* s_bits, const uint16_t* s_pref, int n_words,
-                                            const int32_t* s_chan, __nv_bfloat16* s_res, int res_base) {
-  const bool valid = c < a.K;
-  // block absmax on packed bf16 pairs (exact: a max of bf16 values)
-  __nv_bfloat162 m2 = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.x));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.y)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.z)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw0.w)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.x)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.y)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.z)));
-  m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&raw1.w)));
-  const float am = fmaxf(__low2float(m2), __high2float(m2));
-  // block scale: sigma = E4M3((a / 6) / g), d = sigma * g
-  const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), g);
-  const uint32_t sig = cvt_e4m3(t);
-  const float d = __fmul_rn(e4m3_to_f32(sig), g);
+// Running per-half magnitude maximum over the 4 packed words of v.
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, const uint4& v) {
+  return bf16x2_absmax(bf16x2_absmax(m, v.x), bf16x2_absmax(bf16x2_absmax(v.y, v.z), v.w));
+}
+
+// Largest magnitude of the two halves of a running magnitude maximum.
+__device__ __forceinline__ float absmax_of(uint32_t m) {
+  return fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
+}
+
+// Per-thread constants of the block-scale step.
+struct ScaleCtx {
+  float g, yg;
+  bool fast;
+  const float2* dr;  // shared: (d, 1/d) for every scale byte
+};
+
+// Quantize one 16-element block owned by this thread (`valid` = the block
+// lies inside the row): its 8 code bytes go to `code_ptr`, and the 4 scale
+// bytes of a 64-element group are gathered into one 32-bit store at
+// `scale_ptr` by lane % 4 == 0 (blocks past the row end contribute 0).
+// Returns the block's scale byte.
+__device__ __forceinline__ uint32_t quant_block(const uint4& raw0, const uint4& raw1, bool valid, int lane,
+                                                const ScaleCtx& sc, uint8_t* code_ptr, uint8_t* scale_ptr) {
+  // block absmax (exact: a max of bf16 magnitudes)
+  const float am = absmax_of(absmax8(absmax8(raw0.x, raw0), raw1));
+  uint32_t sig = block_scale_byte(am, sc.g, sc.yg, sc.fast);
+  sig = valid ? sig : 0u;
+  const float2 dr = sc.dr[sig];
   uint32_t lo = 0, hi = 0;
-  if (d != 0.f) {
-    const float rcp = __frcp_rn(d);
-    const uint32_t w0[4] = {raw0.x, raw0.y, raw0.z, raw0.w}, w1[4] = {raw1.x, raw1.y, raw1.z, raw1.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      lo |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w0[i] << 16), rcp), __fmul_rn(__uint_as_float(w0[i] & 0xFFFF0000u), rcp))
-            << (8 * i);
-      hi |= cvt_e2m1x2(__fmul_rn(__uint_as_float(w1[i] << 16), rcp), __fmul_rn(__uint_as_float(w1[i] & 0xFFFF0000u), rcp))
-            << (8 * i);
-    }
+  if (dr.x != 0.f) {
+    const uint64_t s2 = ((uint64_t)__float_as_uint(dr.y) << 32) | __float_as_uint(dr.y);
+    lo = bf16x8_mul_e2m1(raw0, s2);
+    hi = bf16x8_mul_e2m1(raw1, s2);
   }
-  if (valid) *reinterpret_cast<uint2*>(a.codes + r * (a.K / 2) + c / 2) = make_uint2(lo, hi);
-  // gather the 4 block scales of a 64-element group into lane % 4 == 0
+  if (valid) *reinterpret_cast<uint2*>(code_ptr) = make_uint2(lo, hi);
   const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 1);
   const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 2);
   const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 3);
-  if ((lane & 3) == 0 && valid) {
-    const int64_t blk = c / 16;  // multiple of 4
-    const int64_t nb = a.K / 16;
-    uint32_t word = sig;
-    if (blk + 1 < nb) word |= s1 << 8;
-    if (blk + 2 < nb) word |= s2 << 16;
-    if (blk + 3 < nb) word |= s3 << 24;
-    *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(srow, blk / 4, n_cg)) = word;
+  if ((lane & 3) == 0 && valid)
+    *reinterpret_cast<uint32_t*>(scale_ptr) = sig | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  return sig;
+}
+
+// Compensation residual of one element: x - E2M1(RN(x * rcp)) * d, rounded
+// to bf16 (0-scale blocks have code 0).  The code is the one the block
+// quantizer wrote for this element: the same fp32 product and conversion.
+__device__ __forceinline__ __nv_bfloat16 element_residual(float x, float d, float rcp) {
+  float dq = 0.f;
+  if (d != 0.f) {
+    const uint32_t h2 = cvt_e2m1x2_to_f16x2(cvt_e2m1x2(__fmul_rn(x, rcp), 0.f));
+    dq = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
   }
-  if (!valid || a.k == 0) return;
-  // compensation residual on the channels of S in [c, c+16)
-  if (a.use_map) {
-    // the expert's channel bitmap: bit j%32 of word j/32 is set for j in S;
-    // slot of channel j = set bits before it (prefix count + popcount)
-    const int w = (int)(c >> 5);
-    const uint32_t bits = s_bits[e * n_words + w];
-    const int sh = (int)(c & 31);  // 0 or 16
-    uint32_t mask = (bits >> sh) & 0xFFFFu;
-    int slot = (int)s_pref[e * n_words + w] + (sh ? __popc(bits & 0xFFFFu) : 0);
-    while (mask) {
-      const int j = __ffs(mask) - 1;
-      const __nv_bfloat16 v = block_residual(raw0, raw1, lo, hi, d, j);
-      if (s_res != nullptr) s_res[slot - res_base] = v;  // staged; written out coalesced per row unit
-      else a.resid[r * a.k + slot] = v;
-      ++slot;
-      mask &= mask - 1;
+  return __float2bfloat16_rn(__fsub_rn(x, dq));
+}
+
+// Grid-wide barrier of a cooperative launch, bounded by the wait limit.
+// bar[0] counts arrivals (zero at launch; the last CTA to arrive resets it),
+// bar[1] is a generation number that the last CTA advances.  Returns false in
+// every thread of a CTA that gave up waiting.
+__device__ bool grid_barrier(unsigned int* bar) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    volatile unsigned int* gen = bar + 1;
+    const unsigned int gen0 = *gen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = globaltimer();
+      const uint64_t limit = g_wait_limit_ns;
+      while (*gen == gen0) {
+        if (globaltimer() - t0 > limit) {
+          report_error(kDevErrTimeout, 20);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
     }
-  } else {
-    const int32_t* S = s_chan + e * a.k;
-    int i = lower_bound_i32(S, a.k, (int32_t)c);
-    for (; i < a.k && S[i] < c + 16; ++i) a.resid[r * a.k + i] = block_residual(raw0, raw1, lo, hi, d, S[i] - (int)c);
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Walk over the work units of one warp: unit u = row r x columns
+// [1024 gi, 1024 gi + 1024), units u, u + n_warps, ... (no division per step).
+struct UnitWalk {
+  uint32_t u, r, gi;
+  uint32_t n_units, n_warps, gpr, dr, dg;
+  __device__ __forceinline__ void next() {
+    u += n_warps;
+    r += dr;
+    gi += dg;
+    if (gi >= gpr) { gi -= gpr; ++r; }
+  }
+  __device__ __forceinline__ void prev() {
+    u -= n_warps;
+    r -= dr;
+    if (gi < dg) { gi += gpr; --r; }
+    gi -= dg;
+  }
+};
+
+// Load this lane's 32 bf16 of unit (r, gi): 2 blocks of 16 (zero past K).
+__device__ __forceinline__ void load_unit(const QuantArgs& a, uint32_t r, uint32_t gi, int lane, uint4 (&v)[4]) {
+  const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx + (int64_t)gi * 1024 + lane * 16;
+  const int cols = (int)((a.K - (int64_t)gi * 1024) < 1024 ? (a.K - (int64_t)gi * 1024) : 1024);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    v[2 * h] = make_uint4(0, 0, 0, 0);
+    v[2 * h + 1] = make_uint4(0, 0, 0, 0);
+    if (h * 512 + lane * 16 < cols) {
+      if (a.vec32) {
+        ldg_stream32(row + h * 512, v[2 * h], v[2 * h + 1]);
+      } else {
+        v[2 * h] = ldg_stream(row + h * 512);
+        v[2 * h + 1] = ldg_stream(row + h * 512 + 8);
+      }
+    }
   }
 }
 
-template <bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
+// Largest |x| over the units of this warp, visited last to first (so the
+// units the quantize pass visits first are the ones read most recently),
+// two units' loads in flight at a time.
+__device__ float warp_units_amax(const QuantArgs& a, UnitWalk w, int lane) {
+  uint32_t m2 = 0u;
+  if (w.u < w.n_units) {
+    uint32_t left = (w.n_units - 1 - w.u) / w.n_warps + 1;  // units of this warp
+    w.u += (left - 1) * w.n_warps;
+    w.r = w.u / w.gpr;
+    w.gi = w.u - w.r * w.gpr;
+    for (; left >= 2; left -= 2) {
+      uint4 v[4], v2[4];
+      load_unit(a, w.r, w.gi, lane, v);
+      w.prev();
+      load_unit(a, w.r, w.gi, lane, v2);
+      w.prev();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m2 = absmax8(m2, v[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m2 = absmax8(m2, v2[i]);
+    }
+    if (left == 1) {
+      uint4 v[4];
+      load_unit(a, w.r, w.gi, lane, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m2 = absmax8(m2, v[i]);
+    }
+  }
+  float m = absmax_of(m2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// Shared-memory tables of the quantize pass.
+struct QTables {
+  const int32_t* off;    // grouped: offsets [E+1]
+  const int32_t* pbase;  // grouped: first padded scale row of each expert [E]
+  const int32_t* chan;   // channel lists [E][k] (when there are no prefix tables)
+  const uint16_t* pref;  // per-expert prefix counts of the channel bitmaps [E][n_words]
+  int n_words;
+};
+
+// Loads of unit (r, gi); kFull: K % 1024 == 0 and 32-byte aligned rows, so
+// every lane's two blocks are inside the row.
+template <bool kFull>
+__device__ __forceinline__ void load_unit_t(const QuantArgs& a, uint32_t r, uint32_t gi, int lane, uint4 (&v)[4]) {
+  if (kFull) {
+    const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx + (int64_t)gi * 1024 + lane * 16;
+    ldg_stream32(row, v[0], v[1]);
+    ldg_stream32(row + 512, v[2], v[3]);
+  } else {
+    load_unit(a, r, gi, lane, v);
+  }
+}
+
+// Quantize the two blocks of unit (r, gi) held in v, then the unit's
+// compensation residuals: the slots [rb, re) of the row's sorted channel list
+// that fall in the unit's columns, one slot per lane (the element is re-read,
+// from L2, and its block's scale byte fetched from the owning lane).
+template <bool kGrouped, bool kFull>
+__device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v)[4], uint32_t r, uint32_t gi,
+                                             int lane, const ScaleCtx& sc, const QTables& t, int64_t n_cg) {
+  int64_t srow = r;
+  int e = 0;
+  if (kGrouped) {  // expert of row r: last e with offsets[e] <= r
+    int l = 0, hh = a.E;
+    while (hh - l > 1) {
+      const int mid = (l + hh) >> 1;
+      if (t.off[mid] <= (int32_t)r) l = mid; else hh = mid;
+    }
+    e = l;
+    srow = (int64_t)t.pbase[e] + ((int64_t)r - t.off[e]);
+  }
+  const int64_t col0 = (int64_t)gi * 1024;
+  const int cols = kFull ? 1024 : (int)((a.K - col0) < 1024 ? (a.K - col0) : 1024);
+  uint8_t* code_ptr = a.codes + (int64_t)r * (a.K / 2) + (int64_t)gi * 512 + lane * 8;
+  uint8_t* scale_ptr = a.scales + tile_group_offset(srow, (int64_t)gi * 16, n_cg) + (lane >> 2) * 512;
+  uint32_t sig[2] = {0u, 0u};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (!kFull && h * 512 >= cols) break;  // warp-uniform
+    sig[h] = quant_block(v[2 * h], v[2 * h + 1], kFull || h * 512 + lane * 16 < cols, lane, sc, code_ptr + h * 256,
+                         scale_ptr + h * 8 * 512);
+  }
+  if (a.k == 0) return;
+  int rb, re;
+  const int32_t* S;
+  if (a.use_map) {
+    const int w0 = (int)(gi * 32);
+    rb = t.pref[e * t.n_words + w0];
+    re = (w0 + 32 < t.n_words) ? (int)t.pref[e * t.n_words + w0 + 32] : a.k;
+    S = a.chan + (int64_t)e * a.k;
+  } else {
+    S = t.chan + e * a.k;
+    rb = lower_bound_i32(S, a.k, (int32_t)col0);
+    re = lower_bound_i32(S, a.k, (int32_t)(col0 + cols));
+  }
+  const __nv_bfloat16* xrow = a.x + (int64_t)r * a.ldx;
+  __nv_bfloat16* rrow = a.resid + (int64_t)r * a.k;
+  for (int base = rb; base < re; base += 32) {  // warp-uniform
+    const int i = base + lane;
+    const bool act = i < re;
+    const int32_t j = act ? S[i] : (int32_t)col0;
+    const bool in = j >= col0 && j < col0 + cols;  // false only for a malformed list
+    const int blk = in ? (int)((j - col0) >> 4) : 0;
+    const uint32_t s0 = __shfl_sync(0xffffffffu, sig[0], blk & 31);
+    const uint32_t s1 = __shfl_sync(0xffffffffu, sig[1], blk & 31);
+    if (act) {
+      __nv_bfloat16 val = __float2bfloat16_rn(0.f);
+      if (in) {
+        const float2 dr = sc.dr[blk >= 32 ? s1 : s0];
+        val = element_residual(__bfloat162float(xrow[j]), dr.x, dr.y);
+      }
+      rrow[i] = val;
+    }
+  }
+}
+
+template <bool kGrouped, bool kFused, bool kFull>
+__global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   extern __shared__ __align__(16) int32_t smem_i32[];
+  __shared__ float2 s_dr[256];
   // offsets [E+1] | padded bases [E] | chan [E*k] (fallback only) |
   // bitmap words [E][n_words] | prefix counts [E][n_words] (uint16)
   const int n_words = (int)((a.K + 31) / 32);
@@ -265,8 +444,35 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
   int32_t* s_chan = s_pbase + a.E;
   uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_chan + (a.use_map ? 0 : a.E * a.k));
   uint16_t* s_pref = reinterpret_cast<uint16_t*>(s_bits + (a.use_map ? a.E * n_words : 0));
-  __nv_bfloat16* s_res_all = reinterpret_cast<__nv_bfloat16*>(
-      reinterpret_cast<uintptr_t>(s_pref + (a.use_map ? a.E * n_words : 0)) + 15 & ~uintptr_t(15));
+  const int lane = threadIdx.x & 31;
+  UnitWalk walk;
+  walk.gpr = (uint32_t)((a.K + 1023) / 1024);
+  walk.n_units = (uint32_t)(a.M * walk.gpr);
+  walk.n_warps = (gridDim.x * blockDim.x) >> 5;
+  walk.dr = walk.n_warps / walk.gpr;
+  walk.dg = walk.n_warps - walk.dr * walk.gpr;
+  walk.u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  walk.r = walk.u / walk.gpr;
+  walk.gi = walk.u - walk.r * walk.gpr;
+
+  float g;
+  if (kFused) {
+    // tensor amax of this launch: per-CTA maxima, one grid barrier, then
+    // every CTA reduces all of them (the quantize pass below re-reads X,
+    // mostly from L2)
+    __shared__ float red[kThreads / 32];
+    const float m = warp_units_amax(a, walk, lane);
+    if (lane == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.f;
+      for (int i = 0; i < kThreads / 32; ++i) b = fmaxf(b, red[i]);
+      a.partials[blockIdx.x] = b;
+    }
+    if (!grid_barrier(a.bar)) return;
+    g = tensor_scale_from_partials(a.partials, (int)gridDim.x);
+  }
+
   if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
   if (a.use_map) {
@@ -315,79 +521,44 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quant_kernel(QuantArgs a) {
       base += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
     }
   }
-  float g;
-  if (a.g_in != nullptr) {
-    g = *a.g_in;
-    __syncthreads();
-  } else {
-    g = tensor_scale_from_partials(a.partials, a.n_partials);  // contains __syncthreads
+  if (!kFused) {
+    if (a.g_in != nullptr) g = *a.g_in;
+    else g = tensor_scale_from_partials(a.partials, a.n_partials);  // contains __syncthreads
   }
+  // (d, 1/d) of every scale byte under this tensor scale
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    const float d = __fmul_rn(e4m3_to_f32((uint32_t)i), g);
+    s_dr[i] = make_float2(d, d != 0.f ? __frcp_rn(d) : 0.f);
+  }
+  __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.g_out != nullptr) *a.g_out = g;
+  ScaleCtx sc;
+  sc.g = g;
+  sc.yg = __frcp_rn(g);
+  sc.fast = g >= 0x1p-100f && g <= 0x1p100f;
+  sc.dr = s_dr;
 
-  // work unit = one row x 1024 columns: each lane owns 2 blocks of 16
-  const int lane = threadIdx.x & 31;
-  const uint32_t gpr = (uint32_t)((a.K + 1023) / 1024);
-  const uint32_t n_units = (uint32_t)(a.M * gpr);
-  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+  // work unit = one row x 1024 columns: each lane owns 2 blocks of 16.
+  // Two register buffers alternate: the next unit's loads are in flight
+  // while the current one is quantized.
   const int64_t n_cg = (a.K / 16 + 3) / 4;
-
-  auto load_unit = [&](uint32_t uu, uint4 (&v)[4]) {
-    const uint32_t r = uu / gpr, gi = uu - r * gpr;
-    const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
-      const bool ok = c < a.K;
-      v[2 * h] = ok ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
-      v[2 * h + 1] = ok ? ldg_stream(row + c + 8) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  uint32_t u = warp_global;
-  uint4 cur[4];
-  if (u < n_units) load_unit(u, cur);
-  while (u < n_units) {
-    const uint32_t nu = u + n_warps;
-    uint4 nxt[4];
-    if (nu < n_units) load_unit(nu, nxt);
-    const uint32_t r = u / gpr, gi = u - r * gpr;
-    int64_t srow = r;
-    int e = 0;
-    if (kGrouped) {  // expert of row r: last e with offsets[e] <= r
-      int l = 0, hh = a.E;
-      while (hh - l > 1) {
-        const int mid = (l + hh) >> 1;
-        if (s_off[mid] <= (int32_t)r) l = mid; else hh = mid;
-      }
-      e = l;
-      srow = (int64_t)s_pbase[e] + ((int64_t)r - s_off[e]);
-    }
-    // residual slots of this row unit form one contiguous range [rb, re)
-    // (S is sorted): stage them per warp, then write the range coalesced
-    __nv_bfloat16* stage_buf = nullptr;
-    int rb = 0, re = 0;
-    if (a.use_map) {
-      const int w0 = (int)(gi * 32);
-      rb = s_pref[e * n_words + w0];
-      re = (w0 + 32 < n_words) ? (int)s_pref[e * n_words + w0 + 32] : a.k;
-      if (re - rb <= kResStage) stage_buf = s_res_all + (threadIdx.x >> 5) * kResStage;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if ((int64_t)gi * 1024 + h * 512 >= a.K) break;  // warp-uniform
-      const int64_t c = (int64_t)gi * 1024 + h * 512 + lane * 16;
-      quant_block<kGrouped>(a, cur[2 * h], cur[2 * h + 1], r, c, lane, g, n_cg, srow, e, s_bits, s_pref, n_words,
-                            s_chan, stage_buf, rb);
-    }
-    if (stage_buf != nullptr && re > rb) {
-      __syncwarp();
-      __nv_bfloat16* dst = a.resid + (int64_t)r * a.k;
-      for (int i = rb + lane; i < re; i += 32) dst[i] = stage_buf[i - rb];
-      __syncwarp();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
-    u = nu;
+  QTables t;
+  t.off = s_off; t.pbase = s_pbase; t.chan = s_chan; t.pref = s_pref;
+  t.n_words = n_words;
+  const uint32_t n = walk.n_units;
+  uint4 va[4], vb[4];
+  UnitWalk wa = walk;
+  if (wa.u < n) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+  while (wa.u < n) {
+    UnitWalk wb = wa;
+    wb.next();
+    if (wb.u < n) load_unit_t<kFull>(a, wb.r, wb.gi, lane, vb);
+    process_unit<kGrouped, kFull>(a, va, wa.r, wa.gi, lane, sc, t, n_cg);
+    if (wb.u >= n) break;
+    wa = wb;
+    wa.next();
+    if (wa.u < n) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+    process_unit<kGrouped, kFull>(a, vb, wb.r, wb.gi, lane, sc, t, n_cg);
   }
 }
 
@@ -750,7 +921,7 @@ int amax_partials_count(int64_t M, int64_t K, int num_sms) {
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  int num_sms, cudaStream_t stream) {
+                                  unsigned int* bar, int num_sms, cudaStream_t stream) {
   if (M == 0) { k = 0; chan = nullptr; resid = nullptr; }
   QuantArgs a{};
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
@@ -761,19 +932,29 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
     const size_t tab = (size_t)a.E * words * (sizeof(uint32_t) + sizeof(uint16_t));
     a.use_map = (k > 0 && k < 65536 && tab <= kMaxTableBytes) ? 1 : 0;
   }
-  if (g_in == nullptr) {
+  a.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
+  const bool fused = g_in == nullptr && bar != nullptr;
+  if (g_in == nullptr && !fused) {
     const int p = amax_partials_count(M, K, num_sms);
     amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
-    a.partials = partials;
     a.n_partials = p;
   }
+  a.partials = partials;
+  a.bar = bar;
   size_t smem = sizeof(int32_t) * (2 * (size_t)a.E + 1);
-  if (a.use_map)
-    smem += (size_t)a.E * (size_t)((K + 31) / 32) * (sizeof(uint32_t) + sizeof(uint16_t)) + 16 +
-            (size_t)(kThreads / 32) * kResStage * sizeof(__nv_bfloat16);
+  if (a.use_map) smem += (size_t)a.E * (size_t)((K + 31) / 32) * (sizeof(uint32_t) + sizeof(uint16_t));
   else smem += sizeof(int32_t) * (size_t)a.E * k;
-  const void* kern = offsets ? (const void*)nvfp4_quant_kernel<true> : (const void*)nvfp4_quant_kernel<false>;
-  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool full = a.vec32 && (K % 1024) == 0;
+  const void* kerns[2][2][2] = {
+      {{(const void*)nvfp4_quant_kernel<false, false, false>, (const void*)nvfp4_quant_kernel<false, false, true>},
+       {(const void*)nvfp4_quant_kernel<false, true, false>, (const void*)nvfp4_quant_kernel<false, true, true>}},
+      {{(const void*)nvfp4_quant_kernel<true, false, false>, (const void*)nvfp4_quant_kernel<true, false, true>},
+       {(const void*)nvfp4_quant_kernel<true, true, false>, (const void*)nvfp4_quant_kernel<true, true, true>}}};
+  const void* kern = kerns[offsets != nullptr][fused][full];
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t n_units = M * ((K + 1023) / 1024);
   int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
   int per_sm = 0;
@@ -781,10 +962,17 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
     per_sm = 1;
   const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
+  if (fused && blocks > kMaxAmaxPartials) blocks = kMaxAmaxPartials;
   if (blocks < 1) blocks = 1;
-  if (offsets != nullptr) nvfp4_quant_kernel<true><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
-  else nvfp4_quant_kernel<false><<<(unsigned)blocks, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  if (fused) {
+    // every CTA must be resident for the in-kernel grid barrier
+    cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    void* args[] = {&a};
+    return cudaLaunchCooperativeKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, smem, stream);
+  }
+  void* args[] = {&a};
+  return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, smem, stream);
 }
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
@@ -880,7 +1068,7 @@ cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int
   const cudaError_t err = noalloc_partials(&partials);
   if (err != cudaSuccess) return err;
   return launch_nvfp4_quantize(x, M, K, ldx, nullptr, g_out, codes, scales, chan, k, resid, nullptr, 1, partials,
-                               num_sms, stream);
+                               nullptr, num_sms, stream);
 }
 
 }  // namespace nv4
