@@ -121,6 +121,72 @@ def test_exhaustive_e4m3_block_scales_of_bf16(nv):
     _check_nvfp4(nv, torch.from_numpy(F.bf16_round(x.reshape(-1, 64))).to(torch.bfloat16))
 
 
+def _g_values():
+    """Static tensor scales that stress the block-scale step: exact powers of
+    two (E4M3 midpoints reached exactly), all-ones significands, thirds, the
+    edges of the reciprocal-multiply range [2^-100, 2^100] and just outside
+    it, and seeded random scales over 2^-40 .. 2^40."""
+    fixed = [1.0, 0.125, 0.75, 2.0 ** -100, 2.0 ** -101, 2.0 ** 100, 2.0 ** 101, 2.0 ** -20, 2.0 ** 17,
+             float(np.float32(1.0) / np.float32(3.0)), float(np.float32(1.0) / np.float32(2688.0))]
+    ones = [float(np.array([b], np.uint32).view(np.float32)[0]) for b in (0x3F7FFFFF, 0x43FFFFFF, 0x2E7FFFFF)]
+    rng = np.random.default_rng(11)
+    exps = rng.integers(127 - 40, 127 + 40, 10).astype(np.uint32)
+    mants = rng.integers(0, 1 << 23, 10).astype(np.uint32)
+    rand = [float(v) for v in ((exps << 23) | mants).view(np.float32)]
+    return fixed + ones + rand
+
+
+@pytest.mark.parametrize("g", _g_values())
+def test_block_scales_every_bf16_max_static_g(nv, g):
+    # every positive finite bf16 value is the maximum of one block, under a
+    # static tensor scale g: scale bytes and codes bit-exact with the oracle
+    # (maxima whose quotient (a / 6) / g overflows fp32 are left out: the
+    # scale step is defined for finite quotients only)
+    bits = np.arange(1, 0x7F80, dtype=np.uint32).astype(np.uint16)
+    a = F.bf16_from_bits(bits)
+    a = a[np.isfinite(a) & (a > 0) & (a.astype(np.float64) / 6.0 / g < 2.0 ** 127)]
+    n = -(-len(a) // 64) * 64
+    col = np.zeros(n, np.float32)
+    col[: len(a)] = a
+    x = np.zeros((n, 16), np.float32)
+    x[:, 0] = col
+    x[:, 5] = -col * np.float32(0.37)
+    x[:, 11] = col * np.float32(0.61)
+    _check_nvfp4(nv, torch.from_numpy(F.bf16_round(x.reshape(-1, 1024))).to(torch.bfloat16), g=g)
+
+
+def test_clustered_channel_set(nv):
+    # whole blocks of compensated channels (16 per block, 80 slots in one
+    # 1024-column unit: several passes of the warp over the unit's slots)
+    # plus scattered ones; ragged row count
+    rng = np.random.default_rng(21)
+    M, K = 203, 2048
+    chan = np.sort(np.concatenate([np.arange(32, 112), np.arange(1040, 1056), rng.choice(np.arange(1200, 2048), 24,
+                                                                                         replace=False)]))
+    x = W.activations(M, K, 20, "t3x20", 5, 6)
+    _check_nvfp4(nv, x, chan=chan.astype(np.int32))
+
+
+def test_grouped_quantize_channel_lists_without_prefix_tables(nv):
+    # 100 experts x K = 4096: the per-expert channel bitmaps would not fit in
+    # shared memory, so each unit finds its slots by binary search
+    rng = np.random.default_rng(22)
+    E, K, k = 100, 4096, 16
+    sizes = rng.integers(0, 9, E)
+    sizes[3] = 0
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = W.activations(int(offs[-1]), K, 10, "t3x20", 7, 8)
+    chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
+    q = nv.nvfp4_quantize_grouped(x.cuda(), torch.from_numpy(offs).cuda(), torch.from_numpy(chan).cuda())
+    torch.cuda.synchronize()
+    ref = onv.quantize_grouped(f32(x), offs, chan)
+    assert f32(q["g"])[0] == ref["g"]
+    assert np.array_equal(u8(q["codes"]), ref["packed"])
+    sc = gather_scales(q["scales"], onv.grouped_scale_tile_offsets(offs, K // 16))
+    assert np.array_equal(sc, ref["sigma"])
+    assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(ref["resid"]))
+
+
 def test_grouped_quantize(nv):
     d = W.moe_inputs(with_weights=False, which=("gate_up",))
     offs = d["offsets"].numpy()
