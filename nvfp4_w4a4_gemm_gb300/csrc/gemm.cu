@@ -63,7 +63,7 @@ static_assert(kColSf + 32 * kStages <= kTmemCols, "TMEM budget");
 
 enum WaitSite : uint32_t {
   kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6,
-  kWaitSfFull = 7, kWaitSfDrain = 8
+  kWaitSfFull = 7, kWaitSfDrain = 8, kWaitSfFull2 = 9
 };
 
 struct GemmParams {
@@ -86,6 +86,7 @@ struct GemmParams {
   int grouped;
   int split;        // narrow kernel: K splits per tile (1 = none)
   float* partial;   // split > 1: fp32 partial sums [split][M][N]
+  int y_vec32;      // Y rows start on 32-byte boundaries: 256-bit stores
 };
 
 struct Tile {
@@ -483,10 +484,13 @@ __global__ void __launch_bounds__(256) splitk_finalize_kernel(const float* __res
 // the compensation term accumulates into the main accumulator: its residual
 // tile is pre-scaled in shared memory by c = 1/g_a (1/(g_a g_b) with BF16
 // weight columns) by a transform warp, and the epilogue applies g_a g_b once.
+// The scale copies of a k-tile are split over two warps (A + B rows 0..127,
+// B rows 128..255): copies issued from different warps proceed side by side.
 // Eight epilogue warps drain the accumulator quickly (two per TMEM lane
-// quarter, 128 columns each) and release it before storing.
-//   warp 0 TMA | warp 1 MMA | warp 2 scale copies | warp 3 residual scaling |
-//   warps 4..11 epilogue
+// quarter, 128 columns each), release it, then store with 256-bit stores
+// (whole 32-byte sectors per lane).
+//   warp 0 TMA | warp 1 MMA | warp 2 scale copies (A, B low) |
+//   warp 3 scale copies (B high) + residual scaling | warps 4..11 epilogue
 constexpr int BNW = 256;
 constexpr int kWStages = 4;
 constexpr int kWTileA = BM * BKB;               // 16 KB
@@ -552,7 +556,8 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint64_t* sf_drain = drain + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint64_t* sf_full2 = sf_drain + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_full2 + kWStages);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
@@ -584,6 +589,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       mbar_init(&empty[i], 1);
       mbar_init(&sf_full[i], 1);
       mbar_init(&comp_ready[i], 1);
+      mbar_init(&sf_full2[i], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -672,6 +678,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
         tc_fence_after();
         for (int kt = 0; kt < n_kt && ok; ++kt) {
           if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
+          if (!mbar_wait(&sf_full2[stage], phase, kWaitSfFull2, s_abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
           const uint32_t sb = sa + kWTileA;
@@ -735,7 +742,6 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
             for (int c = 0; c < nch; ++c) {
               tmem_cp_32x128b_x4(t_sfa + 4u * c, desc_sf(sfa + 512u * c));
               tmem_cp_32x128b_x4(t_sfb + 8u * c, desc_sf(sfb + 512u * c));
-              tmem_cp_32x128b_x4(t_sfb + 8u * c + 4u, desc_sf(sfb + 2048u + 512u * c));
             }
             tc_commit(&sf_full[stage]);
           }
@@ -746,12 +752,12 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       mbar_wait(sf_drain, 0, kWaitSfDrain, nullptr);
     }
   } else if (warp == 3) {
-    // ----------------------------------------- residual pre-scaling ----
+    // ------------ second half of B's scale copies + residual pre-scaling ----
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     const float ga = p.g_a ? *p.g_a : 1.f;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok && n_ct > 0; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       int e = 0;
       if (p.grouped) {
         Tile tl;
@@ -765,8 +771,19 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
         if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
         if (kt < n_kt) {
+          // scale chunks of B rows 128..255 (copies from a second warp run
+          // alongside the first warp's)
           __syncwarp();
-          if (lane == 0) mbar_arrive(&comp_ready[stage]);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t sfb = smem_u32(stages + stage * kWStageBytes) + (uint32_t)(kWTileA + kWTileB + kWSfA);
+            const uint32_t t_sfb = tmem + kWColSf + (uint32_t)stage * 48u + 16u;
+            const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+            const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+            for (int c = 0; c < nch; ++c) tmem_cp_32x128b_x4(t_sfb + 8u * c + 4u, desc_sf(sfb + 2048u + 512u * c));
+            tc_commit(&sf_full2[stage]);
+            mbar_arrive(&comp_ready[stage]);
+          }
         } else {
           uint4* ra = reinterpret_cast<uint4*>(stages + stage * kWStageBytes);
 #pragma unroll 4
@@ -783,7 +800,10 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&comp_ready[stage]);
+          if (lane == 0) {
+            mbar_arrive(&comp_ready[stage]);
+            mbar_arrive(&sf_full2[stage]);
+          }
         }
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
@@ -824,10 +844,16 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       if (lane == 0) mbar_arrive(acc_empty);   // accumulator free: the next tile's MMAs may start
       const int64_t col0 = tl.n0 + h * 128;
       if (r < tl.rows && col0 < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.y + (tl.row0 + r) * p.N + col0);
+        __nv_bfloat16* dst = p.y + (tl.row0 + r) * p.N + col0;
+        if (p.y_vec32) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) stg_256(dst + 16 * i, &packed[8 * i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            reinterpret_cast<uint4*>(dst)[i] =
+                make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
       }
     }
   }
@@ -1009,6 +1035,7 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   p.E = E;
   p.offsets = pr.offsets;
   p.grouped = grouped ? 1 : 0;
+  p.y_vec32 = ((reinterpret_cast<uintptr_t>(pr.y) & 31u) == 0 && (pr.N % 16) == 0) ? 1 : 0;
   const int64_t n_tiles_n = (pr.N + BNW - 1) / BNW;
   const int64_t tiles = grouped ? ((pr.M + BM - 1) / BM + E) * n_tiles_n : ((pr.M + BM - 1) / BM) * n_tiles_n;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);

@@ -274,6 +274,12 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
   asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
+// 32-byte global store of 8 words (256-bit; the address must be 32-byte aligned).
+__device__ __forceinline__ void stg_256(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]),
+               "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 // 32-byte streaming global load (256-bit; the address must be 32-byte aligned).
 __device__ __forceinline__ void ldg_stream32(const void* p, uint4& a, uint4& b) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
