@@ -238,22 +238,26 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------------ producer ----
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues
+    if (elect_one()) {
       tma_prefetch_desc(&p.tm_a);
       tma_prefetch_desc(&p.tm_b);
       if (n_ct > 0) {
         tma_prefetch_desc(&p.tm_r);
         tma_prefetch_desc(&p.tm_w);
       }
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        Tile tl;
-        tile_of(p, sched, u / split, n_tiles_n, tl);
-        const int kt1 = kt_hi(u), n_ct_u = ct_of(u);
-        for (int kt = kt_lo(u); kt < kt1 && ok; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      Tile tl;
+      tile_of(p, sched, u / split, n_tiles_n, tl);
+      const int kt1 = kt_hi(u), n_ct_u = ct_of(u);
+      for (int kt = kt_lo(u); kt < kt1 && ok; ++kt) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
           uint8_t* sa = stages + stage * kStageBytes;
           uint8_t* sb = sa + kTileBytes;
           uint8_t* sfa = sb + kTileBytes;
@@ -268,46 +272,50 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
           bulk_load(sfb, p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride + ((uint64_t)(tl.n0 / BN) * n_cg + cg0) * 512u,
                     sf_bytes, &full[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        for (int ct = 0; ct < n_ct_u && ok; ++ct) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      for (int ct = 0; ct < n_ct_u && ok; ++ct) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
           uint8_t* sa = stages + stage * kStageBytes;
           uint8_t* sb = sa + kTileBytes;
           mbar_arrive_expect_tx(&full[stage], 2u * kTileBytes);
           tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        // wind down: let copies already issued land before the CTA exits
-        for (int i = 0; i < kStages; ++i) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&full[i], 0) && !mbar_try_wait(&full[i], 1)) {
-            if (globaltimer() - t0 > 1000000ull) break;
-          }
+    }
+    if (!ok) {
+      // wind down: let copies already issued land before the CTA exits
+      for (int i = 0; i < kStages; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&full[i], 0) && !mbar_try_wait(&full[i], 1)) {
+          if (globaltimer() - t0 > 1000000ull) break;
         }
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA ----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      uint32_t comp_phase = 0;
-      bool ok = true;
-      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t comp_phase = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
+      if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
+      for (int kt = kt0; kt < kt1 && ok; ++kt) {
+        if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
-        for (int kt = kt0; kt < kt1 && ok; ++kt) {
-          if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
-          tc_fence_after();
+        if (elect_one()) {
           const uint32_t sa = smem_u32(stages + stage * kStageBytes);
           const uint32_t sb = sa + kTileBytes;
           const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
@@ -326,15 +334,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
             }
           }
           tc_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (n_ct_u > 0 && ok) {
-          if (!mbar_wait(comp_empty, comp_phase ^ 1u, kWaitCompEmpty, s_abort)) { ok = false; break; }
-          comp_phase ^= 1u;
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (n_ct_u > 0 && ok) {
+        if (!mbar_wait_warp(comp_empty, comp_phase ^ 1u, kWaitCompEmpty, s_abort)) { ok = false; break; }
+        comp_phase ^= 1u;
+        tc_fence_after();
+        for (int ct = 0; ct < n_ct_u && ok; ++ct) {
+          if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
           tc_fence_after();
-          for (int ct = 0; ct < n_ct_u && ok; ++ct) {
-            if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
-            tc_fence_after();
+          if (elect_one()) {
             const uint32_t sa = smem_u32(stages + stage * kStageBytes);
             const uint32_t sb = sa + kTileBytes;
             const int krem = p.k - ct * 64;
@@ -344,30 +355,33 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
                        (ct > 0 || j > 0) ? 1u : 0u);
             }
             tc_commit(&empty[stage]);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(&acc_full[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
-      // all MMAs issued by this thread complete before TMEM is released
-      tc_commit(drain);
-      mbar_wait(drain, 0, kWaitDrain, nullptr);
+      if (!ok) break;
+      if (elect_one()) tc_commit(&acc_full[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
     }
+    // all MMAs issued by the elected lane complete before TMEM is released
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
   } else if (warp == 2) {
     // ------------------------------------------------- scale copies ----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
-        for (int kt = kt0; kt < kt1 + n_ct_u && ok; ++kt) {
-          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
-          if (kt < kt1) {
-            tc_fence_after();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
+      for (int kt = kt0; kt < kt1 + n_ct_u && ok; ++kt) {
+        if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+        if (kt < kt1) {
+          tc_fence_after();
+          if (elect_one()) {
             const uint32_t sfa = smem_u32(stages + stage * kStageBytes) + 2u * kTileBytes;
             const uint32_t sfb = sfa + kSfBytes;
             const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
@@ -378,15 +392,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
               tmem_cp_32x128b_x4(tmem + col_sf + 16u + 4u * c, desc_sf(sfb + 512u * c));
             }
             tc_commit(&sf_full[stage]);
-          } else {
-            mbar_arrive(&sf_full[stage]);  // compensation k-tile: nothing to copy
           }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        } else {
+          if (elect_one()) mbar_arrive(&sf_full[stage]);  // compensation k-tile: nothing to copy
         }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      tc_commit(sf_drain);
-      mbar_wait(sf_drain, 0, kWaitSfDrain, nullptr);
     }
+    if (elect_one()) tc_commit(sf_drain);
+    __syncwarp();
+    mbar_wait_warp(sf_drain, 0, kWaitSfDrain, nullptr);
   } else {
     // ------------------------------------------------------ epilogue ----
     const int q = warp & 3;  // TMEM lane quarter of this warp
@@ -557,7 +573,8 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   uint64_t* drain = acc_empty + 1;
   uint64_t* sf_drain = drain + 1;
   uint64_t* sf_full2 = sf_drain + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_full2 + kWStages);
+  uint64_t* sf_drain2 = sf_full2 + kWStages;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain2 + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
@@ -595,6 +612,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     mbar_init(acc_empty, 8);
     mbar_init(drain, 1);
     mbar_init(sf_drain, 1);
+    mbar_init(sf_drain2, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -614,22 +632,26 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
 
   if (warp == 0) {
     // ------------------------------------------------------ producer ----
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues
+    if (elect_one()) {
       tma_prefetch_desc(&p.tm_a);
       tma_prefetch_desc(&p.tm_b);
       if (n_ct > 0) {
         tma_prefetch_desc(&p.tm_r);
         tma_prefetch_desc(&p.tm_w);
       }
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        Tile tl;
-        tile_of_w(p, sched, t, n_tiles_n, tl);
-        const uint8_t* sfb_src0 = p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride;
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      Tile tl;
+      tile_of_w(p, sched, t, n_tiles_n, tl);
+      const uint8_t* sfb_src0 = p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride;
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
           uint8_t* sa = stages + stage * kWStageBytes;
           uint8_t* sb = sa + kWTileA;
           uint8_t* sfa = sb + kWTileB;
@@ -645,41 +667,48 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           const uint64_t bt = (uint64_t)(tl.n0 / 128);
           bulk_load(sfb, sfb_src0 + (bt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
           if (tl.n_valid) bulk_load(sfb + 2048, sfb_src0 + ((bt + 1) * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
-        for (int ct = 0; ct < n_ct && ok; ++ct) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        __syncwarp();
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+      }
+      for (int ct = 0; ct < n_ct && ok; ++ct) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
           uint8_t* sa = stages + stage * kWStageBytes;
           uint8_t* sb = sa + kWTileA;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWTileA + kWTileB));
           tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
+        __syncwarp();
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 2000000ull) {
-        }
+    }
+    if (!ok) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 2000000ull) {
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA ----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      const uint32_t idesc_main = idesc_fp4_n(p.fmt, 0, BNW);
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
-        acc_phase ^= 1u;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const uint32_t idesc_main = idesc_fp4_n(p.fmt, 0, BNW);
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+      acc_phase ^= 1u;
+      tc_fence_after();
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort) ||
+            !mbar_wait_warp(&sf_full2[stage], phase, kWaitSfFull2, s_abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
-          if (!mbar_wait(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
-          if (!mbar_wait(&sf_full2[stage], phase, kWaitSfFull2, s_abort)) { ok = false; break; }
-          tc_fence_after();
+        if (elect_one()) {
           const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
           const uint32_t sb = sa + kWTileA;
           const uint32_t t_sfa = tmem + kWColSf + (uint32_t)stage * 48u;
@@ -698,11 +727,14 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
             }
           }
           tc_commit(&empty[stage]);
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
-        for (int ct = 0; ct < n_ct && ok; ++ct) {
-          if (!mbar_wait(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)) { ok = false; break; }
-          tc_fence_after();
+        __syncwarp();
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+      }
+      for (int ct = 0; ct < n_ct && ok; ++ct) {
+        if (!mbar_wait_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
           const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
           const uint32_t sb = sa + kWTileA;
           const int krem = p.k - ct * 64;
@@ -710,29 +742,32 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           for (int j = 0; j < n_mma; ++j)
             mma_bf16(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16_n(BNW), 1u);
           tc_commit(&empty[stage]);
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(acc_full);
+        __syncwarp();
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
-      tc_commit(drain);
-      mbar_wait(drain, 0, kWaitDrain, nullptr);
+      if (!ok) break;
+      if (elect_one()) tc_commit(acc_full);
+      __syncwarp();
     }
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
   } else if (warp == 2) {
-    // ------------------------------------------------- scale copies ----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        // every stage use completes one phase of sf_full[stage] (a plain arrive
-        // for compensation k-tiles), so its parity tracks the stage's
-        for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
-          if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
-          if (kt >= n_kt) {
-            mbar_arrive(&sf_full[stage]);
-          } else {
-            tc_fence_after();
+    // ------------------------------------------ scale copies (A, B low) ----
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      // every stage use completes one phase of sf_full[stage] (a plain arrive
+      // for compensation k-tiles), so its parity tracks the stage's
+      for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
+        if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+        if (kt >= n_kt) {
+          if (elect_one()) mbar_arrive(&sf_full[stage]);
+        } else {
+          tc_fence_after();
+          if (elect_one()) {
             const uint32_t sfa = smem_u32(stages + stage * kWStageBytes) + (uint32_t)(kWTileA + kWTileB);
             const uint32_t sfb = sfa + kWSfA;
             const uint32_t t_sfa = tmem + kWColSf + (uint32_t)stage * 48u;
@@ -745,12 +780,14 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
             }
             tc_commit(&sf_full[stage]);
           }
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
+        __syncwarp();
+        if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
-      tc_commit(sf_drain);
-      mbar_wait(sf_drain, 0, kWaitSfDrain, nullptr);
     }
+    if (elect_one()) tc_commit(sf_drain);
+    __syncwarp();
+    mbar_wait_warp(sf_drain, 0, kWaitSfDrain, nullptr);
   } else if (warp == 3) {
     // ------------ second half of B's scale copies + residual pre-scaling ----
     int stage = 0;
@@ -766,21 +803,21 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       }
       float c = __fdiv_rn(1.0f, ga);
       if (p.flags == 1) c = __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[e] : 1.f));
-      // every stage use completes one phase of comp_ready[stage] (a plain
-      // arrive for FP4 k-tiles), so its parity tracks the stage's
+      // every stage use completes one phase of comp_ready[stage] and of
+      // sf_full2[stage], so their parities track the stage's
       for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
-        if (!mbar_wait(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
         if (kt < n_kt) {
           // scale chunks of B rows 128..255 (copies from a second warp run
           // alongside the first warp's)
-          __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
+          tc_fence_after();
+          if (elect_one()) {
             const uint32_t sfb = smem_u32(stages + stage * kWStageBytes) + (uint32_t)(kWTileA + kWTileB + kWSfA);
             const uint32_t t_sfb = tmem + kWColSf + (uint32_t)stage * 48u + 16u;
             const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
             const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
-            for (int c = 0; c < nch; ++c) tmem_cp_32x128b_x4(t_sfb + 8u * c + 4u, desc_sf(sfb + 2048u + 512u * c));
+            for (int cc = 0; cc < nch; ++cc)
+              tmem_cp_32x128b_x4(t_sfb + 8u * cc + 4u, desc_sf(sfb + 2048u + 512u * cc));
             tc_commit(&sf_full2[stage]);
             mbar_arrive(&comp_ready[stage]);
           }
@@ -800,14 +837,18 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) {
+          if (elect_one()) {
             mbar_arrive(&comp_ready[stage]);
             mbar_arrive(&sf_full2[stage]);
           }
         }
+        __syncwarp();
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
     }
+    if (elect_one()) tc_commit(sf_drain2);
+    __syncwarp();
+    mbar_wait_warp(sf_drain2, 0, kWaitSfDrain, nullptr);
   } else {
     // ------------------------------------------------------ epilogue ----
     const int q = warp & 3;            // TMEM lane quarter

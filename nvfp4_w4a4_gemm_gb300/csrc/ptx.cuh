@@ -40,6 +40,17 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// One elected lane of a fully converged warp (elect.sync).  Issue points of
+// asynchronous work (TMA, tcgen05.mma / cp / commit) use it so the issuing
+// warp stays converged: a single lane running a loop of its own, with
+// shared-memory polls between MMAs, was measured to stall the tensor pipe
+// (about 2.8x lower MMA throughput).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
                : "memory");
@@ -79,6 +90,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
       }
     }
   }
+}
+
+// mbar_wait executed by a whole converged warp; the result is warp-uniform
+// (false in every lane if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t where,
+                                               volatile int* aborted) {
+  const bool ok = mbar_wait(bar, parity, where, aborted);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------ TMA ----
