@@ -715,15 +715,25 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           const uint32_t t_sfb = t_sfa + 16u;
           const int64_t krem = p.K - (int64_t)kt * 256;
           const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
-          for (int j = 0; j < n_mma; ++j) {
-            const uint64_t adesc = desc_sw128(sa + 32u * j);
-            const uint64_t bdesc = desc_sw128(sb + 32u * j);
-            const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
-            if (p.fmt == 1) {
-              mma_mxf4_2x(tmem, adesc, bdesc, idesc_fp4_n(1, (uint32_t)(j & 1) * 2u, BNW), t_sfa + 4u * (j >> 1),
-                          t_sfb + 8u * (j >> 1), accum);
-            } else {
-              mma_nvf4_4x(tmem, adesc, bdesc, idesc_main, t_sfa + 4u * j, t_sfb + 8u * j, accum);
+          if (n_mma == 4 && p.fmt == 0) {
+            // the common case as one straight run of 4 MMAs: the tensor pipe
+            // keeps few MMAs queued, so work between issues shows up directly
+            const uint64_t ad = desc_sw128(sa), bd = desc_sw128(sb);  // +32 B per k-step = +2 in the address field
+            mma_nvf4_4x(tmem, ad, bd, idesc_main, t_sfa, t_sfb, kt > 0 ? 1u : 0u);
+            mma_nvf4_4x(tmem, ad + 2, bd + 2, idesc_main, t_sfa + 4u, t_sfb + 8u, 1u);
+            mma_nvf4_4x(tmem, ad + 4, bd + 4, idesc_main, t_sfa + 8u, t_sfb + 16u, 1u);
+            mma_nvf4_4x(tmem, ad + 6, bd + 6, idesc_main, t_sfa + 12u, t_sfb + 24u, 1u);
+          } else {
+            for (int j = 0; j < n_mma; ++j) {
+              const uint64_t adesc = desc_sw128(sa + 32u * j);
+              const uint64_t bdesc = desc_sw128(sb + 32u * j);
+              const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
+              if (p.fmt == 1) {
+                mma_mxf4_2x(tmem, adesc, bdesc, idesc_fp4_n(1, (uint32_t)(j & 1) * 2u, BNW), t_sfa + 4u * (j >> 1),
+                            t_sfb + 8u * (j >> 1), accum);
+              } else {
+                mma_nvf4_4x(tmem, adesc, bdesc, idesc_main, t_sfa + 4u * j, t_sfb + 8u * j, accum);
+              }
             }
           }
           tc_commit(&empty[stage]);
