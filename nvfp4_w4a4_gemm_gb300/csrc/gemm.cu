@@ -87,6 +87,7 @@ struct GemmParams {
   int split;        // narrow kernel: K splits per tile (1 = none)
   float* partial;   // split > 1: fp32 partial sums [split][M][N]
   int y_vec32;      // Y rows start on 32-byte boundaries: 256-bit stores
+  uint32_t a_rows;  // narrow kernel: rows of A (and R) each TMA load brings in (BM, or M rounded up to 8 when M < BM)
 };
 
 struct Tile {
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
           const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
           const uint32_t sf_bytes = (uint32_t)nch * 512u;
-          mbar_arrive_expect_tx(&full[stage], 2u * kTileBytes + 2u * sf_bytes);
+          mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes + 2u * sf_bytes);
           tma_load_2d(sa, &p.tm_a, &full[stage], kt * BKB, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0, tl.e);
           else tma_load_2d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0);
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         if (elect_one()) {
           uint8_t* sa = stages + stage * kStageBytes;
           uint8_t* sb = sa + kTileBytes;
-          mbar_arrive_expect_tx(&full[stage], 2u * kTileBytes);
+          mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes);
           tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
@@ -975,7 +976,11 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   const uint64_t kb = (uint64_t)(pr.K / 2);
   {
     const uint64_t d[2] = {kb, rows};
-    if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
+    // a single M tile with fewer rows loads only those rows (rounded up to 8):
+    // rows past M are never stored, so the rest of the smem tile may hold anything
+    p.a_rows = (!grouped && pr.M < BM) ? (uint32_t)((pr.M + 7) / 8 * 8) : (uint32_t)BM;
+    if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, p.a_rows))
+      return cudaErrorInvalidValue;
   }
   if (grouped) {
     const uint64_t d[3] = {kb, (uint64_t)pr.N, (uint64_t)E};
@@ -986,7 +991,8 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   }
   if (pr.k > 0) {
     const uint64_t dr[2] = {(uint64_t)pr.k, rows};
-    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, p.a_rows))
+      return cudaErrorInvalidValue;
     if (grouped) {
       const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
       if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BN))
