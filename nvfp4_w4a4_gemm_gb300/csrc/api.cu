@@ -144,7 +144,6 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
   int st = check_quant_args(x, M_total, K, ldx, codes, scales, chan, k, resid, 16);
   if (st != NVFP4_OK) return st;
   if (E <= 0 || E > 4096 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
-  if ((int64_t)E * k + 2 * E + 1 > (200 * 1024) / 4) return NVFP4_ERR_UNSUPPORTED;  // smem copy of chan
   if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
     return NVFP4_ERR_WORKSPACE;
   const DeviceInfo* d = nullptr;

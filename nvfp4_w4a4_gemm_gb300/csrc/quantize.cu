@@ -77,16 +77,6 @@ __device__ float tensor_scale_from_partials(const float* partials, int n) {
   return m > 0.f ? __fdiv_rn(m, kAmaxToScale) : 1.0f;
 }
 
-// First index i in sorted s[0..n) with s[i] >= v.
-__device__ __forceinline__ int lower_bound_i32(const int32_t* s, int n, int32_t v) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (s[mid] < v) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
 // ------------------------------------------------------------- amax -------
 // Work unit = one row x 1024 columns (4 x 16 bytes per lane); one 32-bit
 // division per unit; the next unit's loads are issued before the current
@@ -351,7 +341,6 @@ __device__ float warp_units_amax(const QuantArgs& a, UnitWalk w, int lane) {
 struct QTables {
   const int32_t* off;    // grouped: offsets [E+1]
   const int32_t* pbase;  // grouped: first padded scale row of each expert [E]
-  const int32_t* chan;   // channel lists [E][k] (when there are no prefix tables)
   const uint16_t* pref;  // per-expert prefix counts of the channel bitmaps [E][n_words]
   int n_words;
 };
@@ -378,13 +367,16 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
                                              int lane, const ScaleCtx& sc, const QTables& t, int64_t n_cg) {
   int64_t srow = r;
   int e = 0;
-  if (kGrouped) {  // expert of row r: last e with offsets[e] <= r
-    int l = 0, hh = a.E;
-    while (hh - l > 1) {
-      const int mid = (l + hh) >> 1;
-      if (t.off[mid] <= (int32_t)r) l = mid; else hh = mid;
+  if (kGrouped) {
+    // expert of row r = (number of e in 1..E with offsets[e] <= r), the
+    // warp testing 32 offsets per step (offsets are non-decreasing)
+    int cnt = 0;
+    for (int b = 1; b <= a.E; b += 32) {  // warp-uniform trip count
+      const int i = b + lane;
+      const bool le = i <= a.E && t.off[i] <= (int32_t)r;
+      cnt += __popc(__ballot_sync(0xffffffffu, le));
     }
-    e = l;
+    e = cnt < a.E ? cnt : a.E - 1;
     srow = (int64_t)t.pbase[e] + ((int64_t)r - t.off[e]);
   }
   const int64_t col0 = (int64_t)gi * 1024;
@@ -407,9 +399,17 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
     re = (w0 + 32 < t.n_words) ? (int)t.pref[e * t.n_words + w0 + 32] : a.k;
     S = a.chan + (int64_t)e * a.k;
   } else {
-    S = t.chan + e * a.k;
-    rb = lower_bound_i32(S, a.k, (int32_t)col0);
-    re = lower_bound_i32(S, a.k, (int32_t)(col0 + cols));
+    // slots before the unit / before its end: counted over the sorted list,
+    // 32 entries per step across the warp
+    S = a.chan + (int64_t)e * a.k;
+    rb = 0;
+    re = 0;
+    for (int b = 0; b < a.k; b += 32) {  // warp-uniform trip count
+      const int i = b + lane;
+      const int32_t v = i < a.k ? S[i] : 0x7FFFFFFF;
+      rb += __popc(__ballot_sync(0xffffffffu, v < (int32_t)col0));
+      re += __popc(__ballot_sync(0xffffffffu, v < (int32_t)(col0 + cols)));
+    }
   }
   const __nv_bfloat16* xrow = a.x + (int64_t)r * a.ldx;
   __nv_bfloat16* rrow = a.resid + (int64_t)r * a.k;
@@ -436,13 +436,12 @@ template <bool kGrouped, bool kFused, bool kFull>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   extern __shared__ __align__(16) int32_t smem_i32[];
   __shared__ float2 s_dr[256];
-  // offsets [E+1] | padded bases [E] | chan [E*k] (fallback only) |
-  // bitmap words [E][n_words] | prefix counts [E][n_words] (uint16)
+  // offsets [E+1] | padded bases [E] | dense only: bitmap words [n_words] |
+  // prefix counts [n_words] (uint16)
   const int n_words = (int)((a.K + 31) / 32);
   int32_t* s_off = smem_i32;
   int32_t* s_pbase = s_off + (a.E + 1);
-  int32_t* s_chan = s_pbase + a.E;
-  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_chan + (a.use_map ? 0 : a.E * a.k));
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_pbase + a.E);
   uint16_t* s_pref = reinterpret_cast<uint16_t*>(s_bits + (a.use_map ? a.E * n_words : 0));
   const int lane = threadIdx.x & 31;
   UnitWalk walk;
@@ -476,19 +475,21 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
   if (a.use_map) {
-    // one warp per expert: clear its bitmap, set the bits of its channels,
-    // then prefix counts by a warp scan over per-lane word ranges
+    // channel bitmaps of all experts (bit j%32 of word j/32 set for j in S_e):
+    // cleared, then set from every channel entry at once (independent loads),
+    // then one warp per expert turns them into prefix counts (shared memory only)
+    for (int i = threadIdx.x; i < a.E * n_words; i += blockDim.x) s_bits[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.E * a.k; i += blockDim.x) {
+      const int32_t j = a.chan[i];
+      const int e = i / a.k;
+      if (j >= 0 && j < a.K) atomicOr(&s_bits[e * n_words + (j >> 5)], 1u << (j & 31));
+    }
+    __syncthreads();
     const int warp_id = threadIdx.x >> 5, ln = threadIdx.x & 31, n_wp = blockDim.x >> 5;
     const int per = (n_words + 31) / 32;
     for (int e = warp_id; e < a.E; e += n_wp) {
-      uint32_t* bits = s_bits + e * n_words;
-      for (int w = ln; w < n_words; w += 32) bits[w] = 0u;
-      __syncwarp();
-      for (int i = ln; i < a.k; i += 32) {
-        const int32_t j = a.chan[e * a.k + i];
-        if (j >= 0 && j < a.K) atomicOr(&bits[j >> 5], 1u << (j & 31));
-      }
-      __syncwarp();
+      const uint32_t* bits = s_bits + e * n_words;
       uint32_t cnt = 0;
       for (int q = 0; q < per; ++q) {
         const int w = ln * per + q;
@@ -508,17 +509,36 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
           run += __popc(bits[w]);
         }
       }
-      __syncwarp();
     }
-  } else {
-    for (int i = threadIdx.x; i < a.E * a.k; i += blockDim.x) s_chan[i] = a.chan[i];
   }
   __syncthreads();
-  if (kGrouped && threadIdx.x == 0) {
-    int32_t base = 0;
-    for (int e = 0; e < a.E; ++e) {
-      s_pbase[e] = base;
-      base += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
+  if (kGrouped) {
+    // first padded scale row of each expert: exclusive prefix sum of
+    // round_up(M_e, 128), a block-wide scan (each thread sums a run of experts)
+    __shared__ int32_t s_wsum[kThreads / 32];
+    const int per_t = (a.E + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int e0 = (int)threadIdx.x * per_t;
+    int32_t local = 0;
+    for (int q = 0; q < per_t; ++q) {
+      const int e = e0 + q;
+      if (e < a.E) local += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
+    }
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[threadIdx.x >> 5] = incl;
+    __syncthreads();
+    int32_t run = incl - local;
+    for (int w = 0; w < (int)(threadIdx.x >> 5); ++w) run += s_wsum[w];
+    for (int q = 0; q < per_t; ++q) {
+      const int e = e0 + q;
+      if (e < a.E) {
+        s_pbase[e] = run;
+        run += ((s_off[e + 1] - s_off[e] + 127) >> 7) << 7;
+      }
     }
   }
   if (!kFused) {
@@ -543,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   // while the current one is quantized.
   const int64_t n_cg = (a.K / 16 + 3) / 4;
   QTables t;
-  t.off = s_off; t.pbase = s_pbase; t.chan = s_chan; t.pref = s_pref;
+  t.off = s_off; t.pbase = s_pbase; t.pref = s_pref;
   t.n_words = n_words;
   const uint32_t n = walk.n_units;
   uint4 va[4], vb[4];
@@ -930,7 +950,10 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   {
     const size_t words = (size_t)((K + 31) / 32);
     const size_t tab = (size_t)a.E * words * (sizeof(uint32_t) + sizeof(uint16_t));
-    a.use_map = (k > 0 && k < 65536 && tab <= kMaxTableBytes) ? 1 : 0;
+    // dense: channel bitmap + prefix table per CTA (cheap for one channel
+    // set); grouped: each unit counts over its expert's list instead, so no
+    // CTA builds E tables
+    a.use_map = (a.E == 1 && k > 0 && k < 65536 && tab <= kMaxTableBytes) ? 1 : 0;
   }
   a.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
   const bool fused = g_in == nullptr && bar != nullptr;
@@ -943,7 +966,6 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   a.bar = bar;
   size_t smem = sizeof(int32_t) * (2 * (size_t)a.E + 1);
   if (a.use_map) smem += (size_t)a.E * (size_t)((K + 31) / 32) * (sizeof(uint32_t) + sizeof(uint16_t));
-  else smem += sizeof(int32_t) * (size_t)a.E * k;
   const bool full = a.vec32 && (K % 1024) == 0;
   const void* kerns[2][2][2] = {
       {{(const void*)nvfp4_quant_kernel<false, false, false>, (const void*)nvfp4_quant_kernel<false, false, true>},
