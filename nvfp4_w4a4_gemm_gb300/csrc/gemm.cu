@@ -51,25 +51,15 @@ namespace {
 constexpr int BM = 128;               // output rows per tile (MMA M)
 constexpr int BN = 128;               // output columns per tile (MMA N)
 constexpr int BKB = 128;              // bytes of K per k-tile row: 256 FP4 or 64 bf16
+constexpr int kStages = 4;             // = number of TMEM scale slots
 constexpr int kTileBytes = BM * BKB;  // 16 KB (A); B the same since BN == BM
 constexpr int kSfBytes = 2048;        // 4 scale chunks of 128 rows x 4 scales
+constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfBytes;  // 36 KB
 constexpr int kThreads = 224;
-constexpr uint32_t kTmemCols = 512;
 
-// Narrow-kernel configurations.  NST = 4: 36 KB stages, two FP4 accumulators
-// (the epilogue of one tile overlaps the next tile's main loop), TMEM
-// acc0 0 | acc1 128 | comp 256 | scales 384 + 32 s.  NST = 8, for a single
-// small M tile (decode): A stages hold only the real rows, so 8 stages of
-// ~22 KB keep twice the weight bytes in flight; one accumulator,
-// TMEM acc 0 | comp 128 | scales 256 + 32 s.
-template <int NST>
-struct NarrowCfg {
-  static constexpr bool kDual = NST == 4;
-  static constexpr uint32_t kColAcc1 = 128;
-  static constexpr uint32_t kColComp = kDual ? 256 : 128;
-  static constexpr uint32_t kColSf = kDual ? 384 : 256;
-  static_assert(kColSf + 32 * NST <= kTmemCols, "TMEM budget");
-};
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColComp = 256, kColSf = 384;  // SF: kStages x (16 A + 16 B)
+static_assert(kColSf + 32 * kStages <= kTmemCols, "TMEM budget");
 
 enum WaitSite : uint32_t {
   kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6,
@@ -98,7 +88,6 @@ struct GemmParams {
   float* partial;   // split > 1: fp32 partial sums [split][M][N]
   int y_vec32;      // Y rows start on 32-byte boundaries: 256-bit stores
   uint32_t a_rows;  // narrow kernel: rows of A (and R) each TMA load brings in (BM, or M rounded up to 8 when M < BM)
-  uint32_t a_stage; // narrow kernel: bytes of A per stage (16 KB, or a_rows x 128 with 8 stages)
 };
 
 struct Tile {
@@ -167,16 +156,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_des
 // Scale chunk for tcgen05.cp: 32 rows x 16 bytes, no swizzle, 8-row groups 128 bytes apart.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 
-template <int NST>
 __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = NarrowCfg<NST>;
-  constexpr int kStages = NST;
-  const uint32_t stage_bytes = p.a_stage + (uint32_t)kTileBytes + 2u * kSfBytes;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled stages
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -274,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       for (int kt = kt_lo(u); kt < kt1 && ok; ++kt) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
-          uint8_t* sa = stages + stage * stage_bytes;
-          uint8_t* sb = sa + p.a_stage;
+          uint8_t* sa = stages + stage * kStageBytes;
+          uint8_t* sb = sa + kTileBytes;
           uint8_t* sfa = sb + kTileBytes;
           uint8_t* sfb = sfa + kSfBytes;
           const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
@@ -295,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       for (int ct = 0; ct < n_ct_u && ok; ++ct) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
-          uint8_t* sa = stages + stage * stage_bytes;
-          uint8_t* sb = sa + p.a_stage;
+          uint8_t* sa = stages + stage * kStageBytes;
+          uint8_t* sb = sa + kTileBytes;
           mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes);
           tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
@@ -327,14 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
       if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_acc = tmem + (acc ? Cfg::kColAcc1 : 0u);
+      const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
       for (int kt = kt0; kt < kt1 && ok; ++kt) {
         if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t sa = smem_u32(stages + stage * stage_bytes);
-          const uint32_t sb = sa + p.a_stage;
-          const uint32_t col_sf = Cfg::kColSf + (uint32_t)stage * 32u;
+          const uint32_t sa = smem_u32(stages + stage * kStageBytes);
+          const uint32_t sb = sa + kTileBytes;
+          const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
           const uint32_t t_sfa = tmem + col_sf, t_sfb = tmem + col_sf + 16u;
           const int64_t krem = p.K - (int64_t)kt * 256;
           const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
@@ -362,12 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t sa = smem_u32(stages + stage * stage_bytes);
-            const uint32_t sb = sa + p.a_stage;
+            const uint32_t sa = smem_u32(stages + stage * kStageBytes);
+            const uint32_t sb = sa + kTileBytes;
             const int krem = p.k - ct * 64;
             const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
             for (int j = 0; j < n_mma; ++j) {
-              mma_bf16(tmem + Cfg::kColComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
+              mma_bf16(tmem + kColComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
                        (ct > 0 || j > 0) ? 1u : 0u);
             }
             tc_commit(&empty[stage]);
@@ -379,12 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       if (!ok) break;
       if (elect_one()) tc_commit(&acc_full[acc]);
       __syncwarp();
-      if (Cfg::kDual) {
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      } else {
-        acc_phase ^= 1u;
-      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
     }
     // all MMAs issued by the elected lane complete before TMEM is released
     if (elect_one()) tc_commit(drain);
@@ -402,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         if (kt < kt1) {
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t sfa = smem_u32(stages + stage * stage_bytes) + p.a_stage + (uint32_t)kTileBytes;
+            const uint32_t sfa = smem_u32(stages + stage * kStageBytes) + 2u * kTileBytes;
             const uint32_t sfb = sfa + kSfBytes;
-            const uint32_t col_sf = Cfg::kColSf + (uint32_t)stage * 32u;
+            const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
             const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
             const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
             for (int c = 0; c < nch; ++c) {
@@ -442,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         alpha = ga * gb;
         beta = (p.flags == 1) ? 1.f : gb;
       }
-      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? Cfg::kColAcc1 : 0u);
-      const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + Cfg::kColComp;
+      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kColAcc1 : kColAcc0);
+      const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kColComp;
       const bool row_ok = r < tl.rows;
       __nv_bfloat16* yrow = p.y + (tl.row0 + r) * p.N + tl.n0;
 #pragma unroll 1
@@ -484,12 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         mbar_arrive(&acc_empty[acc]);
         if (n_ct_u > 0) mbar_arrive(comp_empty);
       }
-      if (Cfg::kDual) {
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      } else {
-        acc_phase ^= 1u;
-      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
     }
   }
 
@@ -975,6 +952,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
 // K splits for the narrow kernel: when its tiles leave most SMs idle (few
 // rows and a narrow N), each tile's K range is split so the units cover about
@@ -1002,13 +980,9 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   const uint64_t kb = (uint64_t)(pr.K / 2);
   {
     const uint64_t d[2] = {kb, rows};
-    // a single M tile with fewer rows loads only those rows (rounded up to 8),
-    // and its stages reserve only those rows: the MMA still reads 128 rows,
-    // the ones past the loaded rows come from the stage's B and scale bytes,
-    // and those output rows are never stored
+    // a single M tile with fewer rows loads only those rows (rounded up to 8):
+    // rows past M are never stored, so the rest of the smem tile may hold anything
     p.a_rows = (!grouped && pr.M < BM) ? (uint32_t)((pr.M + 7) / 8 * 8) : (uint32_t)BM;
-    // 8 stages of (a_rows x 128 + 20 KB) fit the 227 KB of shared memory up to 64 rows
-    p.a_stage = (!grouped && p.a_rows <= 64) ? p.a_rows * (uint32_t)BKB : (uint32_t)kTileBytes;
     if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, p.a_rows))
       return cudaErrorInvalidValue;
   }
@@ -1061,15 +1035,10 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   const int64_t units = tiles * p.split;
   int grid = (int)(units < num_sms ? units : num_sms);
   if (grid < 1) grid = 1;
-  const bool deep = p.a_stage < (uint32_t)kTileBytes;  // small A: 8 stages, one accumulator
-  const size_t stage_bytes = (size_t)p.a_stage + kTileBytes + 2 * kSfBytes;
-  const size_t smem = 1024 + (deep ? 8 : 4) * stage_bytes + 512 + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
-  const void* kern = deep ? (const void*)w4a4_gemm_kernel<8> : (const void*)w4a4_gemm_kernel<4>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = kSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
+  cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  void* args[] = {&p};
-  err = cudaLaunchKernel(kern, dim3((unsigned)grid), dim3(kThreads), args, smem, stream);
-  if (err != cudaSuccess) return err;
+  w4a4_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
   if (p.split > 1) {
     const int64_t n4 = pr.M * pr.N / 4;
     int64_t blocks = (n4 + 255) / 256;
