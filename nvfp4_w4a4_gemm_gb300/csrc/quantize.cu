@@ -16,11 +16,11 @@
 // error" (arXiv 2605.20402v2) abstract -- scale bias + deadzone truncation +
 // grid noise.
 //
-// Thread mapping (NVFP4): one thread owns 8 consecutive bf16 of a row (one
-// 16-byte load), two adjacent lanes own one 16-element block and combine
-// their absmax with one shuffle; a warp covers a 256-element row segment and
-// writes 128 contiguous code bytes.  Each warp keeps several segments' loads
-// in flight before doing any arithmetic.
+// Thread mapping: one warp per unit of 1024 columns of a row.  NVFP4: each
+// lane owns two 16-element blocks (32-byte loads), 4 lanes' scale bytes are
+// gathered by shuffles into one store in the MMA's tile layout, and the
+// unit's residual slots are computed one per lane after the unit is
+// quantized.  MXFP4: each lane owns one 32-element block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -34,7 +34,6 @@ namespace nv4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;            // row segments in flight per warp (MXFP4)
 constexpr size_t kMaxTableBytes = 64 * 1024;  // channel bitmaps + prefixes kept in shared memory up to this size
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
@@ -590,6 +589,7 @@ struct MxArgs {
   uint8_t* scales;     // tiled, K/32 scales per row
   float* stats;        // [M*K/32][4] or nullptr
   uint8_t* dead;       // [M*K/32] or nullptr
+  int vec32;           // rows start on 32-byte boundaries: 256-bit loads
 };
 
 // floor(log2 a) - 2 clamped to [-127, 127], from the fp32 bit pattern.
@@ -612,117 +612,120 @@ __device__ __forceinline__ float pow2f(int e) {  // exact 2^e for e in [-149, 12
   return __uint_as_float(1u << (e + 149));
 }
 
+// Magnitude of an E2M1 code (its low 3 bits).
 __device__ __forceinline__ float e2m1_mag(uint32_t code) {
   const uint32_t h2 = cvt_e2m1x2_to_f16x2(code & 0x7u);
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-__global__ void __launch_bounds__(kThreads) mxfp4_quant_kernel(MxArgs a) {
-  // one thread = 8 elements, 4 lanes = one 32-element block
+// x / s* rounded to fp32 for the code at the ideal scale s*: x * RN(1/s*)
+// is within 2 fp32 ulps of RN(x / s*), so it rounds to the same E2M1 code
+// unless it lies within a few ulps of an E2M1 rounding midpoint (0.25, 0.75,
+// 1.25, 1.75, 2.5, 3.5, 5: fp32 patterns whose low 21 bits are zero); those
+// elements, and blocks with a tiny or huge s*, take the IEEE division.
+__device__ __forceinline__ float ideal_quotient(float x, float ss, float rss, bool fast) {
+  const float y = __fmul_rn(x, rss);
+  const uint32_t m = (__float_as_uint(y) + 8u) & 0x1FFFFFu;
+  return (!fast || m <= 16u) ? __fdiv_rn(x, ss) : y;
+}
+
+// Two E2M1 codes (one byte, low nibble first) -> their two values.
+__device__ __forceinline__ float2 e2m1x2_vals(uint32_t byte) {
+  const uint32_t h2 = cvt_e2m1x2_to_f16x2(byte);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// One warp per unit of 1024 columns of a row; each lane owns one 32-element
+// block (64 bytes: two sector-aligned 32-byte loads).
+template <bool kStats>
+__global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
   const int lane = threadIdx.x & 31;
-  const int64_t seg_per_row = (a.K + 255) / 256;
-  const int64_t n_seg = a.M * seg_per_row;
-  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t nblk = a.K / 32;
   const int64_t n_cg = (nblk + 3) / 4;
-  for (int64_t s0 = warp_global * kUnroll; s0 < n_seg; s0 += n_warps * kUnroll) {
-    uint4 v[kUnroll];
+  UnitWalk w;
+  w.gpr = (uint32_t)((a.K + 1023) / 1024);
+  w.n_units = (uint32_t)(a.M * w.gpr);
+  w.n_warps = (gridDim.x * blockDim.x) >> 5;
+  w.dr = w.n_warps / w.gpr;
+  w.dg = w.n_warps - w.dr * w.gpr;
+  w.u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  w.r = w.u / w.gpr;
+  w.gi = w.u - w.r * w.gpr;
+  for (; w.u < w.n_units; w.next()) {
+    const int64_t r = w.r, gi = w.gi;
+    const int64_t col = gi * 1024 + lane * 32;
+    const bool valid = col < a.K;
+    uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (valid) {
+      const __nv_bfloat16* src = a.x + r * a.ldx + col;
+      if (a.vec32) {
+        ldg_stream32(src, v[0], v[1]);
+        ldg_stream32(src + 16, v[2], v[3]);
+      } else {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t s = s0 + u;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (s < n_seg) {
-        const int64_t r = s / seg_per_row;
-        const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
-        if (c < a.K) v[u] = ldg_stream(a.x + r * a.ldx + c);
+        for (int i = 0; i < 4; ++i) v[i] = ldg_stream(src + 8 * i);
       }
     }
+    // block absmax, E8M0 scale 2^e with e = floor(log2 a) - 2
+    const float am = absmax_of(absmax8(absmax8(absmax8(absmax8(v[0].x, v[0]), v[1]), v[2]), v[3]));
+    const int e = mx_exponent(am);
+    const float inv = pow2f(-e);
+    const uint64_t s2 = ((uint64_t)__float_as_uint(inv) << 32) | __float_as_uint(inv);
+    uint4 cw;
+    cw.x = bf16x8_mul_e2m1(v[0], s2);
+    cw.y = bf16x8_mul_e2m1(v[1], s2);
+    cw.z = bf16x8_mul_e2m1(v[2], s2);
+    cw.w = bf16x8_mul_e2m1(v[3], s2);
+    if (valid) *reinterpret_cast<uint4*>(a.codes + r * (a.K / 2) + col / 2) = cw;
+    // 4 blocks of a 128-element group -> one 32-bit store in the tile layout
+    const uint32_t sb = valid ? (uint32_t)(e + 127) : 0u;
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 1);
+    const uint32_t s2b = __shfl_down_sync(0xffffffffu, sb, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 3);
+    if ((lane & 3) == 0 && valid)
+      *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(r, (gi * 32 + lane) / 4, n_cg)) =
+          sb | (s1 << 8) | (s2b << 16) | (s3 << 24);
+    if (kStats && valid) {
+      // decomposition through the ideal scale s* = a / 6 (fp32):
+      //   B = Q_s - Q*,  D / G = Q* - x on zero / non-zero codes at s*,  E = Q_s - x
+      float eb = 0.f, ed = 0.f, eg = 0.f, ee = 0.f;
+      uint32_t nd = 0;
+      if (am > 0.f) {
+        const float ss = div6_rn(am);
+        const float rss = __frcp_rn(ss);
+        const bool fast = ss >= 0x1p-120f && ss <= 0x1p120f;
+        const float sc = pow2f(e);
+        const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                                 v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+        const uint32_t cq4[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t s = s0 + u;
-      if (s >= n_seg) break;
-      const int64_t r = s / seg_per_row;
-      const int64_t c = (s - r * seg_per_row) * 256 + lane * 8;
-      const bool valid = c < a.K;
-      float f[8];
-      unpack8(v[u], f);
-      float am = 0.f;
+        for (int pr = 0; pr < 16; ++pr) {  // element pairs (2pr, 2pr + 1)
+          const uint32_t word = wv[pr];
+          const float x2[2] = {__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u)};
+          const uint32_t cqb = (cq4[pr >> 2] >> (8 * (pr & 3))) & 0xFFu;
+          const uint32_t csb = cvt_e2m1x2(ideal_quotient(x2[0], ss, rss, fast), ideal_quotient(x2[1], ss, rss, fast));
+          const float2 vq = e2m1x2_vals(cqb), vs = e2m1x2_vals(csb);
+          const float q2[2] = {vq.x, vq.y}, s2v[2] = {vs.x, vs.y};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      const int e = mx_exponent(am);
-      const float inv = pow2f(-e);
-      uint32_t packed = 0;
-      uint32_t cds[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t b = cvt_e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
-        packed |= b << (8 * i);
-        cds[2 * i] = b & 0xF;
-        cds[2 * i + 1] = b >> 4;
-      }
-      if (valid) *reinterpret_cast<uint32_t*>(a.codes + r * (a.K / 2) + c / 2) = packed;
-      const uint32_t sb = (uint32_t)(e + 127);
-      // 4 blocks of 32 per 128 elements = 16 lanes; gather into lane%16 == 0
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 4);
-      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 8);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 12);
-      if ((lane & 15) == 0 && valid) {
-        const int64_t blk = c / 32;
-        uint32_t word = sb;
-        if (blk + 1 < nblk) word |= s1 << 8;
-        if (blk + 2 < nblk) word |= s2 << 16;
-        if (blk + 3 < nblk) word |= s3 << 24;
-        *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(r, blk / 4, n_cg)) = word;
-      }
-      if (a.stats != nullptr || a.dead != nullptr) {
-        // decomposition through the ideal scale s* = a / 6 (fp32)
-        float eb = 0.f, ed = 0.f, eg = 0.f, ee = 0.f;
-        uint32_t nd = 0;
-        if (am > 0.f) {
-          const float ss = __fdiv_rn(am, 6.0f);
-          const float sc = pow2f(e);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t bs = cvt_e2m1x2(__fdiv_rn(f[2 * i], ss), __fdiv_rn(f[2 * i + 1], ss));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float xv = f[2 * i + h];
-              const uint32_t cs = (bs >> (4 * h)) & 0xF;
-              const uint32_t cq = cds[2 * i + h];
-              const float qs = copysignf(__fmul_rn(e2m1_mag(cq), sc), (cq & 8) ? -1.f : 1.f);
-              const float qst = copysignf(__fmul_rn(e2m1_mag(cs), ss), (cs & 8) ? -1.f : 1.f);
-              const float E = __fsub_rn(qs, xv);
-              const float B = __fsub_rn(qs, qst);
-              const float R = __fsub_rn(qst, xv);
-              ee = __fmaf_rn(E, E, ee);
-              eb = __fmaf_rn(B, B, eb);
-              if ((cs & 7u) == 0u) {
-                ed = __fmaf_rn(R, R, ed);
-                nd += (xv != 0.f) ? 1u : 0u;
-              } else {
-                eg = __fmaf_rn(R, R, eg);
-              }
-            }
+          for (int h = 0; h < 2; ++h) {
+            const float qs = __fmul_rn(q2[h], sc);
+            const float qst = __fmul_rn(s2v[h], ss);
+            const float E = __fsub_rn(qs, x2[h]);
+            const float B = __fsub_rn(qs, qst);
+            const float R = __fsub_rn(qst, x2[h]);
+            ee = __fmaf_rn(E, E, ee);
+            eb = __fmaf_rn(B, B, eb);
+            const bool dz = ((csb >> (4 * h)) & 7u) == 0u;
+            const float R2 = __fmul_rn(R, R);
+            ed += dz ? R2 : 0.f;
+            eg += dz ? 0.f : R2;
+            nd += (dz && x2[h] != 0.f) ? 1u : 0u;
           }
         }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          eb += __shfl_xor_sync(0xffffffffu, eb, o);
-          ed += __shfl_xor_sync(0xffffffffu, ed, o);
-          eg += __shfl_xor_sync(0xffffffffu, eg, o);
-          ee += __shfl_xor_sync(0xffffffffu, ee, o);
-          nd += __shfl_xor_sync(0xffffffffu, nd, o);
-        }
-        if ((lane & 3) == 0 && valid) {
-          const int64_t bidx = r * nblk + c / 32;
-          if (a.stats != nullptr)
-            *reinterpret_cast<float4*>(a.stats + bidx * 4) = make_float4(eb, ed, eg, ee);
-          if (a.dead != nullptr) a.dead[bidx] = (uint8_t)nd;
-        }
       }
+      const int64_t bidx = r * nblk + gi * 32 + lane;
+      if (a.stats != nullptr) *reinterpret_cast<float4*>(a.stats + bidx * 4) = make_float4(eb, ed, eg, ee);
+      if (a.dead != nullptr) a.dead[bidx] = (uint8_t)nd;
     }
   }
 }
@@ -1000,14 +1003,19 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
-  MxArgs a{x, M, K, ldx, codes, scales, stats, dead};
-  const int64_t n_seg = M * ((K + 255) / 256);
-  int64_t blocks = ((n_seg + kUnroll - 1) / kUnroll + 7) / 8;
-  const int64_t cap = (int64_t)num_sms * 4;
+  MxArgs a{x, M, K, ldx, codes, scales, stats, dead, 0};
+  a.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
+  const bool st = stats != nullptr || dead != nullptr;
+  const void* kern = st ? (const void*)mxfp4_quant_kernel<true> : (const void*)mxfp4_quant_kernel<false>;
+  const int64_t n_units = M * ((K + 1023) / 1024);
+  int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  mxfp4_quant_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  void* args[] = {&a};
+  return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
 }
 
 cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
