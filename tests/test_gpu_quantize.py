@@ -222,6 +222,46 @@ def test_mxfp4_quantize_and_decomposition(nv, M, K):
     assert np.all(np.abs(g - st) <= tol)
 
 
+def _mx_midpoint_blocks():
+    """32-element blocks whose elements sit on (or next to) the E2M1 rounding
+    midpoints at the ideal scale s* = a/6: exact s* (a = 6 * 2^k, 6 * 1.5 * 2^k)
+    puts x/s* exactly on 0.25, 0.75, ... 5 (ties to even), inexact s*
+    (a = 7 * 2^k) puts it within rounding noise of them, and bf16 neighbours of
+    the midpoint elements land just off them."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    rows = []
+    for amax in (6.0, 9.0, 7.0, 6.0 * 2.0 ** -9, 9.0 * 2.0 ** 11, 7.0 * 2.0 ** -20):
+        s_star = amax / 6.0
+        for sign in (1.0, -1.0):
+            v = np.zeros(32)
+            v[0] = amax
+            v[1:8] = sign * mids * s_star
+            v[8:15] = sign * mids * s_star
+            rows.append(v)
+    x = F.bf16_round(np.stack(rows).astype(np.float32))
+    # bf16 neighbours of elements 8..14 (one step up / down in the bit pattern)
+    up, dn = x.copy(), x.copy()
+    b = F.bf16_bits(x[:, 8:15]).astype(np.int32)
+    up[:, 8:15] = F.bf16_from_bits((b + 1).astype(np.uint16))
+    dn[:, 8:15] = F.bf16_from_bits((b - 1).astype(np.uint16))
+    return np.concatenate([x, up, dn]).reshape(-1, 128)
+
+
+def test_mxfp4_ideal_scale_codes_at_midpoints(nv):
+    x = torch.from_numpy(_mx_midpoint_blocks()).to(torch.bfloat16)
+    M, K = x.shape
+    q = nv.mxfp4_quantize(x.cuda(), stats=True)
+    torch.cuda.synchronize()
+    st, cnt, d = omx.block_stats(f32(x))
+    assert np.array_equal(u8(q["codes"]), d["packed"])
+    assert np.array_equal(gather_scales(q["scales"], onv.scale_tile_offsets(M, K // 32)), d["scale"])
+    assert np.array_equal(u8(q["dead"]).reshape(M, K // 32), cnt)
+    assert cnt.sum() > 0  # the 0.25 midpoints tie to code 0
+    g = f32(q["stats"]).reshape(M, K // 32, 4).astype(np.float64)
+    tol = 1e-5 * (st[..., 3:4] + st.sum(-1, keepdims=True)) + 1e-30
+    assert np.all(np.abs(g - st) <= tol)
+
+
 def test_comp_weights_both_modes(nv):
     wt = W.weights_t(256, 512, 11)
     qw = nv.nvfp4_quantize(wt.cuda())
