@@ -63,7 +63,7 @@ static_assert(kColSf + 32 * kStages <= kTmemCols, "TMEM budget");
 
 enum WaitSite : uint32_t {
   kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6,
-  kWaitSfFull = 7, kWaitSfDrain = 8, kWaitSfFull2 = 9
+  kWaitSfFull = 7, kWaitSfDrain = 8, kWaitSfFull2 = 9, kWaitCtLanded = 10
 };
 
 struct GemmParams {
@@ -500,14 +500,17 @@ __global__ void __launch_bounds__(256) splitk_finalize_kernel(const float* __res
 // 256-column accumulator and 4 scale slots of 48 columns (A 16 + B 32), so
 // the compensation term accumulates into the main accumulator: its residual
 // tile is pre-scaled in shared memory by c = 1/g_a (1/(g_a g_b) with BF16
-// weight columns) by a transform warp, and the epilogue applies g_a g_b once.
+// weight columns) and the epilogue applies g_a g_b once.  The eight epilogue
+// warps, idle while a tile's FP4 k-tiles run, do that scaling (2 KB each per
+// compensation k-tile); warp 3 relays each compensation tile's arrival to
+// them through ct_landed[stage].
 // The scale copies of a k-tile are split over two warps (A + B rows 0..127,
 // B rows 128..255): copies issued from different warps proceed side by side.
-// Eight epilogue warps drain the accumulator quickly (two per TMEM lane
+// The epilogue warps drain the accumulator quickly (two per TMEM lane
 // quarter, 128 columns each), release it, then store with 256-bit stores
 // (whole 32-byte sectors per lane).
 //   warp 0 TMA | warp 1 MMA | warp 2 scale copies (A, B low) |
-//   warp 3 scale copies (B high) + residual scaling | warps 4..11 epilogue
+//   warp 3 scale copies (B high) | warps 4..11 residual scaling + epilogue
 constexpr int BNW = 256;
 constexpr int kWStages = 4;
 constexpr int kWTileA = BM * BKB;               // 16 KB
@@ -575,7 +578,8 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   uint64_t* sf_drain = drain + 1;
   uint64_t* sf_full2 = sf_drain + 1;
   uint64_t* sf_drain2 = sf_full2 + kWStages;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain2 + 1);
+  uint64_t* ct_landed = sf_drain2 + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(ct_landed + kWStages);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
@@ -606,8 +610,9 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
       mbar_init(&sf_full[i], 1);
-      mbar_init(&comp_ready[i], 1);
+      mbar_init(&comp_ready[i], 8);
       mbar_init(&sf_full2[i], 1);
+      mbar_init(&ct_landed[i], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -743,7 +748,13 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
       for (int ct = 0; ct < n_ct && ok; ++ct) {
-        if (!mbar_wait_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)) { ok = false; break; }
+        // sf_full too (warp 2's plain arrive): a stage is refilled only after
+        // every role that waits on its full barrier has seen this use
+        if (!mbar_wait_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort) ||
+            !mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         if (elect_one()) {
           const uint32_t sa = smem_u32(stages + stage * kWStageBytes);
@@ -800,20 +811,11 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     __syncwarp();
     mbar_wait_warp(sf_drain, 0, kWaitSfDrain, nullptr);
   } else if (warp == 3) {
-    // ------------ second half of B's scale copies + residual pre-scaling ----
+    // ---------- second half of B's scale copies + compensation relay ----
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    const float ga = p.g_a ? *p.g_a : 1.f;
     for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      int e = 0;
-      if (p.grouped) {
-        Tile tl;
-        tile_of_w(p, sched, t, n_tiles_n, tl);
-        e = tl.e;
-      }
-      float c = __fdiv_rn(1.0f, ga);
-      if (p.flags == 1) c = __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[e] : 1.f));
       // every stage use completes one phase of comp_ready[stage] and of
       // sf_full2[stage], so their parities track the stage's
       for (int kt = 0; kt < n_kt + n_ct && ok; ++kt) {
@@ -829,28 +831,16 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
             const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
             for (int cc = 0; cc < nch; ++cc)
               tmem_cp_32x128b_x4(t_sfb + 8u * cc + 4u, desc_sf(sfb + 2048u + 512u * cc));
+            mbar_arrive_n(&comp_ready[stage], 8);  // whole phase; before the commit the MMA warp waits for
             tc_commit(&sf_full2[stage]);
-            mbar_arrive(&comp_ready[stage]);
           }
         } else {
-          uint4* ra = reinterpret_cast<uint4*>(stages + stage * kWStageBytes);
-#pragma unroll 4
-          for (int i = lane; i < kWTileA / 16; i += 32) {
-            uint4 v = ra[i];
-            uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(w[q] << 16) * c,
-                                                              __uint_as_float(w[q] & 0xFFFF0000u) * c);
-              w[q] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            ra[i] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
+          // compensation k-tile landed: hand it to the epilogue warps, which
+          // wait on ct_landed[stage] (at most one phase ahead of them: the
+          // stage's next compensation use needs their comp_ready arrivals)
           if (elect_one()) {
-            mbar_arrive(&comp_ready[stage]);
             mbar_arrive(&sf_full2[stage]);
+            mbar_arrive(&ct_landed[stage]);
           }
         }
         __syncwarp();
@@ -866,9 +856,46 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     const int h = (warp - 4) >> 2;     // column half
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
+    const int et = threadIdx.x - 128;
+    int stage = 0;
+    uint32_t ct_phase = 0;  // bit s: parity of ct_landed[s]'s next phase
+    const float ga = p.g_a ? *p.g_a : 1.f;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       Tile tl;
       tile_of_w(p, sched, t, n_tiles_n, tl);
+      if (n_ct > 0) {
+        // the compensation k-tiles of this tile: scale the residual tile in
+        // shared memory by c, then release it to the MMA warp
+        float c = __fdiv_rn(1.0f, ga);
+        if (p.flags == 1) c = __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[tl.e] : 1.f));
+        stage = (stage + n_kt) % kWStages;
+        bool okc = true;
+        for (int ct = 0; ct < n_ct; ++ct) {
+          if (!mbar_wait_warp(&ct_landed[stage], (ct_phase >> stage) & 1u, kWaitCtLanded, s_abort)) {
+            okc = false;
+            break;
+          }
+          ct_phase ^= 1u << stage;
+          uint4* ra = reinterpret_cast<uint4*>(stages + stage * kWStageBytes);
+#pragma unroll
+          for (int i = et; i < kWTileA / 16; i += 256) {
+            uint4 v = ra[i];
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(w[qq] << 16) * c,
+                                                              __uint_as_float(w[qq] & 0xFFFF0000u) * c);
+              w[qq] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            ra[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (elect_one()) mbar_arrive(&comp_ready[stage]);  // one of 8 warp arrivals
+          if (++stage == kWStages) stage = 0;
+        }
+        if (!okc) break;
+      }
       if (!mbar_wait(acc_full, acc_phase, kWaitAccFull, s_abort)) break;
       acc_phase ^= 1u;
       tc_fence_after();
