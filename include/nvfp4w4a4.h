@@ -60,6 +60,8 @@ enum { NVFP4_FMT_NVFP4 = 0, NVFP4_FMT_MXFP4 = 1 };
  * the correction then uses the same weights as the W4A4 product), or the
  * original bf16 weight columns. */
 enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1 };
+/* GEMM flag bit, OR-ed with the compensation mode (see w4a4_gemm_comp). */
+enum { NVFP4_GEMM_WEIGHTS_READY = 0x100 };
 
 /* Library version (major*10000 + minor*100 + patch). */
 int nvfp4_version(void);
@@ -235,6 +237,16 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  * resid [M, k] bf16, w_sel [N, k] bf16 (k % 16 == 0; NULL if k == 0)
  * y [M, N] bf16 (16-byte aligned)
  * workspace / ws_bytes: >= w4a4_gemm_workspace_bytes(M, N, K) (may be 0)
+ * flags   NVFP4_COMP_W_DEQ or NVFP4_COMP_W_BF16 (the mode w_sel was prepared
+ *         in), optionally | NVFP4_GEMM_WEIGHTS_READY.
+ * The kernel is a programmatic dependent launch: it may start while the
+ * preceding kernel of the stream is still running (the library's quantizers
+ * let it).  By default it waits for that kernel before touching global
+ * memory, so stream order is kept.  NVFP4_GEMM_WEIGHTS_READY promises that
+ * b_codes, b_scales, g_b and w_sel (and, grouped, offsets) are not written by
+ * work still in flight on the stream; the kernel then starts streaming its
+ * first weight tiles before that wait.  A wrong promise gives wrong results,
+ * not an error.
  */
 size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_codes, const uint8_t* a_scales,

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libnvfp4w4a4.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 COMP_W_DEQ, COMP_W_BF16 = 0, 1
+GEMM_WEIGHTS_READY = 0x100  # flag bit: the weights are not written by work still pending on the stream
 
 _lib = None
 
@@ -237,9 +238,14 @@ def nvfp4_calibrate_channels(x_cal, k, offsets=None):
     return out[0] if offsets is None else out
 
 
-def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_NVFP4, y=None, ws=None):
+def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_NVFP4, y=None, ws=None,
+                   weights_ready=False):
     """y [M, N] bf16 = block-scaled W4A4 product (+ compensation).  qa / qb
-    are the dicts returned by the quantizers (qb for W^T [N, K])."""
+    are the dicts returned by the quantizers (qb for W^T [N, K]).
+    weights_ready: qb and w_sel are not being written by work still pending on
+    the stream, so the kernel may stream them while the preceding kernel runs."""
+    if weights_ready:
+        flags |= GEMM_WEIGHTS_READY
     lib = load()
     a_codes, b_codes = qa["codes"], qb["codes"]
     M, Kh = a_codes.shape
@@ -259,8 +265,12 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
 
 
 def w4a4_grouped_gemm_comp(qa, offsets, b_codes, b_scales, g_b, N, resid=None, w_sel=None, flags=COMP_W_DEQ,
-                           y=None):
-    """MoE: y [M_total, N] bf16; b_codes [E, N, K/2], b_scales E tiles, g_b [E]."""
+                           y=None, weights_ready=False):
+    """MoE: y [M_total, N] bf16; b_codes [E, N, K/2], b_scales E tiles, g_b [E].
+    weights_ready: the weights, g_b, w_sel and offsets are not being written by
+    work still pending on the stream."""
+    if weights_ready:
+        flags |= GEMM_WEIGHTS_READY
     lib = load()
     a_codes = qa["codes"]
     M, Kh = a_codes.shape

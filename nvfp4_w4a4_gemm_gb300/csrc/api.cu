@@ -237,7 +237,8 @@ static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uin
                              const uint8_t* a_scales, const uint8_t* b_codes, const uint8_t* b_scales,
                              const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y) {
   if (fmt != NVFP4_FMT_NVFP4 && fmt != NVFP4_FMT_MXFP4) return NVFP4_ERR_INVALID_ARG;
-  if (flags != NVFP4_COMP_W_DEQ && flags != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
+  const int mode = flags & ~NVFP4_GEMM_WEIGHTS_READY;
+  if (mode != NVFP4_COMP_W_DEQ && mode != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
   if (M < 0 || N <= 0 || K <= 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % (fmt == NVFP4_FMT_MXFP4 ? 128 : 64) != 0) return NVFP4_ERR_UNSUPPORTED;
   if (M > ((int64_t)1 << 31) - 256 || N > ((int64_t)1 << 31) - 256 || K > ((int64_t)1 << 30)) return NVFP4_ERR_UNSUPPORTED;

@@ -55,7 +55,11 @@ constexpr int kStages = 4;             // = number of TMEM scale slots
 constexpr int kTileBytes = BM * BKB;  // 16 KB (A); B the same since BN == BM
 constexpr int kSfBytes = 2048;        // 4 scale chunks of 128 rows x 4 scales
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfBytes;  // 36 KB
-constexpr int kThreads = 224;
+// warps: 0 TMA, 1 MMA, 2..2+kCopyWarps-1 scale copies (one 512-byte chunk
+// each per k-tile: a lone warp issuing all 8 copies of a k-tile paced the
+// decode GEMM), then 4 epilogue warps
+constexpr int kCopyWarps = 4;
+constexpr int kThreads = 32 * (2 + kCopyWarps + 4);
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColComp = 256, kColSf = 384;  // SF: kStages x (16 A + 16 B)
@@ -88,6 +92,10 @@ struct GemmParams {
   float* partial;   // split > 1: fp32 partial sums [split][M][N]
   int y_vec32;      // Y rows start on 32-byte boundaries: 256-bit stores
   uint32_t a_rows;  // narrow kernel: rows of A (and R) each TMA load brings in (BM, or M rounded up to 8 when M < BM)
+  int early_w;      // weights (B codes / scales, W_S, g_b, offsets) are ready: stream them before the wait
+                    // for the preceding kernel (programmatic dependent launch)
+  int swap;         // narrow kernel, M <= 64: weight rows take the MMA's M = 128 slot, tokens its N slot
+  uint32_t n_mma;   // swap: MMA N = M rounded up to 16
 };
 
 struct Tile {
@@ -150,32 +158,54 @@ __device__ __forceinline__ uint32_t idesc_bf16() {
   // D f32 (=1) at bit 4, A/B bf16 (=1) at bits 7 / 10, K-major both.
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+// the same two forms with MMA N = n (swap: the token count rounded up to 16)
+__device__ __forceinline__ uint32_t idesc_fp4_swap(int fmt, uint32_t sf_id, uint32_t n) {
+  uint32_t d = (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  if (fmt == 1) d |= (1u << 23) | (sf_id << 29) | (sf_id << 4);
+  return d;
+}
+__device__ __forceinline__ uint32_t idesc_bf16_swap(uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
 // 128-byte swizzled, K-major operand tile: 8-row atoms of 1024 bytes.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
 // Scale chunk for tcgen05.cp: 32 rows x 16 bytes, no swizzle, 8-row groups 128 bytes apart.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 
+// kSt smem stages (= TMEM scale slots) of kAB bytes of A (or R) plus a 128-row
+// B tile and both scale blocks.  kAB < 16 KB is the swapped-operand form
+// (M <= 64): its accumulators are at most 64 columns wide, so TMEM packs
+// them tighter and holds more scale slots.
+template <int kSt, int kAB>
 __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int kStageB = kAB + kTileBytes + 2 * kSfBytes;
+  constexpr bool kCompact = kAB < kTileBytes;
+  constexpr uint32_t kAcc0 = kColAcc0, kAcc1 = kCompact ? 64u : kColAcc1, kComp = kCompact ? 128u : kColComp,
+                     kSf = kCompact ? 192u : kColSf;
+  static_assert(kSf + 32u * kSt <= kTmemCols, "TMEM budget");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled stages
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSt * kStageB);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* empty = bars + kSt;
+  uint64_t* acc_full = bars + 2 * kSt;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* comp_empty = acc_empty + 2;
   uint64_t* drain = comp_empty + 1;
   uint64_t* sf_full = drain + 1;
-  uint64_t* sf_drain = sf_full + kStages;
+  uint64_t* sf_drain = sf_full + kSt;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // launched as a programmatic dependent: without the early-weights promise
+  // nothing touches global memory before the preceding kernel has finished
+  if (!p.early_w) pdl_wait();
 
   SchedSmem sched{};
   int64_t num_tiles;
@@ -200,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     }
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSt; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -210,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     }
     mbar_init(comp_empty, 4);
     mbar_init(drain, 1);
-    for (int i = 0; i < kStages; ++i) mbar_init(&sf_full[i], 1);
-    mbar_init(sf_drain, 1);
+    for (int i = 0; i < kSt; ++i) mbar_init(&sf_full[i], kCopyWarps);
+    mbar_init(sf_drain, kCopyWarps);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -249,6 +279,48 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       }
     }
     __syncwarp();
+    // one FP4 k-tile: the A half (activations: written by the preceding
+    // kernel) and the B half (weights)
+    auto sf_bytes_of = [&](int kt) {
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+      return (uint32_t)nch * 512u;
+    };
+    auto issue_b = [&](int stg, const Tile& tl, int kt) {
+      uint8_t* sb = stages + stg * kStageB + kAB;
+      uint8_t* sfb = sb + kTileBytes + kSfBytes;
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stg], kt * BKB, tl.n0, tl.e);
+      else tma_load_2d(sb, &p.tm_b, &full[stg], kt * BKB, tl.n0);
+      bulk_load(sfb, p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride + ((uint64_t)(tl.n0 / BN) * n_cg + cg0) * 512u,
+                sf_bytes_of(kt), &full[stg]);
+    };
+    auto issue_a = [&](int stg, const Tile& tl, int kt) {
+      uint8_t* sa = stages + stg * kStageB;
+      uint8_t* sfa = sa + kAB + kTileBytes;
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      tma_load_2d(sa, &p.tm_a, &full[stg], kt * BKB, (int32_t)tl.row0);
+      bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes_of(kt), &full[stg]);
+    };
+    // early weights: the B halves of this CTA's first k-tiles go out before
+    // the wait for the preceding kernel (the ring starts empty)
+    int pre = 0;
+    if (p.early_w && blockIdx.x < num_units) {
+      Tile tl;
+      tile_of(p, sched, blockIdx.x / split, n_tiles_n, tl);
+      const int kt0 = kt_lo(blockIdx.x);
+      pre = kt_hi(blockIdx.x) - kt0;
+      if (pre > kSt) pre = kSt;
+      if (elect_one()) {
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], p.a_rows * BKB + kTileBytes + 2u * sf_bytes_of(kt0 + i));
+          issue_b(i, tl, kt0 + i);
+        }
+      }
+      __syncwarp();
+    }
+    if (p.early_w) pdl_wait();
+    int issued = 0;  // FP4 k-tiles this CTA has issued
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -257,43 +329,33 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       tile_of(p, sched, u / split, n_tiles_n, tl);
       const int kt1 = kt_hi(u), n_ct_u = ct_of(u);
       for (int kt = kt_lo(u); kt < kt1 && ok; ++kt) {
-        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        const bool early = issued++ < pre;  // B half already in flight, stage known empty
+        if (!early && !mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
-          uint8_t* sa = stages + stage * kStageBytes;
-          uint8_t* sb = sa + kTileBytes;
-          uint8_t* sfa = sb + kTileBytes;
-          uint8_t* sfb = sfa + kSfBytes;
-          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
-          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
-          const uint32_t sf_bytes = (uint32_t)nch * 512u;
-          mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes + 2u * sf_bytes);
-          tma_load_2d(sa, &p.tm_a, &full[stage], kt * BKB, (int32_t)tl.row0);
-          if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0, tl.e);
-          else tma_load_2d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0);
-          bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
-          bulk_load(sfb, p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride + ((uint64_t)(tl.n0 / BN) * n_cg + cg0) * 512u,
-                    sf_bytes, &full[stage]);
+          if (!early) mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes + 2u * sf_bytes_of(kt));
+          issue_a(stage, tl, kt);
+          if (!early) issue_b(stage, tl, kt);
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
       for (int ct = 0; ct < n_ct_u && ok; ++ct) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
-          uint8_t* sa = stages + stage * kStageBytes;
-          uint8_t* sb = sa + kTileBytes;
+          uint8_t* sa = stages + stage * kStageB;
+          uint8_t* sb = sa + kAB;
           mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes);
           tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
           if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok) {
       // wind down: let copies already issued land before the CTA exits
-      for (int i = 0; i < kStages; ++i) {
+      for (int i = 0; i < kSt; ++i) {
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(&full[i], 0) && !mbar_try_wait(&full[i], 1)) {
           if (globaltimer() - t0 > 1000000ull) break;
@@ -312,14 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
       const int kt0 = kt_lo(u), kt1 = kt_hi(u), n_ct_u = ct_of(u);
       if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_acc = tmem + (acc ? kColAcc1 : kColAcc0);
+      const uint32_t d_acc = tmem + (acc ? kAcc1 : kAcc0);
       for (int kt = kt0; kt < kt1 && ok; ++kt) {
         if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t sa = smem_u32(stages + stage * kStageBytes);
-          const uint32_t sb = sa + kTileBytes;
-          const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
+          const uint32_t sa = smem_u32(stages + stage * kStageB);
+          const uint32_t sb = sa + kAB;
+          const uint32_t col_sf = kSf + (uint32_t)stage * 32u;
           const uint32_t t_sfa = tmem + col_sf, t_sfb = tmem + col_sf + 16u;
           const int64_t krem = p.K - (int64_t)kt * 256;
           const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
@@ -327,7 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
             const uint64_t adesc = desc_sw128(sa + 32u * j);
             const uint64_t bdesc = desc_sw128(sb + 32u * j);
             const uint32_t accum = (kt > kt0 || j > 0) ? 1u : 0u;
-            if (p.fmt == 1) {
+            if (p.swap) {
+              // D^T = W X^T: the weight tile is the MMA's A, the token tile its B
+              if (p.fmt == 1) {
+                mma_mxf4_2x(d_acc, bdesc, adesc, idesc_fp4_swap(1, (uint32_t)(j & 1) * 2u, p.n_mma),
+                            t_sfb + 4u * (j >> 1), t_sfa + 4u * (j >> 1), accum);
+              } else {
+                mma_nvf4_4x(d_acc, bdesc, adesc, idesc_fp4_swap(0, 0, p.n_mma), t_sfb + 4u * j, t_sfa + 4u * j,
+                            accum);
+              }
+            } else if (p.fmt == 1) {
               mma_mxf4_2x(d_acc, adesc, bdesc, idesc_fp4(1, (uint32_t)(j & 1) * 2u), t_sfa + 4u * (j >> 1),
                           t_sfb + 4u * (j >> 1), accum);
             } else {
@@ -337,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           tc_commit(&empty[stage]);
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
       if (n_ct_u > 0 && ok) {
         if (!mbar_wait_warp(comp_empty, comp_phase ^ 1u, kWaitCompEmpty, s_abort)) { ok = false; break; }
@@ -347,18 +418,22 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) { ok = false; break; }
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t sa = smem_u32(stages + stage * kStageBytes);
-            const uint32_t sb = sa + kTileBytes;
+            const uint32_t sa = smem_u32(stages + stage * kStageB);
+            const uint32_t sb = sa + kAB;
             const int krem = p.k - ct * 64;
             const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
             for (int j = 0; j < n_mma; ++j) {
-              mma_bf16(tmem + kColComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
-                       (ct > 0 || j > 0) ? 1u : 0u);
+              if (p.swap)
+                mma_bf16(tmem + kComp, desc_sw128(sb + 32u * j), desc_sw128(sa + 32u * j),
+                         idesc_bf16_swap(p.n_mma), (ct > 0 || j > 0) ? 1u : 0u);
+              else
+                mma_bf16(tmem + kComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
+                         (ct > 0 || j > 0) ? 1u : 0u);
             }
             tc_commit(&empty[stage]);
           }
           __syncwarp();
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == kSt) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) break;
@@ -371,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
-  } else if (warp == 2) {
+  } else if (warp < 2 + kCopyWarps) {
     // ------------------------------------------------- scale copies ----
     int stage = 0;
     uint32_t phase = 0;
@@ -383,22 +458,22 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         if (kt < kt1) {
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t sfa = smem_u32(stages + stage * kStageBytes) + 2u * kTileBytes;
+            const uint32_t sfa = smem_u32(stages + stage * kStageB) + (uint32_t)(kAB + kTileBytes);
             const uint32_t sfb = sfa + kSfBytes;
-            const uint32_t col_sf = kColSf + (uint32_t)stage * 32u;
+            const uint32_t col_sf = kSf + (uint32_t)stage * 32u;
             const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
             const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
-            for (int c = 0; c < nch; ++c) {
+            for (int c = warp - 2; c < nch; c += kCopyWarps) {
               tmem_cp_32x128b_x4(tmem + col_sf + 4u * c, desc_sf(sfa + 512u * c));
               tmem_cp_32x128b_x4(tmem + col_sf + 16u + 4u * c, desc_sf(sfb + 512u * c));
             }
-            tc_commit(&sf_full[stage]);
+            tc_commit(&sf_full[stage]);  // one of kCopyWarps arrivals (a warp with no chunk commits at once)
           }
         } else {
           if (elect_one()) mbar_arrive(&sf_full[stage]);  // compensation k-tile: nothing to copy
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
     }
     if (elect_one()) tc_commit(sf_drain);
@@ -407,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   } else {
     // ------------------------------------------------------ epilogue ----
     const int q = warp & 3;  // TMEM lane quarter of this warp
+    if (p.early_w) pdl_wait();  // g_a and the output may belong to the preceding kernel
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -423,8 +499,38 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         alpha = ga * gb;
         beta = (p.flags == 1) ? 1.f : gb;
       }
-      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kColAcc1 : kColAcc0);
-      const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kColComp;
+      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kAcc1 : kAcc0);
+      const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kComp;
+      if (p.swap) {
+        // accumulator lane r = output column n0 + r, TMEM column m = token row
+#pragma unroll 1
+        for (int c = 0; c < (int)p.n_mma; c += 16) {
+          uint32_t v[16], w[16];
+          tmem_ld_32x32b_x16(t_acc + c, v);
+          if (n_ct_u > 0) tmem_ld_32x32b_x16(t_cmp + c, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float yv = alpha * __uint_as_float(v[i]);
+            if (n_ct_u > 0) yv = fmaf(beta, __uint_as_float(w[i]), yv);
+            const int m = c + i;
+            if (m < tl.rows) {
+              const int64_t off = (tl.row0 + m) * p.N + tl.n0 + r;
+              if (split > 1) p.partial[(u % split) * p.M * p.N + off] = yv;
+              else p.y[off] = __float2bfloat16_rn(yv);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[acc]);
+          if (n_ct_u > 0) mbar_arrive(comp_empty);
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
       const bool row_ok = r < tl.rows;
       __nv_bfloat16* yrow = p.y + (tl.row0 + r) * p.N + tl.n0;
 #pragma unroll 1
@@ -585,6 +691,9 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // launched as a programmatic dependent: without the early-weights promise
+  // nothing touches global memory before the preceding kernel has finished
+  if (!p.early_w) pdl_wait();
   SchedSmem sched{};
   const int n_tiles_n = (int)((p.N + BNW - 1) / BNW);
   if (p.grouped) {
@@ -648,31 +757,65 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       }
     }
     __syncwarp();
+    // one FP4 k-tile: the A half (activations: written by the preceding
+    // kernel) and the B half (weights)
+    auto sf_bytes_of = [&](int kt) {
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
+      return (uint32_t)nch * 512u;
+    };
+    auto tx_of = [&](const Tile& tl, int kt) {
+      return (uint32_t)(kWTileA + kWTileB) + sf_bytes_of(kt) * (tl.n_valid ? 3u : 2u);
+    };
+    auto issue_b = [&](int stg, const Tile& tl, int kt) {
+      uint8_t* sb = stages + stg * kWStageBytes + kWTileA;
+      uint8_t* sfb = sb + kWTileB + kWSfA;
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      const uint32_t sf_bytes = sf_bytes_of(kt);
+      const uint8_t* sfb_src0 = p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride;
+      if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stg], kt * BKB, tl.n0, tl.e);
+      else tma_load_2d(sb, &p.tm_b, &full[stg], kt * BKB, tl.n0);
+      const uint64_t bt = (uint64_t)(tl.n0 / 128);
+      bulk_load(sfb, sfb_src0 + (bt * n_cg + cg0) * 512u, sf_bytes, &full[stg]);
+      if (tl.n_valid) bulk_load(sfb + 2048, sfb_src0 + ((bt + 1) * n_cg + cg0) * 512u, sf_bytes, &full[stg]);
+    };
+    auto issue_a = [&](int stg, const Tile& tl, int kt) {
+      uint8_t* sa = stages + stg * kWStageBytes;
+      uint8_t* sfa = sa + kWTileA + kWTileB;
+      const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
+      tma_load_2d(sa, &p.tm_a, &full[stg], kt * BKB, (int32_t)tl.row0);
+      bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes_of(kt), &full[stg]);
+    };
+    // early weights: the B halves of this CTA's first k-tiles go out before
+    // the wait for the preceding kernel (the ring starts empty)
+    int pre = 0;
+    if (p.early_w && blockIdx.x < num_tiles) {
+      Tile tl;
+      tile_of_w(p, sched, blockIdx.x, n_tiles_n, tl);
+      pre = n_kt < kWStages ? n_kt : kWStages;
+      if (elect_one()) {
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], tx_of(tl, i));
+          issue_b(i, tl, i);
+        }
+      }
+      __syncwarp();
+    }
+    if (p.early_w) pdl_wait();
+    int issued = 0;  // FP4 k-tiles this CTA has issued
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       Tile tl;
       tile_of_w(p, sched, t, n_tiles_n, tl);
-      const uint8_t* sfb_src0 = p.b_sf + (uint64_t)tl.e * p.b_sf_expert_stride;
       for (int kt = 0; kt < n_kt && ok; ++kt) {
-        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        const bool early = issued++ < pre;  // B half already in flight, stage known empty
+        if (!early && !mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
-          uint8_t* sa = stages + stage * kWStageBytes;
-          uint8_t* sb = sa + kWTileA;
-          uint8_t* sfa = sb + kWTileB;
-          uint8_t* sfb = sfa + kWSfA;
-          const int64_t cg0 = (int64_t)kt * sf_chunks_per_kt;
-          const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
-          const uint32_t sf_bytes = (uint32_t)nch * 512u;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWTileA + kWTileB) + sf_bytes * (tl.n_valid ? 3u : 2u));
-          tma_load_2d(sa, &p.tm_a, &full[stage], kt * BKB, (int32_t)tl.row0);
-          if (p.grouped) tma_load_3d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0, tl.e);
-          else tma_load_2d(sb, &p.tm_b, &full[stage], kt * BKB, tl.n0);
-          bulk_load(sfa, p.a_sf + ((uint64_t)tl.sf_rt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
-          const uint64_t bt = (uint64_t)(tl.n0 / 128);
-          bulk_load(sfb, sfb_src0 + (bt * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
-          if (tl.n_valid) bulk_load(sfb + 2048, sfb_src0 + ((bt + 1) * n_cg + cg0) * 512u, sf_bytes, &full[stage]);
+          if (!early) mbar_arrive_expect_tx(&full[stage], tx_of(tl, kt));
+          issue_a(stage, tl, kt);
+          if (!early) issue_b(stage, tl, kt);
         }
         __syncwarp();
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
@@ -853,6 +996,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   } else {
     // ------------------------------------------------------ epilogue ----
     const int q = warp & 3;            // TMEM lane quarter
+    if (p.early_w) pdl_wait();  // g_a and the output may belong to the preceding kernel
     const int h = (warp - 4) >> 2;     // column half
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
@@ -980,6 +1124,9 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
 }
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+// swapped-operand form: 8 KB A regions (64 rows), 7 stages (TMEM holds 7 scale slots after the packed accumulators)
+constexpr int kSwapStages = 7, kSwapA = 64 * BKB;
+constexpr size_t kSwapSmemBytes = 1024 + (size_t)kSwapStages * (kSwapA + kTileBytes + 2 * kSfBytes) + 256;
 
 // K splits for the narrow kernel: when its tiles leave most SMs idle (few
 // rows and a narrow N), each tile's K range is split so the units cover about
@@ -999,6 +1146,25 @@ int narrow_split(int64_t M, int64_t N, int64_t K, int num_sms) {
   return (int)(s < 1 ? 1 : s);
 }
 
+// Every GEMM is a programmatic dependent launch: its CTAs may start while
+// the preceding kernel of the stream (normally the activation quantizer,
+// which releases its dependents as it starts) is still running; the kernel
+// itself decides what may run before griddepcontrol.wait (GemmParams::early_w).
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream, const GemmParams& p) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -1010,6 +1176,10 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
     // a single M tile with fewer rows loads only those rows (rounded up to 8):
     // rows past M are never stored, so the rest of the smem tile may hold anything
     p.a_rows = (!grouped && pr.M < BM) ? (uint32_t)((pr.M + 7) / 8 * 8) : (uint32_t)BM;
+    // up to 64 tokens: swap the operands so the MMA's 128-row slot holds weight
+    // rows (all valid) and its N slot the tokens, rounded up to 16
+    p.swap = (!grouped && pr.M <= 64) ? 1 : 0;
+    p.n_mma = (uint32_t)((pr.M + 15) / 16 * 16);
     if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, p.a_rows))
       return cudaErrorInvalidValue;
   }
@@ -1045,7 +1215,8 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   p.N = pr.N;
   p.K = pr.K;
   p.k = pr.k;
-  p.flags = pr.flags;
+  p.flags = pr.flags & kGemmCompBf16;
+  p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
   p.fmt = pr.fmt;
   p.E = E;
   p.offsets = pr.offsets;
@@ -1062,10 +1233,13 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   const int64_t units = tiles * p.split;
   int grid = (int)(units < num_sms ? units : num_sms);
   if (grid < 1) grid = 1;
-  const size_t smem = kSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
-  cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem =
+      (p.swap ? kSwapSmemBytes : kSmemBytes) + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
+  auto kern = p.swap ? w4a4_gemm_kernel<kSwapStages, kSwapA> : w4a4_gemm_kernel<kStages, kTileBytes>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  w4a4_gemm_kernel<<<grid, kThreads, smem, stream>>>(p);
+  err = launch_dependent(kern, grid, kThreads, smem, stream, p);
+  if (err != cudaSuccess) return err;
   if (p.split > 1) {
     const int64_t n4 = pr.M * pr.N / 4;
     int64_t blocks = (n4 + 255) / 256;
@@ -1118,7 +1292,8 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   p.N = pr.N;
   p.K = pr.K;
   p.k = pr.k;
-  p.flags = pr.flags;
+  p.flags = pr.flags & kGemmCompBf16;
+  p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
   p.fmt = pr.fmt;
   p.E = E;
   p.offsets = pr.offsets;
@@ -1131,7 +1306,10 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   const size_t smem = kWSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
   cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  w4a4_gemm_wide_kernel<<<grid, kWThreads, smem, stream>>>(p);
+  {
+    const cudaError_t err = launch_dependent(w4a4_gemm_wide_kernel, grid, kWThreads, smem, stream, p);
+    if (err != cudaSuccess) return err;
+  }
   return cudaGetLastError();
 }
 

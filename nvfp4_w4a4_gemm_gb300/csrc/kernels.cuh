@@ -49,6 +49,9 @@ cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int
                                           __nv_bfloat16* resid, int num_sms, cudaStream_t stream);
 
 // ----------------------------------------------------------------- GEMM ----
+// GemmProblem::flags bits (the C ABI's values)
+constexpr int kGemmCompBf16 = 1;          // compensation columns are the BF16 weights
+constexpr int kGemmWeightsReady = 0x100;  // weights may be read before the preceding kernel ends
 struct GemmProblem {
   int fmt = 0;  // 0 NVFP4, 1 MXFP4
   int64_t M = 0, N = 0, K = 0;

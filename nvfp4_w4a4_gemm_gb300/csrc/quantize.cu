@@ -433,6 +433,7 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
 
 template <bool kGrouped, bool kFused, bool kFull>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
+  pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
   extern __shared__ __align__(16) int32_t smem_i32[];
   __shared__ float2 s_dr[256];
   // offsets [E+1] | padded bases [E] | dense only: bitmap words [n_words] |
@@ -453,24 +454,12 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   walk.r = walk.u / walk.gpr;
   walk.gi = walk.u - walk.r * walk.gpr;
 
-  float g;
-  if (kFused) {
-    // tensor amax of this launch: per-CTA maxima, one grid barrier, then
-    // every CTA reduces all of them (the quantize pass below re-reads X,
-    // mostly from L2)
-    __shared__ float red[kThreads / 32];
-    const float m = warp_units_amax(a, walk, lane);
-    if (lane == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float b = 0.f;
-      for (int i = 0; i < kThreads / 32; ++i) b = fmaxf(b, red[i]);
-      a.partials[blockIdx.x] = b;
-    }
-    if (!grid_barrier(a.bar)) return;
-    g = tensor_scale_from_partials(a.partials, (int)gridDim.x);
-  }
-
+  // the first unit's loads go out before anything else (the fused pass
+  // issues them after its grid barrier); the channel tables below do not
+  // depend on g, so they are built before that barrier
+  uint4 va[4], vb[4];
+  UnitWalk wa = walk;
+  if (!kFused && wa.u < walk.n_units) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
   if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
   if (a.use_map) {
@@ -540,6 +529,26 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
       }
     }
   }
+  float g;
+  if (kFused) {
+    // tensor amax of this launch: per-CTA maxima, one grid barrier, then
+    // every CTA reduces all of them (the quantize pass below re-reads X,
+    // mostly from L2)
+    __shared__ float red[kThreads / 32];
+    const float m = warp_units_amax(a, walk, lane);
+    if (lane == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.f;
+      for (int i = 0; i < kThreads / 32; ++i) b = fmaxf(b, red[i]);
+      a.partials[blockIdx.x] = b;
+    }
+    if (!grid_barrier(a.bar)) return;
+    // this warp's first unit (mostly in L2) is in flight while g is reduced
+    if (wa.u < walk.n_units) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+    g = tensor_scale_from_partials(a.partials, (int)gridDim.x);
+  }
+
   if (!kFused) {
     if (a.g_in != nullptr) g = *a.g_in;
     else g = tensor_scale_from_partials(a.partials, a.n_partials);  // contains __syncthreads
@@ -565,9 +574,6 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   t.off = s_off; t.pbase = s_pbase; t.pref = s_pref;
   t.n_words = n_words;
   const uint32_t n = walk.n_units;
-  uint4 va[4], vb[4];
-  UnitWalk wa = walk;
-  if (wa.u < n) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
   while (wa.u < n) {
     UnitWalk wb = wa;
     wb.next();
@@ -639,6 +645,7 @@ __device__ __forceinline__ float2 e2m1x2_vals(uint32_t byte) {
 // block (64 bytes: two sector-aligned 32-byte loads).
 template <bool kStats>
 __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
+  pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
   const int lane = threadIdx.x & 31;
   const int64_t nblk = a.K / 32;
   const int64_t n_cg = (nblk + 3) / 4;

@@ -53,7 +53,9 @@ def test_tiny_workload(nv):
 
 
 @pytest.mark.parametrize("M,N,K,k", [(128, 128, 256, 0), (300, 384, 1024, 64), (77, 256, 320, 72),
-                                     (1, 128, 64, 8), (513, 128, 2048, 128), (16, 640, 4096, 64)])
+                                     (1, 128, 64, 8), (513, 128, 2048, 128), (16, 640, 4096, 64),
+                                     # up to 64 tokens the operands are swapped (MMA N = M rounded up to 16)
+                                     (40, 256, 1024, 16), (5, 384, 512, 24), (64, 128, 768, 0), (17, 1024, 2048, 64)])
 def test_shapes(nv, M, N, K, k):
     x = W.activations(M, K, max(1, K // 100), "t3x20", K + 1, M + 2)
     wt = W.weights_t(N, K, N + K)
@@ -71,6 +73,14 @@ def test_bf16_weight_flag(nv):
     _assert_close(y, y_ref)
 
 
+def test_bf16_weight_flag_swapped_operands(nv):
+    x = W.activations(48, 512, 5, "t3x20", 11, 11)
+    wt = W.weights_t(384, 512, 12)
+    chan = np.arange(3, 512, 16)
+    y, y_ref = _dense_case(nv, x, wt, chan, flags=1)
+    _assert_close(y, y_ref)
+
+
 def test_full_compensation_k_equals_K(nv):
     x = W.activations(64, 256, 4, "x50", 1, 1)
     wt = W.weights_t(128, 256, 2)
@@ -78,7 +88,8 @@ def test_full_compensation_k_equals_K(nv):
     _assert_close(y, y_ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 384, 640), (8192 // 16, 5120 // 10, 5120)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 384, 640), (8192 // 16, 5120 // 10, 5120),
+                                   (16, 256, 512), (33, 384, 1024)])
 def test_mxfp4_gemm(nv, M, N, K):
     N = (N + 127) // 128 * 128
     x = W.activations(M, K, max(1, K // 100), "t3x20", 5, M)
@@ -127,3 +138,65 @@ def test_grouped_gemm_small(nv):
     ws = np.stack([og.comp_weight_rows(bq[e], chan[e]) for e in range(E)])
     y_ref = og.grouped_reference(a, offs, b, rq["resid"], ws)
     _assert_close(f32(y), y_ref)
+
+
+@pytest.mark.parametrize("M,N,K,k", [(16, 1024, 4096, 64), (200, 384, 1024, 32), (600, 512, 2048, 128)])
+def test_weights_ready_overlap_is_bit_identical(nv, M, N, K, k):
+    """The GEMM starts while the activation quantizer before it still runs
+    (programmatic dependent launch).  With the weights-ready flag it also
+    streams weight tiles before waiting for that quantizer: the output must be
+    bit-identical to the default order, and within tolerance of the oracle."""
+    x = W.activations(M, K, max(1, K // 100), "t3x20", 21, 22)
+    wt = W.weights_t(N, K, 23)
+    ch = torch.arange(0, K, K // k, dtype=torch.int32)[:k].cuda().contiguous()
+    qw = nv.nvfp4_quantize(wt.cuda())
+    ws = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], ch)
+    xd = x.cuda()
+    torch.cuda.synchronize()
+    ys = []
+    for ready in (False, True, True):
+        qx = nv.nvfp4_quantize(xd, chan=ch)  # the kernel just before the GEMM
+        ys.append(nv.w4a4_gemm_comp(qx, qw, N, resid=qx["resid"], w_sel=ws, weights_ready=ready))
+    torch.cuda.synchronize()
+    st, _ = nv.check_status()
+    assert st == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    y_ref, _, _ = og.linear_comp(f32(x), f32(wt), ch.cpu().numpy().astype(np.int64))
+    _assert_close(f32(ys[1]).astype(np.float64), y_ref)
+
+
+def test_weights_ready_grouped_and_mxfp4(nv):
+    counts = [3, 0, 200, 57]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, K, N, k, E = int(offs[-1]), 1024, 256, 16, len(counts)
+    x = W.activations(M, K, 5, "t3x20", 31, 32).cuda()
+    wt = W.weights_t(N, K, 33, experts=E)
+    rng = np.random.default_rng(3)
+    chan_t = torch.from_numpy(np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)])
+                              .astype(np.int32)).cuda()
+    offs_t = torch.from_numpy(offs).cuda()
+    qs = [nv.nvfp4_quantize(wt[e].cuda()) for e in range(E)]
+    b_codes = torch.stack([q["codes"] for q in qs])
+    b_scales = torch.cat([q["scales"] for q in qs])
+    g_b = torch.cat([q["g"] for q in qs])
+    w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan_t, E=E)
+    torch.cuda.synchronize()
+    ys = []
+    for ready in (False, True):
+        qx = nv.nvfp4_quantize_grouped(x, offs_t, chan_t)
+        ys.append(nv.w4a4_grouped_gemm_comp(qx, offs_t, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel,
+                                            weights_ready=ready))
+    xm = W.activations(48, 512, 5, "t3x20", 34, 35).cuda()
+    qwm = nv.mxfp4_quantize(W.weights_t(256, 512, 36).cuda())
+    torch.cuda.synchronize()
+    ym = []
+    for ready in (False, True):
+        qxm = nv.mxfp4_quantize(xm)
+        ym.append(nv.w4a4_gemm_comp(dict(codes=qxm["codes"], scales=qxm["scales"]),
+                                    dict(codes=qwm["codes"], scales=qwm["scales"]), 256, fmt=nv.FMT_MXFP4,
+                                    weights_ready=ready))
+    torch.cuda.synchronize()
+    st, _ = nv.check_status()
+    assert st == 0
+    assert torch.equal(ys[0], ys[1])
+    assert torch.equal(ym[0], ym[1])
