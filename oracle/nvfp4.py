@@ -24,6 +24,9 @@ Readings (the pages name NVFP4 but do not define its arithmetic):
   residual R_i = x_i - deq_i in fp32; the emitted slice is bf16(R_i) on the
   channel set S.  The exact value of the quantized representation (used by
   the reference GEMM) is E2M1(code) * sigma * g in fp64.
+* Trainer-side fake quantization (QDQ, asymmetric W4A16 QAT): the same
+  codes and scales, and per element bf16_rn(deq_i), deq_i as above (the
+  fp32 product rounded once more to bf16, the trainer's weight dtype).
 * Packing: two codes per byte, byte j = code[2j] | code[2j+1] << 4.
 * Block-scale storage for the GEMM: 128-row x 4-scale tiles of 512 bytes,
   byte offset inside a tile = (r % 32) * 16 + ((r % 128) // 32) * 4 + (s % 4)
@@ -137,6 +140,30 @@ def unpack(packed):
     out[..., 0::2] = packed & 0xF
     out[..., 1::2] = packed >> 4
     return out
+
+
+def qdq(x, g=None):
+    """Trainer-side weight fake quantization (quantize, then dequantize) of
+    ``x`` [M, K] (float32 values of bf16 numbers, K the reduction axis).
+
+    Source: gist.science explainer of QUADS, Technisches Resuemee 2.2 A
+    (asymmetric W4A16 QAT: the trainer fake-quantizes its weights to NVFP4 so
+    its forward pass sees the discretized weights the rollout engine uses;
+    activations stay BF16) and section 2.1 (the same quantize-dequantize path
+    on both sides removes the weight-induced mismatch).
+
+    Reading: the same quantization as :func:`quantize` (same g, sigma and
+    codes), and the element value the residual is measured against,
+    deq = fp32(E2M1(code) * d), delivered in the trainer's dtype:
+    bf16_rn(deq).  Returns (w_qdq [M, K] float32 holding bf16 values, the
+    :func:`quantize` dict).
+    """
+    q = quantize(x, g=g)
+    M, K = q["codes"].shape
+    d = (e4m3_decode(q["sigma"]).astype(np.float32) * np.float32(q["g"])).astype(np.float32)
+    v = e2m1_value(q["codes"]).astype(np.float32).reshape(M, K // BLOCK, BLOCK)
+    deq = (v * d[:, :, None]).astype(np.float32).reshape(M, K)
+    return bf16_round(deq), q
 
 
 def dequantize(codes, sigma, g):

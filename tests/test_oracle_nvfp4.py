@@ -124,3 +124,110 @@ def test_comp_weights_exact_in_bf16():
     assert np.array_equal(F.bf16_round(ws.astype(np.float32)).astype(np.float64), ws)
     deq = nvfp4.dequantize(q["codes"], q["sigma"], q["g"])
     assert np.array_equal(ws * np.float64(q["g"]), deq[:, chan])
+
+
+# ------------------------------------------------------------ QDQ pins ----
+@pytest.mark.parametrize("idx", [0, 1])
+def test_qdq_worked_examples(golden_dir, idx):
+    ex = _golden(golden_dir)[idx]
+    x = np.array(ex["x"], np.float32)[None, :]
+    w, q = nvfp4.qdq(x)
+    want = np.array(ex["qdq"], np.float32)
+    assert np.array_equal(w[0], want)
+    assert np.array_equal(np.signbit(w[0]), np.signbit(want)), "signs of zero"
+
+
+def _e4m3_values():
+    """Every finite non-negative E4M3 value from the format definition
+    (4 exponent bits, bias 7, 3 mantissa bits, subnormals at exponent 0)."""
+    b = np.arange(0x7F)
+    e, m = b >> 3, b & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def _nearest_even(values, t):
+    """Index of the entry of sorted `values` nearest to each t (ties: even
+    index), saturating at the ends: a brute-force search."""
+    dist = np.abs(values[None, :] - t[:, None])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    idx = np.where(cand, np.arange(len(values))[None, :], 1 << 20)
+    even = np.where(cand & (np.arange(len(values))[None, :] % 2 == 0), idx, 1 << 20).min(axis=1)
+    return np.where(even < (1 << 20), even, idx.min(axis=1))
+
+
+def _qdq_brute_force(x, g):
+    """QDQ of a [1, 16*nb] row re-derived by enumeration over both grids."""
+    import torch
+    f = np.float32
+    xb = x.reshape(-1, 16).astype(np.float32)
+    e4 = _e4m3_values()
+    e2 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    out = np.zeros_like(xb)
+    for i, blk in enumerate(xb):
+        a = np.max(np.abs(blk))
+        t = f(f(a / f(6)) / f(g))
+        sig = e4[min(_nearest_even(e4, np.array([float(t)]))[0], 0x7E)]
+        d = f(f(sig) * f(g))
+        if d == 0:
+            continue
+        y = (blk * f(f(1) / d)).astype(np.float32)
+        mag = e2[_nearest_even(e2, np.minimum(np.abs(y).astype(np.float64), 6.0))]
+        val = np.where(np.signbit(y), -mag, mag).astype(np.float32)
+        deq = (val * d).astype(np.float32)
+        out[i] = torch.from_numpy(deq).to(torch.bfloat16).float().numpy()
+    return out.reshape(x.shape)
+
+
+@pytest.mark.parametrize("g", [None, 1.0, 1.0 / 3.0, 0.0123, 2.0 ** -9])
+def test_qdq_matches_brute_force_grids(g):
+    x = W.activations(6, 256, 4, "t3x20", 5, 6).float().numpy()
+    w, q = nvfp4.qdq(x, g=g)
+    gg = q["g"]
+    for r in range(x.shape[0]):
+        want = _qdq_brute_force(x[r], gg)
+        assert np.array_equal(w[r], want), f"row {r}"
+        assert np.array_equal(np.signbit(w[r]), np.signbit(want))
+
+
+@pytest.mark.parametrize("j", [-12, -4, 0, 3])
+def test_qdq_idempotent_under_power_of_two_scale(j):
+    g = np.float32(2.0 ** j)
+    x = W.activations(8, 512, 5, "t3x20", 7, 8).float().numpy() * np.float32(2.0 ** (j + 8))
+    w1, q1 = nvfp4.qdq(x, g=g)
+    w2, q2 = nvfp4.qdq(w1, g=g)
+    assert np.array_equal(w1, w2)
+    assert np.array_equal(q1["codes"] & 7, q2["codes"] & 7) and np.array_equal(q1["sigma"], q2["sigma"])
+
+
+def test_qdq_error_within_one_scale_step():
+    x = W.activations(16, 1024, 10, "t3x20", 9, 10).float().numpy()
+    w, q = nvfp4.qdq(x)
+    d = (F.e4m3_decode(q["sigma"]) * np.float64(q["g"])).repeat(16, axis=1)
+    err = np.abs(w.astype(np.float64) - x)
+    # E2M1 steps are at most 2 d apart (4 -> 6): rounding moves by <= d, the
+    # bf16 rounding of the product by <= 2^-9 of it
+    assert np.all(err <= d * (1 + 2.0 ** -20) + np.abs(w) * 2.0 ** -9)
+
+
+# A block where the two readings of "round E2M1(code) * d to bf16" differ.
+# g = 1.0130208730697632 is an fp32 value (8498517 * 2^-23); a = 6 gives
+# (6 / 6) / g = 0.98715 -> sigma = E4M3(0.98715) = 1, d = g.  x = 3.03125 has
+# x / d = 2.9923 -> code 5 (E2M1 3).  3 d = 3.0390626192... is not an fp32
+# value: fp32(3 d) = 3.0390625, exactly halfway between the bf16 neighbours
+# 3.03125 (even mantissa) and 3.046875, so bf16(fp32(3 d)) = 3.03125 while
+# rounding the exact product once would give 3.046875.
+DOUBLE_ROUNDING_G = 1.0130208730697632
+DOUBLE_ROUNDING_X = [6.0, 3.03125, -3.03125, 0.0] + [0.0] * 12
+
+
+def test_qdq_rounds_the_fp32_product_to_bf16():
+    g = np.float32(DOUBLE_ROUNDING_G)
+    assert float(g) == DOUBLE_ROUNDING_G
+    x = np.array([DOUBLE_ROUNDING_X], np.float32)
+    w, q = nvfp4.qdq(x, g=g)
+    assert q["sigma"][0, 0] == 0x38 and list(q["codes"][0, :3]) == [7, 5, 13]
+    assert w[0, 1] == np.float32(3.03125) and w[0, 2] == np.float32(-3.03125)
+    # the block maximum too: 6 d = 6.0781252384... -> fp32 6.078125, halfway
+    # between bf16 6.0625 (even) and 6.09375 -> 6.0625
+    assert w[0, 0] == np.float32(6.0625)
