@@ -469,6 +469,25 @@ def other_workloads(nv, pk, steps=10):
     out["mxfp4"] = {"shape": "X[8192,5120] x W[5120,5120], MXFP4 + per-block decomposition", "ms_per_step": round(ms, 4),
                     "tflops": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12, 1),
                     "frac_fp4_peak": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12 / fp4_peak, 4)}
+    del qw, x, y, box
+
+    # trainer-side fake quantization (asymmetric W4A16 QAT) of a layer's
+    # weights, emitting the rollout's packed codes and scales in the same pass
+    s = W.SPECS["decode"]
+    wq = W.dense_inputs("decode")["wt"].to(dev)
+    w_out = torch.empty_like(wq)
+
+    def qdq():
+        nv.nvfp4_qdq(wq, with_codes=True, out=w_out)
+    ms = _time_steps(qdq, steps, flush)
+    n_el = wq.numel()
+    byts = n_el * 2 + n_el * 2 + n_el // 2 + nv.load().nvfp4_scale_bytes(s.N, s.K)
+    out["qdq"] = {"shape": "W^T[14336,4096] bf16 -> bf16 QDQ + NVFP4 codes/scales, dynamic tensor scale",
+                  "ms_per_step": round(ms, 4), "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                  "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "bytes_per_step": byts,
+                  "bound": "hbm",
+                  "note": "bytes = W read once + QDQ written + codes + scales; the amax pre-pass reads W a second "
+                          "time (not counted)"}
     return out
 
 

@@ -108,7 +108,7 @@ size_t nvfp4_quantize_workspace_bytes(void);
  * K      multiple of 16;  M >= 0
  * g_in   device float or NULL (dynamic scale; needs workspace)
  * g_out  device float or NULL: receives the tensor scale used
- * codes  [M, K/2] bytes (4-byte aligned)
+ * codes  [M, K/2] bytes (16-byte aligned)
  * scales nvfp4_scale_bytes(M, K) bytes, tiled layout (16-byte aligned)
  * chan   device int32 [k], sorted ascending, unique, in [0, K); NULL if k == 0
  * resid  [M, k] bf16; NULL if k == 0
@@ -163,6 +163,35 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
  */
 int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* g_out, uint8_t* codes,
                            uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* stream);
+
+/*
+ * nvfp4_qdq -- trainer-side NVFP4 fake quantization of a weight matrix
+ * (quantize, then dequantize), the weight half of asymmetric W4A16 QAT.
+ * Source: gist.science explainer of QUADS, Technisches Resuemee 2.2 A (the
+ * trainer fake-quantizes its weights to NVFP4 so that its forward pass sees
+ * the discretized weights the rollout uses; activations stay BF16) and 2.1
+ * (one quantize-dequantize path on both sides removes the weight mismatch).
+ *
+ * Same g, sigma and codes as nvfp4_quantize on the same input (the same
+ * kernels' arithmetic), and per element
+ *   w_qdq[m, i] = bf16_rn(fp32(E2M1(code) * d))     d = fp32(sigma * g)
+ * (the value the compensation residual is measured against, rounded to the
+ * trainer's bf16).  When codes / scales are given they receive the packed
+ * codes and tiled scales of that quantization (what nvfp4_quantize writes),
+ * so the rollout's W4 weights come from the same pass.
+ *
+ * w      [M, K] bf16, rows = output features, K = reduction axis (the W^T
+ *        layout the GEMM's B operand uses), row stride ldw (16-byte aligned
+ *        base, ldw % 8 == 0);  K % 16 == 0
+ * w_qdq  [M, K] bf16 output, row stride ld_out (16-byte aligned, ld_out % 8 == 0);
+ *        may not overlap w
+ * codes, scales  both NULL, or [M, K/2] bytes and nvfp4_scale_bytes(M, K)
+ *        bytes (16-byte aligned)
+ * g_in / g_out / workspace: as nvfp4_quantize (the dynamic scale is an amax
+ *        pre-pass, a second launch; workspace >= nvfp4_quantize_workspace_bytes())
+ */
+int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float* g_in, float* g_out, uint16_t* w_qdq,
+              int64_t ld_out, uint8_t* codes, uint8_t* scales, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * mxfp4_quantize -- MXFP4 quantization (32-element blocks, power-of-two

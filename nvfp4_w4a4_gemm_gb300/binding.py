@@ -41,6 +41,7 @@ _SIGS = {
                                ctypes.c_int),
     "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "nvfp4_qdq": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_prepare_comp_weights": ([_I32, _I64, _I64, _P, _P, _P, _P, _I32, ctypes.c_int, _P, _P], ctypes.c_int),
     "nvfp4_calibrate_workspace_bytes": ([_I64, _I32], _SZ),
     "nvfp4_calibrate_channels": ([_P, _I64, _I64, _I64, _I32, _P, _I32, _P, _P, _SZ, _P], ctypes.c_int),
@@ -142,6 +143,39 @@ def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None):
                             0 if ws is None else ws.numel(), _stream())
     _check("nvfp4_quantize", st)
     return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+
+
+def _need_rows(t, dtype, name):
+    """A CUDA tensor of `dtype` whose rows are contiguous (any row stride)."""
+    if not (t.is_cuda and t.dtype == dtype and t.dim() == 2 and t.stride(1) == 1):
+        raise ValueError(f"{name}: expected a row-contiguous 2-D CUDA {dtype} tensor")
+
+
+def nvfp4_qdq(w, g=None, with_codes=False, out=None):
+    """Trainer-side fake quantization: w bf16 [M, K] -> dict(w_qdq bf16 [M, K],
+    g f32 [1]) and, with with_codes, the packed codes and tiled scales of the
+    same quantization (what nvfp4_quantize returns for w)."""
+    lib = load()
+    _need_rows(w, torch.bfloat16, "w")
+    M, K = w.shape
+    dev = w.device
+    if g is not None:
+        _need(g, torch.float32, "g")
+    w_qdq = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    _need_rows(w_qdq, torch.bfloat16, "out")
+    g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    codes = scales = None
+    if with_codes:
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(lib.nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    ws = None if g is not None else torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    st = lib.nvfp4_qdq(_ptr(w), M, K, w.stride(0), _ptr(g), _ptr(g_out), _ptr(w_qdq), w_qdq.stride(0), _ptr(codes),
+                       _ptr(scales), _ptr(ws), 0 if ws is None else ws.numel(), _stream())
+    _check("nvfp4_qdq", st)
+    r = dict(w_qdq=w_qdq, g=g_out)
+    if with_codes:
+        r.update(codes=codes, scales=scales)
+    return r
 
 
 def nvfp4_quantize_noalloc(x, chan=None, out=None, g_out=None):

@@ -73,7 +73,8 @@ int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8
   // the quantizers index (row, 1024-column group) work units with 32 bits
   if (M * ((K + 1023) / 1024) >= ((int64_t)1 << 31)) return NVFP4_ERR_UNSUPPORTED;
   if (M == 0) return NVFP4_OK;
-  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) || !aligned(scales, 16))
+  // codes go out in 8-byte (NVFP4) and 16-byte (MXFP4) stores
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16))
     return NVFP4_ERR_INVALID_ARG;
   if (k < 0 || k > K) return NVFP4_ERR_INVALID_ARG;
   if (k > 0 && (!chan || !resid || !aligned(chan, 4) || !aligned(resid, 2))) return NVFP4_ERR_INVALID_ARG;
@@ -175,6 +176,24 @@ int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   return from_cuda(nv4::launch_mxfp4_quantize(bf(x), M, K, ldx, codes, scales, stats, deadzone, d->num_sms,
                                               as_stream(stream)));
+}
+
+int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float* g_in, float* g_out, uint16_t* w_qdq,
+              int64_t ld_out, uint8_t* codes, uint8_t* scales, void* workspace, size_t ws_bytes, void* stream) {
+  if (M < 0 || K <= 0 || K % 16 != 0 || ldw < K || ldw % 8 != 0 || ld_out < K || ld_out % 8 != 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (K > (int64_t)1 << 30 || M * ((K + 1023) / 1024) >= ((int64_t)1 << 31)) return NVFP4_ERR_UNSUPPORTED;
+  if ((codes == nullptr) != (scales == nullptr)) return NVFP4_ERR_INVALID_ARG;
+  if (M > 0 && (!w || !w_qdq || !aligned(w, 16) || !aligned(w_qdq, 16))) return NVFP4_ERR_INVALID_ARG;
+  if (codes != nullptr && (!aligned(codes, 16) || !aligned(scales, 16))) return NVFP4_ERR_INVALID_ARG;
+  if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
+    return NVFP4_ERR_WORKSPACE;
+  const DeviceInfo* d = nullptr;
+  int st;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if (M == 0 && g_in != nullptr) return NVFP4_OK;
+  return from_cuda(nv4::launch_nvfp4_qdq(bf(w), M, K, ldw, g_in, g_out, bf(w_qdq), ld_out, codes, scales,
+                                         static_cast<float*>(workspace), d->num_sms, as_stream(stream)));
 }
 
 int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b_codes, const uint8_t* b_scales,

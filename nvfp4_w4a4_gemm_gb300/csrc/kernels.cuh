@@ -22,6 +22,13 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
 
+// Weight fake quantization: y = bf16(E2M1(code) * d) per element, optionally
+// the codes and tiled scales of the same quantization (dynamic scale: amax
+// pre-pass into `partials`).
+cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
+                             float* g_out, __nv_bfloat16* y, int64_t ldy, uint8_t* codes, uint8_t* scales,
+                             float* partials, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
                                 int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
                                 __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream);

@@ -737,6 +737,111 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
   }
 }
 
+// --------------------------------------------- weight fake quantization ----
+// The trainer's half of asymmetric W4A16 QAT (QUADS 2.2 A): every element
+// becomes bf16_rn(fp32(E2M1(code) * d)) with the codes and block scales of
+// nvfp4_quant_kernel (the same helpers, hence the same bits), and the packed
+// codes and tiled scales can be written in the same pass, so the rollout's
+// W4 weights and the trainer's fake-quantized ones come from one read of W.
+// Work unit: one row x 1024 columns per warp, two 16-element blocks per lane;
+// the next unit's loads are in flight while the current one is converted.
+struct QdqArgs {
+  QuantArgs src;           // x, M, K, ldx, vec32 (the loads of the quantizer)
+  const float* g_in;
+  const float* partials;
+  int n_partials;
+  float* g_out;
+  __nv_bfloat16* y;        // [M, K] row stride ldy
+  int64_t ldy;
+  uint8_t* codes;          // or nullptr
+  uint8_t* scales;         // or nullptr
+  int y_vec32;             // y rows on 32-byte boundaries: 256-bit stores
+};
+
+template <bool kFull>
+__device__ __forceinline__ void qdq_unit(const QdqArgs& q, const uint4 (&v)[4], uint32_t r, uint32_t gi, int lane,
+                                         const ScaleCtx& sc, int64_t n_cg) {
+  const int64_t K = q.src.K;
+  const int64_t col0 = (int64_t)gi * 1024;
+  const int cols = kFull ? 1024 : (int)((K - col0) < 1024 ? (K - col0) : 1024);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (!kFull && h * 512 >= cols) break;  // warp-uniform
+    const bool valid = kFull || h * 512 + lane * 16 < cols;
+    const uint4& raw0 = v[2 * h];
+    const uint4& raw1 = v[2 * h + 1];
+    const float am = absmax_of(absmax8(absmax8(raw0.x, raw0), raw1));
+    uint32_t sig = block_scale_byte(am, sc.g, sc.yg, sc.fast);
+    sig = valid ? sig : 0u;
+    const float2 dr = sc.dr[sig];
+    uint32_t lo = 0, hi = 0;
+    if (dr.x != 0.f) {
+      const uint64_t s2 = ((uint64_t)__float_as_uint(dr.y) << 32) | __float_as_uint(dr.y);
+      lo = bf16x8_mul_e2m1(raw0, s2);
+      hi = bf16x8_mul_e2m1(raw1, s2);
+    }
+    if (q.codes != nullptr && valid)
+      *reinterpret_cast<uint2*>(q.codes + (int64_t)r * (K / 2) + col0 / 2 + h * 256 + lane * 8) = make_uint2(lo, hi);
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 1);
+    const uint32_t s2b = __shfl_down_sync(0xffffffffu, sig, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 3);
+    if (q.scales != nullptr && (lane & 3) == 0 && valid)
+      *reinterpret_cast<uint32_t*>(q.scales + tile_group_offset(r, (int64_t)gi * 16, n_cg) + (lane >> 2) * 512 +
+                                   h * 8 * 512) = sig | (s1 << 8) | (s2b << 16) | (s3 << 24);
+    // dequantized value of each code, element pair (2b, 2b + 1) from code byte b
+    uint32_t out[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const float2 ev = e2m1x2_vals(((b < 4 ? lo : hi) >> (8 * (b & 3))) & 0xFFu);
+      const __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(ev.x, dr.x), __fmul_rn(ev.y, dr.x));
+      out[b] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    if (valid) {
+      __nv_bfloat16* dst = q.y + (int64_t)r * q.ldy + col0 + h * 512 + lane * 16;
+      if (q.y_vec32) {
+        stg_256(dst, out);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+      }
+    }
+  }
+}
+
+template <bool kFull>
+__global__ void __launch_bounds__(kThreads, 3) nvfp4_qdq_kernel(QdqArgs q) {
+  __shared__ float2 s_dr[256];
+  const int lane = threadIdx.x & 31;
+  const uint32_t gpr = (uint32_t)((q.src.K + 1023) / 1024);
+  const uint32_t n = (uint32_t)(q.src.M * gpr);
+  const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+  uint32_t u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  uint4 va[4], vb[4];
+  if (u < n) load_unit_t<kFull>(q.src, u / gpr, u % gpr, lane, va);  // in flight while g and the table are set up
+  const float g = q.g_in != nullptr ? *q.g_in : tensor_scale_from_partials(q.partials, q.n_partials);
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    const float d = __fmul_rn(e4m3_to_f32((uint32_t)i), g);
+    s_dr[i] = make_float2(d, d != 0.f ? __frcp_rn(d) : 0.f);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && q.g_out != nullptr) *q.g_out = g;
+  ScaleCtx sc;
+  sc.g = g;
+  sc.yg = __frcp_rn(g);
+  sc.fast = g >= 0x1p-100f && g <= 0x1p100f;
+  sc.dr = s_dr;
+  const int64_t n_cg = (q.src.K / 16 + 3) / 4;
+  while (u < n) {
+    const uint32_t ub = u + n_warps;
+    if (ub < n) load_unit_t<kFull>(q.src, ub / gpr, ub % gpr, lane, vb);
+    qdq_unit<kFull>(q, va, u / gpr, u % gpr, lane, sc, n_cg);
+    if (ub >= n) break;
+    u = ub + n_warps;
+    if (u < n) load_unit_t<kFull>(q.src, u / gpr, u % gpr, lane, va);
+    qdq_unit<kFull>(q, vb, ub / gpr, ub % gpr, lane, sc, n_cg);
+  }
+}
+
 // ------------------------------------------------ compensation weights -----
 // w_sel[e][n][i] = E2M1(code[e][n][S_e[i]]) * sigma[e][n][S_e[i]/16] (exact in
 // bf16), or the original bf16 W^T[e][n][S_e[i]] when `wt` is given.
@@ -1022,6 +1127,33 @@ cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void* args[] = {&a};
+  return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
+}
+
+cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
+                             float* g_out, __nv_bfloat16* y, int64_t ldy, uint8_t* codes, uint8_t* scales,
+                             float* partials, int num_sms, cudaStream_t stream) {
+  QdqArgs q{};
+  q.src.x = x; q.src.M = M; q.src.K = K; q.src.ldx = ldx;
+  q.src.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
+  q.g_in = g_in; q.g_out = g_out; q.y = y; q.ldy = ldy; q.codes = codes; q.scales = scales;
+  q.y_vec32 = ((reinterpret_cast<uintptr_t>(y) & 31u) == 0 && (ldy & 15) == 0) ? 1 : 0;
+  if (g_in == nullptr) {
+    const int p = amax_partials_count(M, K, num_sms);
+    amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
+    q.partials = partials;
+    q.n_partials = p;
+  }
+  const bool full = q.src.vec32 && (K % 1024) == 0;
+  const void* kern = full ? (const void*)nvfp4_qdq_kernel<true> : (const void*)nvfp4_qdq_kernel<false>;
+  const int64_t n_units = M * ((K + 1023) / 1024);
+  int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  if (blocks > (int64_t)num_sms * per_sm) blocks = (int64_t)num_sms * per_sm;
+  if (blocks < 1) blocks = 1;
+  void* args[] = {&q};
   return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
 }
 

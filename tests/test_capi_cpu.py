@@ -76,6 +76,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize(fake, 4, 32, 32, fake, None, fake, fake, None, 4, fake, None, 0, None) == 1
     # MXFP4 needs K % 32
     assert lib.mxfp4_quantize(fake, 4, 48, 48, fake, fake, None, None, None) == 1
+    # code buffers only 8-byte aligned (the kernels store 8 and 16 bytes at a time)
+    odd8 = P((1 << 20) + 8)
+    assert lib.nvfp4_quantize(fake, 4, 32, 32, fake, None, odd8, fake, None, 0, None, None, 0, None) == 1
+    assert lib.mxfp4_quantize(fake, 4, 64, 64, odd8, fake, None, None, None) == 1
     # GEMM: bad format / flag / N not a multiple of 128
     assert lib.w4a4_gemm_comp(7, 4, 128, 64, fake, fake, None, fake, fake, None, None, None, 0, 0, fake,
                               None, 0, None) == 1
