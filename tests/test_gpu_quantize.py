@@ -59,7 +59,9 @@ def test_tiny_workload(nv):
 
 
 @pytest.mark.parametrize("M,K,k", [(1, 16, 1), (3, 48, 5), (130, 80, 7), (257, 1040, 33), (64, 4096, 128),
-                                   (517, 2064, 64)])
+                                   (517, 2064, 64),
+                                   # decode-sized inputs (a few CTAs: the grid barrier over few arrivals)
+                                   (16, 4096, 64), (31, 2000, 8), (65, 1024, 16), (8, 8192, 32)])
 def test_ragged_shapes(nv, M, K, k):
     x = W.activations(M, K, max(1, K // 100), "t3x20", M + K, M * 7 + 1)
     rng = np.random.default_rng(M * 31 + K)
