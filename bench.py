@@ -151,13 +151,18 @@ def gemm_traffic():
 
 
 def dist_setup():
+    """One process per GPU under torchrun (NCCL); without a GPU (the CPU tests
+    of this host logic) the same ranks meet over gloo."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
         rank = int(os.environ["RANK"])
         local = int(os.environ.get("LOCAL_RANK", rank))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
         return dist, rank, ws
     return None, 0, 1
 
