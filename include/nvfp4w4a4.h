@@ -8,7 +8,9 @@
  *
  * X [M, K] bf16 activations, quantized online to NVFP4; W^T [N, K] the
  * pre-quantized weights; R_S = bf16(X - deq(q(X))) on a fixed set S of k
- * high-error channels; W_S [N, k] the matching weight columns.
+ * high-error channels; W_S [N, k] the matching weight columns.  The
+ * trainer-side counterpart, nvfp4_qdq, returns deq(q(W)) in bf16 (the
+ * weights a W4A16 QAT forward pass uses) together with the W4 operands.
  *
  * Conventions shared by every entry point:
  *   - bf16 tensors are passed as uint16_t bit patterns; every tensor is
@@ -17,6 +19,9 @@
  *     library allocates nothing and keeps no pointer after a call returns.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous on it and never synchronize (except nvfp4_check_status).
+ *     Stream order is kept; the GEMMs are programmatic dependent launches
+ *     that may start their setup while the preceding kernel still runs
+ *     (w4a4_gemm_comp says what they may read before it ends).
  *   - Return value: NVFP4_OK or an NVFP4_ERR_* code.  Argument errors are
  *     detected on the host before anything is launched; a launch failure is
  *     NVFP4_ERR_CUDA; errors detected inside kernels (a bounded wait that
