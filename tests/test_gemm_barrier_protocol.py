@@ -1,4 +1,4 @@
-"""Randomized model of the wide W4A4 GEMM kernel's mbarrier protocol (CPU).
+"""Randomized models of the W4A4 GEMM kernels' mbarrier protocols (CPU).
 
 `w4a4_gemm_wide_kernel` (nvfp4_w4a4_gemm_gb300/csrc/gemm.cu) runs six roles
 on a 4-stage shared-memory ring: the TMA warp, two scale-copy warps, the MMA
@@ -20,6 +20,10 @@ The model is run with the kernel's protocol and with two protocols that are
 known to be wrong (the MMA warp not waiting for the first copy warp on
 compensation uses; the epilogue warps waiting on the stage's `full` barrier
 with a parity computed from the use count), which the checks must reject.
+
+`NarrowGemmModel` does the same for `w4a4_gemm_kernel` (four copy warps on one
+barrier, two accumulators plus a compensation accumulator, split-K units, and
+the early weight loads issued before the wait for the preceding kernel).
 """
 import random
 
@@ -29,12 +33,27 @@ import pytest
 class Barrier:
     def __init__(self, name, count):
         self.name, self.count, self.pending, self.done = name, count, count, 0
+        self.tx = 0
 
     def arrive(self, n=1):
         self.pending -= n
         if self.pending < 0:
             raise AssertionError(f"arrival overflow on {self.name} in phase {self.done}")
-        if self.pending == 0:
+        self._maybe_complete()
+
+    def expect_tx(self, nbytes):
+        """mbarrier.arrive.expect_tx: one arrival plus bytes still to land."""
+        self.tx += nbytes
+        self.arrive()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        if self.tx < 0:
+            raise AssertionError(f"transaction bytes below zero on {self.name}")
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
             self.done += 1
             self.pending = self.count
 
@@ -175,9 +194,12 @@ class WideGemmModel:
             self.later(lambda: stored.__setitem__(0, True), f"epi{w}", 0, 80)
             yield lambda: stored[0]
 
+    def roles(self):
+        return ([self.tma(), self.copy_warp_a(), self.copy_warp_b(), self.mma()]
+                + [self.epilogue_warp(w) for w in range(8)])
+
     def run(self):
-        roles = [self.tma(), self.copy_warp_a(), self.copy_warp_b(), self.mma()]
-        roles += [self.epilogue_warp(w) for w in range(8)]
+        roles = self.roles()
         waiting = {}
         for g in roles:
             waiting[g] = next(g)
@@ -197,6 +219,178 @@ class WideGemmModel:
                 fn()
             else:
                 raise AssertionError(f"deadlock with {len(waiting)} roles waiting")
+
+
+class NarrowGemmModel(WideGemmModel):
+    """Roles of `w4a4_gemm_kernel` (128-row tiles, decode and small M): the
+    TMA warp, four scale-copy warps that each commit once per stage on
+    `sf_full` (count 4), the MMA warp with two accumulators and one
+    compensation accumulator, and four epilogue warps.  Work units carry a
+    k-tile range (split-K) and compensation k-tiles only on their first split.
+    With early weights the producer issues the weight half of its first
+    stages (one arrive.expect_tx for the whole stage) before the wait for the
+    preceding kernel, and the activation half after it."""
+
+    def __init__(self, seed, units, protocol="kernel", stages=4, early=False):
+        self.r = random.Random(seed)
+        self.S, self.units, self.protocol, self.early = stages, units, protocol, early
+        ring = lambda name, count: [Barrier(f"{name}[{i}]", count) for i in range(stages)]
+        self.full, self.empty = ring("full", 1), ring("empty", 1)
+        self.sf_full = ring("sf_full", 3 if protocol == "sf_full_count_3" else 4)
+        self.acc_full = [Barrier(f"acc_full[{i}]", 1) for i in range(2)]
+        self.acc_empty = [Barrier(f"acc_empty[{i}]", 4) for i in range(2)]
+        self.comp_empty = Barrier("comp_empty", 4)
+        self.a_part = [None] * stages     # use whose activation half landed
+        self.b_part = [None] * stages     # use whose weight half landed
+        self.chunks = [dict() for _ in range(stages)]  # copy warp -> use whose chunk is in TMEM
+        self.acc = [None, None]           # (unit, complete?) held by each accumulator
+        self.comp = None
+        self.events, self.now, self.seq, self.last_async = [], 0.0, 0, {}
+        self.waited = False               # the producer's wait for the preceding kernel
+
+    def walk(self):
+        """(unit index, k-tile index within the unit, is compensation, use)."""
+        u = 0
+        for i, (n_kt, n_ct) in enumerate(self.units):
+            for j in range(n_kt + n_ct):
+                yield i, j, j >= n_kt, u
+                u += 1
+
+    def tma(self):
+        first_kt = self.units[0][0] if self.units else 0
+        pre = min(self.S, first_kt) if self.early else 0
+        for i in range(pre):               # weight halves before the wait, ring known empty
+            self.full[i].expect_tx(2)
+            self.later(lambda i=i: (self.b_part.__setitem__(i, i), self.full[i].complete_tx(1)), "tma", 5, 60)
+            if self.protocol == "early_double_arrive":
+                self.full[i].expect_tx(0)
+        yield lambda: True
+        self.waited = True
+        for _, _, comp, u in self.walk():
+            st, ph = self.slot(u)
+            early = u < pre
+            if not early:
+                yield lambda: self.empty[st].passed(ph ^ 1)
+                self.full[st].expect_tx(2)
+                self.later(lambda st=st, u=u: (self.b_part.__setitem__(st, u), self.full[st].complete_tx(1)),
+                           "tma", 5, 60)
+            self.later(lambda st=st, u=u: (self.a_part.__setitem__(st, u), self.full[st].complete_tx(1)),
+                       "tma", 5, 60)
+
+    def copy_warp(self, w):
+        for _, _, comp, u in self.walk():
+            st, ph = self.slot(u)
+            yield lambda: self.full[st].passed(ph)
+            assert (self.a_part[st], self.b_part[st]) == (u, u), ("copy warp", w, "use", u)
+            if comp:
+                self.sf_full[st].arrive()
+            else:
+                def copied(st=st, u=u):
+                    self.chunks[st][w] = u
+                    self.sf_full[st].arrive()
+                self.later(copied, f"cp{w}", 2, 20)
+
+    def mma(self):
+        acc, acc_ph, comp_ph = 0, 0, 0
+        walk = self.walk()
+        for i, (n_kt, n_ct) in enumerate(self.units):
+            yield lambda: self.acc_empty[acc].passed(acc_ph ^ 1)
+            assert self.acc[acc] is None or self.acc[acc][1] == "read", ("accumulator still unread", i)
+            self.acc[acc] = (i, "writing")
+            for j in range(n_kt + n_ct):
+                _, _, comp, u = next(walk)
+                st, ph = self.slot(u)
+                if j == n_kt:  # as the kernel: the compensation accumulator is claimed after the FP4 k-tiles
+                    if self.protocol != "mma_skips_comp_empty":
+                        yield lambda: self.comp_empty.passed(comp_ph ^ 1)
+                    comp_ph ^= 1
+                yield lambda: self.sf_full[st].passed(ph)
+                assert (self.a_part[st], self.b_part[st]) == (u, u), ("MMA", u)
+                if comp:
+                    if j == n_kt:  # the unit's first compensation k-tile
+                        assert self.comp is None or self.comp[1] == "read", ("compensation accumulator unread", i)
+                        self.comp = (i, "writing")
+                else:
+                    assert all(self.chunks[st].get(w) == u for w in range(4)), ("MMA before all scale chunks", u)
+
+                def consumed(st=st):
+                    self.a_part[st] = self.b_part[st] = "consumed"
+                    self.empty[st].arrive()
+                self.later(consumed, "mma", 5, 40)
+
+            def done(a=acc, i=i, c=bool(n_ct)):
+                self.acc[a] = (i, "complete")
+                if c:
+                    self.comp = (i, "complete")
+                self.acc_full[a].arrive()
+            self.later(done, "mma", 5, 40)
+            acc ^= 1
+            if acc == 0:
+                acc_ph ^= 1
+
+    def epilogue_warp(self, w):
+        acc, acc_ph = 0, 0
+        for i, (n_kt, n_ct) in enumerate(self.units):
+            yield lambda: self.acc_full[acc].passed(acc_ph)
+            assert self.acc[acc] == (i, "complete"), ("epilogue read", self.acc[acc], "for unit", i)
+            if n_ct:
+                assert self.comp == (i, "complete"), ("epilogue compensation read", self.comp, "for unit", i)
+            stored = [False]
+            self.later(lambda stored=stored: stored.__setitem__(0, True), f"epi{w}", 0, 30)
+            yield lambda stored=stored: stored[0]
+            self.epi_done = getattr(self, "epi_done", {})
+            self.epi_done[(i, w)] = True
+            if all(self.epi_done.get((i, x)) for x in range(4)):
+                self.acc[acc] = (i, "read")
+                if n_ct:
+                    self.comp = (i, "read")
+            self.acc_empty[acc].arrive()
+            if n_ct:
+                self.comp_empty.arrive()
+            acc ^= 1
+            if acc == 0:
+                acc_ph ^= 1
+
+    def roles(self):
+        return [self.tma(), self.mma()] + [self.copy_warp(w) for w in range(4)] + \
+               [self.epilogue_warp(w) for w in range(4)]
+
+
+def _narrow_units(seed):
+    """A CTA's work units: (FP4 k-tiles, compensation k-tiles); compensation
+    only on a unit's first split."""
+    r = random.Random(seed)
+    units = []
+    for _ in range(r.randint(1, 4)):
+        split = r.choice([1, 1, 2, 3])
+        n_kt, n_ct = r.choice([1, 2, 4, 16]), r.choice([0, 1, 2])
+        for p in range(split):
+            lo, hi = p * n_kt // split, (p + 1) * n_kt // split
+            if hi > lo or p == 0:
+                units.append((max(hi - lo, 1), n_ct if p == 0 else 0))
+    return units
+
+
+def _narrow_failures(protocol, n, early):
+    bad = 0
+    for seed in range(n):
+        try:
+            NarrowGemmModel(seed, _narrow_units(seed), protocol, stages=random.Random(seed).choice([4, 7]),
+                            early=early).run()
+        except AssertionError:
+            bad += 1
+    return bad
+
+
+@pytest.mark.parametrize("early", [False, True])
+def test_narrow_kernel_protocol_holds_under_random_schedules(early):
+    assert _narrow_failures("kernel", 300, early) == 0
+
+
+@pytest.mark.parametrize("protocol,early", [("sf_full_count_3", False), ("mma_skips_comp_empty", False),
+                                            ("early_double_arrive", True)])
+def test_narrow_model_rejects_known_wrong_protocols(protocol, early):
+    assert _narrow_failures(protocol, 300, early) > 0
 
 
 def _shapes(seed):
