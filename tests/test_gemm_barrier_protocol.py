@@ -68,10 +68,10 @@ class WideGemmModel:
     `uses` numbers the ring's stage uses in the order every role walks them:
     per output tile, n_kt FP4 k-tiles then n_ct compensation k-tiles."""
 
-    def __init__(self, seed, n_tiles, n_kt, n_ct, protocol="kernel", stages=4):
+    def __init__(self, seed, n_tiles, n_kt, n_ct, protocol="kernel", stages=4, early=False):
         self.r = random.Random(seed)
         self.S, self.n_kt, self.n_ct, self.T = stages, n_kt, n_ct, n_tiles
-        self.protocol = protocol
+        self.protocol, self.early = protocol, early
         ring = lambda name, count: [Barrier(f"{name}[{i}]", count) for i in range(stages)]
         self.full, self.empty = ring("full", 1), ring("empty", 1)
         self.sf_full, self.sf_full2 = ring("sf_full", 1), ring("sf_full2", 1)
@@ -104,15 +104,29 @@ class WideGemmModel:
         return u % self.S, (u // self.S) & 1
 
     def tma(self):
-        for _, _, u in self.uses():
-            st, ph = self.slot(u)
-            yield lambda: self.empty[st].passed(ph ^ 1)
+        # each stage use lands in two halves (activations, weights); with
+        # early weights the weight halves of the first FP4 k-tiles go out
+        # before the wait for the preceding kernel, under one expect_tx
+        pre = min(self.S, self.n_kt) if (self.early and self.T) else 0
+        halves = [dict() for _ in range(self.S)]
 
-            def land(st=st, u=u):
+        def land(st, u, half):
+            halves[st][half] = u
+            if halves[st].get("a") == u and halves[st].get("b") == u:
                 self.content[st] = u
                 self.scaled[st] = set()
-                self.full[st].arrive()
-            self.later(land, "tma", 5, 60)
+            self.full[st].complete_tx(1)
+        for i in range(pre):
+            self.full[i].expect_tx(2)
+            self.later(lambda i=i: land(i, i, "b"), "tma", 5, 60)
+        yield lambda: True  # griddepcontrol.wait
+        for _, _, u in self.uses():
+            st, ph = self.slot(u)
+            if u >= pre:
+                yield lambda: self.empty[st].passed(ph ^ 1)
+                self.full[st].expect_tx(2)
+                self.later(lambda st=st, u=u: land(st, u, "b"), "tma", 5, 60)
+            self.later(lambda st=st, u=u: land(st, u, "a"), "tma", 5, 60)
 
     def copy_warp_a(self):          # warp 2: A + B rows 0..127 scale copies
         for _, j, u in self.uses():
@@ -398,19 +412,20 @@ def _shapes(seed):
     return r.randint(1, 5), r.choice([1, 2, 3, 5, 16]), r.choice([0, 1, 2, 3, 4, 5, 8])
 
 
-def _failures(protocol, n):
+def _failures(protocol, n, early=False):
     bad = 0
     for seed in range(n):
         n_tiles, n_kt, n_ct = _shapes(seed)
         try:
-            WideGemmModel(seed, n_tiles, n_kt, n_ct, protocol).run()
+            WideGemmModel(seed, n_tiles, n_kt, n_ct, protocol, early=early).run()
         except AssertionError:
             bad += 1
     return bad
 
 
-def test_kernel_protocol_holds_under_random_schedules():
-    assert _failures("kernel", 400) == 0
+@pytest.mark.parametrize("early", [False, True])
+def test_kernel_protocol_holds_under_random_schedules(early):
+    assert _failures("kernel", 400, early) == 0
 
 
 @pytest.mark.parametrize("protocol", ["mma_skips_copy_warp", "epilogue_waits_full"])
