@@ -233,17 +233,6 @@ def grouped_scale_tile_offsets(offsets, n_scale):
     return tile_offset(prow, s, ncp)
 
 
-def to_tiled(sigma, offsets_map=None, nbytes=None):
-    """Scatter row-major scales into a tiled buffer (padding left 0)."""
-    M, n = sigma.shape
-    off = scale_tile_offsets(M, n) if offsets_map is None else offsets_map
-    if nbytes is None:
-        nbytes = int(off.max()) + 1 if off.size else 0
-    buf = np.zeros(nbytes, np.uint8)
-    buf[off.ravel()] = sigma.ravel()
-    return buf
-
-
 def comp_weights(codes_w, sigma_w, chan):
     """Compensation weight rows for the default mode, without the tensor
     scale: Wt_S[n, i] = E2M1(code_w[n, S_i]) * sigma_w[n, S_i // 16], shape

@@ -100,3 +100,16 @@ def test_block_stats_consistent():
     assert st.shape == (16, 8, 4) and cnt.shape == (16, 8)
     np.testing.assert_allclose(st[..., 3], (d["E"] ** 2).reshape(16, 8, 32).sum(-1))
     assert np.array_equal(cnt, d["dead"].reshape(16, 8, 32).sum(-1))
+
+
+def test_block_exponent_closed_forms():
+    # e = floor(log2 a) - 2: exact powers of two, their bf16 neighbours below,
+    # zero, and both clamps
+    from oracle.mxfp4 import block_exponent
+    ks = np.arange(-120, 121, 7)
+    assert np.array_equal(block_exponent(2.0 ** ks), ks - 2)
+    below = (2.0 ** ks) * (1 - 2.0 ** -8)     # the next bf16 value down
+    assert np.array_equal(block_exponent(below), ks - 3)
+    assert block_exponent(np.array([0.0]))[0] == -127
+    assert block_exponent(np.array([2.0 ** 200]))[0] == 127
+    assert block_exponent(np.array([2.0 ** -140]))[0] == -127

@@ -231,3 +231,18 @@ def test_qdq_rounds_the_fp32_product_to_bf16():
     # the block maximum too: 6 d = 6.0781252384... -> fp32 6.078125, halfway
     # between bf16 6.0625 (even) and 6.09375 -> 6.0625
     assert w[0, 0] == np.float32(6.0625)
+
+
+def test_grouped_scale_offsets_are_distinct_and_in_bounds():
+    # every (row, scale) of an expert-sorted operand gets its own byte inside
+    # the grouped buffer, each expert's rows starting on a fresh 128-row tile
+    offs = np.array([0, 0, 5, 135, 136, 400, 400, 529])
+    E, K = len(offs) - 1, 192
+    o = nvfp4.grouped_scale_tile_offsets(offs, K // 16)
+    assert o.shape == (offs[-1], K // 16)
+    assert len(np.unique(o)) == o.size
+    assert o.min() >= 0 and o.max() < nvfp4.grouped_scale_bytes(int(offs[-1]), K, E)
+    rows = nvfp4.grouped_row_map(offs)
+    for e in range(E):
+        if offs[e + 1] > offs[e]:
+            assert rows[offs[e]] % 128 == 0
