@@ -738,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
 }
 
 // --------------------------------------------- weight fake quantization ----
-// The trainer's half of asymmetric W4A16 QAT (QUADS 2.2 A): every element
+// The trainer's half of asymmetric W4A16 QAT (gist.science explainer of
+// QUADS, section 2.2 A): every element
 // becomes bf16_rn(fp32(E2M1(code) * d)) with the codes and block scales of
 // nvfp4_quant_kernel (the same helpers, hence the same bits), and the packed
 // codes and tiled scales can be written in the same pass, so the rollout's
