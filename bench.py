@@ -246,8 +246,10 @@ def run_ours(args):
         raise RuntimeError(f"device status {st} after the timed region")
     t_q = [e[0].elapsed_time(e[1]) for e in evs]
     t_g = [e[1].elapsed_time(e[2]) for e in evs]
-    ms_step = statistics.mean(a + b for a, b in zip(t_q, t_g))
-    ms_step = max_over_ranks(dist, ms_step, dev)
+    t_step = [a + b for a, b in zip(t_q, t_g)]
+    ms_step = max_over_ranks(dist, statistics.mean(t_step), dev)
+    ms_med = max_over_ranks(dist, statistics.median(t_step), dev)
+    ms_min = max_over_ranks(dist, min(t_step), dev)
     ms_gemm = max_over_ranks(dist, statistics.mean(t_g), dev)
     ms_quant = max_over_ranks(dist, statistics.mean(t_q), dev)
 
@@ -334,6 +336,8 @@ def run_ours(args):
                      "algorithmic": "2*M*N*K per launch (compensation FLOPs excluded, its time included)"},
         "components": {
             "gemm_ms": round(ms_gemm, 4), "gemm_tflops": round(gemm_tflops, 1),
+            "gemm_tflops_incl_comp": round((flops + 2.0 * s.M * s.N * s.k) / (ms_gemm * 1e-3) / 1e12, 1),
+            "step_ms_median": round(ms_med, 4), "step_ms_min": round(ms_min, 4),
             "quantize_ms": round(ms_quant, 4), "quantize_gbs": round(quant_gbs, 1),
             "quantize_frac_hbm": round(quant_gbs / pk["hbm_gbs"], 4),
             "quantize_bytes": q_bytes, "hbm_peak_gbs": pk["hbm_gbs"],
@@ -453,6 +457,11 @@ def other_workloads(nv, pk, steps=10):
                   "gbs": round(tot_bytes / (tot_ms * 1e-3) / 1e9, 1),
                   "frac_hbm": round(tot_bytes / (tot_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                   "bytes_per_step": tot_bytes, "per_projection": res,
+                  # attainable = min(FP4 peak, arithmetic intensity x HBM bandwidth): these layers sit
+                  # below the ridge, so their ceiling is the memory one
+                  "attainable_tflops": round(min(fp4_peak, tot_flops / tot_bytes * pk["hbm_gbs"] / 1e3), 1),
+                  "frac_attainable": round((tot_flops / (tot_ms * 1e-3) / 1e12)
+                                           / min(fp4_peak, tot_flops / tot_bytes * pk["hbm_gbs"] / 1e3), 4),
                   "note": "each projection: grouped dynamic-scale quantize + grouped GEMM with compensation"}
     del dm
 
