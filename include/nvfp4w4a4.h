@@ -218,6 +218,16 @@ int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t
                    float* stats, uint8_t* deadzone, void* stream);
 
 /*
+ * mxfp4_decompose_elements -- the decomposition of mxfp4_quantize per
+ * element instead of per block, a checking aid for small shapes: the same
+ * fp32 arithmetic, E = B + D + G for every element.
+ * Source: as mxfp4_quantize.
+ * x   [M, K] bf16 (K % 32 == 0, row stride ldx, 16-byte aligned, ldx % 8 == 0)
+ * bdg float [M*K][3]: (B, D, G) of element (m, i) at (m*K + i)*3 (4-byte aligned)
+ */
+int mxfp4_decompose_elements(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* bdg, void* stream);
+
+/*
  * nvfp4_prepare_comp_weights -- the compensation weight columns W_S, once,
  * offline.  Source: gist.science explainer of QUADS, 2.2 B (the residual term
  * is multiplied into the output); FourSight abstract (BF16 channels).

@@ -41,6 +41,7 @@ _SIGS = {
                                ctypes.c_int),
     "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "mxfp4_decompose_elements": ([_P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "nvfp4_qdq": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_prepare_comp_weights": ([_I32, _I64, _I64, _P, _P, _P, _P, _I32, ctypes.c_int, _P, _P], ctypes.c_int),
     "nvfp4_calibrate_workspace_bytes": ([_I64, _I32], _SZ),
@@ -176,6 +177,18 @@ def nvfp4_qdq(w, g=None, with_codes=False, out=None):
     if with_codes:
         r.update(codes=codes, scales=scales)
     return r
+
+
+def mxfp4_decompose_elements(x):
+    """x bf16 [M, K] -> float32 [M, K, 3]: per-element (B, D, G) of the MXFP4
+    error decomposition (small shapes; a checking aid)."""
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    out = torch.empty((M, K, 3), dtype=torch.float32, device=x.device)
+    st = lib.mxfp4_decompose_elements(_ptr(x), M, K, x.stride(0), _ptr(out), _stream())
+    _check("mxfp4_decompose_elements", st)
+    return out
 
 
 def nvfp4_quantize_noalloc(x, chan=None, out=None, g_out=None):

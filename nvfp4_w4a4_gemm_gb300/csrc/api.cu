@@ -196,6 +196,17 @@ int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float*
                                          static_cast<float*>(workspace), d->num_sms, as_stream(stream)));
 }
 
+int mxfp4_decompose_elements(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* bdg, void* stream) {
+  if (M < 0 || K <= 0 || K % 32 != 0 || ldx < K || ldx % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (K > (int64_t)1 << 30 || M > ((int64_t)1 << 40) / K) return NVFP4_ERR_UNSUPPORTED;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !bdg || !aligned(x, 16) || !aligned(bdg, 4)) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  int st;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  return from_cuda(nv4::launch_mxfp4_decompose(bf(x), M, K, ldx, bdg, d->num_sms, as_stream(stream)));
+}
+
 int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b_codes, const uint8_t* b_scales,
                                const uint16_t* wt_bf16, const int32_t* chan, int32_t k, int flags,
                                uint16_t* w_sel, void* stream) {

@@ -29,6 +29,10 @@ cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64
                              float* g_out, __nv_bfloat16* y, int64_t ldy, uint8_t* codes, uint8_t* scales,
                              float* partials, int num_sms, cudaStream_t stream);
 
+// Per-element (B, D, G) of the MXFP4 decomposition into bdg [M*K][3].
+cudaError_t launch_mxfp4_decompose(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* bdg, int num_sms,
+                                   cudaStream_t stream);
+
 cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
                                 int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
                                 __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream);

@@ -737,6 +737,42 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
   }
 }
 
+// Per-element MXFP4 decomposition (a checking aid for small shapes): one
+// warp per 32-element block, lane = element, the fp32 arithmetic of the
+// stats path of mxfp4_quant_kernel: Q_s = E2M1(x 2^-e) 2^e, Q* = E2M1(x / s*) s*
+// with s* = RN(a / 6), B = Q_s - Q*, and Q* - x as D (code 0 at s*) or G.
+__global__ void __launch_bounds__(kThreads) mxfp4_decompose_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
+                                                                  int64_t K, int64_t ldx, float* __restrict__ bdg) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nblk = K / 32;
+  const int64_t n_blocks = M * nblk;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < n_blocks; b += n_warps) {
+    const int64_t r = b / nblk;
+    const int64_t col = (b - r * nblk) * 32 + lane;
+    const float xv = __bfloat162float(x[r * ldx + col]);
+    float am = fabsf(xv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    float eb = 0.f, ed = 0.f, eg = 0.f;
+    if (am > 0.f) {
+      const int e = mx_exponent(am);
+      const uint32_t cs = cvt_e2m1x2(__fmul_rn(xv, pow2f(-e)), 0.f);
+      const float qs = __fmul_rn(e2m1x2_vals(cs).x, pow2f(e));
+      const float ss = div6_rn(am);
+      const uint32_t ci = cvt_e2m1x2(__fdiv_rn(xv, ss), 0.f);
+      const float qst = __fmul_rn(e2m1x2_vals(ci).x, ss);
+      const float rr = __fsub_rn(qst, xv);
+      eb = __fsub_rn(qs, qst);
+      if ((ci & 7u) == 0u) ed = rr; else eg = rr;
+    }
+    float* o = bdg + (r * K + col) * 3;
+    o[0] = eb;
+    o[1] = ed;
+    o[2] = eg;
+  }
+}
+
 // --------------------------------------------- weight fake quantization ----
 // The trainer's half of asymmetric W4A16 QAT (gist.science explainer of
 // QUADS, section 2.2 A): every element
@@ -1111,6 +1147,16 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   }
   void* args[] = {&a};
   return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, smem, stream);
+}
+
+cudaError_t launch_mxfp4_decompose(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* bdg, int num_sms,
+                                   cudaStream_t stream) {
+  const int64_t n_blocks = M * (K / 32);
+  if (n_blocks == 0) return cudaSuccess;
+  int64_t grid = (n_blocks + (kThreads / 32) - 1) / (kThreads / 32);
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  mxfp4_decompose_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(x, M, K, ldx, bdg);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,

@@ -111,6 +111,12 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_qdq(fake, 4, 32, 32, g, None, fake, 32, fake, None, None, 0, None) == 1
     assert lib.nvfp4_qdq(fake, 4, 32, 32, g, None, fake, 32, odd8, fake, None, 0, None) == 1
     assert lib.nvfp4_qdq(fake, 4, 32, 32, None, None, fake, 32, None, None, None, 0, None) == 5
+    # per-element MXFP4 decomposition: K % 32, stride, alignment
+    assert lib.mxfp4_decompose_elements(fake, 4, 48, 48, fake, None) == 1
+    assert lib.mxfp4_decompose_elements(fake, 4, 64, 32, fake, None) == 1
+    assert lib.mxfp4_decompose_elements(P((1 << 20) + 2), 4, 64, 64, fake, None) == 1
+    assert lib.mxfp4_decompose_elements(fake, 4, 64, 64, P((1 << 20) + 2), None) == 1
+    assert lib.mxfp4_decompose_elements(None, 0, 64, 64, None, None) == 0
 
 
 def test_empty_problem_is_a_no_op(lib):

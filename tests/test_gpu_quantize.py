@@ -249,6 +249,38 @@ def _mx_midpoint_blocks():
     return np.concatenate([x, up, dn]).reshape(-1, 128)
 
 
+def _check_elementwise(nv, x):
+    """Per-element (B, D, G) of the GPU against the oracle's fp64 components:
+    each within fp32 rounding of the block's scale, D and G on the same
+    elements, and B + D + G equal to the oracle's E."""
+    M, K = x.shape
+    bdg = f32(nv.mxfp4_decompose_elements(x.cuda())).astype(np.float64)
+    torch.cuda.synchronize()
+    d = omx.decompose(f32(x))
+    blk = np.abs(f32(x)).reshape(M, K // 32, 32).max(axis=2).repeat(32, axis=1).astype(np.float64)
+    tol = blk * 2.0 ** -20 + 1e-38
+    for i, name in enumerate(("B", "D", "G")):
+        assert np.all(np.abs(bdg[..., i] - d[name]) <= tol), name
+    dead_at_star = (d["D"] != 0) | d["dead"]
+    assert not np.any((bdg[..., 2] != 0) & dead_at_star), "grid noise on a deadzone element"
+    assert not np.any((bdg[..., 1] != 0) & ~dead_at_star), "deadzone error on a non-deadzone element"
+    assert np.all(np.abs(bdg.sum(-1) - d["E"]) <= 3 * tol)
+
+
+@pytest.mark.parametrize("M,K", [(64, 256), (33, 160), (8, 1024)])
+def test_mxfp4_decomposition_per_element(nv, M, K):
+    x = W.activations(M, K, max(1, K // 100), "t3x20", K + 11, M + 13).clone()
+    x[0, :32] = 0                                   # zero block: all components 0
+    x[1, :32] = torch.tensor([3.0] + [0.01] * 31)   # mostly deadzone at s* = 0.5
+    x[2, :32] = torch.tensor([6.0 * 2.0 ** 3] * 32)  # a = 6 * 2^k: no scale bias
+    _check_elementwise(nv, x)
+
+
+def test_mxfp4_decomposition_per_element_at_midpoints(nv):
+    x = torch.from_numpy(_mx_midpoint_blocks().astype(np.float32)).to(torch.bfloat16)
+    _check_elementwise(nv, x)
+
+
 def test_mxfp4_ideal_scale_codes_at_midpoints(nv):
     x = torch.from_numpy(_mx_midpoint_blocks()).to(torch.bfloat16)
     M, K = x.shape
