@@ -500,8 +500,8 @@ def other_workloads(nv, pk, steps=10):
                   "ms_per_step": round(ms, 4), "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
                   "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "bytes_per_step": byts,
                   "bound": "hbm",
-                  "note": "bytes = W read once + QDQ written + codes + scales; the amax pre-pass reads W a second "
-                          "time (not counted)"}
+                  "note": "bytes = W read once + QDQ written + codes + scales; one cooperative launch whose amax "
+                          "phase reads W a second time (not counted)"}
     return out
 
 

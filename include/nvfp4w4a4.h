@@ -192,8 +192,10 @@ int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
  *        may not overlap w
  * codes, scales  both NULL, or [M, K/2] bytes and nvfp4_scale_bytes(M, K)
  *        bytes (16-byte aligned)
- * g_in / g_out / workspace: as nvfp4_quantize (the dynamic scale is an amax
- *        pre-pass, a second launch; workspace >= nvfp4_quantize_workspace_bytes())
+ * g_in / g_out / workspace: as nvfp4_quantize (the dynamic scale is one
+ *        cooperative launch: amax phase, bounded grid barrier, conversion
+ *        phase; workspace >= nvfp4_quantize_workspace_bytes(), NVFP4_ERR_CUDA
+ *        if the cooperative launch is refused)
  */
 int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float* g_in, float* g_out, uint16_t* w_qdq,
               int64_t ld_out, uint8_t* codes, uint8_t* scales, void* workspace, size_t ws_bytes, void* stream);

@@ -193,7 +193,9 @@ int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float*
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   if (M == 0 && g_in != nullptr) return NVFP4_OK;
   return from_cuda(nv4::launch_nvfp4_qdq(bf(w), M, K, ldw, g_in, g_out, bf(w_qdq), ld_out, codes, scales,
-                                         static_cast<float*>(workspace), d->num_sms, as_stream(stream)));
+                                         static_cast<float*>(workspace),
+                                         g_in == nullptr ? quant_barrier(workspace) : nullptr, d->num_sms,
+                                         as_stream(stream)));
 }
 
 int mxfp4_decompose_elements(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* bdg, void* stream) {

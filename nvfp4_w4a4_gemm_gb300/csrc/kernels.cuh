@@ -23,11 +23,12 @@ cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
 
 // Weight fake quantization: y = bf16(E2M1(code) * d) per element, optionally
-// the codes and tiled scales of the same quantization (dynamic scale: amax
+// the codes and tiled scales of the same quantization (dynamic scale: one
+// cooperative launch with a grid barrier on `bar`, or, without `bar`, an amax
 // pre-pass into `partials`).
 cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                              float* g_out, __nv_bfloat16* y, int64_t ldy, uint8_t* codes, uint8_t* scales,
-                             float* partials, int num_sms, cudaStream_t stream);
+                             float* partials, unsigned int* bar, int num_sms, cudaStream_t stream);
 
 // Per-element (B, D, G) of the MXFP4 decomposition into bdg [M*K][3].
 cudaError_t launch_mxfp4_decompose(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, float* bdg, int num_sms,

@@ -785,8 +785,9 @@ __global__ void __launch_bounds__(kThreads) mxfp4_decompose_kernel(const __nv_bf
 struct QdqArgs {
   QuantArgs src;           // x, M, K, ldx, vec32 (the loads of the quantizer)
   const float* g_in;
-  const float* partials;
+  float* partials;         // dynamic scale: pre-pass partials, or one slot per CTA (fused)
   int n_partials;
+  unsigned int* bar;       // fused dynamic scale: grid barrier {arrivals (zero at launch), generation}
   float* g_out;
   __nv_bfloat16* y;        // [M, K] row stride ldy
   int64_t ldy;
@@ -845,7 +846,10 @@ __device__ __forceinline__ void qdq_unit(const QdqArgs& q, const uint4 (&v)[4], 
   }
 }
 
-template <bool kFull>
+// kFused: the dynamic tensor scale in the same (cooperative) launch, as in
+// nvfp4_quant_kernel: amax over the CTA's own units, a grid barrier, then
+// the conversion pass, whose reads mostly hit L2.
+template <bool kFull, bool kFused>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_qdq_kernel(QdqArgs q) {
   __shared__ float2 s_dr[256];
   const int lane = threadIdx.x & 31;
@@ -854,8 +858,33 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_qdq_kernel(QdqArgs q) {
   const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
   uint32_t u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   uint4 va[4], vb[4];
-  if (u < n) load_unit_t<kFull>(q.src, u / gpr, u % gpr, lane, va);  // in flight while g and the table are set up
-  const float g = q.g_in != nullptr ? *q.g_in : tensor_scale_from_partials(q.partials, q.n_partials);
+  float g;
+  if (kFused) {
+    UnitWalk walk;
+    walk.gpr = gpr;
+    walk.n_units = n;
+    walk.n_warps = n_warps;
+    walk.dr = n_warps / gpr;
+    walk.dg = n_warps - walk.dr * gpr;
+    walk.u = u;
+    walk.r = u / gpr;
+    walk.gi = u - walk.r * gpr;
+    __shared__ float red[kThreads / 32];
+    const float m = warp_units_amax(q.src, walk, lane);
+    if (lane == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.f;
+      for (int i = 0; i < kThreads / 32; ++i) b = fmaxf(b, red[i]);
+      q.partials[blockIdx.x] = b;
+    }
+    if (!grid_barrier(q.bar)) return;
+    if (u < n) load_unit_t<kFull>(q.src, u / gpr, u % gpr, lane, va);  // in flight while g is reduced
+    g = tensor_scale_from_partials(q.partials, (int)gridDim.x);
+  } else {
+    if (u < n) load_unit_t<kFull>(q.src, u / gpr, u % gpr, lane, va);  // in flight while g and the table are set up
+    g = q.g_in != nullptr ? *q.g_in : tensor_scale_from_partials(q.partials, q.n_partials);
+  }
   for (int i = threadIdx.x; i < 256; i += blockDim.x) {
     const float d = __fmul_rn(e4m3_to_f32((uint32_t)i), g);
     s_dr[i] = make_float2(d, d != 0.f ? __frcp_rn(d) : 0.f);
@@ -1179,28 +1208,39 @@ cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
 
 cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                              float* g_out, __nv_bfloat16* y, int64_t ldy, uint8_t* codes, uint8_t* scales,
-                             float* partials, int num_sms, cudaStream_t stream) {
+                             float* partials, unsigned int* bar, int num_sms, cudaStream_t stream) {
   QdqArgs q{};
   q.src.x = x; q.src.M = M; q.src.K = K; q.src.ldx = ldx;
   q.src.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
   q.g_in = g_in; q.g_out = g_out; q.y = y; q.ldy = ldy; q.codes = codes; q.scales = scales;
   q.y_vec32 = ((reinterpret_cast<uintptr_t>(y) & 31u) == 0 && (ldy & 15) == 0) ? 1 : 0;
-  if (g_in == nullptr) {
+  const bool fused = g_in == nullptr && bar != nullptr;
+  q.partials = partials;
+  q.bar = bar;
+  if (g_in == nullptr && !fused) {
     const int p = amax_partials_count(M, K, num_sms);
     amax_kernel<<<p, kThreads, 0, stream>>>(x, M, K, ldx, partials);
-    q.partials = partials;
     q.n_partials = p;
   }
   const bool full = q.src.vec32 && (K % 1024) == 0;
-  const void* kern = full ? (const void*)nvfp4_qdq_kernel<true> : (const void*)nvfp4_qdq_kernel<false>;
+  const void* kerns[2][2] = {{(const void*)nvfp4_qdq_kernel<false, false>, (const void*)nvfp4_qdq_kernel<false, true>},
+                             {(const void*)nvfp4_qdq_kernel<true, false>, (const void*)nvfp4_qdq_kernel<true, true>}};
+  const void* kern = kerns[full][fused];
   const int64_t n_units = M * ((K + 1023) / 1024);
   int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   if (blocks > (int64_t)num_sms * per_sm) blocks = (int64_t)num_sms * per_sm;
+  if (fused && blocks > kMaxAmaxPartials) blocks = kMaxAmaxPartials;
   if (blocks < 1) blocks = 1;
   void* args[] = {&q};
+  if (fused) {
+    // every CTA must be resident for the in-kernel grid barrier
+    const cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchCooperativeKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
+  }
   return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
 }
 
