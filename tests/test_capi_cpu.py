@@ -125,3 +125,16 @@ def test_empty_problem_is_a_no_op(lib):
     assert lib.w4a4_gemm_comp(0, 0, 128, 64, None, None, None, None, None, None, None, None, 0, 0, None,
                               None, 0, None) == 0
     assert lib.nvfp4_prepare_comp_weights(1, 128, 64, fake, fake, None, fake, 0, 0, fake, None) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # the product path has no fallback: a missing library is an error, not a
+    # silent switch to other code
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from nvfp4_w4a4_gemm_gb300 import binding\n"
+            "binding.LIB_PATH = %r\n"
+            "try:\n    binding.load()\nexcept RuntimeError as e:\n    print('raised', e)\n") % (ROOT, str(tmp_path / "absent.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.startswith("raised"), r.stdout + r.stderr
