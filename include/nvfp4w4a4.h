@@ -280,7 +280,8 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  * a_codes [M, K/2], a_scales tiled [M, K] (16-byte aligned)
  * b_codes [N, K/2] (= W^T), b_scales tiled [N, K]
  * g_a, g_b device floats (NVFP4), or NULL for 1
- * resid [M, k] bf16, w_sel [N, k] bf16 (k % 16 == 0; NULL if k == 0)
+ * resid [M, k] bf16, w_sel [N, k] bf16 (k % 8 == 0 so rows are 16-byte
+ *         aligned for the tensor copies, 0 <= k <= K; NULL if k == 0)
  * y [M, N] bf16 (16-byte aligned)
  * workspace / ws_bytes: >= w4a4_gemm_workspace_bytes(M, N, K) (may be 0)
  * flags   NVFP4_COMP_W_DEQ or NVFP4_COMP_W_BF16 (the mode w_sel was prepared
@@ -324,8 +325,19 @@ int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M
  * receives which wait gave up. */
 int nvfp4_check_status(int clear, uint32_t* detail);
 
-/* Upper bound in nanoseconds of every device-side wait (default 2 s). */
+/* Upper bound in nanoseconds of every device-side wait of every kernel
+ * family (default 2 s): the GEMMs' mbarrier waits and the dynamic-scale
+ * quantizers' grid barrier.  Applies to launches issued after the call. */
 int nvfp4_set_wait_limit_ns(uint64_t ns);
+
+/* Testing aid for the failure path (the paper has no counterpart): the next
+ * dynamic-scale launch of nvfp4_quantize, nvfp4_quantize_grouped or
+ * nvfp4_qdq (g_in == NULL) starts its grid barrier one arrival short, so no
+ * CTA is ever released: every CTA's bounded wait runs out after the wait
+ * limit, the launch writes none of its outputs, and nvfp4_check_status
+ * returns NVFP4_ERR_TIMEOUT with detail 20 (the grid barrier).  One-shot;
+ * later launches are unaffected.  Nothing faults or hangs. */
+void nvfp4_inject_barrier_timeout(void);
 
 #ifdef __cplusplus
 }

@@ -54,6 +54,7 @@ _SIGS = {
                                 ctypes.c_int, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_check_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "nvfp4_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
+    "nvfp4_inject_barrier_timeout": ([], None),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -343,3 +344,9 @@ def check_status(clear=True):
 
 def set_wait_limit_ns(ns):
     _check("nvfp4_set_wait_limit_ns", load().nvfp4_set_wait_limit_ns(int(ns)))
+
+
+def inject_barrier_timeout():
+    """Testing aid: the next dynamic-scale quantize launch's grid barrier is
+    started one arrival short, so its bounded waits run out (one-shot)."""
+    load().nvfp4_inject_barrier_timeout()

@@ -346,9 +346,12 @@ int nvfp4_check_status(int clear, uint32_t* detail) {
   return hit[0] == 0 ? NVFP4_OK : (int)hit[0];
 }
 
+void nvfp4_inject_barrier_timeout(void) { nv4::quant_inject_barrier_timeout(); }
+
 int nvfp4_set_wait_limit_ns(uint64_t ns) {
   if (ns == 0) return NVFP4_ERR_INVALID_ARG;
-  return from_cuda(nv4::gemm_set_wait_limit(ns));
+  const cudaError_t e = nv4::gemm_set_wait_limit(ns);
+  return from_cuda(e == cudaSuccess ? nv4::quant_set_wait_limit(ns) : e);
 }
 
 }  // extern "C"

@@ -146,6 +146,24 @@ __device__ __forceinline__ bool tile_of(const GemmParams& p, const SchedSmem& s,
   return true;
 }
 
+// Grouped schedules: the routing offsets (already in shared memory, not yet
+// synchronized) must partition the M rows -- off[0] = 0, non-decreasing,
+// off[E] = M -- or the tiles would read and write rows outside A, R and Y.
+// Every CTA sees the same offsets, so on a bad table all of them latch an
+// argument error and return before allocating TMEM or issuing any copy.
+// Contains a __syncthreads.
+__device__ __forceinline__ bool offsets_valid(const GemmParams& p, const int32_t* off) {
+  __syncthreads();
+  bool bad = false;
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) bad |= off[e + 1] < off[e];
+  if (threadIdx.x == 0) bad |= off[0] != 0 || (int64_t)off[p.E] != p.M;
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) report_error(kDevErrInvalidArg, 0x300u);
+    return false;
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint32_t idesc_fp4(int fmt, uint32_t sf_id) {
   // a/b format E2M1 (=1) at bits 7 and 10, N>>3 at 17, scale type at 23
   // (0 = UE4M3, 1 = UE8M0), M>>4 at 24, scale-factor ids at 29 (A) / 4 (B).
@@ -215,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     sched.tile_start = s_sched + (p.E + 1);
     sched.pbase = s_sched + 2 * (p.E + 1);
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sched.off[i] = p.offsets[i];
-    __syncthreads();
+    if (!offsets_valid(p, sched.off)) return;
     if (threadIdx.x == 0) {
       int32_t ts = 0, pb = 0;
       for (int e = 0; e < p.E; ++e) {
@@ -701,7 +719,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     sched.tile_start = s_sched + (p.E + 1);
     sched.pbase = s_sched + 2 * (p.E + 1);
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sched.off[i] = p.offsets[i];
-    __syncthreads();
+    if (!offsets_valid(p, sched.off)) return;
     if (threadIdx.x == 0) {
       int32_t ts = 0, pb = 0;
       for (int e = 0; e < p.E; ++e) {

@@ -52,6 +52,8 @@ cudaError_t launch_tensor_scale(const __nv_bfloat16* x, int64_t M, int64_t K, in
                                 float* g_out, int num_sms, cudaStream_t stream);
 
 cudaError_t quant_status(uint32_t* out2, bool clear);
+cudaError_t quant_set_wait_limit(uint64_t ns);
+void quant_inject_barrier_timeout();
 
 // Dynamic-scale NVFP4 quantize with its amax scratch in a library-owned
 // device array (no caller workspace, no allocation).

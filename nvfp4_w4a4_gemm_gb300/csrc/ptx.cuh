@@ -16,7 +16,9 @@ namespace nv4 {
 // it).  Word 0 = first error code, word 1 = which wait gave up.
 enum : uint32_t { kDevErrNone = 0, kDevErrInvalidArg = 1, kDevErrTimeout = 4 };
 static __device__ uint32_t g_dev_status[2] = {0u, 0u};
-// Spin limit for every mbarrier wait, in %globaltimer nanoseconds (2 s).
+// Spin limit for every bounded wait of the translation unit, in %globaltimer
+// nanoseconds (2 s); like the status word, each .cu file has its own copy and
+// its own host setter (nvfp4_set_wait_limit_ns calls all of them).
 static __device__ uint64_t g_wait_limit_ns = 2000000000ull;
 
 __device__ __forceinline__ void report_error(uint32_t code, uint32_t where) {
@@ -135,42 +137,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* desc, 
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// Multicast variants: the same box lands at the same smem offset in every
-// CTA of `mask` (cluster ranks) and completes bytes on each one's mbarrier at
-// the same offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* desc, uint64_t* bar, int32_t x,
-                                               int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* desc, uint64_t* bar, int32_t x,
-                                               int32_t y, int32_t z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// Cluster helpers.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -202,14 +168,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
-               : "memory");
-}
-// Arrive on the mbarrier at the same offset in every CTA of `mask` once all
-// tcgen05 operations issued so far by this thread have completed.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(mask)
                : "memory");
 }
 // Block-scaled FP4 MMA: D[tmem] (+)= (A*sfa) x (B*sfb)^T, K = 64 per issue.

@@ -23,6 +23,7 @@
 // quantized.  MXFP4: each lane owns one 32-element block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -500,6 +501,20 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
     }
   }
   __syncthreads();
+  if (kGrouped) {
+    // the routing offsets must be a partition of the rows (offsets[0] = 0,
+    // non-decreasing, offsets[E] = M): anything else would index rows and
+    // scale tiles outside the buffers, so the launch latches an argument
+    // error and writes nothing (every CTA sees the same offsets and returns
+    // here, before the grid barrier)
+    bool bad = false;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) bad |= s_off[e + 1] < s_off[e];
+    if (threadIdx.x == 0) bad |= s_off[0] != 0 || (int64_t)s_off[a.E] != a.M;
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) report_error(kDevErrInvalidArg, 0x200u);
+      return;
+    }
+  }
   if (kGrouped) {
     // first padded scale row of each expert: exclusive prefix sum of
     // round_up(M_e, 128), a block-wide scan (each thread sums a run of experts)
@@ -1093,6 +1108,20 @@ __global__ void __launch_bounds__(1024) channel_compact_kernel(const int32_t* __
 }  // namespace
 
 // ------------------------------------------------------------ launchers ---
+// One-shot failure injection for the tests of the timeout path: the next
+// fused dynamic-scale launch starts its grid barrier's arrival counter at
+// 0xFFFFFFFF instead of 0, so the last CTA to arrive sees one arrival too
+// few and nobody releases the barrier: every CTA's bounded wait runs out,
+// latches a timeout and returns without writing any output.
+namespace {
+std::atomic<int> g_fail_next_barrier{0};
+int barrier_preset() { return g_fail_next_barrier.exchange(0) ? 0xFF : 0; }
+}  // namespace
+
+void quant_inject_barrier_timeout() { g_fail_next_barrier.store(1); }
+
+cudaError_t quant_set_wait_limit(uint64_t ns) { return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns)); }
+
 cudaError_t quant_status(uint32_t* out2, bool clear) {
   cudaError_t err = cudaMemcpyFromSymbol(out2, g_dev_status, sizeof(uint32_t) * 2);
   if (err == cudaSuccess && clear) {
@@ -1169,7 +1198,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   if (blocks < 1) blocks = 1;
   if (fused) {
     // every CTA must be resident for the in-kernel grid barrier
-    cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), stream);
+    cudaError_t e = cudaMemsetAsync(bar, barrier_preset(), sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
     void* args[] = {&a};
     return cudaLaunchCooperativeKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, smem, stream);
@@ -1237,7 +1266,7 @@ cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64
   void* args[] = {&q};
   if (fused) {
     // every CTA must be resident for the in-kernel grid barrier
-    const cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), stream);
+    const cudaError_t e = cudaMemsetAsync(bar, barrier_preset(), sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
     return cudaLaunchCooperativeKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
   }

@@ -113,3 +113,76 @@ def test_block_exponent_closed_forms():
     assert block_exponent(np.array([0.0]))[0] == -127
     assert block_exponent(np.array([2.0 ** 200]))[0] == 127
     assert block_exponent(np.array([2.0 ** -140]))[0] == -127
+
+
+# --- block_stats energy columns (|B|^2, |D|^2, |G|^2), pinned to values that
+# do not come from the oracle: the hand-derived components of the worked
+# example and two closed-form blocks ("Decomposing MXFP4 quantization
+# error", abstract: the error splits exactly into scale bias, deadzone
+# truncation and grid noise).
+
+def _stats_pins(stats_fn, golden_dir):
+    """Raise AssertionError unless ``stats_fn(x) -> (stats [M, nb, 4], ...)``
+    gives the independently derived energies on three blocks."""
+    with open(os.path.join(golden_dir, "mxfp4_worked.json")) as f:
+        ex = json.load(f)
+    # 1) the worked block: its non-zero head holds every non-zero component,
+    #    so each energy is the sum of squares of the hand-derived head values
+    x = np.zeros((1, ex["block_len"]), np.float32)
+    x[0, :4] = ex["x_head"]
+    st = stats_fn(x)[0][0, 0]
+    want = [sum(v * v for v in ex[k + "_head"]) for k in "BDGE"]
+    np.testing.assert_allclose(st, want, rtol=1e-12, atol=1e-15)
+    # 2) deadzone block: a = 24 = 6 * 2^2 puts the maximum on the grid at
+    #    both scales (s = s* = 4) and every other |x| < 1 < s/2 is zeroed at
+    #    both, so B = G = 0 and D = E = -x on the small entries
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 24.0
+    x[0, 1:] = F.bf16_round(np.linspace(-0.99, 0.99, 31).astype(np.float32))
+    small = float(np.sum(x[0, 1:].astype(np.float64) ** 2))
+    np.testing.assert_allclose(stats_fn(x)[0][0, 0], [0.0, small, 0.0, small], rtol=1e-12, atol=0)
+    # 3) bias-only block: a = 7 with every entry in {+-7, +-3.5, +-1.75} puts
+    #    each x/s* (s* = 7/6, fp32) within fp32 rounding of a grid point
+    #    {6, 3, 1.5}, so G is a few fp32 ulps; at s = 1 they round to 6, 4
+    #    (tie 3.5 -> even code 4) and 2 (tie 1.75 -> 2): the whole error is
+    #    scale bias, B = E up to those ulps, and D = 0
+    x = np.array([[7, -3.5, 1.75, -7] * 8], np.float32)
+    st = stats_fn(x)[0][0, 0]
+    e_energy = 8 * (1.0 + 0.25 + 0.0625 + 1.0)
+    assert st[1] == 0.0
+    assert st[2] < 1e-9
+    np.testing.assert_allclose(st[3], e_energy, rtol=0, atol=0)
+    np.testing.assert_allclose(st[0], e_energy, rtol=1e-6)
+
+
+def test_block_stats_energy_columns_pinned(golden_dir):
+    _stats_pins(mxfp4.block_stats, golden_dir)
+
+
+def test_block_stats_pins_reject_planted_mistakes(golden_dir):
+    import pytest
+
+    def swapped_bd(x):
+        st, cnt, d = mxfp4.block_stats(x)
+        return st[..., [1, 0, 2, 3]], cnt, d
+
+    def swapped_dg(x):
+        st, cnt, d = mxfp4.block_stats(x)
+        return st[..., [0, 2, 1, 3]], cnt, d
+
+    def no_square(x):
+        d = mxfp4.decompose(x)
+        M, K = d["E"].shape
+        s1 = lambda t: np.sum(np.abs(t.reshape(M, K // 32, 32)), axis=2)
+        sq = lambda t: np.sum(t.reshape(M, K // 32, 32) ** 2, axis=2)
+        return np.stack([s1(d["B"]), s1(d["D"]), s1(d["G"]), sq(d["E"])], -1), None, d
+
+    def bias_against_x(x):   # B measured as Q_s - x (i.e. the total error)
+        st, cnt, d = mxfp4.block_stats(x)
+        st = st.copy()
+        st[..., 0] = st[..., 3]
+        return st, cnt, d
+
+    for bad in (swapped_bd, swapped_dg, no_square, bias_against_x):
+        with pytest.raises(AssertionError):
+            _stats_pins(bad, golden_dir)

@@ -6,7 +6,7 @@ so they cannot hand nvfp4_quantize the workspace its dynamic tensor scale
 needs.  nvfp4_quantize_noalloc keeps that scratch in a device array owned by
 the library.  This test calls it through the C ABI and checks that its codes,
 scale bytes, tensor scale and residuals are identical to those of the
-allocating entry point, on two calls in a row with different inputs (the
+allocating entry point, on three calls in a row with different inputs (the
 shared scratch keeps the previous call's contents).  This file is collected
 last on purpose.
 """
@@ -21,11 +21,16 @@ from tests.helpers import bf16_bits_of, u8
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_matches_allocating_quantizer_on_two_calls():
+def test_noalloc_matches_allocating_quantizer_on_successive_calls():
     from nvfp4_w4a4_gemm_gb300 import binding as nv
     nv.load()
-    for call, (M, K, k, seed) in enumerate([(300, 1040, 33, 21), (517, 4096, 128, 22)]):
-        x = W.activations(M, K, max(1, K // 100), "t3x20", seed, seed).cuda()
+    # the third call follows the large second one with a much smaller shape
+    # and a 1000x smaller amax: the scratch then still holds the second
+    # call's larger partial maxima past the third call's own partials, so a
+    # read past them would change the tensor scale
+    shapes = [(300, 1040, 33, 21, 1.0), (517, 4096, 128, 22, 1.0), (40, 512, 16, 23, 1e-3)]
+    for call, (M, K, k, seed, amp) in enumerate(shapes):
+        x = (W.activations(M, K, max(1, K // 100), "t3x20", seed, seed).float() * amp).bfloat16().cuda()
         rng = np.random.default_rng(seed)
         chan = torch.from_numpy(np.sort(rng.choice(K, size=k, replace=False)).astype(np.int32)).cuda()
         ref = nv.nvfp4_quantize(x, chan=chan)            # existing entry point, caller workspace
