@@ -24,6 +24,11 @@ Readings (the pages name NVFP4 but do not define its arithmetic):
   residual R_i = x_i - deq_i in fp32; the emitted slice is bf16(R_i) on the
   channel set S.  The exact value of the quantized representation (used by
   the reference GEMM) is E2M1(code) * sigma * g in fp64.
+* Pre-scaled residual (an operand form for the GEMM, not a different
+  method): the fp32 residual R_i times fp32(1 / g) (the correctly rounded
+  reciprocal of the tensor scale, fp32 multiply), rounded once to bf16.  The
+  GEMM multiplies the compensation product by g again, so R_S . W_S is
+  unchanged up to that rounding.
 * Trainer-side fake quantization (QDQ, asymmetric W4A16 QAT): the same
   codes and scales, and per element bf16_rn(deq_i), deq_i as above (the
   fp32 product rounded once more to bf16, the trainer's weight dtype).
@@ -88,6 +93,7 @@ def quantize(x, g=None, chan=None):
       g       float32          tensor scale used
       resid_f32 [M, K]  float32 residual x - deq (before bf16 rounding)
       resid   [M, k]    float32 bf16-rounded residual on S (if chan given)
+      resid_scaled [M, k] float32 bf16(resid_f32 * fp32(1/g)) on S (if chan given)
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     M, K = x.shape
@@ -105,7 +111,14 @@ def quantize(x, g=None, chan=None):
     if chan is not None:
         chan = np.asarray(chan, dtype=np.int64)
         out["resid"] = bf16_round(resid_f32[:, chan])
+        out["resid_scaled"] = bf16_round((resid_f32[:, chan] * reciprocal(g)).astype(np.float32))
     return out
+
+
+def reciprocal(g):
+    """fp32(1 / g): numpy's float32 division is the correctly rounded IEEE
+    quotient."""
+    return np.float32(np.float32(1.0) / np.float32(g))
 
 
 def quantize_grouped(x, offsets, chan, g=None):
@@ -119,11 +132,16 @@ def quantize_grouped(x, offsets, chan, g=None):
     M = x.shape[0]
     k = chan.shape[1]
     resid = np.zeros((M, k), np.float32)
+    resid_scaled = np.zeros((M, k), np.float32)
+    rg = reciprocal(out["g"])
     for e in range(len(offsets) - 1):
         lo, hi = offsets[e], offsets[e + 1]
         if hi > lo:
-            resid[lo:hi] = bf16_round(out["resid_f32"][lo:hi][:, chan[e]])
+            rf = out["resid_f32"][lo:hi][:, chan[e]]
+            resid[lo:hi] = bf16_round(rf)
+            resid_scaled[lo:hi] = bf16_round((rf * rg).astype(np.float32))
     out["resid"] = resid
+    out["resid_scaled"] = resid_scaled
     return out
 
 

@@ -246,3 +246,53 @@ def test_grouped_scale_offsets_are_distinct_and_in_bounds():
     for e in range(E):
         if offs[e + 1] > offs[e]:
             assert rows[offs[e]] % 128 == 0
+
+
+# --- the pre-scaled residual (the GEMM's compensation operand R / g) -----
+
+def test_prescaled_residual_power_of_two_scale_is_exact_rescaling():
+    # with g = 2^j, fp32(1/g) = 2^-j exactly and the product is exact, so the
+    # pre-scaled residual is the bf16 residual times 2^-j, bit for bit (the
+    # values stay far from the subnormal and overflow ranges)
+    x = F.bf16_round(np.random.default_rng(5).standard_normal((24, 128)).astype(np.float32) * 3)
+    chan = np.arange(0, 128, 5)
+    for j in (-9, -3, 0, 4, 11):
+        q = nvfp4.quantize(x, g=np.float32(2.0 ** j), chan=chan)
+        assert np.array_equal(q["resid_scaled"], (q["resid"] * np.float32(2.0 ** -j)).astype(np.float32))
+
+
+def test_prescaled_residual_within_one_bf16_rounding_of_the_quotient():
+    # any g: |resid_scaled - R/g| <= 2^-8 |R/g| (one bf16 rounding, plus the
+    # fp32 reciprocal's and product's 2^-24-level errors); the dynamic scale
+    # of a workload, and a planted mistake (R * g) must fail the bound
+    x = W.activations(64, 512, 5, "t3x20", 1, 2).float().numpy()
+    chan = np.arange(1, 512, 7)
+    q = nvfp4.quantize(x, chan=chan)
+    exact = q["resid_f32"][:, chan].astype(np.float64) / np.float64(q["g"])
+    err = np.abs(q["resid_scaled"] - exact)
+    assert np.all(err <= 2.0 ** -8 * np.abs(exact) + 1e-45)
+    wrong = q["resid"] * np.float64(q["g"])
+    assert not np.all(np.abs(wrong - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-45)
+
+
+def test_prescaled_residual_grouped_matches_dense_rows():
+    # grouped: each expert's rows take that expert's channels, same rule
+    x = W.activations(40, 256, 3, "t3x20", 3, 4).float().numpy()
+    offs = np.array([0, 10, 10, 31, 40])
+    chan = np.array([[0, 16, 100, 255], [1, 2, 3, 4], [5, 50, 150, 250], [7, 8, 9, 200]])
+    qg = nvfp4.quantize_grouped(x, offs, chan)
+    qd = nvfp4.quantize(x)
+    rg = nvfp4.reciprocal(qd["g"])
+    for e in range(4):
+        lo, hi = offs[e], offs[e + 1]
+        want = np.asarray(torch_free_bf16(qd["resid_f32"][lo:hi][:, chan[e]] * rg))
+        assert np.array_equal(qg["resid_scaled"][lo:hi], want)
+
+
+def torch_free_bf16(v):
+    """bf16 round-to-nearest-even of float32 values by bit arithmetic (an
+    independent restatement of the rounding, not the library routine)."""
+    b = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    r = ((b + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32)
