@@ -65,8 +65,10 @@ enum { NVFP4_FMT_NVFP4 = 0, NVFP4_FMT_MXFP4 = 1 };
  * the correction then uses the same weights as the W4A4 product), or the
  * original bf16 weight columns. */
 enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1 };
-/* GEMM flag bit, OR-ed with the compensation mode (see w4a4_gemm_comp). */
-enum { NVFP4_GEMM_WEIGHTS_READY = 0x100 };
+/* GEMM flag bits, OR-ed with the compensation mode (see w4a4_gemm_comp). */
+enum { NVFP4_GEMM_WEIGHTS_READY = 0x100, NVFP4_GEMM_RESID_SCALED = 0x200 };
+/* Quantizer flag bit (nvfp4_quantize_ex / nvfp4_quantize_grouped_ex). */
+enum { NVFP4_QUANT_RESID_SCALED = 1 };
 
 /* Library version (major*10000 + minor*100 + patch). */
 int nvfp4_version(void);
@@ -128,6 +130,23 @@ int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const f
                    void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * nvfp4_quantize_ex -- nvfp4_quantize with flags.  NVFP4_QUANT_RESID_SCALED
+ * writes the residual divided by the tensor scale, the operand form the
+ * GEMM's compensation term consumes without a rescaling step of its own:
+ *   resid[m, i] = bf16(fp32(x - E2M1(code) * d) * fp32(1 / g))
+ * (the fp32 residual of nvfp4_quantize times the correctly rounded
+ * reciprocal of g, one rounding to bf16).  Pass it to w4a4_gemm_comp with
+ * NVFP4_GEMM_RESID_SCALED.  Codes, scales and g are those of nvfp4_quantize.
+ * Source: as nvfp4_quantize (the residual term R_S of Residual Activation
+ * Compensation); the division by g is this library's operand form.
+ * flags  0 (exactly nvfp4_quantize) or NVFP4_QUANT_RESID_SCALED; other bits
+ *        give NVFP4_ERR_INVALID_ARG
+ */
+int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
+                      uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * nvfp4_quantize_grouped -- nvfp4_quantize over expert-sorted MoE rows.
  * Row r belongs to the expert e with offsets[e] <= r < offsets[e+1] and takes
  * its residual slice on that expert's channels chan[e*k .. e*k+k).  One
@@ -143,6 +162,11 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
                            const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
                            uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* workspace,
                            size_t ws_bytes, void* stream);
+/* nvfp4_quantize_grouped with the flags of nvfp4_quantize_ex. */
+int nvfp4_quantize_grouped_ex(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
+                              const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                              uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
+                              void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * nvfp4_quantize_noalloc -- nvfp4_quantize with the dynamic tensor scale,
@@ -285,7 +309,12 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  * y [M, N] bf16 (16-byte aligned)
  * workspace / ws_bytes: >= w4a4_gemm_workspace_bytes(M, N, K) (may be 0)
  * flags   NVFP4_COMP_W_DEQ or NVFP4_COMP_W_BF16 (the mode w_sel was prepared
- *         in), optionally | NVFP4_GEMM_WEIGHTS_READY.
+ *         in), optionally | NVFP4_GEMM_WEIGHTS_READY, optionally |
+ *         NVFP4_GEMM_RESID_SCALED: resid is the pre-scaled residual of
+ *         nvfp4_quantize_ex (R / g_a), so the epilogue term is
+ *         y = bf16_rn(ga*gb*acc + c*accc) with c = ga*gb (COMP_W_DEQ) or ga
+ *         (COMP_W_BF16).  Dense GEMMs with more than 256 rows then feed the
+ *         compensation tiles to the tensor core with no rescaling pass.
  * The kernel is a programmatic dependent launch: it may start while the
  * preceding kernel of the stream is still running (the library's quantizers
  * let it).  By default it waits for that kernel before touching global

@@ -20,6 +20,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = ran
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 COMP_W_DEQ, COMP_W_BF16 = 0, 1
 GEMM_WEIGHTS_READY = 0x100  # flag bit: the weights are not written by work still pending on the stream
+GEMM_RESID_SCALED = 0x200   # flag bit: resid is the pre-scaled residual of nvfp4_quantize(..., resid_scaled=True)
+QUANT_RESID_SCALED = 1
 
 _lib = None
 
@@ -39,6 +41,10 @@ _SIGS = {
     "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_quantize_grouped": ([_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
                                ctypes.c_int),
+    "nvfp4_quantize_ex": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, ctypes.c_int, _P, _SZ, _P],
+                          ctypes.c_int),
+    "nvfp4_quantize_grouped_ex": ([_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, ctypes.c_int, _P,
+                                   _SZ, _P], ctypes.c_int),
     "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
     "mxfp4_decompose_elements": ([_P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
@@ -118,9 +124,11 @@ def grouped_scale_bytes(M_total, K, E):
     return load().nvfp4_grouped_scale_bytes(M_total, K, E)
 
 
-def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None):
+def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None, resid_scaled=False):
     """x bf16 [M, K] -> dict(codes u8 [M, K/2], scales u8 tiled, g f32 [1],
-    resid bf16 [M, k]).  g: None (dynamic) or device float32 [1]."""
+    resid bf16 [M, k]).  g: None (dynamic) or device float32 [1].
+    resid_scaled: the residual comes divided by g (the GEMM's pre-scaled
+    compensation operand; pass resid_scaled=True to the GEMM too)."""
     lib = load()
     _need(x, torch.bfloat16, "x")
     M, K = x.shape
@@ -140,11 +148,12 @@ def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None):
     ws = o.get("ws")
     if ws is None and g is None:
         ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
-    st = lib.nvfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(g), _ptr(g_out), _ptr(codes), _ptr(scales),
-                            _ptr(chan) if k else None, k, _ptr(resid) if k else None, _ptr(ws),
-                            0 if ws is None else ws.numel(), _stream())
-    _check("nvfp4_quantize", st)
-    return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+    st = lib.nvfp4_quantize_ex(_ptr(x), M, K, x.stride(0), _ptr(g), _ptr(g_out), _ptr(codes), _ptr(scales),
+                               _ptr(chan) if k else None, k, _ptr(resid) if k else None,
+                               QUANT_RESID_SCALED if resid_scaled else 0, _ptr(ws),
+                               0 if ws is None else ws.numel(), _stream())
+    _check("nvfp4_quantize_ex", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
 
 
 def _need_rows(t, dtype, name):
@@ -216,7 +225,7 @@ def nvfp4_quantize_noalloc(x, chan=None, out=None, g_out=None):
     return dict(codes=codes, scales=scales, g=g_out, resid=resid)
 
 
-def nvfp4_quantize_grouped(x, offsets, chan, g=None, g_out=None):
+def nvfp4_quantize_grouped(x, offsets, chan, g=None, g_out=None, resid_scaled=False):
     """Expert-sorted rows x [M_total, K], offsets int32 [E+1], chan int32 [E, k]."""
     lib = load()
     _need(x, torch.bfloat16, "x")
@@ -232,11 +241,12 @@ def nvfp4_quantize_grouped(x, offsets, chan, g=None, g_out=None):
     if g_out is None:
         g_out = torch.empty(1, dtype=torch.float32, device=dev)
     ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
-    st = lib.nvfp4_quantize_grouped(_ptr(x), M, K, x.stride(0), E, _ptr(offsets), _ptr(g), _ptr(g_out),
-                                    _ptr(codes), _ptr(scales), _ptr(chan) if k else None, k,
-                                    _ptr(resid) if k else None, _ptr(ws), ws.numel(), _stream())
-    _check("nvfp4_quantize_grouped", st)
-    return dict(codes=codes, scales=scales, g=g_out, resid=resid)
+    st = lib.nvfp4_quantize_grouped_ex(_ptr(x), M, K, x.stride(0), E, _ptr(offsets), _ptr(g), _ptr(g_out),
+                                       _ptr(codes), _ptr(scales), _ptr(chan) if k else None, k,
+                                       _ptr(resid) if k else None, QUANT_RESID_SCALED if resid_scaled else 0,
+                                       _ptr(ws), ws.numel(), _stream())
+    _check("nvfp4_quantize_grouped_ex", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
 
 
 def mxfp4_quantize(x, stats=False):
@@ -294,6 +304,8 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
     the stream, so the kernel may stream them while the preceding kernel runs."""
     if weights_ready:
         flags |= GEMM_WEIGHTS_READY
+    if resid is not None and qa.get("resid_scaled"):
+        flags |= GEMM_RESID_SCALED
     lib = load()
     a_codes, b_codes = qa["codes"], qb["codes"]
     M, Kh = a_codes.shape
@@ -319,6 +331,8 @@ def w4a4_grouped_gemm_comp(qa, offsets, b_codes, b_scales, g_b, N, resid=None, w
     work still pending on the stream."""
     if weights_ready:
         flags |= GEMM_WEIGHTS_READY
+    if resid is not None and qa.get("resid_scaled"):
+        flags |= GEMM_RESID_SCALED
     lib = load()
     a_codes = qa["codes"]
     M, Kh = a_codes.shape

@@ -123,11 +123,12 @@ size_t nvfp4_grouped_scale_bytes(int64_t M_total, int64_t K, int32_t E) {
 
 size_t nvfp4_quantize_workspace_bytes(void) { return kQuantWs; }
 
-int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
-                   uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid,
-                   void* workspace, size_t ws_bytes, void* stream) {
+int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
+                      uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
+                      void* workspace, size_t ws_bytes, void* stream) {
   int st = check_quant_args(x, M, K, ldx, codes, scales, chan, k, resid, 16);
   if (st != NVFP4_OK) return st;
+  if ((flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
   if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
     return NVFP4_ERR_WORKSPACE;
   const DeviceInfo* d = nullptr;
@@ -135,15 +136,23 @@ int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const f
   if (M == 0 && g_in != nullptr) return NVFP4_OK;
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M, K, ldx, g_in, g_out, codes, scales, chan, k, bf(resid),
                                               nullptr, 1, static_cast<float*>(workspace), quant_barrier(workspace),
-                                              d->num_sms, as_stream(stream)));
+                                              d->num_sms, as_stream(stream),
+                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0));
 }
 
-int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
-                           const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
-                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* workspace,
-                           size_t ws_bytes, void* stream) {
+int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
+                   uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid,
+                   void* workspace, size_t ws_bytes, void* stream) {
+  return nvfp4_quantize_ex(x, M, K, ldx, g_in, g_out, codes, scales, chan, k, resid, 0, workspace, ws_bytes, stream);
+}
+
+int nvfp4_quantize_grouped_ex(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
+                              const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                              uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
+                              void* workspace, size_t ws_bytes, void* stream) {
   int st = check_quant_args(x, M_total, K, ldx, codes, scales, chan, k, resid, 16);
   if (st != NVFP4_OK) return st;
+  if ((flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0 || E > 4096 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
   if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
     return NVFP4_ERR_WORKSPACE;
@@ -152,7 +161,16 @@ int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_
   if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
                                               bf(resid), offsets, E, static_cast<float*>(workspace),
-                                              quant_barrier(workspace), d->num_sms, as_stream(stream)));
+                                              quant_barrier(workspace), d->num_sms, as_stream(stream),
+                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0));
+}
+
+int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,
+                           const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                           uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  return nvfp4_quantize_grouped_ex(x, M_total, K, ldx, E, offsets, g_in, g_out, codes, scales, chan, k, resid, 0,
+                                   workspace, ws_bytes, stream);
 }
 
 int nvfp4_quantize_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* g_out, uint8_t* codes,
@@ -269,7 +287,7 @@ static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uin
                              const uint8_t* a_scales, const uint8_t* b_codes, const uint8_t* b_scales,
                              const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y) {
   if (fmt != NVFP4_FMT_NVFP4 && fmt != NVFP4_FMT_MXFP4) return NVFP4_ERR_INVALID_ARG;
-  const int mode = flags & ~NVFP4_GEMM_WEIGHTS_READY;
+  const int mode = flags & ~(NVFP4_GEMM_WEIGHTS_READY | NVFP4_GEMM_RESID_SCALED);
   if (mode != NVFP4_COMP_W_DEQ && mode != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
   if (M < 0 || N <= 0 || K <= 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % (fmt == NVFP4_FMT_MXFP4 ? 128 : 64) != 0) return NVFP4_ERR_UNSUPPORTED;

@@ -75,6 +75,8 @@ struct GemmParams {
   CUtensorMap tm_b;  // B codes [N, K/2] u8, or [E, N, K/2]
   CUtensorMap tm_r;  // R_S [rows, k] bf16
   CUtensorMap tm_w;  // W_S [N, k] bf16, or [E, N, k]
+  CUtensorMap tm_sfa;  // pair kernel: A's tiled scales as rows of 256 bytes
+  CUtensorMap tm_sfb;  // pair kernel: B's tiled scales as rows of 256 bytes
   const uint8_t* a_sf;
   const uint8_t* b_sf;
   uint64_t b_sf_expert_stride;
@@ -95,6 +97,7 @@ struct GemmParams {
   int early_w;      // weights (B codes / scales, W_S, g_b, offsets) are ready: stream them before the wait
                     // for the preceding kernel (programmatic dependent launch)
   int swap;         // narrow kernel, M <= 64: weight rows take the MMA's M = 128 slot, tokens its N slot
+  int resid_scaled; // the residual was divided by g_a in the quantizer
   uint32_t n_mma;   // swap: MMA N = M rounded up to 16
 };
 
@@ -516,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         const float gb = p.g_b ? p.g_b[tl.e] : 1.f;
         alpha = ga * gb;
         beta = (p.flags == 1) ? 1.f : gb;
+        if (p.resid_scaled) beta *= ga;  // the residual came divided by g_a
       }
       const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kAcc1 : kAcc0);
       const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kComp;
@@ -1028,8 +1032,11 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       if (n_ct > 0) {
         // the compensation k-tiles of this tile: scale the residual tile in
         // shared memory by c, then release it to the MMA warp
-        float c = __fdiv_rn(1.0f, ga);
-        if (p.flags == 1) c = __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[tl.e] : 1.f));
+        float c;
+        if (p.resid_scaled)  // the residual came divided by g_a
+          c = p.flags == 1 ? __fdiv_rn(1.0f, p.g_b ? p.g_b[tl.e] : 1.f) : 1.0f;
+        else
+          c = p.flags == 1 ? __fdiv_rn(1.0f, ga * (p.g_b ? p.g_b[tl.e] : 1.f)) : __fdiv_rn(1.0f, ga);
         stage = (stage + n_kt) % kWStages;
         bool okc = true;
         for (int ct = 0; ct < n_ct; ++ct) {
@@ -1107,6 +1114,495 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   }
 }
 
+// ===================================================== pair-tile kernel ====
+// 256 x 256 output tiles on a pair of CTAs (a 2-CTA cluster on two SMs) with
+// tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of A and its own
+// 128 rows (half) of B, so per unit of MMA work every SM takes in 2/3 of the
+// operand bytes of a 128 x 256 single-SM tile.  Both CTAs also load the block
+// scales of all 256 B rows (each CTA's MMA half reads them from its own TMEM).
+//
+// Scale factors travel in a ring of their own, ahead of the operands.  The
+// tensor pipe runs MMAs and scale copies (tcgen05.cp) in issue order, so a
+// k-tile's copies must be queued before the MMAs of the k-tile ahead of it
+// are; with the scales in the operand stages the copies could only start
+// when the operands landed (just in time: the kernel is bound by the bytes
+// each SM takes in) and the MMA warp waited for them every k-tile.
+//
+// Roles (12 warps per CTA):
+//   warp 0 (both)     operand TMA: A / B code tiles (or the compensation
+//                     tiles R_S / W_S) into a 5-stage ring; completions on the
+//                     leader's `full` barrier
+//   warp 1            leader: MMAs for both CTAs; both: TMEM allocation
+//   warp 2 (both)     scale TMA: this CTA's A scales and all 256 B rows'
+//                     scales per FP4 k-tile into an 8-stage scale ring
+//   warp 3 (leader)   scale copies smem -> TMEM of both CTAs, as soon as a
+//                     k-tile's scales have landed and its TMEM slot (that of
+//                     the operand stage it goes with) is free; relays the
+//                     compensation tiles' arrival to the epilogue warps
+//   warps 4..11 (both) epilogue of the CTA's 128 accumulator rows (and, unless
+//                     the residual comes pre-scaled, the compensation residual
+//                     scaling)
+// The compensation term folds into the accumulator: the residual tile is
+// multiplied by c so that the epilogue's single factor g_a g_b applies to
+// both parts -- c = 1/g_a (1/(g_a g_b) with BF16 weight columns), or, for a
+// residual the quantizer already divided by g_a, c = 1 (1/g_b): with c = 1
+// the compensation tiles go to the MMA as they land.
+constexpr int BNP = 256;                  // output columns per pair tile
+constexpr int BMP = 2 * BM;               // output rows per pair tile
+constexpr int kPStages = 5;               // operand ring (= TMEM scale slots)
+constexpr int kPTileA = BM * BKB;         // 16 KB: this CTA's 128 rows of A (or R)
+constexpr int kPTileB = 128 * BKB;        // 16 KB: this CTA's 128 rows of B (or W_S)
+constexpr int kPStageBytes = kPTileA + kPTileB;
+constexpr int kPSfStages = 8;             // scale ring
+constexpr int kPSfA = 2048, kPSfB = 4096; // this CTA's A rows, all 256 B rows
+constexpr int kPSfStageBytes = kPSfA + kPSfB;
+constexpr int kPThreads = 384;
+constexpr uint32_t kPColSf = 256;         // TMEM: accumulator [0, 256), 48-column scale slots after it
+static_assert(kPColSf + 48 * kPStages <= kTmemCols, "TMEM budget");
+static_assert(kPStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStageBytes + (size_t)kPSfStages * kPSfStageBytes + 512;
+
+__device__ __forceinline__ uint32_t idesc_fp4_pair(int fmt, uint32_t sf_id) {
+  uint32_t d = (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
+  if (fmt == 1) d |= (1u << 23) | (sf_id << 29) | (sf_id << 4);
+  return d;
+}
+__device__ __forceinline__ uint32_t idesc_bf16_pair() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  uint8_t* sf_ring = smem + kPStages * kPStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_ring + kPSfStages * kPSfStageBytes);
+  uint64_t* full = bars;                        // leader: 1 arrival + both CTAs' operand bytes
+  uint64_t* empty = full + kPStages;            // each CTA: the leader's MMA commit
+  uint64_t* sf_full = empty + kPStages;         // leader: warp 3 (copy commit / plain arrive)
+  uint64_t* comp_ready = sf_full + kPStages;    // leader: 16 epilogue warps (or warp 3 at once)
+  uint64_t* ct_landed = comp_ready + kPStages;  // each CTA: the leader's warp 3
+  uint64_t* sfl_full = ct_landed + kPStages;    // leader: 1 arrival + both CTAs' scale bytes
+  uint64_t* sfl_empty = sfl_full + kPSfStages;  // each CTA: warp 3's copy commit
+  uint64_t* acc_full = sfl_empty + kPSfStages;  // each CTA: the leader's MMA commit
+  uint64_t* acc_empty = acc_full + 1;           // leader: 16 epilogue warps
+  uint64_t* drain = acc_empty + 1;
+  uint64_t* sf_drain = drain + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cta_rank_in_cluster();
+  const bool leader = rank == 0;
+  const uint32_t peer = rank ^ 1u;
+  // launched as a programmatic dependent: without the early-weights promise
+  // nothing touches global memory before the preceding kernel has finished
+  if (!p.early_w) pdl_wait();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&sf_full[i], 1);
+      mbar_init(&comp_ready[i], 16);
+      mbar_init(&ct_landed[i], 1);
+    }
+    for (int i = 0; i < kPSfStages; ++i) {
+      mbar_init(&sfl_full[i], 1);
+      mbar_init(&sfl_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);
+    mbar_init(drain, 1);
+    mbar_init(sf_drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(s_tmem, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // both CTAs' barriers exist before any remote arrival or TMA completion
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int n_tiles_n = (int)((p.N + BNP - 1) / BNP);
+  const int64_t num_tiles = ((p.M + BMP - 1) / BMP) * (int64_t)n_tiles_n;
+  const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int cpk = p.fmt == 1 ? 2 : 4;                     // 512-byte scale chunks per 256-element k-tile
+  const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
+  const int n_kt = (int)((p.K + 255) / 256);
+  const int n_ct = (p.k + 63) / 64;
+  const int n_uses_tile = n_kt + n_ct;
+  const int64_t my_tiles = pair < num_tiles ? (num_tiles - 1 - pair) / n_pairs + 1 : 0;
+  // compensation residual scaling in shared memory by the epilogue warps,
+  // unless the residual already carries every factor but g_a g_b
+  const bool scale_r = n_ct > 0 && !(p.resid_scaled && p.flags == 0);
+
+  if (warp == 0) {
+    // ----------------------------------------------- operand producer ----
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_a);
+      tma_prefetch_desc(&p.tm_b);
+      if (n_ct > 0) {
+        tma_prefetch_desc(&p.tm_r);
+        tma_prefetch_desc(&p.tm_w);
+      }
+    }
+    __syncwarp();
+    const uint32_t full0 = cluster_addr(full, 0);  // the leader's full[0]; full[i] is 8 bytes further
+    constexpr uint32_t kTx = 2u * (uint32_t)(kPTileA + kPTileB);
+    auto issue_b = [&](int stg, int64_t nt, int kt) {
+      tma_load_2d_pair(stages + stg * kPStageBytes + kPTileA, &p.tm_b, full0 + 8u * (uint32_t)stg, kt * BKB,
+                       (int32_t)(nt * BNP + BM * rank));
+    };
+    auto issue_a = [&](int stg, int64_t mt, int kt) {
+      tma_load_2d_pair(stages + stg * kPStageBytes, &p.tm_a, full0 + 8u * (uint32_t)stg, kt * BKB,
+                       (int32_t)((mt * 2 + rank) * BM));
+    };
+    // early weights: the B halves of this pair's first k-tiles go out before
+    // the wait for the preceding kernel (the ring starts empty)
+    int pre = 0;
+    if (p.early_w && pair < num_tiles) {
+      pre = n_kt < kPStages ? n_kt : kPStages;
+      if (elect_one()) {
+        for (int i = 0; i < pre; ++i) {
+          if (leader) mbar_arrive_expect_tx(&full[i], kTx);
+          issue_b(i, pair % n_tiles_n, i);
+        }
+      }
+      __syncwarp();
+    }
+    if (p.early_w) pdl_wait();
+    int issued = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
+      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        const bool early = issued++ < pre;  // B half already in flight, stage known empty
+        if (!early && !mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
+          if (!early && leader) mbar_arrive_expect_tx(&full[stage], kTx);
+          issue_a(stage, mt, kt);
+          if (!early) issue_b(stage, nt, kt);
+        }
+        __syncwarp();
+        if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+      }
+      for (int ct = 0; ct < n_ct && ok; ++ct) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
+          uint8_t* sa = stages + stage * kPStageBytes;
+          const uint32_t fb = full0 + 8u * (uint32_t)stage;
+          if (leader) mbar_arrive_expect_tx(&full[stage], kTx);
+          tma_load_2d_pair(sa, &p.tm_r, fb, ct * 64, (int32_t)((mt * 2 + rank) * BM));
+          tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, (int32_t)(nt * BNP + BM * rank));
+        }
+        __syncwarp();
+        if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // wind-down: every stage use issued so far is released by the MMA warp
+    // (its commits reach this CTA's empty barriers) before the CTA may exit,
+    // so no copy or remote arrival is still landing in this CTA afterwards
+    const int64_t uses = my_tiles * n_uses_tile;
+    for (int i = 0; i < kPStages && ok; ++i) {
+      if (uses > i) {
+        const int64_t last = (uses - 1 - i) / kPStages;  // this stage's last use index
+        if (!mbar_wait_warp(&empty[i], (uint32_t)(last & 1), kWaitDrain, s_abort)) ok = false;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA (leader only) ----
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t empty_own0 = smem_u32(empty), empty_peer0 = cluster_addr(empty, peer);
+      const uint32_t idesc_main = idesc_fp4_pair(p.fmt, 0);
+      int64_t done_tiles = 0;
+      for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
+        if (!mbar_wait_cl_warp(acc_empty, acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+        acc_phase ^= 1u;
+        tc_fence_after();
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+          if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort) ||
+              !mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t sa = smem_u32(stages + stage * kPStageBytes);
+            const uint32_t sb = sa + kPTileA;
+            const uint32_t t_sfa = tmem + kPColSf + (uint32_t)stage * 48u;
+            const uint32_t t_sfb = t_sfa + 16u;
+            const int64_t krem = p.K - (int64_t)kt * 256;
+            const int n_mma = krem >= 256 ? 4 : (int)(krem / 64);
+            if (n_mma == 4 && p.fmt == 0) {
+              const uint64_t ad = desc_sw128(sa), bd = desc_sw128(sb);  // +32 B per k-step = +2
+              mma_nvf4_4x_pair(tmem, ad, bd, idesc_main, t_sfa, t_sfb, kt > 0 ? 1u : 0u);
+              mma_nvf4_4x_pair(tmem, ad + 2, bd + 2, idesc_main, t_sfa + 4u, t_sfb + 8u, 1u);
+              mma_nvf4_4x_pair(tmem, ad + 4, bd + 4, idesc_main, t_sfa + 8u, t_sfb + 16u, 1u);
+              mma_nvf4_4x_pair(tmem, ad + 6, bd + 6, idesc_main, t_sfa + 12u, t_sfb + 24u, 1u);
+            } else {
+              for (int j = 0; j < n_mma; ++j) {
+                const uint64_t adesc = desc_sw128(sa + 32u * j);
+                const uint64_t bdesc = desc_sw128(sb + 32u * j);
+                const uint32_t accum = (kt > 0 || j > 0) ? 1u : 0u;
+                if (p.fmt == 1)
+                  mma_mxf4_2x_pair(tmem, adesc, bdesc, idesc_fp4_pair(1, (uint32_t)(j & 1) * 2u),
+                                   t_sfa + 4u * (j >> 1), t_sfb + 8u * (j >> 1), accum);
+                else
+                  mma_nvf4_4x_pair(tmem, adesc, bdesc, idesc_main, t_sfa + 4u * j, t_sfb + 8u * j, accum);
+              }
+            }
+            tc_commit_pair(empty_own0 + 8u * (uint32_t)stage);
+            tc_commit_pair(empty_peer0 + 8u * (uint32_t)stage);
+          }
+          __syncwarp();
+          if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+        }
+        for (int ct = 0; ct < n_ct && ok; ++ct) {
+          // sf_full: warp 3's plain arrival for this use (a stage is refilled
+          // only after every role that waits on its full barrier saw the use);
+          // scaled residual: all 16 epilogue warps are done with the tile
+          if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort) ||
+              (scale_r ? !mbar_wait_cl_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)
+                       : !mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t sa = smem_u32(stages + stage * kPStageBytes);
+            const uint32_t sb = sa + kPTileA;
+            const int krem = p.k - ct * 64;
+            const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
+            for (int j = 0; j < n_mma; ++j)
+              mma_bf16_pair(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16_pair(), 1u);
+            tc_commit_pair(empty_own0 + 8u * (uint32_t)stage);
+            tc_commit_pair(empty_peer0 + 8u * (uint32_t)stage);
+          }
+          __syncwarp();
+          if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (elect_one()) {
+          tc_commit_pair(smem_u32(acc_full));
+          tc_commit_pair(cluster_addr(acc_full, peer));
+        }
+        __syncwarp();
+        ++done_tiles;
+      }
+      if (elect_one()) tc_commit_pair(smem_u32(drain));
+      __syncwarp();
+      mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
+      // the last tile's accumulator release (16 epilogue arrivals, half of
+      // them remote) lands before the CTA may exit
+      if (ok && done_tiles > 0) mbar_wait_cl_warp(acc_empty, acc_phase ^ 1u, kWaitDrain, s_abort);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- scale producer ----
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_sfa);
+      tma_prefetch_desc(&p.tm_sfb);
+    }
+    __syncwarp();
+    if (p.early_w) pdl_wait();  // A's scales come from the preceding kernel
+    const uint32_t sfl0 = cluster_addr(sfl_full, 0);
+    const int sf_rows = 2 * cpk;  // 256-byte rows of one scale box (one k-tile of one 128-row tile)
+    const uint32_t tx = 2u * 3u * (uint32_t)(sf_rows * 256);
+    int slot = 0;
+    uint32_t sphase = 0;
+    bool ok = true;
+    for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
+      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
+      const int64_t at = mt * 2 + rank, bt = nt * 2;
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        if (!mbar_wait_warp(&sfl_empty[slot], sphase ^ 1u, kWaitSfDrain, s_abort)) { ok = false; break; }
+        if (elect_one()) {
+          uint8_t* dst = sf_ring + slot * kPSfStageBytes;
+          const uint32_t fb = sfl0 + 8u * (uint32_t)slot;
+          const int64_t ck = (int64_t)kt * cpk;
+          if (leader) mbar_arrive_expect_tx(&sfl_full[slot], tx);
+          tma_load_2d_pair(dst, &p.tm_sfa, fb, 0, (int32_t)((at * n_cg + ck) * 2));
+          tma_load_2d_pair(dst + kPSfA, &p.tm_sfb, fb, 0, (int32_t)((bt * n_cg + ck) * 2));
+          tma_load_2d_pair(dst + kPSfA + 2048, &p.tm_sfb, fb, 0, (int32_t)(((bt + 1) * n_cg + ck) * 2));
+        }
+        __syncwarp();
+        if (++slot == kPSfStages) { slot = 0; sphase ^= 1u; }
+      }
+    }
+    // wind-down: warp 3's last copy commits (they arrive on this CTA's
+    // sfl_empty) have landed
+    const int64_t loads = my_tiles * n_kt;
+    for (int i = 0; i < kPSfStages && ok; ++i) {
+      if (loads > i) {
+        const int64_t last = (loads - 1 - i) / kPSfStages;
+        if (!mbar_wait_warp(&sfl_empty[i], (uint32_t)(last & 1), kWaitDrain, s_abort)) ok = false;
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------- scale copies + compensation relay (leader) ----
+    if (leader) {
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, sphase = 0;
+      bool ok = true;
+      const uint32_t ct_peer0 = cluster_addr(ct_landed, peer);
+      const uint32_t sfle_own0 = smem_u32(sfl_empty), sfle_peer0 = cluster_addr(sfl_empty, peer);
+      for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
+        for (int kt = 0; kt < n_uses_tile && ok; ++kt) {
+          // this use's TMEM scale slot (its operand stage's) is free once the
+          // MMAs of the stage's previous use are done
+          if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+          if (kt < n_kt) {
+            if (!mbar_wait_warp(&sfl_full[slot], sphase, kWaitFull, s_abort)) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t sfa = smem_u32(sf_ring + slot * kPSfStageBytes);
+              const uint32_t sfb = sfa + kPSfA;
+              const uint32_t t_sfa = tmem + kPColSf + (uint32_t)stage * 48u;
+              const uint32_t t_sfb = t_sfa + 16u;
+              const int64_t cg0 = (int64_t)kt * cpk;
+              const int nch = (int)((n_cg - cg0) < cpk ? (n_cg - cg0) : cpk);
+              for (int c = 0; c < nch; ++c) {
+                tmem_cp_32x128b_x4_pair(t_sfa + 4u * c, desc_sf(sfa + 512u * c));
+                tmem_cp_32x128b_x4_pair(t_sfb + 8u * c, desc_sf(sfb + 512u * c));
+                tmem_cp_32x128b_x4_pair(t_sfb + 8u * c + 4u, desc_sf(sfb + 2048u + 512u * c));
+              }
+              if (scale_r) mbar_arrive_n(&comp_ready[stage], 16);  // whole phase: parity tracks the stage's uses
+              tc_commit_pair(smem_u32(&sf_full[stage]));
+              tc_commit_pair(sfle_own0 + 8u * (uint32_t)slot);
+              tc_commit_pair(sfle_peer0 + 8u * (uint32_t)slot);
+            }
+            __syncwarp();
+            if (++slot == kPSfStages) { slot = 0; sphase ^= 1u; }
+          } else {
+            if (scale_r) {
+              // compensation tile landed in both CTAs: hand it to the epilogue
+              // warps of both (at most one phase ahead of them: the stage's next
+              // compensation use needs their comp_ready arrivals)
+              if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+              if (elect_one()) {
+                mbar_arrive(&ct_landed[stage]);
+                mbar_arrive_cluster(ct_peer0 + 8u * (uint32_t)stage);
+              }
+            }
+            if (elect_one()) mbar_arrive(&sf_full[stage]);
+            __syncwarp();
+          }
+          if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (elect_one()) tc_commit_pair(smem_u32(sf_drain));
+      __syncwarp();
+      mbar_wait_warp(sf_drain, 0, kWaitSfDrain, nullptr);
+    }
+  } else {
+    // ------------------------------------------- epilogue (both CTAs) ----
+    const int q = warp & 3;         // TMEM lane quarter
+    if (p.early_w) pdl_wait();      // g_a and the output may belong to the preceding kernel
+    const int h = (warp - 4) >> 2;  // column half of the tile
+    const int r = q * 32 + lane;
+    uint32_t acc_phase = 0;
+    const int et = threadIdx.x - 128;
+    int stage = 0;
+    uint32_t ct_phase = 0;  // bit s: parity of ct_landed[s]'s next phase
+    const float ga = p.g_a ? *p.g_a : 1.f;
+    const float gb = p.g_b ? *p.g_b : 1.f;
+    float c = 1.f;
+    if (p.resid_scaled) {
+      if (p.flags == 1) c = __fdiv_rn(1.0f, gb);
+    } else {
+      c = p.flags == 1 ? __fdiv_rn(1.0f, ga * gb) : __fdiv_rn(1.0f, ga);
+    }
+    const uint32_t comp_ready_l0 = cluster_addr(comp_ready, 0);
+    const uint32_t acc_empty_l = cluster_addr(acc_empty, 0);
+    for (int64_t t = pair; t < num_tiles; t += n_pairs) {
+      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
+      if (scale_r) {
+        stage = (stage + n_kt) % kPStages;
+        bool okc = true;
+        for (int ct = 0; ct < n_ct; ++ct) {
+          if (!mbar_wait_cl_warp(&ct_landed[stage], (ct_phase >> stage) & 1u, kWaitCtLanded, s_abort)) {
+            okc = false;
+            break;
+          }
+          ct_phase ^= 1u << stage;
+          uint4* ra = reinterpret_cast<uint4*>(stages + stage * kPStageBytes);
+#pragma unroll
+          for (int i = et; i < kPTileA / 16; i += 256) {
+            uint4 v = ra[i];
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(w[qq] << 16) * c,
+                                                              __uint_as_float(w[qq] & 0xFFFF0000u) * c);
+              w[qq] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            ra[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (elect_one()) mbar_arrive_cluster(comp_ready_l0 + 8u * (uint32_t)stage);  // one of 16 warp arrivals
+          if (++stage == kPStages) stage = 0;
+        }
+        if (!okc) break;
+      }
+      if (!mbar_wait(acc_full, acc_phase, kWaitAccFull, s_abort)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const float alpha = p.fmt == 0 ? ga * gb : 1.f;
+      const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+      // the whole 128-column half row in registers, then the accumulator is
+      // released before any conversion or store
+      uint32_t v[8][16];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) tmem_ld_32x32b_x16(t_acc + (uint32_t)(cc * 16), v[cc]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_l);  // accumulator free: the next tile's MMAs may start
+      const int64_t row = (mt * 2 + rank) * BM + r;
+      const int64_t col0 = nt * BNP + h * 128;
+      if (row < p.M && col0 < p.N) {
+        __nv_bfloat16* dst = p.y + row * p.N + col0;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(alpha * __uint_as_float(v[cc][2 * i]),
+                                                            alpha * __uint_as_float(v[cc][2 * i + 1]));
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if (p.y_vec32) {
+            stg_256(dst + 16 * cc, w);
+          } else {
+            reinterpret_cast<uint4*>(dst + 16 * cc)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(dst + 16 * cc)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+      }
+    }
+  }
+
+  // every role of both CTAs is done (the MMA warp drained its work, each
+  // producer saw its last stage released): no remote access is in flight
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------- host side ---
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1128,7 +1624,8 @@ EncodeFn get_encode() {
 
 // rank-2 or rank-3 row-major tensor: dims innermost first
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, int rank,
-              const uint64_t* dims, uint32_t box0, uint32_t box1) {
+              const uint64_t* dims, uint32_t box0, uint32_t box1,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
   cuuint64_t gdim[3], gstr[2];
@@ -1137,7 +1634,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void
   gstr[0] = dims[0] * esize;
   if (rank == 3) gstr[1] = dims[0] * dims[1] * esize;
   return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1235,6 +1732,7 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   p.k = pr.k;
   p.flags = pr.flags & kGemmCompBf16;
   p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
+  p.resid_scaled = (pr.flags & kGemmResidScaled) ? 1 : 0;
   p.fmt = pr.fmt;
   p.E = E;
   p.offsets = pr.offsets;
@@ -1312,6 +1810,7 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   p.k = pr.k;
   p.flags = pr.flags & kGemmCompBf16;
   p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
+  p.resid_scaled = (pr.flags & kGemmResidScaled) ? 1 : 0;
   p.fmt = pr.fmt;
   p.E = E;
   p.offsets = pr.offsets;
@@ -1331,9 +1830,118 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   return cudaGetLastError();
 }
 
+// Clusters of two pair-kernel CTAs that fit on the device at once (0 when
+// the device cannot co-schedule them), per device.
+int pair_clusters(int num_sms) {
+  static int cached[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::call_once(once[dev], [dev, num_sms] {
+    int n = 0;
+    if (cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPSmemBytes) == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+      cfg.blockDim = dim3(kPThreads);
+      cfg.dynamicSmemBytes = kPSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, w4a4_gemm_pair_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cached[dev] = n;
+  });
+  return cached[dev];
+}
+
+cudaError_t launch_pair(const GemmProblem& pr, int clusters_max, cudaStream_t stream) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  const uint64_t kb = (uint64_t)(pr.K / 2);
+  {
+    const uint64_t d[2] = {kb, (uint64_t)pr.M};
+    if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t d[2] = {kb, (uint64_t)pr.N};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
+  }
+  // tiled scales viewed as rows of 256 bytes; one box = one k-tile's chunks
+  // of one 128-row scale tile (4 x 512 B NVFP4, 2 x 512 B MXFP4)
+  const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
+  const uint32_t sf_rows = pr.fmt == 1 ? 4u : 8u;
+  {
+    const uint64_t bytes = (uint64_t)((pr.M + 127) / 128) * 128u * (uint64_t)n_sf_cols;
+    const uint64_t d[2] = {256, bytes / 256};
+    if (!make_map(&p.tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_scales, 2, d, 256, sf_rows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t bytes = (uint64_t)((pr.N + 127) / 128) * 128u * (uint64_t)n_sf_cols;
+    const uint64_t d[2] = {256, bytes / 256};
+    if (!make_map(&p.tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_scales, 2, d, 256, sf_rows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  if (pr.k > 0) {
+    const uint64_t dr[2] = {(uint64_t)pr.k, (uint64_t)pr.M};
+    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
+    const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
+    if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BM)) return cudaErrorInvalidValue;
+  }
+  p.g_a = pr.g_a;
+  p.g_b = pr.g_b;
+  p.y = pr.y;
+  p.M = pr.M;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.k = pr.k;
+  p.flags = pr.flags & kGemmCompBf16;
+  p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
+  p.resid_scaled = (pr.flags & kGemmResidScaled) ? 1 : 0;
+  p.fmt = pr.fmt;
+  p.E = 1;
+  p.y_vec32 = ((reinterpret_cast<uintptr_t>(pr.y) & 31u) == 0 && (pr.N % 16) == 0) ? 1 : 0;
+  const int64_t tiles = ((pr.M + BMP - 1) / BMP) * ((pr.N + BNP - 1) / BNP);
+  const int64_t clusters = tiles < clusters_max ? tiles : clusters_max;
+  cudaError_t err =
+      cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  err = cudaLaunchKernelEx(&cfg, w4a4_gemm_pair_kernel, p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
 cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
-  // few rows: 128 x 128 tiles keep more SMs busy; otherwise 128 x 256 tiles
+  // few rows: 128 x 128 tiles keep more SMs busy; dense layers with more
+  // rows: 256 x 256 tiles on CTA pairs; grouped: 128 x 256 tiles (one expert
+  // per tile, so the pair tile's 256 rows would mostly be padding)
   if (!grouped && pr.M <= 2 * BM) return launch_narrow(pr, grouped, num_sms, stream);
+  if (!grouped) {
+    const int clusters = pair_clusters(num_sms);
+    if (clusters > 0) return launch_pair(pr, clusters, stream);
+  }
   return launch_wide(pr, grouped, num_sms, stream);
 }
 

@@ -17,7 +17,7 @@ int amax_partials_count(int64_t M, int64_t K, int num_sms);
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  unsigned int* bar, int num_sms, cudaStream_t stream);
+                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled = 0);
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
@@ -66,6 +66,7 @@ cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int
 // GemmProblem::flags bits (the C ABI's values)
 constexpr int kGemmCompBf16 = 1;          // compensation columns are the BF16 weights
 constexpr int kGemmWeightsReady = 0x100;  // weights may be read before the preceding kernel ends
+constexpr int kGemmResidScaled = 0x200;   // the residual was divided by g_a (nvfp4_quantize_for_gemm)
 struct GemmProblem {
   int fmt = 0;  // 0 NVFP4, 1 MXFP4
   int64_t M = 0, N = 0, K = 0;

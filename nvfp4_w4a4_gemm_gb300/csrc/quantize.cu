@@ -142,6 +142,7 @@ struct QuantArgs {
   int E;
   int use_map;              // channel bitmaps + prefix counts in shared memory
   int vec32;                // rows start on 32-byte boundaries: 256-bit loads
+  int resid_scaled;         // residual written divided by g (times RN(1/g))
 };
 
 constexpr float kRcp6 = 0x1.555556p-3f;  // 1/6 rounded to nearest fp32
@@ -189,6 +190,7 @@ struct ScaleCtx {
   float g, yg;
   bool fast;
   const float2* dr;  // shared: (d, 1/d) for every scale byte
+  float rs;          // residual factor: 1, or RN(1/g) for the pre-scaled residual
 };
 
 // Quantize one 16-element block owned by this thread (`valid` = the block
@@ -218,16 +220,18 @@ __device__ __forceinline__ uint32_t quant_block(const uint4& raw0, const uint4& 
   return sig;
 }
 
-// Compensation residual of one element: x - E2M1(RN(x * rcp)) * d, rounded
-// to bf16 (0-scale blocks have code 0).  The code is the one the block
-// quantizer wrote for this element: the same fp32 product and conversion.
-__device__ __forceinline__ __nv_bfloat16 element_residual(float x, float d, float rcp) {
+// Compensation residual of one element: x - E2M1(RN(x * rcp)) * d in fp32,
+// times rs (1, or RN(1/g) for the pre-scaled residual; a product with 1 is
+// exact), rounded to bf16 (0-scale blocks have code 0).  The code is the one
+// the block quantizer wrote for this element: the same fp32 product and
+// conversion.
+__device__ __forceinline__ __nv_bfloat16 element_residual(float x, float d, float rcp, float rs) {
   float dq = 0.f;
   if (d != 0.f) {
     const uint32_t h2 = cvt_e2m1x2_to_f16x2(cvt_e2m1x2(__fmul_rn(x, rcp), 0.f));
     dq = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
   }
-  return __float2bfloat16_rn(__fsub_rn(x, dq));
+  return __float2bfloat16_rn(__fmul_rn(__fsub_rn(x, dq), rs));
 }
 
 // Grid-wide barrier of a cooperative launch, bounded by the wait limit.
@@ -425,7 +429,7 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
       __nv_bfloat16 val = __float2bfloat16_rn(0.f);
       if (in) {
         const float2 dr = sc.dr[blk >= 32 ? s1 : s0];
-        val = element_residual(__bfloat162float(xrow[j]), dr.x, dr.y);
+        val = element_residual(__bfloat162float(xrow[j]), dr.x, dr.y, sc.rs);
       }
       rrow[i] = val;
     }
@@ -580,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   sc.yg = __frcp_rn(g);
   sc.fast = g >= 0x1p-100f && g <= 0x1p100f;
   sc.dr = s_dr;
+  sc.rs = a.resid_scaled ? sc.yg : 1.0f;
 
   // work unit = one row x 1024 columns: each lane owns 2 blocks of 16.
   // Two register buffers alternate: the next unit's loads are in flight
@@ -911,6 +916,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_qdq_kernel(QdqArgs q) {
   sc.yg = __frcp_rn(g);
   sc.fast = g >= 0x1p-100f && g <= 0x1p100f;
   sc.dr = s_dr;
+  sc.rs = 1.0f;
   const int64_t n_cg = (q.src.K / 16 + 3) / 4;
   while (u < n) {
     const uint32_t ub = u + n_warps;
@@ -1151,12 +1157,13 @@ int amax_partials_count(int64_t M, int64_t K, int num_sms) {
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  unsigned int* bar, int num_sms, cudaStream_t stream) {
+                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled) {
   if (M == 0) { k = 0; chan = nullptr; resid = nullptr; }
   QuantArgs a{};
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
+  a.resid_scaled = resid_scaled;
   {
     const size_t words = (size_t)((K + 31) / 32);
     const size_t tab = (size_t)a.E * words * (sizeof(uint32_t) + sizeof(uint16_t));

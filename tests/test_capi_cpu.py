@@ -95,12 +95,17 @@ def test_invalid_arguments_rejected_on_host(lib):
                                       0, 0, fake, None, 0, None) == 1
     # dynamic tensor scale without workspace
     assert lib.nvfp4_quantize(fake, 4, 32, 32, None, None, fake, fake, None, 0, None, None, 0, None) == 5
-    # GEMM flag bits: only the compensation mode and the weights-ready bit exist
-    for bad in (2, 0x200, 0x101 | 0x400):
+    # GEMM flag bits: only the compensation mode, the weights-ready and the
+    # pre-scaled-residual bits exist
+    for bad in (2, 0x400, 0x101 | 0x400, 0x800 | 0x200):
         assert lib.w4a4_gemm_comp(0, 4, 128, 64, fake, fake, None, fake, fake, None, None, None, 0, bad, fake,
                                   None, 0, None) == 1
     assert lib.w4a4_grouped_gemm_comp(0, 4, fake, 8, 128, 64, fake, fake, None, fake, fake, None, None, None,
-                                      0, 0x300, fake, None, 0, None) == 1
+                                      0, 0x500, fake, None, 0, None) == 1
+    # quantizer flags: only the pre-scaled-residual bit exists
+    assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 2, None, 0, None) == 1
+    assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 4, None,
+                                         0, None) == 1
     # QDQ: K % 16, strides, misaligned buffers, codes without scales, dynamic scale without workspace
     g = fake
     assert lib.nvfp4_qdq(fake, 4, 24, 24, g, None, fake, 24, None, None, None, 0, None) == 1

@@ -431,3 +431,298 @@ def test_kernel_protocol_holds_under_random_schedules(early):
 @pytest.mark.parametrize("protocol", ["mma_skips_copy_warp", "epilogue_waits_full"])
 def test_model_rejects_known_wrong_protocols(protocol):
     assert _failures(protocol, 400) > 0
+
+
+# ------------------------------------------------------- pair-tile kernel --
+class SignedTxBarrier(Barrier):
+    """An mbarrier whose transaction count may go below zero for a while: in
+    the pair kernel the peer CTA's copies can land on the leader's `full`
+    barrier before the leader's arrive.expect_tx of that phase."""
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._maybe_complete()
+
+
+class PairGemmModel(WideGemmModel):
+    """Roles of `w4a4_gemm_pair_kernel`: two CTAs (rank 0 = leader, rank 1 =
+    peer).  Each CTA runs an operand TMA warp (a 5-stage ring), a scale TMA
+    warp (an 8-stage ring of its own, running ahead of the operands) and
+    eight epilogue warps; the leader alone runs the MMA warp and the copy warp,
+    which moves a k-tile's scales into the TMEM slot of its operand stage as
+    soon as they have landed and the slot's previous MMAs are done.  Barrier
+    homes as in the kernel: `full`, `sf_full`, `comp_ready` (16), `sfl_full`
+    and `acc_empty` (16) in the leader; `empty`, `acc_full`, `ct_landed` and
+    `sfl_empty` in each CTA.  Both CTAs' copies complete on the leader's
+    barriers; the MMA and copy warps' commits and the leader's relays arrive on
+    both CTAs; the peer's epilogue warps arrive remotely on the leader.  Remote
+    arrivals are asynchronous and unordered with the leader's own.  With
+    `scale_r` the epilogue warps scale each compensation residual tile before
+    the MMA reads it; without it (a residual the quantizer pre-scaled) the
+    compensation tiles go straight to the MMA.  Besides the wide model's
+    checks, the model asserts that no TMEM scale slot or scale stage is
+    overwritten while still in use, and that when both CTAs have finished every
+    role (the final cluster barrier, after which a CTA may exit) nothing is
+    still in flight towards either CTA."""
+
+    SF_STAGES = 8
+
+    def __init__(self, seed, n_tiles, n_kt, n_ct, protocol="kernel", stages=5, early=False, scale_r=True):
+        self.r = random.Random(seed)
+        self.S, self.n_kt, self.n_ct, self.T = stages, n_kt, n_ct, n_tiles
+        self.protocol, self.early, self.scale_r = protocol, early, scale_r and n_ct > 0
+        ring = lambda name, count, cls=Barrier, n=stages: [cls(f"{name}[{i}]", count) for i in range(n)]
+        self.full = ring("full", 1, SignedTxBarrier)
+        self.sf_full = ring("sf_full", 1)
+        self.comp_ready = ring("comp_ready", 16)
+        self.sfl_full = ring("sfl_full", 1, SignedTxBarrier, self.SF_STAGES)
+        self.acc_empty = Barrier("acc_empty", 16)
+        self.empty = [ring(f"empty.{c}", 1) for c in range(2)]
+        self.ct_landed = [ring(f"ct_landed.{c}", 1) for c in range(2)]
+        self.sfl_empty = [ring(f"sfl_empty.{c}", 1, Barrier, self.SF_STAGES) for c in range(2)]
+        self.acc_full = [Barrier(f"acc_full.{c}", 1) for c in range(2)]
+        self.content = [[None] * stages for _ in range(2)]
+        self.sf_content = [[None] * self.SF_STAGES for _ in range(2)]
+        self.sf_copied = [None] * self.SF_STAGES   # k-tile whose scales the copies finished reading
+        self.tmem_sf = [None] * stages             # use whose scales are in the stage's TMEM slot
+        self.mma_done = [None] * stages            # last use of the stage whose MMAs completed
+        self.scaled = [[set() for _ in range(stages)] for _ in range(2)]
+        self.acc = [None, None]
+        self.events, self.now, self.seq, self.last_async = [], 0.0, 0, {}
+        self.finished = 0
+
+    def fp4_index(self, u):
+        """FP4 k-tile counter of use u (compensation uses carry none)."""
+        t, j = divmod(u, self.n_kt + self.n_ct)
+        return t * self.n_kt + j if j < self.n_kt else None
+
+    def tma_cta(self, c):
+        leader = c == 0
+        pre = min(self.S, self.n_kt) if (self.early and self.T) else 0
+        halves = [dict() for _ in range(self.S)]
+
+        def land(st, u, half):
+            halves[st][half] = u
+            if halves[st].get("a") == u and halves[st].get("b") == u:
+                self.content[c][st] = u
+                self.scaled[c][st] = set()
+            self.full[st].complete_tx(1)
+        for i in range(pre):
+            if leader:
+                self.full[i].expect_tx(4)
+            self.later(lambda i=i: land(i, i, "b"), f"tma{c}", 5, 60)
+        yield lambda: True  # griddepcontrol.wait
+        n_uses = 0
+        for _, _, u in self.uses():
+            st, ph = self.slot(u)
+            if u >= pre:
+                yield lambda: self.empty[c][st].passed(ph ^ 1)
+                if leader:
+                    self.full[st].expect_tx(4)
+                self.later(lambda st=st, u=u: land(st, u, "b"), f"tma{c}", 5, 60)
+            self.later(lambda st=st, u=u: land(st, u, "a"), f"tma{c}", 5, 60)
+            n_uses += 1
+        if self.protocol != "no_wind_down":
+            for i in range(self.S):
+                if n_uses > i:
+                    last = (n_uses - 1 - i) // self.S
+                    yield lambda i=i, last=last: self.empty[c][i].passed(last & 1)
+        self.finished += 1
+
+    def sf_producer(self, c):
+        leader = c == 0
+        R = self.SF_STAGES
+        n = self.T * self.n_kt
+
+        def land(sl, g):
+            assert self.sf_copied[sl] == (g - R if g >= R else None), ("scale stage overwritten", sl, g)
+            self.sf_content[c][sl] = g
+            self.sfl_full[sl].complete_tx(1)
+        yield lambda: True  # griddepcontrol.wait
+        for g in range(n):
+            sl, ph = g % R, (g // R) & 1
+            yield lambda sl=sl, ph=ph: self.sfl_empty[c][sl].passed(ph ^ 1)
+            if leader:
+                self.sfl_full[sl].expect_tx(2)
+            self.later(lambda sl=sl, g=g: land(sl, g), f"sftma{c}", 5, 40)
+        if self.protocol != "no_wind_down":
+            for i in range(R):
+                if n > i:
+                    last = (n - 1 - i) // R
+                    yield lambda i=i, last=last: self.sfl_empty[c][i].passed(last & 1)
+        self.finished += 1
+
+    def copy_warp(self):
+        R = self.SF_STAGES
+        for _, j, u in self.uses():
+            st, ph = self.slot(u)
+            if self.protocol != "copier_skips_slot_wait":
+                yield lambda: self.empty[0][st].passed(ph ^ 1)
+            if j < self.n_kt:
+                g = self.fp4_index(u)
+                sl, sph = g % R, (g // R) & 1
+                yield lambda sl=sl, sph=sph: self.sfl_full[sl].passed(sph)
+                assert self.sf_content[0][sl] == g and self.sf_content[1][sl] == g, ("copy warp scales", g)
+                assert self.mma_done[st] == (u - self.S if u >= self.S else None), ("TMEM scale slot in use", u)
+                if self.scale_r:
+                    self.comp_ready[st].arrive(16)
+
+                def copied(st=st, u=u, sl=sl, g=g):
+                    # the commits arrive once the copies are done: on the
+                    # leader's barriers, and (remote, unordered) on the peer's
+                    self.tmem_sf[st] = u
+                    self.sf_copied[sl] = g
+                    self.sf_full[st].arrive()
+                    self.sfl_empty[0][sl].arrive()
+                    self.later(lambda: self.sfl_empty[1][sl].arrive(), "w3peer", 0, 40)
+                self.later(copied, "w3", 2, 20)
+            else:
+                if self.scale_r:
+                    yield lambda: self.full[st].passed(ph)
+                    assert self.content[0][st] == u and self.content[1][st] == u, ("relay", u)
+                    self.ct_landed[0][st].arrive()
+                    self.later(self.ct_landed[1][st].arrive, "w3remote", 1, 15)
+                self.sf_full[st].arrive()
+        self.finished += 1
+
+    def mma(self):
+        acc_ph = 0
+        walk = self.uses()
+        for t in range(self.T):
+            yield lambda: self.acc_empty.passed(acc_ph ^ 1)
+            acc_ph ^= 1
+            for c in range(2):
+                assert self.acc[c] is None or self.acc[c][1] == "read", ("accumulator unread", c, t)
+                self.acc[c] = (t, "writing")
+            for j in range(self.n_kt + self.n_ct):
+                _, _, u = next(walk)
+                st, ph = self.slot(u)
+                if j < self.n_kt:
+                    yield lambda: self.full[st].passed(ph) and self.sf_full[st].passed(ph)
+                    assert self.tmem_sf[st] == u, ("MMA scales", u)
+                elif self.scale_r:
+                    yield lambda: self.sf_full[st].passed(ph) and self.comp_ready[st].passed(ph)
+                    assert all(len(self.scaled[c][st]) == 8 for c in range(2)), ("MMA on unscaled residual", u)
+                else:
+                    yield lambda: self.sf_full[st].passed(ph) and self.full[st].passed(ph)
+                assert self.content[0][st] == u and self.content[1][st] == u, ("MMA operands", u)
+
+                def consumed(st, c, u):
+                    if c == 0:
+                        self.mma_done[st] = u
+                    self.content[c][st] = "consumed"
+                    self.empty[c][st].arrive()
+                self.later(lambda st=st, u=u: consumed(st, 0, u), "mma", 5, 40)
+                self.later(lambda st=st, u=u: consumed(st, 1, u), "mma_peer", 5, 60)
+
+            def done(c, t=t):
+                self.acc[c] = (t, "complete")
+                self.acc_full[c].arrive()
+            self.later(lambda: done(0), "mma", 5, 40)
+            self.later(lambda: done(1), "mma_peer", 5, 60)
+        if self.T and self.protocol != "no_wind_down":
+            yield lambda: self.acc_empty.passed(acc_ph ^ 1)
+        self.finished += 1
+
+    def epilogue_warp_cta(self, c, w):
+        acc_ph, stage, ct_phase, u0 = 0, 0, 0, 0
+        for t in range(self.T):
+            if self.scale_r:
+                stage = (stage + self.n_kt) % self.S
+                for ct in range(self.n_ct):
+                    u, st = u0 + self.n_kt + ct, stage
+                    par = (ct_phase >> st) & 1
+                    yield lambda st=st, par=par: self.ct_landed[c][st].passed(par)
+                    ct_phase ^= 1 << st
+                    assert self.content[c][st] == u, ("epilogue", c, w, "saw", self.content[c][st], "for", u)
+                    self.scaled[c][st].add(w)
+                    if c == 0:
+                        self.comp_ready[st].arrive()
+                    else:
+                        self.later(lambda st=st: self.comp_ready[st].arrive(), f"e{c}{w}", 1, 15)
+                    stage = (stage + 1) % self.S
+            u0 += self.n_kt + self.n_ct
+            yield lambda: self.acc_full[c].passed(acc_ph)
+            acc_ph ^= 1
+            assert self.acc[c] == (t, "complete"), ("epilogue read", self.acc[c], "for tile", t)
+            self.epi_read = getattr(self, "epi_read", {})
+            self.epi_read[(c, t, w)] = True
+            if all(self.epi_read.get((c, t, x)) for x in range(8)):
+                self.acc[c] = (t, "read")
+            if c == 0:
+                self.acc_empty.arrive()
+            else:
+                self.later(self.acc_empty.arrive, f"e{c}{w}", 1, 120)
+            stored = [False]
+            self.later(lambda stored=stored: stored.__setitem__(0, True), f"st{c}{w}", 0, 80)
+            yield lambda stored=stored: stored[0]
+        self.finished += 1
+
+    def roles(self):
+        return ([self.tma_cta(0), self.tma_cta(1), self.sf_producer(0), self.sf_producer(1), self.copy_warp(),
+                 self.mma()] + [self.epilogue_warp_cta(c, w) for c in range(2) for w in range(8)])
+
+    def check_quiet_at_exit(self):
+        """Called when every role has finished: nothing may still land."""
+        assert not self.events, ("in flight at exit", len(self.events))
+
+
+def _pair_failures(protocol, n, early=False, scale_r=True):
+    bad = 0
+    for seed in range(n):
+        n_tiles, n_kt, n_ct = _shapes(seed)
+        m = PairGemmModel(seed, n_tiles, n_kt, n_ct, protocol, early=early, scale_r=scale_r)
+        try:
+            m.run_to_exit()
+        except AssertionError:
+            bad += 1
+    return bad
+
+
+def _run_to_exit(self):
+    """run(), but stop as soon as every role has finished and check that no
+    asynchronous copy or arrival is still pending at that moment."""
+    roles = self.roles()
+    n = len(roles)
+    waiting = {g: next(g) for g in roles}
+    while True:
+        if self.finished == n and not waiting:
+            self.check_quiet_at_exit()
+            return
+        ready = [g for g, pred in waiting.items() if pred()]
+        if ready and (not self.events or self.r.random() < 0.7):
+            g = self.r.choice(ready)
+            try:
+                waiting[g] = g.send(None)
+            except StopIteration:
+                del waiting[g]
+            self.now += self.r.uniform(0, 2)
+        elif self.events:
+            self.events.sort()
+            t, _, fn = self.events.pop(0)
+            self.now = max(self.now, t)
+            fn()
+        else:
+            raise AssertionError(f"deadlock with {len(waiting)} roles waiting")
+
+
+PairGemmModel.run_to_exit = _run_to_exit
+
+
+@pytest.mark.parametrize("early", [False, True])
+@pytest.mark.parametrize("scale_r", [False, True])
+def test_pair_kernel_protocol_holds_under_random_schedules(early, scale_r):
+    assert _pair_failures("kernel", 400, early, scale_r) == 0
+
+
+def test_pair_model_rejects_a_missing_wind_down():
+    # without the producers' and the MMA warp's final waits, commits and
+    # remote arrivals can still be in flight when the CTAs pass the final
+    # cluster barrier
+    assert _pair_failures("no_wind_down", 400) > 0
+
+
+def test_pair_model_rejects_copies_into_a_busy_scale_slot():
+    # the copy warp must wait for the MMAs of the stage's previous use before
+    # it overwrites that stage's TMEM scale slot
+    assert _pair_failures("copier_skips_slot_wait", 400) > 0

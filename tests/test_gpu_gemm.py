@@ -20,12 +20,15 @@ def nv():
     return binding
 
 
-def _dense_case(nv, x, wt, chan, flags=0):
+def _dense_case(nv, x, wt, chan, flags=0, resid_scaled=False):
     """Run quantize(X) + quantize(W^T) + comp weights + GEMM on the GPU and
-    the oracle on the same inputs; returns (y_gpu fp64, y_ref fp64)."""
+    the oracle on the same inputs; returns (y_gpu fp64, y_ref fp64).
+    resid_scaled: the quantizer emits the residual divided by g_x and the GEMM
+    consumes it as such (the reference keeps the plain bf16 residual: the two
+    differ by one bf16 rounding of the compensation operand)."""
     N = wt.shape[0]
     ch = torch.as_tensor(np.asarray(chan), dtype=torch.int32).cuda() if len(chan) else None
-    qx = nv.nvfp4_quantize(x.cuda(), chan=ch)
+    qx = nv.nvfp4_quantize(x.cuda(), chan=ch, resid_scaled=resid_scaled)
     qw = nv.nvfp4_quantize(wt.cuda())
     ws = None
     if len(chan):
@@ -56,20 +59,24 @@ def test_tiny_workload(nv):
                                      (1, 128, 64, 8), (513, 128, 2048, 128), (16, 640, 4096, 64),
                                      # up to 64 tokens the operands are swapped (MMA N = M rounded up to 16)
                                      (40, 256, 1024, 16), (5, 384, 512, 24), (64, 128, 768, 0), (17, 1024, 2048, 64)])
-def test_shapes(nv, M, N, K, k):
+@pytest.mark.parametrize("resid_scaled", [False, True])
+def test_shapes(nv, M, N, K, k, resid_scaled):
     x = W.activations(M, K, max(1, K // 100), "t3x20", K + 1, M + 2)
     wt = W.weights_t(N, K, N + K)
     rng = np.random.default_rng(M + N + K)
     chan = np.sort(rng.choice(K, size=k, replace=False))
-    y, y_ref = _dense_case(nv, x, wt, chan)
+    y, y_ref = _dense_case(nv, x, wt, chan, resid_scaled=resid_scaled)
     _assert_close(y, y_ref)
 
 
-def test_bf16_weight_flag(nv):
-    x = W.activations(200, 512, 5, "t3x20", 9, 9)
+@pytest.mark.parametrize("M", [200, 700])
+@pytest.mark.parametrize("resid_scaled", [False, True])
+def test_bf16_weight_flag(nv, M, resid_scaled):
+    # 700 rows: the 256 x 256 pair-tile kernel; 200: the 128-row kernel
+    x = W.activations(M, 512, 5, "t3x20", 9, 9)
     wt = W.weights_t(256, 512, 10)
     chan = np.arange(0, 512, 8)
-    y, y_ref = _dense_case(nv, x, wt, chan, flags=1)
+    y, y_ref = _dense_case(nv, x, wt, chan, flags=1, resid_scaled=resid_scaled)
     _assert_close(y, y_ref)
 
 
@@ -105,7 +112,8 @@ def test_mxfp4_gemm(nv, M, N, K):
     _assert_close(f32(y), y_ref)
 
 
-def test_grouped_gemm_small(nv):
+@pytest.mark.parametrize("resid_scaled", [False, True])
+def test_grouped_gemm_small(nv, resid_scaled):
     # 6 experts with ragged (and one empty) row counts
     counts = [0, 5, 130, 1, 256, 77]
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -117,7 +125,7 @@ def test_grouped_gemm_small(nv):
     chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
     offs_t = torch.from_numpy(offs).cuda()
     chan_t = torch.from_numpy(chan).cuda()
-    qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t)
+    qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t, resid_scaled=resid_scaled)
     # per-expert weight quantization (each expert its own tensor scale)
     codes, scales, gs = [], [], []
     for e in range(E):

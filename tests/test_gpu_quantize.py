@@ -23,11 +23,11 @@ def nv():
     return binding
 
 
-def _check_nvfp4(nv, x_cpu, chan=None, g=None):
+def _check_nvfp4(nv, x_cpu, chan=None, g=None, resid_scaled=False):
     x = x_cpu.cuda()
     ch = None if chan is None else torch.as_tensor(chan, dtype=torch.int32).cuda()
     gt = None if g is None else torch.tensor([g], dtype=torch.float32).cuda()
-    q = nv.nvfp4_quantize(x, g=gt, chan=ch)
+    q = nv.nvfp4_quantize(x, g=gt, chan=ch, resid_scaled=resid_scaled)
     torch.cuda.synchronize()
     ref = onv.quantize(f32(x_cpu), g=g, chan=chan)
     M, K = x_cpu.shape
@@ -36,7 +36,7 @@ def _check_nvfp4(nv, x_cpu, chan=None, g=None):
     sc = gather_scales(q["scales"], onv.scale_tile_offsets(M, K // 16))
     assert np.array_equal(sc, ref["sigma"]), "scale bytes differ"
     if chan is not None and len(chan):
-        want = F.bf16_bits(ref["resid_f32"][:, np.asarray(chan)])
+        want = F.bf16_bits(ref["resid_scaled"] if resid_scaled else ref["resid_f32"][:, np.asarray(chan)])
         assert np.array_equal(bf16_bits_of(q["resid"]), want), "residual differs"
     return q, ref
 
@@ -67,6 +67,17 @@ def test_ragged_shapes(nv, M, K, k):
     rng = np.random.default_rng(M * 31 + K)
     chan = np.sort(rng.choice(K, size=k, replace=False))
     _check_nvfp4(nv, x, chan=chan)
+
+
+@pytest.mark.parametrize("M,K,k,g", [(130, 80, 7, None), (257, 1040, 33, None), (517, 2064, 64, None),
+                                     (16, 4096, 64, None), (64, 4096, 128, 0.0123), (300, 512, 32, 2.0 ** -7)])
+def test_prescaled_residual(nv, M, K, k, g):
+    # the residual divided by the tensor scale, bit-exact with the oracle's
+    # bf16(fp32(x - deq) * fp32(1/g)); codes and scales unchanged
+    x = W.activations(M, K, max(1, K // 100), "t3x20", M + 3 * K, M + 5)
+    rng = np.random.default_rng(M * 3 + K)
+    chan = np.sort(rng.choice(K, size=k, replace=False))
+    _check_nvfp4(nv, x, chan=chan, g=g, resid_scaled=True)
 
 
 def test_static_scale_and_g_out(nv):
@@ -187,6 +198,23 @@ def test_grouped_quantize_channel_lists_without_prefix_tables(nv):
     sc = gather_scales(q["scales"], onv.grouped_scale_tile_offsets(offs, K // 16))
     assert np.array_equal(sc, ref["sigma"])
     assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(ref["resid"]))
+
+
+def test_grouped_quantize_prescaled_residual(nv):
+    rng = np.random.default_rng(23)
+    E, K, k = 9, 1024, 24
+    sizes = rng.integers(0, 150, E)
+    sizes[2] = 0
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = W.activations(int(offs[-1]), K, 10, "t3x20", 17, 18)
+    chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
+    q = nv.nvfp4_quantize_grouped(x.cuda(), torch.from_numpy(offs).cuda(), torch.from_numpy(chan).cuda(),
+                                  resid_scaled=True)
+    torch.cuda.synchronize()
+    ref = onv.quantize_grouped(f32(x), offs, chan)
+    assert f32(q["g"])[0] == ref["g"]
+    assert np.array_equal(u8(q["codes"]), ref["packed"])
+    assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(ref["resid_scaled"]))
 
 
 def test_grouped_quantize(nv):
