@@ -300,19 +300,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* d
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_caddr), "r"(x), "r"(y)
       : "memory");
 }
-// 2D tiled tensor store shared -> global (bulk-group completion).  Rows and
-// columns outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* desc, const void* src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(desc)),
-               "r"(smem_u32(src)), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// The shared-memory sources of this thread's committed bulk stores have been read.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// This thread's committed bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Generic-proxy shared-memory writes of this thread become visible to later
 // async-proxy (TMA, tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
