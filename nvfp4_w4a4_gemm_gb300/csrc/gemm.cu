@@ -149,6 +149,25 @@ __device__ __forceinline__ bool tile_of(const GemmParams& p, const SchedSmem& s,
   return true;
 }
 
+// Abort wind-down of a producer warp: the bulk copies it issued land in this
+// CTA's shared memory on their own time, so before the CTA frees TMEM and
+// exits, wait (bounded, 1 ms per stage) for the last armed phase of every
+// stage.  `armed` counts the stage uses armed so far, in ring order from
+// stage 0; every armed use had all its copies issued (an abort happens only
+// at a wait before arming), so each such phase completes.  Phases complete in
+// order, and none of this producer's later phases exist, so a parity test
+// of the last armed phase is unambiguous.
+__device__ __forceinline__ void land_armed_copies(uint64_t* full, int stages, int armed) {
+  for (int i = 0; i < stages && i < armed; ++i) {
+    const int last = (armed - 1 - i) / stages;  // last armed use of stage i, counted per stage
+    const uint32_t parity = (uint32_t)(last & 1);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&full[i], parity)) {
+      if (globaltimer() - t0 > 1000000ull) break;
+    }
+  }
+}
+
 // Grouped schedules: the routing offsets (already in shared memory, not yet
 // synchronized) must partition the M rows -- off[0] = 0, non-decreasing,
 // off[E] = M -- or the tiles would read and write rows outside A, R and Y.
@@ -342,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
     }
     if (p.early_w) pdl_wait();
     int issued = 0;  // FP4 k-tiles this CTA has issued
+    int armed = 0;   // stage uses armed (arrive.expect_tx) and issued in full
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -358,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           if (!early) issue_b(stage, tl, kt);
         }
         __syncwarp();
+        ++armed;
         if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
       for (int ct = 0; ct < n_ct_u && ok; ++ct) {
@@ -371,18 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
         }
         __syncwarp();
+        ++armed;
         if (++stage == kSt) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok) {
-      // wind down: let copies already issued land before the CTA exits
-      for (int i = 0; i < kSt; ++i) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&full[i], 0) && !mbar_try_wait(&full[i], 1)) {
-          if (globaltimer() - t0 > 1000000ull) break;
-        }
-      }
-    }
+    if (!ok) land_armed_copies(full, kSt, armed);
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA ----
     int stage = 0;
@@ -825,6 +839,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     }
     if (p.early_w) pdl_wait();
     int issued = 0;  // FP4 k-tiles this CTA has issued
+    int armed = 0;   // stage uses armed (arrive.expect_tx) and issued in full
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -840,6 +855,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           if (!early) issue_b(stage, tl, kt);
         }
         __syncwarp();
+        ++armed;
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
       for (int ct = 0; ct < n_ct && ok; ++ct) {
@@ -853,14 +869,11 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
         }
         __syncwarp();
+        ++armed;
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok) {
-      const uint64_t t0 = globaltimer();
-      while (globaltimer() - t0 < 2000000ull) {
-      }
-    }
+    if (!ok) land_armed_copies(full, kWStages, armed);
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA ----
     int stage = 0;

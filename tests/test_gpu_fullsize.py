@@ -9,9 +9,9 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import gemm as og, mxfp4 as omx, nvfp4 as onv
+from oracle import formats as F, gemm as og, mxfp4 as omx, nvfp4 as onv
 from nvfp4_w4a4_gemm_gb300 import workloads as W
-from tests.helpers import f32, gather_scales, gemm_within_tol, u8
+from tests.helpers import bf16_bits_of, f32, gather_scales, gemm_within_tol, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -87,11 +87,14 @@ def test_moe_full_size(nv, which):
     wt = d["wt_gate_up"] if which == "gate_up" else d["wt_down"]
     E, N, K = wt.shape
     offs = d["offsets"].numpy().astype(np.int32)
-    rng = np.random.default_rng(3)
-    chan = np.stack([np.sort(rng.choice(K, s.k, replace=False)) for _ in range(E)]).astype(np.int32)
+    # per-expert channel sets calibrated on the calibration batch (residual
+    # variance over the rows routed to each expert), as the bench uses them
+    dc = W.moe_inputs(calibration=True, with_weights=False, which=(which,))
+    xc = dc["x_gate_up"] if which == "gate_up" else dc["x_down"]
+    chan_t = nv.nvfp4_calibrate_channels(xc.cuda(), s.k, offsets=dc["offsets"].cuda())
+    chan = chan_t.cpu().numpy().astype(np.int32)
     offs_t = torch.from_numpy(offs).cuda()
-    chan_t = torch.from_numpy(chan).cuda()
-    qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t)
+    qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t, resid_scaled=True)
     codes, scales, gs = [], [], []
     for e in range(E):
         q = nv.nvfp4_quantize(wt[e].cuda())
@@ -120,6 +123,9 @@ def test_moe_full_size(nv, which):
         a = onv.dequantize(rq["codes"], rq["sigma"], g_x)
         b = onv.dequantize(wq["codes"], wq["sigma"], wq["g"])
         ws = og.comp_weight_rows(wq, chan[e])
+        # the GEMM consumed the pre-scaled residual: bit-exact against the
+        # oracle's, and the output within tolerance of the plain-residual product
+        assert np.array_equal(bf16_bits_of(qx["resid"][lo:hi]), F.bf16_bits(rq["resid_scaled"]))
         _assert_close(yg[rows], og.reference(a, b, rq["resid"], ws), f"moe {which} expert {e}")
 
 

@@ -349,3 +349,47 @@ def test_calibration_selects_like_oracle(nv):
             diff = set(got.tolist()) ^ set(want.tolist())
             kth = np.sort(var)[::-1][k - 1]
             assert all(abs(var[j] - kth) <= 1e-9 * kth for j in diff)
+
+
+def _same_up_to_near_ties(got, want, var, k):
+    """The selected sets agree except for channels whose variance ties the
+    k-th largest within fp64 summation-order noise."""
+    if np.array_equal(np.sort(got), want):
+        return True
+    diff = set(np.asarray(got).tolist()) ^ set(np.asarray(want).tolist())
+    kth = np.sort(var)[::-1][k - 1]
+    return all(abs(var[j] - kth) <= 1e-9 * kth for j in diff)
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_grouped_calibration_selects_like_oracle(nv, which):
+    # per-expert channel sets of the MoE calibration batch: residual variance
+    # over each expert's routed rows (experts with < 2 rows use all rows)
+    s = W.SPECS["moe"]
+    d = W.moe_inputs(calibration=True, with_weights=False, which=(which,))
+    x = d["x_gate_up"] if which == "gate_up" else d["x_down"]
+    offs = d["offsets"].numpy().astype(np.int64)
+    got = nv.nvfp4_calibrate_channels(x.cuda(), s.k, offsets=d["offsets"].cuda()).cpu().numpy()
+    want = calib.calibrate_grouped(f32(x), offs, s.k)
+    rf = onv.quantize(f32(x))["resid_f32"]
+    var_all = calib.channel_variance(rf)
+    for e in range(s.experts):
+        lo, hi = offs[e], offs[e + 1]
+        var = calib.channel_variance(rf[lo:hi]) if hi - lo >= 2 else var_all
+        assert np.all(np.diff(got[e]) > 0), f"expert {e}: set not sorted / unique"
+        assert _same_up_to_near_ties(got[e], want[e], var, s.k), f"expert {e}"
+
+
+def test_grouped_calibration_small_experts_use_all_rows(nv):
+    # experts with 0 and 1 calibration rows take the all-row statistics
+    x = W.activations(40, 256, 3, "t3x20", 51, 52)
+    offs = np.array([0, 0, 1, 20, 40], np.int32)
+    k = 16
+    got = nv.nvfp4_calibrate_channels(x.cuda(), k, offsets=torch.from_numpy(offs).cuda()).cpu().numpy()
+    want = calib.calibrate_grouped(f32(x), offs, k)
+    rf = onv.quantize(f32(x))["resid_f32"]
+    var_all = calib.channel_variance(rf)
+    assert _same_up_to_near_ties(got[0], want[0], var_all, k)
+    assert _same_up_to_near_ties(got[1], want[1], var_all, k)
+    assert np.array_equal(np.sort(got[0]), np.sort(got[1]))
+
