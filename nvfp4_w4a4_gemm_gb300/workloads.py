@@ -122,14 +122,18 @@ def weights_t(N, K, seed, experts=None):
     return w
 
 
-def route(tokens, experts, top, seed):
+def route(tokens, experts, top, seed, with_weights=False):
     """Top-``top`` routing of softmax(N(0,1) logits); routed (token, expert)
     pairs sorted by (expert, token).  Returns (token_of_row int64 [T*top],
-    offsets int32 [E+1])."""
+    offsets int32 [E+1]); with_weights also returns the routing weight of every
+    sorted row (the token's top-``top`` softmax probabilities renormalized to
+    sum to 1, fp32; the router's output, an input of the combine) and the
+    logits."""
     g = _gen(seed)
     logits = torch.randn(tokens, experts, generator=g)
     p = torch.softmax(logits, dim=1)
-    order = torch.sort(p, dim=1, descending=True, stable=True).indices[:, :top]
+    srt = torch.sort(p, dim=1, descending=True, stable=True)
+    order = srt.indices[:, :top]
     tok = torch.arange(tokens).repeat_interleave(top)
     exp = order.reshape(-1)
     key = exp * tokens + tok
@@ -138,7 +142,11 @@ def route(tokens, experts, top, seed):
     counts = torch.bincount(exp, minlength=experts)
     offsets = torch.zeros(experts + 1, dtype=torch.int32)
     offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
-    return tok_sorted, offsets
+    if not with_weights:
+        return tok_sorted, offsets
+    w = srt.values[:, :top]
+    w = (w / w.sum(dim=1, keepdim=True)).reshape(-1)[perm].to(torch.float32)
+    return tok_sorted, offsets, w, logits
 
 
 def dense_inputs(name, calibration=False, with_weights=True):
@@ -153,12 +161,13 @@ def dense_inputs(name, calibration=False, with_weights=True):
 
 def moe_inputs(calibration=False, with_weights=True, which=("gate_up", "down")):
     """MoE workload inputs (CPU).  Keys: x_gate_up [T*top, hidden] (sorted
-    rows), x_down [T*top, inter], offsets, token_of_row, and the weights
+    rows), x_down [T*top, inter], offsets, token_of_row, route_weight (per
+    sorted row), and the weights
     wt_gate_up [E, 2*inter, hidden], wt_down [E, hidden, inter]."""
     s = SPECS["moe"]
     vs = s.seed + (1000 if calibration else 0)
-    tok, offsets = route(s.tokens, s.experts, s.top, vs + 7)
-    out = dict(spec=s, offsets=offsets, token_of_row=tok)
+    tok, offsets, w_rows, _ = route(s.tokens, s.experts, s.top, vs + 7, with_weights=True)
+    out = dict(spec=s, offsets=offsets, token_of_row=tok, route_weight=w_rows)
     if "gate_up" in which:
         xt = activations(s.tokens, s.hidden, _n_outliers(s.hidden), "t3x20", s.seed, vs)
         out["x_gate_up"] = xt[tok].contiguous()
