@@ -352,7 +352,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": s.M * s.K * 2, "d2h_bytes_per_step": s.M * s.N * 2,
                 "ms_per_step": round(ms_e2e, 4),
                 "pipelining": "X copy-in, the step's kernels and Y copy-out on three streams, two buffers each"},
-        "gpu_launches": 2 * args.steps,  # per step: nvfp4_quant_kernel (cooperative) + w4a4_gemm_wide_kernel
+        "gpu_launches": 2 * args.steps,  # per step: nvfp4_quant_kernel (cooperative) + w4a4_gemm_pair_kernel
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -523,6 +523,7 @@ def other_workloads(nv, pk, steps=10):
                   "note": "each projection: grouped dynamic-scale quantize + grouped GEMM with compensation; "
                           "channel sets calibrated per expert (residual variance on the calibration batch's "
                           "rows routed to that expert)"}
+    out["moe"]["fused_layer"] = moe_fused_layer(nv, pk, flush, steps)
     del dm
 
     # MXFP4: X[8192,5120] x W[5120,5120], 32-blocks, decomposition statistics
@@ -579,6 +580,65 @@ def other_workloads(nv, pk, steps=10):
                   "note": "bytes = W read once + QDQ written + codes + scales; one cooperative launch whose amax "
                           "phase reads W a second time (not counted)"}
     return out
+
+
+def moe_fused_layer(nv, pk, flush, steps):
+    """The whole MoE FFN on the routed rows with both fused epilogues:
+    grouped dynamic-scale quantize of x, gate/up GEMM with SwiGLU and the down
+    input's static-scale NVFP4 quantize in its epilogue, down GEMM with the
+    routing-weighted combine into fp32 token rows (zeroed first)."""
+    dev = torch.device("cuda")
+    s = W.SPECS["moe"]
+    d = W.moe_inputs()
+    dc = W.moe_inputs(calibration=True, with_weights=False)
+    E, inter, hidden = s.experts, s.inter, s.hidden
+    offs = d["offsets"].to(dev)
+    x = d["x_gate_up"].to(dev)
+    chan = nv.nvfp4_calibrate_channels(dc["x_gate_up"].to(dev), s.k, offsets=dc["offsets"].to(dev))
+    h_chan = nv.nvfp4_calibrate_channels(dc["x_down"].to(dev), s.k, offsets=dc["offsets"].to(dev))
+
+    def experts(wt):
+        qs = [nv.nvfp4_quantize(wt[e].to(dev)) for e in range(E)]
+        return torch.stack([q["codes"] for q in qs]), torch.cat([q["scales"] for q in qs]), torch.cat([q["g"] for q in qs])
+    gu_codes, gu_scales, gu_g = experts(nv.interleave_gate_up_rows(d["wt_gate_up"]))
+    gu_sel = nv.nvfp4_prepare_comp_weights(gu_codes, gu_scales, chan, E=E)
+    dn_codes, dn_scales, dn_g = experts(d["wt_down"])
+    dn_sel = nv.nvfp4_prepare_comp_weights(dn_codes, dn_scales, h_chan, E=E)
+    # static scale of h: the dynamic scale of the calibration batch's h
+    qc = nv.nvfp4_quantize_grouped(dc["x_gate_up"].to(dev), dc["offsets"].to(dev), chan, resid_scaled=True)
+    hc = nv.w4a4_grouped_gemm_swiglu_quant(qc, dc["offsets"].to(dev), gu_codes, gu_scales, gu_g, 2 * inter,
+                                           torch.ones(1, device=dev), h_chan, resid=qc["resid"], w_sel=gu_sel,
+                                           with_h=True)["h"]
+    g_h = nv.nvfp4_quantize(hc)["g"]
+    del qc, hc
+    tok = d["token_of_row"].to(torch.int32).to(dev)
+    w_row = d["route_weight"].to(dev)
+    out = torch.empty((s.tokens, hidden), dtype=torch.float32, device=dev)
+
+    def layer():
+        qx = nv.nvfp4_quantize_grouped(x, offs, chan, resid_scaled=True)
+        qh = nv.w4a4_grouped_gemm_swiglu_quant(qx, offs, gu_codes, gu_scales, gu_g, 2 * inter, g_h, h_chan,
+                                               resid=qx["resid"], w_sel=gu_sel, h_resid_scaled=True,
+                                               weights_ready=True)
+        out.zero_()
+        nv.w4a4_grouped_gemm_combine(qh, offs, dn_codes, dn_scales, dn_g, hidden, tok, w_row, s.tokens,
+                                     resid=qh["resid"], w_sel=dn_sel, out=out, weights_ready=True)
+    ms = _time_steps(layer, steps, flush)
+    rows = x.shape[0]
+    flops = 2.0 * rows * (2 * inter) * hidden + 2.0 * rows * hidden * inter
+    byts = (gu_codes.numel() + gu_scales.numel() + gu_sel.numel() * 2 + dn_codes.numel() + dn_scales.numel()
+            + dn_sel.numel() * 2 + x.numel() * 2 + out.numel() * 4)
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    att = min(fp4_peak, flops / byts * pk["hbm_gbs"] / 1e3)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"ms_per_step": round(ms, 4), "tflops": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4),
+            "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "bytes_per_step": byts,
+            "attainable_tflops": round(att, 1), "frac_attainable": round(tf / att, 4),
+            "note": "one step = the whole FFN on 32768 routed rows: grouped dynamic-scale quantize of x; gate/up "
+                    "GEMM with SwiGLU + static-scale NVFP4 quantize of h (with its residual slice) in the "
+                    "epilogue; zeroing of the fp32 output; down GEMM with the routing-weighted combine into "
+                    "token rows in the epilogue (fp32 vector atomics). Bytes = weights + compensation columns + x "
+                    "read + fp32 output; the gate/up output and h never reach memory as bf16"}
 
 
 # ------------------------------------------------------ the oracle arm ----

@@ -348,6 +348,62 @@ int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M
                            const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * w4a4_grouped_gemm_swiglu_quant -- the MoE gate/up projection with the gated
+ * activation and the down projection's NVFP4 quantization fused into its
+ * epilogue: the bf16 gate/up output never goes to memory.
+ * Source: QUADS abstract (MoE rollout on native W4A4 GEMMs) and the
+ * gist.science explainer of QUADS section 4 (the MoE model); the pages do not
+ * define the gated activation, so this library's reading is SwiGLU:
+ *   y = the grouped GEMM's bf16 output (as w4a4_grouped_gemm_comp writes it)
+ *   h = bf16_rn(silu(y_gate) * y_up),  silu(z) = z / (1 + e^-z) in fp32
+ *       with the fast exponential and division (within a few fp32 ulps)
+ *   h is NVFP4-quantized with the STATIC tensor scale *g_h (a dynamic scale
+ *   needs the amax of all of h before any block can be coded), exactly as
+ *   nvfp4_quantize_grouped_ex with g_in = g_h and the same offsets would:
+ *   h_codes [M_total, N/4], h_scales in the grouped tiled layout of an
+ *   [M_total, N/2] operand (nvfp4_grouped_scale_bytes(M_total, N/2, E)),
+ *   h_resid [M_total, h_k] on the expert's channels h_chan[e*h_k ..]
+ *   (divided by g_h when h_flags has NVFP4_QUANT_RESID_SCALED).
+ * Weight layout: b_codes / b_scales / w_sel hold W^T with its 2I = N rows
+ * interleaved in blocks of 128: rows [256 j, 256 j + 128) are gate rows
+ * [128 j, 128 j + 128) and rows [256 j + 128, 256 j + 256) the matching up
+ * rows, so one 256-column output tile carries both halves of 128 activations.
+ * N % 256 == 0.  h_out: NULL, or [M_total, N/2] bf16 receiving h itself (a
+ * checking aid; costs the write the fusion saves).
+ * Other arguments as w4a4_grouped_gemm_comp.
+ */
+int w4a4_grouped_gemm_swiglu_quant(int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                                   const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                                   const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                                   const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags,
+                                   const float* g_h, const int32_t* h_chan, int32_t h_k, int h_flags,
+                                   uint8_t* h_codes, uint8_t* h_scales, uint16_t* h_resid, uint16_t* h_out,
+                                   void* stream);
+
+/*
+ * w4a4_grouped_gemm_combine -- the MoE down projection with the weighted
+ * combine of the experts' outputs fused into its epilogue:
+ *   out[token_of_row[r], :] += w_row[r] * (ga*gb*acc + c*accc)[r, :]   (fp32)
+ * for every expert-sorted routed row r, with the accumulator of
+ * w4a4_grouped_gemm_comp (no bf16 rounding of the per-expert output).
+ * Source: as w4a4_grouped_gemm_swiglu_quant; the combine is this library's
+ * reading (each token's output is the routing-weighted sum of its experts'
+ * outputs; the weights -- the router's renormalized top-8 softmax -- are an
+ * input).
+ * token_of_row int32 [M_total], w_row float [M_total] (device); out float
+ * [n_tokens, N] (16-byte aligned), which the caller zeroes (the kernel only
+ * adds; the order of the additions is not fixed, so the result is
+ * reproducible to fp32 rounding, not bit for bit).
+ * Other arguments as w4a4_grouped_gemm_comp.
+ */
+int w4a4_grouped_gemm_combine(int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                              const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                              const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                              const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags,
+                              const int32_t* token_of_row, const float* w_row, int64_t n_tokens, float* out,
+                              void* stream);
+
 /* Reads (and with clear != 0 resets) the device-side error latch of every
  * kernel family on the current device.  Synchronizes the device.  Returns
  * NVFP4_OK, NVFP4_ERR_TIMEOUT or NVFP4_ERR_INVALID_ARG; *detail (may be NULL)

@@ -58,6 +58,11 @@ _SIGS = {
     "w4a4_grouped_gemm_workspace_bytes": ([_I32, _I64, _I64, _I64], _SZ),
     "w4a4_grouped_gemm_comp": ([ctypes.c_int, _I32, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
                                 ctypes.c_int, _P, _P, _SZ, _P], ctypes.c_int),
+    "w4a4_grouped_gemm_swiglu_quant": ([_I32, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
+                                        ctypes.c_int, _P, _P, _I32, ctypes.c_int, _P, _P, _P, _P, _P],
+                                       ctypes.c_int),
+    "w4a4_grouped_gemm_combine": ([_I32, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32, ctypes.c_int,
+                                   _P, _P, _I64, _P, _P], ctypes.c_int),
     "nvfp4_check_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "nvfp4_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
     "nvfp4_inject_barrier_timeout": ([], None),
@@ -347,6 +352,82 @@ def w4a4_grouped_gemm_comp(qa, offsets, b_codes, b_scales, g_b, N, resid=None, w
                                     None, 0, _stream())
     _check("w4a4_grouped_gemm_comp", st)
     return y
+
+
+def w4a4_grouped_gemm_swiglu_quant(qa, offsets, b_codes, b_scales, g_b, N, g_h, h_chan, resid=None, w_sel=None,
+                                   flags=COMP_W_DEQ, h_resid_scaled=False, with_h=False, weights_ready=False):
+    """MoE gate/up projection with SwiGLU and the down input's NVFP4 quantize
+    (static scale g_h) in its epilogue.  b_codes/b_scales/w_sel hold the
+    gate/up rows interleaved in blocks of 128 (N = 2 I).  Returns the down
+    projection's quantized input dict(codes, scales, g, resid, resid_scaled)
+    and, with with_h, h itself (bf16 [M, I])."""
+    if weights_ready:
+        flags |= GEMM_WEIGHTS_READY
+    if resid is not None and qa.get("resid_scaled"):
+        flags |= GEMM_RESID_SCALED
+    lib = load()
+    a_codes = qa["codes"]
+    M, Kh = a_codes.shape
+    K = Kh * 2
+    E = offsets.numel() - 1
+    k = 0 if resid is None else resid.shape[1]
+    I = N // 2
+    _need(h_chan, torch.int32, "h_chan")
+    h_k = h_chan.shape[-1]
+    dev = a_codes.device
+    h_codes = torch.empty((M, I // 2), dtype=torch.uint8, device=dev)
+    h_scales = torch.zeros(lib.nvfp4_grouped_scale_bytes(M, I, E), dtype=torch.uint8, device=dev)
+    h_resid = torch.empty((M, h_k), dtype=torch.bfloat16, device=dev)
+    h_out = torch.empty((M, I), dtype=torch.bfloat16, device=dev) if with_h else None
+    st = lib.w4a4_grouped_gemm_swiglu_quant(E, _ptr(offsets), M, N, K, _ptr(a_codes), _ptr(qa["scales"]),
+                                            _ptr(qa.get("g")), _ptr(b_codes), _ptr(b_scales), _ptr(g_b),
+                                            _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags,
+                                            _ptr(g_h), _ptr(h_chan), h_k, QUANT_RESID_SCALED if h_resid_scaled else 0,
+                                            _ptr(h_codes), _ptr(h_scales), _ptr(h_resid), _ptr(h_out), _stream())
+    _check("w4a4_grouped_gemm_swiglu_quant", st)
+    out = dict(codes=h_codes, scales=h_scales, g=g_h, resid=h_resid, resid_scaled=bool(h_resid_scaled))
+    if with_h:
+        out["h"] = h_out
+    return out
+
+
+def w4a4_grouped_gemm_combine(qa, offsets, b_codes, b_scales, g_b, N, token_of_row, w_row, n_tokens, resid=None,
+                              w_sel=None, flags=COMP_W_DEQ, out=None, weights_ready=False):
+    """MoE down projection with the routing-weighted combine in its epilogue:
+    returns out fp32 [n_tokens, N] (zeroed here unless given; the kernel adds)."""
+    if weights_ready:
+        flags |= GEMM_WEIGHTS_READY
+    if resid is not None and qa.get("resid_scaled"):
+        flags |= GEMM_RESID_SCALED
+    lib = load()
+    a_codes = qa["codes"]
+    M, Kh = a_codes.shape
+    K = Kh * 2
+    E = offsets.numel() - 1
+    k = 0 if resid is None else resid.shape[1]
+    _need(token_of_row, torch.int32, "token_of_row")
+    _need(w_row, torch.float32, "w_row")
+    if out is None:
+        out = torch.zeros((n_tokens, N), dtype=torch.float32, device=a_codes.device)
+    st = lib.w4a4_grouped_gemm_combine(E, _ptr(offsets), M, N, K, _ptr(a_codes), _ptr(qa["scales"]),
+                                       _ptr(qa.get("g")), _ptr(b_codes), _ptr(b_scales), _ptr(g_b),
+                                       _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags,
+                                       _ptr(token_of_row), _ptr(w_row), n_tokens, _ptr(out), _stream())
+    _check("w4a4_grouped_gemm_combine", st)
+    return out
+
+
+def interleave_gate_up_rows(wt):
+    """Weight-row layout of w4a4_grouped_gemm_swiglu_quant: W^T [..., 2I, K]
+    with gate rows [0, I) and up rows [I, 2I) reordered so rows [256 j, 256 j
+    + 128) are gate rows [128 j, 128 j + 128) and the next 128 the matching up
+    rows (a one-time, offline reordering of the weights)."""
+    two_i = wt.shape[-2]
+    inter = two_i // 2
+    if inter % 128:
+        raise ValueError("the gate width must be a multiple of 128")
+    idx = torch.arange(two_i).view(2, inter // 128, 128).transpose(0, 1).reshape(-1)
+    return wt.index_select(wt.dim() - 2, idx.to(wt.device))
 
 
 def check_status(clear=True):

@@ -354,6 +354,63 @@ int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M
   return from_cuda(nv4::launch_grouped_gemm(p, d->num_sms, as_stream(stream)));
 }
 
+int w4a4_grouped_gemm_swiglu_quant(int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                                   const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                                   const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                                   const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags,
+                                   const float* g_h, const int32_t* h_chan, int32_t h_k, int h_flags,
+                                   uint8_t* h_codes, uint8_t* h_scales, uint16_t* h_resid, uint16_t* h_out,
+                                   void* stream) {
+  int st = check_gemm_common(NVFP4_FMT_NVFP4, M_total, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k,
+                             flags, reinterpret_cast<uint16_t*>(h_codes));
+  if (st != NVFP4_OK) return st;
+  if (E <= 0 || E > 65536 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
+  if (N % 256 != 0) return NVFP4_ERR_UNSUPPORTED;  // each 256-column tile: 128 gate + 128 up columns
+  if ((h_flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
+  if (h_k < 0 || h_k > N / 2) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  if (!g_h || !h_scales || !aligned(h_scales, 16) || (h_out && !aligned(h_out, 16))) return NVFP4_ERR_INVALID_ARG;
+  if (h_k > 0 && (!h_chan || !h_resid || !aligned(h_chan, 4) || !aligned(h_resid, 2))) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  nv4::GemmProblem p;
+  p.fmt = NVFP4_FMT_NVFP4; p.M = M_total; p.N = N; p.K = K;
+  p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
+  p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
+  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.flags = flags;
+  p.E = E; p.offsets = offsets;
+  p.epi = 1;
+  p.h_codes = h_codes; p.h_scales = h_scales; p.h_resid = bf(h_resid); p.h_out = bf(h_out);
+  p.h_chan = h_chan; p.h_k = h_k; p.g_h = g_h; p.h_resid_scaled = (h_flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0;
+  return from_cuda(nv4::launch_grouped_gemm(p, d->num_sms, as_stream(stream)));
+}
+
+int w4a4_grouped_gemm_combine(int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,
+                              const uint8_t* a_codes, const uint8_t* a_scales, const float* g_a,
+                              const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
+                              const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags,
+                              const int32_t* token_of_row, const float* w_row, int64_t n_tokens, float* out,
+                              void* stream) {
+  int st = check_gemm_common(NVFP4_FMT_NVFP4, M_total, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k,
+                             flags, reinterpret_cast<uint16_t*>(out));
+  if (st != NVFP4_OK) return st;
+  if (E <= 0 || E > 65536 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
+  if (n_tokens < 0) return NVFP4_ERR_INVALID_ARG;
+  if (M_total == 0) return NVFP4_OK;
+  if (!token_of_row || !w_row || !aligned(token_of_row, 4) || !aligned(w_row, 4)) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  nv4::GemmProblem p;
+  p.fmt = NVFP4_FMT_NVFP4; p.M = M_total; p.N = N; p.K = K;
+  p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
+  p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
+  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.flags = flags;
+  p.E = E; p.offsets = offsets;
+  p.epi = 2;
+  p.token_of_row = token_of_row; p.w_row = w_row; p.out_f32 = out;
+  return from_cuda(nv4::launch_grouped_gemm(p, d->num_sms, as_stream(stream)));
+}
+
 int nvfp4_check_status(int clear, uint32_t* detail) {
   if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
   uint32_t q[2] = {0, 0}, g[2] = {0, 0};

@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "nvfp4_block.cuh"
 #include "ptx.cuh"
 
 namespace nv4 {
@@ -99,7 +100,26 @@ struct GemmParams {
   int swap;         // narrow kernel, M <= 64: weight rows take the MMA's M = 128 slot, tokens its N slot
   int resid_scaled; // the residual was divided by g_a in the quantizer
   uint32_t n_mma;   // swap: MMA N = M rounded up to 16
+  // wide kernel, grouped: what the epilogue makes of the accumulator
+  int epi;                    // kEpiStore, kEpiSwigluQuant or kEpiCombine
+  // kEpiSwigluQuant: each 256-column tile holds 128 gate and the 128 matching
+  // up columns; h = bf16(silu(y_gate) * y_up) is NVFP4-quantized with the
+  // static tensor scale *g_h into the down projection's operands
+  uint8_t* h_codes;           // [M, h_cols / 2]
+  uint8_t* h_scales;          // grouped tiled layout of [M, h_cols]
+  __nv_bfloat16* h_resid;     // [M, h_k] on the expert's channels h_chan[e]
+  __nv_bfloat16* h_out;       // [M, h_cols] bf16 or nullptr (a checking aid)
+  const int32_t* h_chan;      // [E, h_k] sorted per expert
+  int h_k;
+  const float* g_h;
+  int64_t h_cols;             // N / 2
+  int h_resid_scaled;         // residual divided by g_h
+  // kEpiCombine: out[token_of_row[r]] += w_row[r] * y[r] (fp32)
+  const int32_t* token_of_row;
+  const float* w_row;
+  float* out_f32;             // [tokens, N]
 };
+constexpr int kEpiStore = 0, kEpiSwigluQuant = 1, kEpiCombine = 2;
 
 struct Tile {
   int e;          // expert (0 for dense)
@@ -705,6 +725,150 @@ __device__ __forceinline__ void tile_of_w(const GemmParams& p, const SchedSmem& 
   out.n_valid = out.n0 + 128 < p.N;  // second 128-row half of B exists
 }
 
+// silu(z) * u in fp32 with the fast exponential and division (a few fp32
+// ulps; h is rounded to bf16 right after, and the codes are those of that
+// rounded h): z / (1 + e^-z), times u.
+__device__ __forceinline__ float swiglu_f32(float z, float u) {
+  return __fmul_rn(__fdividef(z, __fadd_rn(1.0f, __expf(-z))), u);
+}
+__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// kEpiSwigluQuant epilogue of one 128 x 256 tile for the warp of TMEM lane
+// quarter q and column half hh: gate columns [64 hh, 64 hh + 64) and the
+// matching up columns 128 further; 64 activations h of row q*32+lane, i.e.
+// four 16-element NVFP4 blocks (one 4-scale group) of the down projection's
+// input.  Releases the accumulator (acc_empty) once its last columns are in
+// registers.
+__device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile& tl, int q, int hh, int lane,
+                                                 uint32_t tmem, float alpha, const float2* s_dr, float g_h, float yg_h,
+                                                 bool fast_h, float rs_h, uint64_t* acc_empty) {
+  const int r = q * 32 + lane;
+  const bool row_ok = r < tl.rows;
+  const int64_t row = tl.row0 + r;
+  const int64_t prow = tl.sf_rt * 128 + r;  // padded row of the grouped scale layout
+  const int64_t hcol0 = (int64_t)(tl.n0 / 2) + 64 * hh;
+  const int64_t n_cg_h = (p.h_cols / 16 + 3) / 4;
+  const int32_t* S = p.h_chan + (int64_t)tl.e * p.h_k;
+  // slots [s_lo, s_hi) of the expert's sorted channel list that fall in this
+  // warp's 64 columns (binary searches, the same for the whole warp)
+  int s_lo = 0, s_hi = p.h_k;
+  {
+    int lo = 0, hi = p.h_k;
+    while (lo < hi) { const int mid = (lo + hi) >> 1; if (S[mid] < hcol0) lo = mid + 1; else hi = mid; }
+    s_lo = lo;
+    hi = p.h_k;
+    while (lo < hi) { const int mid = (lo + hi) >> 1; if (S[mid] < hcol0 + 64) lo = mid + 1; else hi = mid; }
+    s_hi = lo;
+  }
+  const uint32_t t_g = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(64 * hh);
+  uint32_t scale_word = 0;
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    uint32_t vg[2][16], vu[2][16];
+    tmem_ld_32x32b_x16(t_g + (uint32_t)(32 * b), vg[0]);
+    tmem_ld_32x32b_x16(t_g + (uint32_t)(32 * b + 16), vg[1]);
+    tmem_ld_32x32b_x16(t_g + 128u + (uint32_t)(32 * b), vu[0]);
+    tmem_ld_32x32b_x16(t_g + 128u + (uint32_t)(32 * b + 16), vu[1]);
+    tmem_ld_wait();
+    if (b == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);  // accumulator free: the next tile's MMAs may start
+    }
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float hv[16];
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        // the projection's bf16 outputs, then h rounded to bf16
+        const float yg = bf16r(alpha * __uint_as_float(vg[blk][i]));
+        const float yu = bf16r(alpha * __uint_as_float(vu[blk][i]));
+        hv[i] = bf16r(swiglu_f32(yg, yu));
+        am = fmaxf(am, fabsf(hv[i]));
+      }
+      const uint32_t sig = block_scale_byte(am, g_h, yg_h, fast_h);
+      const float2 dr = s_dr[sig];
+      uint32_t w0 = 0, w1 = 0;
+      if (dr.x != 0.f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w0 |= cvt_e2m1x2(__fmul_rn(hv[2 * i], dr.y), __fmul_rn(hv[2 * i + 1], dr.y)) << (8 * i);
+          w1 |= cvt_e2m1x2(__fmul_rn(hv[8 + 2 * i], dr.y), __fmul_rn(hv[8 + 2 * i + 1], dr.y)) << (8 * i);
+        }
+      }
+      scale_word |= sig << (8 * (2 * b + blk));
+      const int64_t c0 = hcol0 + 32 * b + 16 * blk;  // first column of this block
+      if (row_ok) {
+        *reinterpret_cast<uint2*>(p.h_codes + row * (p.h_cols / 2) + c0 / 2) = make_uint2(w0, w1);
+        if (p.h_out != nullptr) {
+          uint32_t hb[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * i], hv[2 * i + 1]);
+            hb[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.h_cols + c0);
+          dst[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+          dst[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        }
+        // residual slots of the expert's channel set that fall in this block
+        for (int i = s_lo; i < s_hi; ++i) {
+          const int32_t j = S[i];
+          if (j >= c0 && j < c0 + 16) {
+            float x = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x = (j - c0 == e) ? hv[e] : x;
+            p.h_resid[row * p.h_k + i] = element_residual(x, dr.x, dr.y, rs_h);
+          }
+        }
+      }
+    }
+  }
+  if (row_ok)
+    *reinterpret_cast<uint32_t*>(p.h_scales + ((uint64_t)(prow >> 7) * n_cg_h + (hcol0 >> 6)) * 512u +
+                                 (uint64_t)(prow & 31) * 16u + (uint64_t)((prow >> 5) & 3) * 4u) = scale_word;
+}
+
+// kEpiCombine epilogue: row q*32+lane of the tile, 128 columns of half hh,
+// out[token] += w * alpha * acc in fp32 (vector atomic adds); releases the
+// accumulator once its last columns are in registers.
+__device__ __forceinline__ void epi_combine(const GemmParams& p, const Tile& tl, int q, int hh, int lane,
+                                            uint32_t tmem, float alpha, uint64_t* acc_empty) {
+  const int r = q * 32 + lane;
+  const bool row_ok = r < tl.rows;
+  const int64_t row = tl.row0 + r;
+  const int64_t col0 = tl.n0 + hh * 128;
+  float* dst = nullptr;
+  float w = 0.f;
+  if (row_ok && col0 < p.N) {
+    dst = p.out_f32 + (int64_t)p.token_of_row[row] * p.N + col0;
+    w = alpha * p.w_row[row];
+  }
+  const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hh * 128);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    uint32_t v[4][16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(t_acc + (uint32_t)(b * 64 + c * 16), v[c]);
+    tmem_ld_wait();
+    if (b == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+    if (dst != nullptr) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          atomicAdd(reinterpret_cast<float4*>(dst + b * 64 + c * 16 + 4 * i),
+                    make_float4(w * __uint_as_float(v[c][4 * i]), w * __uint_as_float(v[c][4 * i + 1]),
+                                w * __uint_as_float(v[c][4 * i + 2]), w * __uint_as_float(v[c][4 * i + 3])));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -780,6 +944,9 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;
   const int n_kt = (int)((p.K + 255) / 256);
   const int n_ct = (p.k + 63) / 64;
+  // compensation residual scaling in shared memory by the epilogue warps,
+  // unless the residual already carries every factor but g_a g_b
+  const bool scale_r = n_ct > 0 && !(p.resid_scaled && p.flags == 0);
 
   if (warp == 0) {
     // ------------------------------------------------------ producer ----
@@ -926,10 +1093,13 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
         if (++stage == kWStages) { stage = 0; phase ^= 1u; }
       }
       for (int ct = 0; ct < n_ct && ok; ++ct) {
-        // sf_full too (warp 2's plain arrive): a stage is refilled only after
-        // every role that waits on its full barrier has seen this use
-        if (!mbar_wait_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort) ||
-            !mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort)) {
+        // sf_full (and, without the residual scaling, sf_full2) too: the copy
+        // warps' plain arrivals -- a stage is refilled only after every role
+        // that waits on its full barrier has seen this use
+        if (!mbar_wait_warp(&sf_full[stage], phase, kWaitSfFull, s_abort) ||
+            (scale_r ? !mbar_wait_warp(&comp_ready[stage], phase, kWaitCompEmpty, s_abort)
+                     : (!mbar_wait_warp(&sf_full2[stage], phase, kWaitSfFull2, s_abort) ||
+                        !mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)))) {
           ok = false;
           break;
         }
@@ -1009,7 +1179,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
             const int nch = (int)((n_cg - cg0) < sf_chunks_per_kt ? (n_cg - cg0) : sf_chunks_per_kt);
             for (int cc = 0; cc < nch; ++cc)
               tmem_cp_32x128b_x4(t_sfb + 8u * cc + 4u, desc_sf(sfb + 2048u + 512u * cc));
-            mbar_arrive_n(&comp_ready[stage], 8);  // whole phase; before the commit the MMA warp waits for
+            if (scale_r) mbar_arrive_n(&comp_ready[stage], 8);  // whole phase; before the commit the MMA warp waits for
             tc_commit(&sf_full2[stage]);
           }
         } else {
@@ -1018,7 +1188,7 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
           // stage's next compensation use needs their comp_ready arrivals)
           if (elect_one()) {
             mbar_arrive(&sf_full2[stage]);
-            mbar_arrive(&ct_landed[stage]);
+            if (scale_r) mbar_arrive(&ct_landed[stage]);
           }
         }
         __syncwarp();
@@ -1039,10 +1209,26 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
     int stage = 0;
     uint32_t ct_phase = 0;  // bit s: parity of ct_landed[s]'s next phase
     const float ga = p.g_a ? *p.g_a : 1.f;
+    // SwiGLU + quantize: (d, 1/d) of every scale byte under the static scale
+    // of h, as the quantizer builds it, in shared memory after the schedule
+    float2* s_dr = reinterpret_cast<float2*>(s_sched + (p.grouped ? 4 * (p.E + 1) : 0));
+    float g_h = 1.f, yg_h = 1.f, rs_h = 1.f;
+    bool fast_h = true;
+    if (p.epi == kEpiSwigluQuant) {
+      g_h = *p.g_h;
+      yg_h = __frcp_rn(g_h);
+      fast_h = g_h >= 0x1p-100f && g_h <= 0x1p100f;
+      rs_h = p.h_resid_scaled ? yg_h : 1.0f;
+      for (int i = et; i < 256; i += 256) {
+        const float d = __fmul_rn(e4m3_to_f32((uint32_t)i), g_h);
+        s_dr[i] = make_float2(d, d != 0.f ? __frcp_rn(d) : 0.f);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps
+    }
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       Tile tl;
       tile_of_w(p, sched, t, n_tiles_n, tl);
-      if (n_ct > 0) {
+      if (scale_r) {
         // the compensation k-tiles of this tile: scale the residual tile in
         // shared memory by c, then release it to the MMA warp
         float c;
@@ -1083,6 +1269,14 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
       tc_fence_after();
       float alpha = 1.f;
       if (p.fmt == 0) alpha = (p.g_a ? *p.g_a : 1.f) * (p.g_b ? p.g_b[tl.e] : 1.f);
+      if (p.epi == kEpiSwigluQuant) {
+        epi_swiglu_quant(p, tl, q, h, lane, tmem, alpha, s_dr, g_h, yg_h, fast_h, rs_h, acc_empty);
+        continue;
+      }
+      if (p.epi == kEpiCombine) {
+        epi_combine(p, tl, q, h, lane, tmem, alpha, acc_empty);
+        continue;
+      }
       const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
       uint32_t packed[64];
 #pragma unroll
@@ -1780,6 +1974,13 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
 }
 
 
+// Dynamic shared memory of the wide kernel: stages, barriers, the grouped
+// schedule (offsets, tile starts and padded bases in 4 * (E + 1) ints) and,
+// for the SwiGLU + quantize epilogue, the (d, 1/d) table of the scale bytes.
+size_t wide_smem_bytes(int E, int epi) {
+  return kWSmemBytes + (E > 0 ? sizeof(int32_t) * 4 * ((size_t)E + 1) : 0) + (epi == kEpiSwigluQuant ? 2048 : 0);
+}
+
 cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -1829,11 +2030,24 @@ cudaError_t launch_wide(const GemmProblem& pr, bool grouped, int num_sms, cudaSt
   p.offsets = pr.offsets;
   p.grouped = grouped ? 1 : 0;
   p.y_vec32 = ((reinterpret_cast<uintptr_t>(pr.y) & 31u) == 0 && (pr.N % 16) == 0) ? 1 : 0;
+  p.epi = pr.epi;
+  p.h_codes = pr.h_codes;
+  p.h_scales = pr.h_scales;
+  p.h_resid = pr.h_resid;
+  p.h_out = pr.h_out;
+  p.h_chan = pr.h_chan;
+  p.h_k = pr.h_k;
+  p.g_h = pr.g_h;
+  p.h_cols = pr.N / 2;
+  p.h_resid_scaled = pr.h_resid_scaled;
+  p.token_of_row = pr.token_of_row;
+  p.w_row = pr.w_row;
+  p.out_f32 = pr.out_f32;
   const int64_t n_tiles_n = (pr.N + BNW - 1) / BNW;
   const int64_t tiles = grouped ? ((pr.M + BM - 1) / BM + E) * n_tiles_n : ((pr.M + BM - 1) / BM) * n_tiles_n;
   int grid = (int)(tiles < num_sms ? tiles : num_sms);
   if (grid < 1) grid = 1;
-  const size_t smem = kWSmemBytes + (grouped ? sizeof(int32_t) * (3 * (size_t)E + 2) : 0);
+  const size_t smem = wide_smem_bytes(grouped ? E : 0, pr.epi);
   cudaError_t err = cudaFuncSetAttribute(w4a4_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   {
@@ -1970,7 +2184,7 @@ cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) 
 }
 
 cudaError_t launch_grouped_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {
-  if ((size_t)p.E * 12 + 8 > 227 * 1024 - kWSmemBytes) return cudaErrorInvalidValue;
+  if (wide_smem_bytes(p.E, p.epi) > 227 * 1024) return cudaErrorInvalidValue;
   return launch(p, true, num_sms, stream);
 }
 

@@ -85,6 +85,20 @@ struct GemmProblem {
   const int32_t* offsets = nullptr; // grouped: [E+1]
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // grouped only: fused epilogues (0 = store Y; 1 = SwiGLU + NVFP4 quantize of
+  // the down projection's input; 2 = routing-weighted combine into token rows)
+  int epi = 0;
+  uint8_t* h_codes = nullptr;
+  uint8_t* h_scales = nullptr;
+  __nv_bfloat16* h_resid = nullptr;
+  __nv_bfloat16* h_out = nullptr;
+  const int32_t* h_chan = nullptr;
+  int h_k = 0;
+  const float* g_h = nullptr;
+  int h_resid_scaled = 0;
+  const int32_t* token_of_row = nullptr;
+  const float* w_row = nullptr;
+  float* out_f32 = nullptr;
 };
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int num_sms);

@@ -102,6 +102,15 @@ def test_invalid_arguments_rejected_on_host(lib):
                                   None, 0, None) == 1
     assert lib.w4a4_grouped_gemm_comp(0, 4, fake, 8, 128, 64, fake, fake, None, fake, fake, None, None, None,
                                       0, 0x500, fake, None, 0, None) == 1
+    # fused MoE GEMMs: the SwiGLU tile needs N % 256, h flags, h_k within N/2, the combine its row tables
+    assert lib.w4a4_grouped_gemm_swiglu_quant(4, fake, 8, 384, 64, fake, fake, None, fake, fake, None, None, None,
+                                              0, 0, fake, fake, 4, 0, fake, fake, fake, None, None) == 2
+    assert lib.w4a4_grouped_gemm_swiglu_quant(4, fake, 8, 512, 64, fake, fake, None, fake, fake, None, None, None,
+                                              0, 0, fake, fake, 4, 2, fake, fake, fake, None, None) == 1
+    assert lib.w4a4_grouped_gemm_swiglu_quant(4, fake, 8, 512, 64, fake, fake, None, fake, fake, None, None, None,
+                                              0, 0, fake, fake, 257, 0, fake, fake, fake, None, None) == 1
+    assert lib.w4a4_grouped_gemm_combine(4, fake, 8, 512, 64, fake, fake, None, fake, fake, None, None, None, 0, 0,
+                                         None, fake, 2, fake, None) == 1
     # quantizer flags: only the pre-scaled-residual bit exists
     assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 2, None, 0, None) == 1
     assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 4, None,

@@ -68,10 +68,13 @@ class WideGemmModel:
     `uses` numbers the ring's stage uses in the order every role walks them:
     per output tile, n_kt FP4 k-tiles then n_ct compensation k-tiles."""
 
-    def __init__(self, seed, n_tiles, n_kt, n_ct, protocol="kernel", stages=4, early=False):
+    def __init__(self, seed, n_tiles, n_kt, n_ct, protocol="kernel", stages=4, early=False, scale_r=True):
         self.r = random.Random(seed)
         self.S, self.n_kt, self.n_ct, self.T = stages, n_kt, n_ct, n_tiles
         self.protocol, self.early = protocol, early
+        # scale_r: the epilogue warps scale each compensation residual tile
+        # (False: a residual pre-scaled by the quantizer goes to the MMA as is)
+        self.scale_r = scale_r and n_ct > 0
         ring = lambda name, count: [Barrier(f"{name}[{i}]", count) for i in range(stages)]
         self.full, self.empty = ring("full", 1), ring("empty", 1)
         self.sf_full, self.sf_full2 = ring("sf_full", 1), ring("sf_full2", 1)
@@ -147,7 +150,8 @@ class WideGemmModel:
             yield lambda: self.full[st].passed(ph)
             assert self.content[st] == u, ("copy warp B saw", self.content[st], "for use", u)
             if j < self.n_kt:
-                self.comp_ready[st].arrive(8)
+                if self.scale_r:
+                    self.comp_ready[st].arrive(8)
 
                 def copied(st=st, u=u):
                     self.sfb2[st] = u
@@ -155,7 +159,8 @@ class WideGemmModel:
                 self.later(copied, "w3", 2, 20)
             else:
                 self.sf_full2[st].arrive()
-                self.ct_landed[st].arrive()
+                if self.scale_r:
+                    self.ct_landed[st].arrive()
 
     def mma(self):
         acc_ph = 0
@@ -169,6 +174,12 @@ class WideGemmModel:
                 if j < self.n_kt:
                     yield lambda: self.sf_full[st].passed(ph) and self.sf_full2[st].passed(ph)
                     assert (self.content[st], self.sfa[st], self.sfb2[st]) == (u, u, u), ("MMA", u)
+                elif not self.scale_r:
+                    # pre-scaled residual: the tile goes to the MMA as it lands,
+                    # once both copy warps (which wait on `full` too) passed it
+                    yield lambda: (self.full[st].passed(ph) and self.sf_full[st].passed(ph)
+                                   and self.sf_full2[st].passed(ph))
+                    assert self.content[st] == u, ("MMA on compensation", u)
                 else:
                     if self.protocol == "mma_skips_copy_warp":
                         yield lambda: self.comp_ready[st].passed(ph)
@@ -185,7 +196,7 @@ class WideGemmModel:
     def epilogue_warp(self, w):
         acc_ph, stage, ct_phase, u0 = 0, 0, 0, 0
         for _ in range(self.T):
-            if self.n_ct:
+            if self.scale_r:
                 stage = (stage + self.n_kt) % self.S
                 for ct in range(self.n_ct):
                     u, st = u0 + self.n_kt + ct, stage
@@ -412,20 +423,21 @@ def _shapes(seed):
     return r.randint(1, 5), r.choice([1, 2, 3, 5, 16]), r.choice([0, 1, 2, 3, 4, 5, 8])
 
 
-def _failures(protocol, n, early=False):
+def _failures(protocol, n, early=False, scale_r=True):
     bad = 0
     for seed in range(n):
         n_tiles, n_kt, n_ct = _shapes(seed)
         try:
-            WideGemmModel(seed, n_tiles, n_kt, n_ct, protocol, early=early).run()
+            WideGemmModel(seed, n_tiles, n_kt, n_ct, protocol, early=early, scale_r=scale_r).run()
         except AssertionError:
             bad += 1
     return bad
 
 
 @pytest.mark.parametrize("early", [False, True])
-def test_kernel_protocol_holds_under_random_schedules(early):
-    assert _failures("kernel", 400, early) == 0
+@pytest.mark.parametrize("scale_r", [False, True])
+def test_kernel_protocol_holds_under_random_schedules(early, scale_r):
+    assert _failures("kernel", 400, early, scale_r) == 0
 
 
 @pytest.mark.parametrize("protocol", ["mma_skips_copy_warp", "epilogue_waits_full"])
