@@ -727,11 +727,18 @@ __device__ __forceinline__ void tile_of_w(const GemmParams& p, const SchedSmem& 
 
 // silu(z) * u in fp32 with the fast exponential and division (a few fp32
 // ulps; h is rounded to bf16 right after, and the codes are those of that
-// rounded h): z / (1 + e^-z), times u.
+// rounded h): z / (1 + e^-z), times u.  (0.5 z (1 + tanh(z/2)) with the
+// hardware tanh would save one special-function operation, but loses the
+// relative accuracy of sigmoid for negative z.)
 __device__ __forceinline__ float swiglu_f32(float z, float u) {
   return __fmul_rn(__fdividef(z, __fadd_rn(1.0f, __expf(-z))), u);
 }
-__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+// Two fp32 values rounded to bf16 (one packed conversion) and back to fp32.
+__device__ __forceinline__ float2 bf16r2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(&v);
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
 
 // kEpiSwigluQuant epilogue of one 128 x 256 tile for the warp of TMEM lane
 // quarter q and column half hh: gate columns [64 hh, 64 hh + 64) and the
@@ -780,12 +787,14 @@ __device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile
       float hv[16];
       float am = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 16; i += 2) {
         // the projection's bf16 outputs, then h rounded to bf16
-        const float yg = bf16r(alpha * __uint_as_float(vg[blk][i]));
-        const float yu = bf16r(alpha * __uint_as_float(vu[blk][i]));
-        hv[i] = bf16r(swiglu_f32(yg, yu));
-        am = fmaxf(am, fabsf(hv[i]));
+        const float2 yg = bf16r2(alpha * __uint_as_float(vg[blk][i]), alpha * __uint_as_float(vg[blk][i + 1]));
+        const float2 yu = bf16r2(alpha * __uint_as_float(vu[blk][i]), alpha * __uint_as_float(vu[blk][i + 1]));
+        const float2 hh2 = bf16r2(swiglu_f32(yg.x, yu.x), swiglu_f32(yg.y, yu.y));
+        hv[i] = hh2.x;
+        hv[i + 1] = hh2.y;
+        am = fmaxf(am, fmaxf(fabsf(hh2.x), fabsf(hh2.y)));
       }
       const uint32_t sig = block_scale_byte(am, g_h, yg_h, fast_h);
       const float2 dr = s_dr[sig];
