@@ -418,14 +418,16 @@ def _time_steps(fn, steps, flush):
     """Mean device time (ms) of `fn` over `steps` runs.  Between runs, outside
     the timed window, a buffer larger than the L2 is written and then read
     back: the write flushes the L2, the read writes its dirty lines back to
-    HBM, so a step does not start behind 129 MB of pending write-backs."""
+    HBM, so a step does not start behind 129 MB of pending write-backs.
+    flush=None: no flush (the step's own inputs are larger than the L2)."""
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(steps):
-        flush.zero_()
-        flush.view(torch.float32).sum()
+        if flush is not None:
+            flush.zero_()
+            flush.view(torch.float32).sum()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda._sleep(2000000)  # keeps the device busy while the host enqueues the step
         e0.record()
@@ -444,28 +446,53 @@ def other_workloads(nv, pk, steps=10):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
 
-    # decode: X[16,4096] x W[4096,14336], k=64 (HBM-bound on the weights)
+    # decode: X[16,4096] x W[4096,14336], k=64 (HBM-bound on the weights).
+    # Six layers' weights (6 x 35 MB > L2) are used in turn, as successive
+    # layers of a model would: every step streams its weights from HBM, with
+    # no flush between steps (X, the channel list and the code stay in L2).
     s = W.SPECS["decode"]
     d = W.dense_inputs("decode")
-    x, wt = d["x"].to(dev), d["wt"].to(dev)
+    x = d["x"].to(dev)
     chan = nv.nvfp4_calibrate_channels(W.dense_inputs("decode", True, False)["x"].to(dev), s.k)
-    qw = nv.nvfp4_quantize(wt)
-    ws = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan)
-    del wt
+    wt0 = d["wt"].to(dev)
+    layers = []
+    for i in range(6):
+        wt = wt0 if i == 0 else torch.roll(wt0, shifts=977 * i, dims=0)
+        qw = nv.nvfp4_quantize(wt)
+        layers.append((qw, nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], chan)))
+        del wt
+    del wt0
     y = torch.empty((s.M, s.N), dtype=torch.bfloat16, device=dev)
+    step_i = [0]
+
+    def layer():
+        step_i[0] += 1
+        return layers[step_i[0] % len(layers)]
 
     def dec():
+        qw, ws = layer()
+        nv.w4a4_decode_linear(x, qw, s.N, chan=chan, w_sel=ws, y=y, weights_ready=True)
+
+    def dec_two():
+        qw, ws = layer()
         qx = nv.nvfp4_quantize(x, chan=chan, resid_scaled=True)
         nv.w4a4_gemm_comp(qx, qw, s.N, resid=qx["resid"], w_sel=ws, y=y, weights_ready=True)
-    ms = _time_steps(dec, steps, flush)
+    ms = _time_steps(dec, steps, None)
+    ms_two = _time_steps(dec_two, steps, None)
+    ms_flush = _time_steps(dec, steps, flush)
+    qw, ws = layers[0]
     byts = qw["codes"].numel() + qw["scales"].numel() + ws.numel() * 2 + x.numel() * 2 + y.numel() * 2
     out["decode"] = {"shape": "X[16,4096] x W[4096,14336], k=64", "ms_per_step": round(ms, 4),
                      "tflops": round(2.0 * s.M * s.N * s.K / (ms * 1e-3) / 1e12, 2),
                      "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                      "bytes_per_step": byts, "bound": "hbm",
-                     "note": "dynamic-scale quantize of X + GEMM (128x128-tile kernel, K split across CTAs, "
-                             "split-order finalize)"}
-    del qw, ws, x, y
+                     "two_launch_ms": round(ms_two, 4), "after_l2_flush_ms": round(ms_flush, 4),
+                     "note": "one launch (w4a4_decode_linear): clusters of 4 CTAs quantize X (dynamic scale) "
+                             "into shared memory, the swapped-operand GEMM with compensation streams the weights; "
+                             "weights of 6 layers used in turn (> L2); two_launch_ms = quantize kernel + GEMM "
+                             "kernel on the same rotation; after_l2_flush_ms = the one launch after a 256 MB "
+                             "L2 flush (code and X also cold)"}
+    del layers, x, y
 
     # MoE: 4096 tokens top-8 of 128 experts; gate/up [2048->1536] and down [768->2048], k=32 per expert
     s = W.SPECS["moe"]

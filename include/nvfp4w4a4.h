@@ -404,6 +404,44 @@ int w4a4_grouped_gemm_combine(int32_t E, const int32_t* offsets, int64_t M_total
                               const int32_t* token_of_row, const float* w_row, int64_t n_tokens, float* out,
                               void* stream);
 
+/*
+ * w4a4_decode_linear -- the whole compensated linear layer for a decode batch
+ * (1 <= M <= 16 tokens) in ONE launch: the activation quantize and the GEMM
+ * with its compensation term, with no intermediate buffers.
+ * Source: QUADS abstract (activations quantized online in front of native
+ * W4A4 GEMMs; Residual Activation Compensation); FourSight abstract (a
+ * dedicated decode datapath -- prior art for having one, not for this one).
+ *
+ * Every CTA quantizes X itself, with nvfp4_quantize's arithmetic (tensor scale
+ * g = amax(X) / 2688, or *g_in; E4M3 block scales; E2M1 codes; the residual on
+ * the channels chan[0..k) divided by g, as nvfp4_quantize_ex with
+ * NVFP4_QUANT_RESID_SCALED), into its shared memory, and multiplies it with
+ * the pre-quantized weights:
+ *   y = bf16_rn(g*gb*acc + c*accc),  c = g*gb (COMP_W_DEQ) or g (COMP_W_BF16)
+ * y is bit-identical to nvfp4_quantize_ex(..., NVFP4_QUANT_RESID_SCALED)
+ * followed by w4a4_gemm_comp(..., flags | NVFP4_GEMM_RESID_SCALED) on the
+ * same inputs.
+ *
+ * x [M, K] bf16 with row stride ldx (ldx >= K, ldx % 8 == 0, 16-byte aligned)
+ * 1 <= M <= 16, N % 128 == 0, K % 64 == 0, K <= 8192, 0 <= k <= min(K, 256),
+ *         k % 8 == 0; chan [k] sorted distinct columns (NULL if k == 0)
+ * g_in    device float (a static tensor scale) or NULL (dynamic: amax of X)
+ * g_out   device float receiving g, or NULL
+ * b_codes [N, K/2], b_scales tiled [N, K], g_b device float or NULL (1),
+ * w_sel   [N, k] bf16 from nvfp4_prepare_comp_weights (NULL if k == 0)
+ * y [M, N] bf16 (16-byte aligned)
+ * flags   NVFP4_COMP_W_DEQ or NVFP4_COMP_W_BF16, optionally |
+ *         NVFP4_GEMM_WEIGHTS_READY (as w4a4_gemm_comp: the weight tiles
+ *         stream before the preceding kernel ends).  X and g_in are always
+ *         read after it ends.
+ * Returns NVFP4_ERR_UNSUPPORTED for shapes outside these limits (use
+ * nvfp4_quantize_ex + w4a4_gemm_comp), NVFP4_ERR_INVALID_ARG for bad
+ * pointers or flags.
+ */
+int w4a4_decode_linear(int64_t M, int64_t N, int64_t K, const uint16_t* x, int64_t ldx, const float* g_in,
+                       float* g_out, const int32_t* chan, int32_t k, const uint8_t* b_codes, const uint8_t* b_scales,
+                       const float* g_b, const uint16_t* w_sel, int flags, uint16_t* y, void* stream);
+
 /* Reads (and with clear != 0 resets) the device-side error latch of every
  * kernel family on the current device.  Synchronizes the device.  Returns
  * NVFP4_OK, NVFP4_ERR_TIMEOUT or NVFP4_ERR_INVALID_ARG; *detail (may be NULL)

@@ -63,6 +63,8 @@ _SIGS = {
                                        ctypes.c_int),
     "w4a4_grouped_gemm_combine": ([_I32, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32, ctypes.c_int,
                                    _P, _P, _I64, _P, _P], ctypes.c_int),
+    "w4a4_decode_linear": ([_I64, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _P, _P, _P, _P, ctypes.c_int, _P, _P],
+                           ctypes.c_int),
     "nvfp4_check_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "nvfp4_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
     "nvfp4_inject_barrier_timeout": ([], None),
@@ -326,6 +328,33 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
                             _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags, _ptr(y),
                             _ptr(ws), 0 if ws is None else ws.numel(), _stream())
     _check("w4a4_gemm_comp", st)
+    return y
+
+
+def w4a4_decode_linear(x, qw, N, chan=None, w_sel=None, g=None, flags=COMP_W_DEQ, y=None, g_out=None,
+                       weights_ready=False):
+    """The whole layer for 1..16 tokens in one launch: y [M, N] bf16 from the
+    bf16 activations x [M, K] (quantized inside the kernel: dynamic tensor
+    scale, or g, a device float32 [1]), the quantized weights qw (the dict of
+    nvfp4_quantize for W^T [N, K]) and the compensation columns w_sel [N, k]
+    of the sorted channel list chan [k].  g_out: optional float32 [1]
+    receiving the tensor scale used."""
+    if weights_ready:
+        flags |= GEMM_WEIGHTS_READY
+    lib = load()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    k = 0 if chan is None else int(chan.numel())
+    if chan is not None:
+        _need(chan, torch.int32, "chan")
+    if g is not None:
+        _need(g, torch.float32, "g")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = lib.w4a4_decode_linear(M, N, K, _ptr(x), x.stride(0), _ptr(g), _ptr(g_out), _ptr(chan) if k else None, k,
+                                _ptr(qw["codes"]), _ptr(qw["scales"]), _ptr(qw.get("g")),
+                                _ptr(w_sel) if k else None, flags, _ptr(y), _stream())
+    _check("w4a4_decode_linear", st)
     return y
 
 

@@ -328,6 +328,31 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
   return from_cuda(nv4::launch_gemm(p, d->num_sms, as_stream(stream)));
 }
 
+int w4a4_decode_linear(int64_t M, int64_t N, int64_t K, const uint16_t* x, int64_t ldx, const float* g_in,
+                       float* g_out, const int32_t* chan, int32_t k, const uint8_t* b_codes, const uint8_t* b_scales,
+                       const float* g_b, const uint16_t* w_sel, int flags, uint16_t* y, void* stream) {
+  const int mode = flags & ~NVFP4_GEMM_WEIGHTS_READY;
+  if (mode != NVFP4_COMP_W_DEQ && mode != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
+  if (M < 1 || N <= 0 || K <= 0 || k < 0 || ldx < K || ldx % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (M > 16 || N % 128 != 0 || K % 64 != 0 || K > 8192 || k > 256 || k > K || k % 8 != 0 ||
+      N > ((int64_t)1 << 31) - 256 || nv4::decode_stages(K, k) == 0)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (!x || !b_codes || !b_scales || !y || !aligned(x, 16) || !aligned(b_codes, 16) || !aligned(b_scales, 16) ||
+      !aligned(y, 16))
+    return NVFP4_ERR_INVALID_ARG;
+  if (k > 0 && (!chan || !w_sel || !aligned(chan, 4) || !aligned(w_sel, 16))) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  int st;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  nv4::DecodeProblem p;
+  p.x = bf(x); p.ldx = ldx; p.M = M; p.N = N; p.K = K; p.k = k; p.chan = chan;
+  p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b; p.w_sel = bf(w_sel);
+  p.g_in = g_in; p.g_out = g_out; p.y = bf(y);
+  p.flags = (mode == NVFP4_COMP_W_BF16 ? nv4::kGemmCompBf16 : 0) |
+            ((flags & NVFP4_GEMM_WEIGHTS_READY) ? nv4::kGemmWeightsReady : 0);
+  return from_cuda(nv4::launch_decode(p, d->num_sms, as_stream(stream)));
+}
+
 size_t w4a4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K) {
   (void)E; (void)M_total; (void)N; (void)K;
   return 0;

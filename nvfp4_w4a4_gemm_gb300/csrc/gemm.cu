@@ -68,7 +68,7 @@ static_assert(kColSf + 32 * kStages <= kTmemCols, "TMEM budget");
 
 enum WaitSite : uint32_t {
   kWaitEmpty = 1, kWaitFull = 2, kWaitAccEmpty = 3, kWaitCompEmpty = 4, kWaitAccFull = 5, kWaitDrain = 6,
-  kWaitSfFull = 7, kWaitSfDrain = 8, kWaitSfFull2 = 9, kWaitCtLanded = 10
+  kWaitSfFull = 7, kWaitSfDrain = 8, kWaitSfFull2 = 9, kWaitCtLanded = 10, kWaitXReady = 11, kWaitRReady = 12
 };
 
 struct GemmParams {
@@ -1819,6 +1819,486 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   }
 }
 
+// ============================================================ decode layer ==
+// The whole compensated linear layer for at most 16 tokens in one launch.
+// The CTAs of a cluster quantize the token rows together (tensor scale, E4M3
+// block scales, E2M1 codes and the pre-scaled compensation residual, with the
+// activation quantizer's arithmetic): each takes every C-th 256-column k-tile
+// of X (and every C-th 64-channel residual tile), writes it into its own
+// shared memory and sends it to the other CTAs of the cluster with bulk
+// copies that complete on their barriers, so the data stays resident in
+// every CTA for all of its output tiles.  Each CTA reads 1/C of X, and the
+// per-CTA work in front of the first MMA shrinks by C.
+// Meanwhile each CTA's producer streams only weight tiles through its ring.
+// Weight rows fill the MMA's 128-row slot and the tokens its N = 16 slot
+// (swapped operands), as in the 128-row kernel's decode form, whose
+// accumulation order (k-tiles ascending, four K = 64 MMAs each, then the
+// compensation MMAs into their own accumulator) and epilogue this kernel
+// repeats, so both give the same output bits.
+//
+// Sources: QUADS (arXiv 2607.15810) abstract -- the activations are quantized
+// online in front of native W4A4 GEMMs, and Residual Activation Compensation
+// corrects the high-error channels; FourSight (arXiv 2611.04887) abstract --
+// separate prefill and decode datapaths (prior art for the split only).
+//
+// Warps: 0 weight TMA producer; 1 TMEM allocation, scale copies and MMA issue
+// (the copies of a k-tile go out from the same thread right before its MMAs,
+// which the tensor core runs in issue order: no hand-off per k-tile);
+// 2..9 quantize the tokens (one 16-element block per thread per k-tile),
+// after which warps 2..5 run the epilogue.
+// TMEM: two accumulator buffers of 32 columns (the FP4 product in columns
+// 32b .. 32b+15, its compensation product in 32b+16 .. 32b+31) and one
+// 32-column scale slot per ring stage from column 64 (tokens 0..15, weights
+// 16..31).
+// Shared memory (1024-byte aligned): the ring of 18 KB stages (a weight code
+// tile or a W_S tile, then the weight scale chunks), the token codes (2 KB
+// per k-tile, 128-byte swizzled K-major: the MMA's B operand), the residual
+// tiles (2 KB per 64 compensated channels, the same layout), the token scale
+// chunks (256 bytes per 64 columns: rows 0..15 of a 32-row copy source, whose
+// rows 16..31 -- unread by an N = 16 MMA -- overlap the next chunk), the
+// (d, 1/d) table of the scale bytes, the cluster's amax partials (16 bytes
+// each, the unit of a bulk copy) and the barriers.
+constexpr int kDecThreads = 320;
+constexpr int kDecRows = 16;                           // tokens per launch (the MMA's N)
+constexpr int kDecMaxKt = 32;                          // K <= 8192
+constexpr int kDecMaxCt = 4;                           // k <= 256
+constexpr int kDecMaxStages = 14;                      // TMEM: 64 + 32 * 14 = 512 columns
+constexpr int kDecStageBytes = kTileBytes + kSfBytes;  // 18 KB
+constexpr int kDecQuantWarps = 8;
+constexpr int kDecCluster = 4;     // CTAs sharing the token quantization
+constexpr int kDecGroup = 8;       // owned k-tiles whose blocks a thread holds in registers at once
+constexpr uint32_t kDecColSf = 64;
+static_assert(kDecColSf + 32u * kDecMaxStages <= kTmemCols, "TMEM budget");
+static_assert(2 + kDecQuantWarps == kDecThreads / 32, "warp roles");
+
+struct DecodeParams {
+  CUtensorMap tm_b;  // weight codes [N, K/2] u8
+  CUtensorMap tm_w;  // W_S [N, k] bf16
+  const __nv_bfloat16* x;
+  int64_t ldx;
+  int M;
+  int64_t N, K;
+  int k;
+  const int32_t* chan;
+  const uint8_t* b_sf;
+  const float* g_in;  // static tensor scale, or nullptr: amax / 2688 of X
+  float* g_out;
+  const float* g_b;
+  __nv_bfloat16* y;
+  int flags;    // compensation weights: 0 dequantized NVFP4, 1 BF16
+  int early_w;  // weights may be streamed before the preceding kernel ends
+  int stages;
+  uint32_t off_tok, off_res, off_tsf, off_dr, off_bar;
+};
+
+// Word i (0..7) of the 16 bf16 of a block held as two uint4.
+__device__ __forceinline__ uint32_t block_word(const uint4& a, const uint4& b, int i) {
+  const uint4 v = (i & 4) ? b : a;
+  const int j = i & 3;
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int S = p.stages;
+  const int n_kt = (int)((p.K + 255) / 256);
+  const int n_ct = (p.k + 63) / 64;
+  const int C = (int)cluster_num_ctas();
+  const int rank = (int)cta_rank_in_cluster();
+  uint8_t* ring = smem;
+  uint8_t* tok = smem + p.off_tok;
+  uint8_t* res = smem + p.off_res;
+  uint8_t* tsf = smem + p.off_tsf;
+  float2* s_dr = reinterpret_cast<float2*>(smem + p.off_dr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint64_t* amax_bar = drain + 1;
+  uint64_t* rready = amax_bar + 1;
+  uint64_t* xready = rready + 1;  // [n_kt]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xready + n_kt);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  float* s_red = reinterpret_cast<float*>(s_tmem + 2);  // [kDecQuantWarps]
+  // [C][4]: the amax partials of the cluster's CTAs, 16-byte slots
+  float* s_amax = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_red + kDecQuantWarps) + 15) &
+                                           ~static_cast<uintptr_t>(15));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // a following layer may start its prologue and weight stream now; its own
+  // wait still covers all of this kernel's writes
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    // token data barriers: one local arrival (this CTA's own part, or the
+    // arrival made here with the bytes expected from the owner's bulk copies)
+    mbar_init(amax_bar, 1);
+    mbar_arrive_expect_tx(amax_bar, 16u * (uint32_t)(C - 1));  // the other CTAs' amax partials
+    mbar_init(rready, 1);
+    uint32_t res_in = 0;
+    for (int ct = 0; ct < n_ct; ++ct) res_in += (ct % C != rank) ? 2048u : 0u;
+    if (res_in > 0) mbar_expect_tx(rready, res_in);
+    for (int i = 0; i < n_kt; ++i) {
+      mbar_init(&xready[i], 1);
+      if (i % C != rank) mbar_arrive_expect_tx(&xready[i], 3072u);  // codes 2 KB + scales 1 KB
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 16) reinterpret_cast<uint4*>(tsf + 1024 * n_kt)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  // this CTA's barriers exist (fence_mbar_init published them to the
+  // cluster): the others may send to it once they have waited for this
+  // arrival (the quantizing warps wait before their first copy)
+  cluster_arrive_relaxed();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int n_tiles = (int)(p.N / BN);
+  const int64_t n_cg = p.K / 64;  // weight scale chunks per 128-row tile row
+  // ring order per output tile: the FP4 k-tiles, then the compensation k-tiles
+  const int n_use = n_kt + n_ct;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer ----
+    // the whole warp runs the loop, one elected lane issues (a loop run by a
+    // lone lane while the rest of the warp waits measured about 1.7x slower
+    // per k-tile on GB300)
+    if (elect_one()) {
+      tma_prefetch_desc(&p.tm_b);
+      if (n_ct > 0) tma_prefetch_desc(&p.tm_w);
+    }
+    __syncwarp();
+    if (!p.early_w) pdl_wait();
+    int stage = 0, armed = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const int n0 = t * BN;
+      for (int i = 0; i < n_use; ++i) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
+        if (elect_one()) {
+          uint8_t* sb = ring + stage * kDecStageBytes;
+          if (i < n_kt) {
+            const int64_t cg0 = (int64_t)i * 4;
+            const uint32_t sfb = (uint32_t)((n_cg - cg0) < 4 ? (n_cg - cg0) : 4) * 512u;
+            mbar_arrive_expect_tx(&full[stage], kTileBytes + sfb);
+            tma_load_2d(sb, &p.tm_b, &full[stage], i * BKB, n0);
+            bulk_load(sb + kTileBytes, p.b_sf + ((uint64_t)t * n_cg + cg0) * 512u, sfb, &full[stage]);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], kTileBytes);
+            tma_load_2d(sb, &p.tm_w, &full[stage], (i - n_kt) * 64, n0);
+          }
+        }
+        __syncwarp();
+        ++armed;
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) land_armed_copies(full, S, armed);
+  } else if (warp == 1) {
+    // ---------------------------------------- scale copies and MMAs ----
+    // a k-tile's copies go out from the elected lane right before its MMAs
+    // (the tensor core runs them in issue order), so no other warp hands
+    // them over; the whole warp runs the loop
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    const uint32_t idesc = idesc_fp4_swap(0, 0, kDecRows), idesc_c = idesc_bf16_swap(kDecRows);
+    const uint32_t ring_s = smem_u32(ring), tok_s = smem_u32(tok), tsf_s = smem_u32(tsf), res_s = smem_u32(res);
+    const bool full_kt = (p.K & 255) == 0;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const bool first = t == (int)blockIdx.x;  // the token data barriers complete during the first tile
+      if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_acc = tmem + 32u * (uint32_t)acc;
+      for (int i = 0; i < n_use; ++i) {
+        if (first && i < n_kt && !mbar_wait_warp(&xready[i], 0, kWaitXReady, s_abort)) { ok = false; break; }
+        if (first && i == n_kt && !mbar_wait_warp(rready, 0, kWaitRReady, s_abort)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t sb = ring_s + (uint32_t)stage * (uint32_t)kDecStageBytes;
+          const uint64_t a0 = desc_sw128(sb);  // + 2 per 32 bytes of K
+          if (i < n_kt) {
+            const uint64_t b0 = desc_sw128(tok_s + (uint32_t)i * 2048u);
+            const uint64_t sfa0 = desc_sf(tsf_s + (uint32_t)i * 1024u);  // + 16 per 256-byte token chunk
+            const uint64_t sfb0 = desc_sf(sb + (uint32_t)kTileBytes);     // + 32 per 512-byte weight chunk
+            const uint32_t col_sf = tmem + kDecColSf + 32u * (uint32_t)stage;
+            const uint32_t acc0 = i > 0 ? 1u : 0u;
+            // the slot's previous MMAs completed before the producer refilled this stage
+            if (full_kt || i + 1 < n_kt) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
+                tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * c);
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
+                            j > 0 ? 1u : acc0);
+            } else {
+              const int nch = (int)(n_cg - (int64_t)i * 4);  // the last, partial k-tile
+              for (int c = 0; c < nch; ++c) {
+                tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
+                tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * c);
+              }
+              for (int j = 0; j < nch; ++j)
+                mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
+                            j > 0 ? 1u : acc0);
+            }
+          } else {
+            const int ct = i - n_kt;
+            const uint64_t r0 = desc_sw128(res_s + (uint32_t)ct * 2048u);
+            const int krem = p.k - ct * 64;
+            const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
+            for (int j = 0; j < n_mma; ++j)
+              mma_bf16(d_acc + 16u, a0 + 2u * j, r0 + 2u * j, idesc_c, (ct > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(&acc_full[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // all MMAs issued by the elected lane complete before TMEM is released
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
+  } else {
+    // ------------------------------------------ token quantization ----
+    // thread qt owns block (row m, 16-column block b) of the k-tiles r, r + C,
+    // r + 2C, ... of this CTA's cluster rank r
+    const int qt = threadIdx.x - 64;
+    const int qw = qt >> 5;
+    const int m = qt >> 4, b = qt & 15;
+    pdl_wait();  // X (and a static tensor scale) may come from the preceding kernel
+    cluster_wait();  // every CTA of the cluster has its barriers set up
+    const bool row_ok = m < p.M;
+    const __nv_bfloat16* xrow = p.x + (int64_t)(row_ok ? m : 0) * p.ldx;
+    const int n_own = rank < n_kt ? (n_kt - rank + C - 1) / C : 0;
+    const int n_groups = (n_own + kDecGroup - 1) / kDecGroup;
+    uint4 v[kDecGroup][2];
+    auto load_group = [&](int g) {
+#pragma unroll
+      for (int i = 0; i < kDecGroup; ++i) {
+        const int j = g * kDecGroup + i;
+        const int64_t col = (int64_t)(rank + j * C) * 256 + b * 16;
+        v[i][0] = make_uint4(0, 0, 0, 0);
+        v[i][1] = make_uint4(0, 0, 0, 0);
+        if (row_ok && j < n_own && col < p.K) ldg_stream32(xrow + col, v[i][0], v[i][1]);
+      }
+    };
+    if (n_groups > 0) load_group(0);
+    float g;
+    if (p.g_in != nullptr) {
+      g = *p.g_in;
+    } else {
+      // tensor scale: the amax of this CTA's k-tiles, then the largest of the
+      // cluster's partials (every CTA of the cluster gets the same value)
+      uint32_t m2 = 0u;
+      for (int gi = 0; gi < n_groups; ++gi) {
+        if (gi > 0) load_group(gi);
+#pragma unroll
+        for (int i = 0; i < kDecGroup; ++i) m2 = absmax8(absmax8(m2, v[i][0]), v[i][1]);
+      }
+      float am = absmax_of(m2);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      if (lane == 0) s_red[qw] = am;
+      named_bar_sync(1, 32 * kDecQuantWarps);
+      am = 0.f;
+      for (int i = 0; i < kDecQuantWarps; ++i) am = fmaxf(am, s_red[i]);
+      if (qt == 0) {
+        s_amax[4 * rank] = am;
+        fence_proxy_async_smem();
+        for (int c = 0; c < C; ++c)
+          if (c != rank)
+            bulk_copy_to_cta(cluster_addr(&s_amax[4 * rank], (uint32_t)c), &s_amax[4 * rank], 16u,
+                             cluster_addr(amax_bar, (uint32_t)c));
+      }
+      mbar_wait(amax_bar, 0, kWaitXReady, s_abort);
+      for (int c = 0; c < C; ++c)
+        if (c != rank) am = fmaxf(am, s_amax[4 * c]);
+      g = am > 0.f ? __fdiv_rn(am, 2688.0f) : 1.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
+      if (n_groups > 1) load_group(0);
+    }
+    {
+      // (d, 1/d) of every scale byte under this tensor scale
+      const float d = __fmul_rn(e4m3_to_f32((uint32_t)qt), g);
+      s_dr[qt] = make_float2(d, d != 0.f ? __frcp_rn(d) : 0.f);
+    }
+    named_bar_sync(1, 32 * kDecQuantWarps);
+    if (blockIdx.x == 0 && qt == 0 && p.g_out != nullptr) *p.g_out = g;
+    const float yg = __frcp_rn(g);
+    const bool fast = g >= 0x1p-100f && g <= 0x1p100f;
+
+    // codes and scale bytes of the owned k-tiles, written locally, released to
+    // this CTA's MMA warp and sent to the other CTAs of the cluster
+    const int sw = m & 7;
+    uint8_t* tdst = tok + (m >> 3) * 1024 + sw * 128 + (((b >> 1) ^ sw) << 4) + (b & 1) * 8;
+    uint8_t* sdst = tsf + m * 16 + (b >> 2) * 256;
+    for (int gi = 0; gi < n_groups; ++gi) {
+      if (gi > 0) load_group(gi);
+#pragma unroll
+      for (int i = 0; i < kDecGroup; ++i) {
+        const int j = gi * kDecGroup + i;
+        if (j >= n_own) break;
+        const int kt = rank + j * C;
+        const bool valid = row_ok && (int64_t)kt * 256 + b * 16 < p.K;
+        const float am = absmax_of(absmax8(absmax8(v[i][0].x, v[i][0]), v[i][1]));
+        uint32_t sig = block_scale_byte(am, g, yg, fast);
+        sig = valid ? sig : 0u;
+        const float2 dr = s_dr[sig];
+        uint32_t lo = 0, hi = 0;
+        if (dr.x != 0.f) {
+          const uint64_t s2 = ((uint64_t)__float_as_uint(dr.y) << 32) | __float_as_uint(dr.y);
+          lo = bf16x8_mul_e2m1(v[i][0], s2);
+          hi = bf16x8_mul_e2m1(v[i][1], s2);
+        }
+        *reinterpret_cast<uint2*>(tdst + kt * 2048) = make_uint2(lo, hi);
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 3);
+        if ((b & 3) == 0)
+          *reinterpret_cast<uint4*>(sdst + kt * 1024) = make_uint4(sig | (s1 << 8) | (s2 << 16) | (s3 << 24), 0, 0, 0);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 32 * kDecQuantWarps);
+        if (qt == 0) {
+          mbar_arrive(&xready[kt]);
+          for (int c = 0; c < C; ++c) {
+            if (c == rank) continue;
+            const uint32_t bar = cluster_addr(&xready[kt], (uint32_t)c);
+            bulk_copy_to_cta(cluster_addr(tok + kt * 2048, (uint32_t)c), tok + kt * 2048, 2048u, bar);
+            bulk_copy_to_cta(cluster_addr(tsf + kt * 1024, (uint32_t)c), tsf + kt * 1024, 1024u, bar);
+          }
+        }
+      }
+    }
+
+    // compensation residual R[m, s] of channel chan[s], divided by g (the
+    // pre-scaled form), for the owned 64-slot tiles ct = rank, rank + C, ...:
+    // 16 rows x 64 slots each, zero past M and past k
+    if (n_ct > 0) {
+      for (int ct = rank; ct < n_ct; ct += C) {
+        uint4 rv[4][2];
+        int js[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = q * 256 + qt;
+          const int mr = e >> 6, s = ct * 64 + (e & 63);
+          int jc = -1;
+          if (mr < p.M && s < p.k) jc = p.chan[s];
+          if (jc < 0 || (int64_t)jc >= p.K) jc = -1;  // a malformed list gives zero residuals
+          js[q] = jc;
+          rv[q][0] = make_uint4(0, 0, 0, 0);
+          rv[q][1] = make_uint4(0, 0, 0, 0);
+          if (jc >= 0) ldg_stream32(p.x + (int64_t)mr * p.ldx + (jc & ~15), rv[q][0], rv[q][1]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = q * 256 + qt;
+          const int mr = e >> 6, sc = e & 63;
+          __nv_bfloat16 val = __float2bfloat16_rn(0.f);
+          if (js[q] >= 0) {
+            const float am = absmax_of(absmax8(absmax8(rv[q][0].x, rv[q][0]), rv[q][1]));
+            const float2 dr = s_dr[block_scale_byte(am, g, yg, fast)];
+            const int w = js[q] & 15;
+            const uint32_t word = block_word(rv[q][0], rv[q][1], w >> 1);
+            const float xv = __uint_as_float((w & 1) ? (word & 0xFFFF0000u) : (word << 16));
+            val = element_residual(xv, dr.x, dr.y, yg);
+          }
+          *reinterpret_cast<__nv_bfloat16*>(res + ct * 2048 + (mr >> 3) * 1024 + (mr & 7) * 128 +
+                                            (((sc >> 3) ^ (mr & 7)) << 4) + (sc & 7) * 2) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 32 * kDecQuantWarps);
+      if (qt == 0) {
+        mbar_arrive(rready);
+        for (int ct = rank; ct < n_ct; ct += C)
+          for (int c = 0; c < C; ++c)
+            if (c != rank)
+              bulk_copy_to_cta(cluster_addr(res + ct * 2048, (uint32_t)c), res + ct * 2048, 2048u,
+                               cluster_addr(rready, (uint32_t)c));
+      }
+    }
+
+    if (warp == 6 && lane == 0) {
+      // every copy into this CTA has landed (so every copy this cluster issued
+      // has completed once all its CTAs pass the closing cluster barrier)
+      for (int i = 0; i < n_kt; ++i) mbar_wait(&xready[i], 0, kWaitXReady, s_abort);
+      if (n_ct > 0) mbar_wait(rready, 0, kWaitRReady, s_abort);
+      if (p.g_in == nullptr) mbar_wait(amax_bar, 0, kWaitXReady, s_abort);
+    }
+
+    if (warp < 6) {
+      // -------------------------------------------------- epilogue ----
+      // warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31: lane r =
+      // output column n0 + r, column i = token row i
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      const float gb = p.g_b ? *p.g_b : 1.f;
+      const float alpha = g * gb;
+      const float beta = (p.flags == 1 ? 1.f : gb) * g;  // the residual came divided by g
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int n0 = t * BN;
+        if (!mbar_wait(&acc_full[acc], acc_phase, kWaitAccFull, s_abort)) break;
+        tc_fence_after();
+        const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + 32u * (uint32_t)acc;
+        uint32_t va[16], wc[16];
+        tmem_ld_32x32b_x16(t_acc, va);
+        if (n_ct > 0) tmem_ld_32x32b_x16(t_acc + 16u, wc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < kDecRows; ++i) {
+          float yv = alpha * __uint_as_float(va[i]);
+          if (n_ct > 0) yv = fmaf(beta, __uint_as_float(wc[i]), yv);
+          if (i < p.M) p.y[(int64_t)i * p.N + n0 + r] = __float2bfloat16_rn(yv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp < 2) cluster_wait();  // the quantizing warps waited for this phase before their copies
+  // no CTA leaves while another CTA of the cluster may still write into its
+  // shared memory or arrive on its barriers
+  cluster_barrier();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------- host side ---
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1881,8 +2361,8 @@ int narrow_split(int64_t M, int64_t N, int64_t K, int num_sms) {
 // the preceding kernel of the stream (normally the activation quantizer,
 // which releases its dependents as it starts) is still running; the kernel
 // itself decides what may run before griddepcontrol.wait (GemmParams::early_w).
-template <typename Kern>
-cudaError_t launch_dependent(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream, const GemmParams& p) {
+template <typename Kern, typename Params>
+cudaError_t launch_dependent(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream, const Params& p) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
@@ -1982,6 +2462,119 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
   return cudaGetLastError();
 }
 
+
+// Clusters of the decode kernel that fit on the device at once (at the
+// largest shared-memory plan; one CTA per SM), per device.
+int decode_clusters(int num_sms) {
+  static int cached[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::call_once(once[dev], [dev, num_sms] {
+    int n = 0;
+    const int smem = 227 * 1024;
+    if (cudaFuncSetAttribute(w4a4_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3((unsigned)(num_sms / kDecCluster * kDecCluster));
+      cfg.blockDim = dim3(kDecThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kDecCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, w4a4_decode_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cached[dev] = n;
+  });
+  return cached[dev];
+}
+
+// Shared-memory plan of the decode layer: the ring takes what the resident
+// token data leaves of the 227 KB a CTA may use, up to the TMEM's 14 scale
+// slots.  Returns the stage count (0: the data does not leave 3 stages).
+int decode_plan(int64_t K, int k, DecodeParams* p, size_t* smem_bytes) {
+  const int n_kt = (int)((K + 255) / 256), n_ct = (k + 63) / 64;
+  const size_t tok = 2048u * (size_t)n_kt, res = 2048u * (size_t)n_ct, tsf = 1024u * (size_t)n_kt + 256u,
+               dr = 256u * sizeof(float2);
+  const size_t bars = 8u * (2u * kDecMaxStages + 7u + (size_t)n_kt) + 8u + 4u * kDecQuantWarps + 16u + 16u * 8u;
+  const size_t resident = tok + res + tsf + dr + bars;
+  const size_t budget = 227u * 1024u - 1024u;  // minus the 1024-byte alignment slack
+  if (resident + 3u * kDecStageBytes > budget) return 0;
+  size_t stages = (budget - resident) / kDecStageBytes;
+  if (stages > (size_t)kDecMaxStages) stages = kDecMaxStages;
+  const size_t ring = stages * kDecStageBytes;
+  p->stages = (int)stages;
+  p->off_tok = (uint32_t)ring;
+  p->off_res = (uint32_t)(ring + tok);
+  p->off_tsf = (uint32_t)(ring + tok + res);
+  p->off_dr = (uint32_t)(ring + tok + res + tsf);
+  p->off_bar = (uint32_t)(ring + tok + res + tsf + dr);
+  *smem_bytes = 1024u + ring + resident;
+  return (int)stages;
+}
+
+cudaError_t launch_decode_layer(const DecodeProblem& pr, int num_sms, cudaStream_t stream) {
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (pr.M < 1 || pr.M > kDecRows || pr.N % BN != 0 || pr.K % 64 != 0 || pr.K > 256 * kDecMaxKt ||
+      pr.k > 64 * kDecMaxCt)
+    return cudaErrorInvalidValue;
+  size_t smem = 0;
+  if (decode_plan(pr.K, pr.k, &p, &smem) == 0) return cudaErrorInvalidValue;
+  {
+    const uint64_t d[2] = {(uint64_t)(pr.K / 2), (uint64_t)pr.N};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BN)) return cudaErrorInvalidValue;
+  }
+  if (pr.k > 0) {
+    const uint64_t d[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
+    if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, d, 64, BN)) return cudaErrorInvalidValue;
+  }
+  p.x = pr.x;
+  p.ldx = pr.ldx;
+  p.M = (int)pr.M;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.k = pr.k;
+  p.chan = pr.chan;
+  p.b_sf = pr.b_scales;
+  p.g_in = pr.g_in;
+  p.g_out = pr.g_out;
+  p.g_b = pr.g_b;
+  p.y = pr.y;
+  p.flags = pr.flags & kGemmCompBf16;
+  p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
+  // clusters of kDecCluster CTAs (those without an output tile of their own
+  // still quantize their share of X), as many as fit at once
+  const int n_tiles = (int)(pr.N / BN);
+  int clusters = (n_tiles + kDecCluster - 1) / kDecCluster;
+  const int max_clusters = decode_clusters(num_sms);
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  if (clusters > max_clusters) clusters = max_clusters;
+  cudaError_t err = cudaFuncSetAttribute(w4a4_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(kDecCluster * clusters));
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kDecCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  err = cudaLaunchKernelEx(&cfg, w4a4_decode_kernel, p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
 
 // Dynamic shared memory of the wide kernel: stages, barriers, the grouped
 // schedule (offsets, tile starts and padded bases in 4 * (E + 1) ints) and,
@@ -2186,6 +2779,16 @@ cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int split = narrow_split(M, N, K, num_sms);
   return split > 1 ? (size_t)split * (size_t)M * (size_t)N * sizeof(float) : 0;
+}
+
+cudaError_t launch_decode(const DecodeProblem& p, int num_sms, cudaStream_t stream) {
+  return launch_decode_layer(p, num_sms, stream);
+}
+
+int decode_stages(int64_t K, int k) {
+  DecodeParams p;
+  size_t smem = 0;
+  return decode_plan(K, k, &p, &smem);
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream) {

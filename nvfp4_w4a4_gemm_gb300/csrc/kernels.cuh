@@ -101,6 +101,27 @@ struct GemmProblem {
   float* out_f32 = nullptr;
 };
 
+// The whole linear layer for at most 16 tokens in one launch: every CTA
+// quantizes X (dynamic tensor scale, or *g_in) into shared memory with the
+// pre-scaled residual, then runs the swapped-operand GEMM with compensation.
+struct DecodeProblem {
+  const __nv_bfloat16* x = nullptr;
+  int64_t ldx = 0;
+  int64_t M = 0, N = 0, K = 0;
+  int k = 0;
+  const int32_t* chan = nullptr;
+  const uint8_t* b_codes = nullptr;
+  const uint8_t* b_scales = nullptr;
+  const float* g_b = nullptr;
+  const __nv_bfloat16* w_sel = nullptr;
+  const float* g_in = nullptr;
+  float* g_out = nullptr;
+  __nv_bfloat16* y = nullptr;
+  int flags = 0;  // kGemmCompBf16 | kGemmWeightsReady
+};
+cudaError_t launch_decode(const DecodeProblem& p, int num_sms, cudaStream_t stream);
+int decode_stages(int64_t K, int k);  // ring stages of the plan (0: K, k too large)
+
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_grouped_gemm(const GemmProblem& p, int num_sms, cudaStream_t stream);

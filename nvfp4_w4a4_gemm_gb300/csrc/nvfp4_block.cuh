@@ -1,7 +1,8 @@
-// NVFP4 block arithmetic shared by the activation quantizer and the fused
-// epilogues that quantize a GEMM's output (the same fp32 operations in the
-// same order, so both produce the same scale bytes, codes and residuals):
-// the E4M3 block scale of a block maximum under a tensor scale, and the
+// NVFP4 block arithmetic shared by the activation quantizer, the fused
+// epilogues that quantize a GEMM's output and the decode layer that quantizes
+// its tokens in every CTA (the same fp32 operations in the same order, so all
+// produce the same scale bytes, codes and residuals): the block absmax, the
+// E4M3 block scale of a block maximum under a tensor scale, and the
 // compensation residual of one element.
 #pragma once
 #include <cuda_bf16.h>
@@ -14,6 +15,16 @@ namespace nv4 {
 namespace {
 
 constexpr float kRcp6 = 0x1.555556p-3f;  // 1/6 rounded to nearest fp32
+
+// Running per-half magnitude maximum over the 4 packed bf16 pairs of v.
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, const uint4& v) {
+  return bf16x2_absmax(bf16x2_absmax(m, v.x), bf16x2_absmax(bf16x2_absmax(v.y, v.z), v.w));
+}
+
+// Largest magnitude of the two halves of a running magnitude maximum.
+__device__ __forceinline__ float absmax_of(uint32_t m) {
+  return fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
+}
 
 // x / 6 rounded to nearest fp32 for a bf16 value x >= 2^-100: a product with
 // RN(1/6) and one fma correction step (Markstein's division refinement).

@@ -76,6 +76,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Adds `bytes` to the transaction count of the current phase (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -247,6 +251,57 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
   return out;
 }
+__device__ __forceinline__ uint32_t cluster_num_ctas() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+// Stores into the shared memory of any CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_cluster_u16(uint32_t caddr, uint16_t v) {
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(caddr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v2(uint32_t caddr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(caddr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// This thread's generic-proxy writes to the shared memory of any CTA of the
+// cluster become visible to later async-proxy (tensor core) accesses.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+// The same location as cluster address `caddr_own` (this CTA's) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr_of(uint32_t caddr_own, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(caddr_own), "r"(rank));
+  return out;
+}
+// Bulk copy (async proxy) of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from this CTA's shared memory into the shared memory of a CTA of
+// the cluster; the bytes complete on that CTA's mbarrier `bar_caddr`.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_caddr, const void* src, uint32_t bytes,
+                                                 uint32_t bar_caddr) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_caddr),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar_caddr)
+               : "memory");
+}
+// The two halves of cluster_barrier, for threads that have work to do
+// between announcing they are here and needing everyone else to be.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrival with no memory ordering: enough after fence_mbar_init when the
+// barriers' initialization is all the other CTAs need to see.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Every thread of every CTA of the cluster (release / acquire at cluster scope).
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -299,6 +354,10 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* d
       "%4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_caddr), "r"(x), "r"(y)
       : "memory");
+}
+// Barrier `id` (1..15) over the first `n` threads that reach it (whole warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 // Generic-proxy shared-memory writes of this thread become visible to later
 // async-proxy (TMA, tensor core) accesses.

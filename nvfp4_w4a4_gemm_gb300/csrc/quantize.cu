@@ -146,16 +146,6 @@ struct QuantArgs {
   int resid_scaled;         // residual written divided by g (times RN(1/g))
 };
 
-// Running per-half magnitude maximum over the 4 packed words of v.
-__device__ __forceinline__ uint32_t absmax8(uint32_t m, const uint4& v) {
-  return bf16x2_absmax(bf16x2_absmax(m, v.x), bf16x2_absmax(bf16x2_absmax(v.y, v.z), v.w));
-}
-
-// Largest magnitude of the two halves of a running magnitude maximum.
-__device__ __forceinline__ float absmax_of(uint32_t m) {
-  return fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
-}
-
 // Per-thread constants of the block-scale step.
 struct ScaleCtx {
   float g, yg;

@@ -111,6 +111,19 @@ def test_invalid_arguments_rejected_on_host(lib):
                                               0, 0, fake, fake, 257, 0, fake, fake, fake, None, None) == 1
     assert lib.w4a4_grouped_gemm_combine(4, fake, 8, 512, 64, fake, fake, None, fake, fake, None, None, None, 0, 0,
                                          None, fake, 2, fake, None) == 1
+    # one-launch decode layer: 1..16 tokens, N % 128, K % 64 and <= 8192, k <= 256 and % 8, known flags
+    dec = lambda M, N, K, ldx, k, flags, chan=fake, ws=fake: lib.w4a4_decode_linear(
+        M, N, K, fake, ldx, None, None, chan, k, fake, fake, None, ws, flags, fake, None)
+    assert dec(17, 128, 256, 256, 0, 0) == 2
+    assert dec(0, 128, 256, 256, 0, 0) == 1
+    assert dec(4, 100, 256, 256, 0, 0) == 2
+    assert dec(4, 128, 96, 96, 0, 0) == 2
+    assert dec(4, 128, 8448, 8448, 0, 0) == 2
+    assert dec(4, 128, 256, 256, 264, 0) == 2
+    assert dec(4, 128, 256, 256, 12, 0) == 2
+    assert dec(4, 128, 256, 200, 0, 0) == 1
+    assert dec(4, 128, 256, 256, 0, 0x200) == 1
+    assert dec(4, 128, 256, 256, 8, 0, chan=None) == 1
     # quantizer flags: only the pre-scaled-residual bit exists
     assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 2, None, 0, None) == 1
     assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 4, None,
