@@ -1859,16 +1859,17 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
 // (d, 1/d) table of the scale bytes, the cluster's amax partials (16 bytes
 // each, the unit of a bulk copy) and the barriers.
 constexpr int kDecThreads = 320;
-constexpr int kDecRows = 16;                           // tokens per launch (the MMA's N)
-constexpr int kDecMaxKt = 32;                          // K <= 8192
-constexpr int kDecMaxCt = 4;                           // k <= 256
-constexpr int kDecMaxStages = 14;                      // TMEM: 64 + 32 * 14 = 512 columns
-constexpr int kDecStageBytes = kTileBytes + kSfBytes;  // 18 KB
+constexpr int kDecRows = 16;     // tokens per launch (the MMA's N)
+constexpr int kDecMaxKt = 32;    // 256-column k-tiles: K <= 8192
+constexpr int kDecMaxCt = 4;     // k <= 256
+constexpr int kDecSub = 2;       // k-tiles per ring stage (halves the per-stage hand-offs)
+constexpr int kDecStageBytes = kDecSub * (kTileBytes + kSfBytes);  // 36 KB: 2 code tiles, then 8 scale chunks
+constexpr int kDecMaxStages = 7;  // TMEM: 64 + 64 * 7 = 512 columns
 constexpr int kDecQuantWarps = 8;
-constexpr int kDecCluster = 4;     // CTAs sharing the token quantization
-constexpr int kDecGroup = 8;       // owned k-tiles whose blocks a thread holds in registers at once
+constexpr int kDecCluster = 4;   // CTAs sharing the token quantization
+constexpr int kDecGroup = 8;     // owned k-tiles whose blocks a thread holds in registers at once
 constexpr uint32_t kDecColSf = 64;
-static_assert(kDecColSf + 32u * kDecMaxStages <= kTmemCols, "TMEM budget");
+static_assert(kDecColSf + 32u * kDecSub * kDecMaxStages <= kTmemCols, "TMEM budget");
 static_assert(2 + kDecQuantWarps == kDecThreads / 32, "warp roles");
 
 struct DecodeParams {
@@ -1903,9 +1904,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = p.stages;
   const int n_kt = (int)((p.K + 255) / 256);
-  const int n_ct = (p.k + 63) / 64;
-  const int C = (int)cluster_num_ctas();
+  const int n_st = (n_kt + kDecSub - 1) / kDecSub;  // FP4 ring uses per output tile
+  const int n_ct = (p.k + 63) / 64;                  // compensation ring uses per output tile
+  const int n_use = n_st + n_ct;
+  constexpr int C = kDecCluster;  // the launch's cluster size
   const int rank = (int)cta_rank_in_cluster();
+  const int n_grp = (n_kt + C - 1) / C;  // k-tile groups: one k-tile of each CTA of the cluster
   uint8_t* ring = smem;
   uint8_t* tok = smem + p.off_tok;
   uint8_t* res = smem + p.off_res;
@@ -1918,8 +1922,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
   uint64_t* drain = acc_empty + 2;
   uint64_t* amax_bar = drain + 1;
   uint64_t* rready = amax_bar + 1;
-  uint64_t* xready = rready + 1;  // [n_kt]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xready + n_kt);
+  uint64_t* xready = rready + 1;  // [n_grp]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(xready + n_grp);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   float* s_red = reinterpret_cast<float*>(s_tmem + 2);  // [kDecQuantWarps]
   // [C][4]: the amax partials of the cluster's CTAs, 16-byte slots
@@ -1928,53 +1932,94 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int n_tiles = (int)(p.N / BN);
+  const int64_t n_cg = p.K / 64;  // scale chunks per 128-row tile row
   // a following layer may start its prologue and weight stream now; its own
   // wait still covers all of this kernel's writes
   pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+
+  // ring use i of output tile t: FP4 stage i (k-tiles 2i, 2i+1) or W_S tile i - n_st
+  auto issue_use = [&](int stage, int t, int i) {
+    uint8_t* sb = ring + stage * kDecStageBytes;
+    const int n0 = t * BN;
+    if (i < n_st) {
+      const int kt0 = i * kDecSub;
+      const int nsub = (n_kt - kt0) < kDecSub ? (n_kt - kt0) : kDecSub;
+      const int64_t cg0 = (int64_t)kt0 * 4;
+      const uint32_t sfb = (uint32_t)((n_cg - cg0) < 4 * kDecSub ? (n_cg - cg0) : 4 * kDecSub) * 512u;
+      mbar_arrive_expect_tx(&full[stage], (uint32_t)nsub * kTileBytes + sfb);
+      for (int s = 0; s < nsub; ++s) tma_load_2d(sb + s * kTileBytes, &p.tm_b, &full[stage], (kt0 + s) * BKB, n0);
+      bulk_load(sb + kDecSub * kTileBytes, p.b_sf + ((uint64_t)t * n_cg + cg0) * 512u, sfb, &full[stage]);
+    } else {
+      mbar_arrive_expect_tx(&full[stage], kTileBytes);
+      tma_load_2d(sb, &p.tm_w, &full[stage], (i - n_st) * 64, n0);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+  };
+
+  // the quantizing threads' blocks of X: loaded before the setup barrier so
+  // their latency overlaps it
+  const int qt = threadIdx.x - 64;
+  const int m = qt >> 4, b = qt & 15;
+  const bool row_ok = warp >= 2 && m < p.M;
+  const int n_own = rank < n_kt ? (n_kt - rank + C - 1) / C : 0;  // k-tiles rank, rank + C, ...
+  const int n_groups = (n_own + kDecGroup - 1) / kDecGroup;
+  const __nv_bfloat16* xrow = p.x + (int64_t)(row_ok ? m : 0) * p.ldx;
+  uint4 v[kDecGroup][2];
+  auto load_group = [&](int g) {
+#pragma unroll
+    for (int i = 0; i < kDecGroup; ++i) {
+      const int j = g * kDecGroup + i;
+      const int64_t col = (int64_t)(rank + j * C) * 256 + b * 16;
+      v[i][0] = make_uint4(0, 0, 0, 0);
+      v[i][1] = make_uint4(0, 0, 0, 0);
+      if (row_ok && j < n_own && col < p.K) ldg_stream32(xrow + col, v[i][0], v[i][1]);
     }
-    mbar_init(drain, 1);
-    // token data barriers: one local arrival (this CTA's own part, or the
-    // arrival made here with the bytes expected from the owner's bulk copies)
-    mbar_init(amax_bar, 1);
-    mbar_arrive_expect_tx(amax_bar, 16u * (uint32_t)(C - 1));  // the other CTAs' amax partials
-    mbar_init(rready, 1);
-    uint32_t res_in = 0;
-    for (int ct = 0; ct < n_ct; ++ct) res_in += (ct % C != rank) ? 2048u : 0u;
-    if (res_in > 0) mbar_expect_tx(rready, res_in);
-    for (int i = 0; i < n_kt; ++i) {
-      mbar_init(&xready[i], 1);
-      if (i % C != rank) mbar_arrive_expect_tx(&xready[i], 3072u);  // codes 2 KB + scales 1 KB
-    }
-    *s_abort = 0;
-    fence_mbar_init();
-  }
-  if (threadIdx.x < 16) reinterpret_cast<uint4*>(tsf + 1024 * n_kt)[threadIdx.x] = make_uint4(0, 0, 0, 0);
-  if (warp == 1) {
-    tmem_alloc(s_tmem, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  // this CTA's barriers exist (fence_mbar_init published them to the
-  // cluster): the others may send to it once they have waited for this
-  // arrival (the quantizing warps wait before their first copy)
-  cluster_arrive_relaxed();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-  const int n_tiles = (int)(p.N / BN);
-  const int64_t n_cg = p.K / 64;  // weight scale chunks per 128-row tile row
-  // ring order per output tile: the FP4 k-tiles, then the compensation k-tiles
-  const int n_use = n_kt + n_ct;
+  };
 
   if (warp == 0) {
+    // barrier setup spread over the warp's lanes (a lone lane's serial
+    // initialization measured about 1.3 us)
+    if (lane < S) {
+      mbar_init(&full[lane], 1);
+      mbar_init(&empty[lane], 1);
+    }
+    if (lane < 2) {
+      mbar_init(&acc_full[lane], 1);
+      mbar_init(&acc_empty[lane], 4);
+    }
+    // token data barriers: one local arrival (after this CTA's own part, or
+    // made here) plus the bytes of the other CTAs' bulk copies
+    if (lane == 2) mbar_init(drain, 1);
+    if (lane == 3) {
+      mbar_init(amax_bar, 1);
+      mbar_arrive_expect_tx(amax_bar, 16u * (uint32_t)(C - 1));  // the other CTAs' amax partials
+    }
+    if (lane == 4) {
+      mbar_init(rready, 1);
+      const int own_ct = rank < n_ct ? (n_ct - 1 - rank) / C + 1 : 0;
+      if (n_ct > own_ct) mbar_expect_tx(rready, 2048u * (uint32_t)(n_ct - own_ct));
+    }
+    if (lane == 5) *s_abort = 0;
+    if (lane < n_grp) {
+      const int g = lane;
+      const int in_grp = (n_kt - g * C) < C ? (n_kt - g * C) : C;
+      const bool owns = g * C + rank < n_kt;
+      const uint32_t bytes = 3072u * (uint32_t)(in_grp - (owns ? 1 : 0));  // codes 2 KB + scales 1 KB each
+      mbar_init(&xready[g], 1);
+      if (owns) {
+        if (bytes > 0) mbar_expect_tx(&xready[g], bytes);
+      } else {
+        mbar_arrive_expect_tx(&xready[g], bytes);  // no k-tile of this CTA in the group
+      }
+    }
+    fence_mbar_init();
+    __syncwarp();
+    // the barriers exist: the other warps may go (the producer does not wait
+    // for them), and so may the other CTAs of the cluster once they have
+    // waited for this CTA's arrival (the quantizing warps wait before their
+    // first copy)
+    named_bar_arrive(2, kDecThreads);
+    cluster_arrive_relaxed();
     // ------------------------------------------------------ producer ----
     // the whole warp runs the loop, one elected lane issues (a loop run by a
     // lone lane while the rest of the warp waits measured about 1.7x slower
@@ -1989,29 +2034,34 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
     uint32_t phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const int n0 = t * BN;
       for (int i = 0; i < n_use; ++i) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
-        if (elect_one()) {
-          uint8_t* sb = ring + stage * kDecStageBytes;
-          if (i < n_kt) {
-            const int64_t cg0 = (int64_t)i * 4;
-            const uint32_t sfb = (uint32_t)((n_cg - cg0) < 4 ? (n_cg - cg0) : 4) * 512u;
-            mbar_arrive_expect_tx(&full[stage], kTileBytes + sfb);
-            tma_load_2d(sb, &p.tm_b, &full[stage], i * BKB, n0);
-            bulk_load(sb + kTileBytes, p.b_sf + ((uint64_t)t * n_cg + cg0) * 512u, sfb, &full[stage]);
-          } else {
-            mbar_arrive_expect_tx(&full[stage], kTileBytes);
-            tma_load_2d(sb, &p.tm_w, &full[stage], (i - n_kt) * 64, n0);
-          }
-        }
+        if (elect_one()) issue_use(stage, t, i);
         __syncwarp();
         ++armed;
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok) land_armed_copies(full, S, armed);
-  } else if (warp == 1) {
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  } else if (warp >= 2) {
+    pdl_wait();  // X (and a static tensor scale) may come from the preceding kernel
+    if (n_groups > 0) load_group(0);  // in flight across the setup barrier
+    if (qt < 16) reinterpret_cast<uint4*>(tsf + 1024 * n_kt)[qt] = make_uint4(0, 0, 0, 0);  // rows 16..31 of the last chunk
+  }
+  uint32_t tmem = 0;
+  if (warp >= 1) {
+    tc_fence_before();
+    named_bar_sync(2, kDecThreads);
+    cluster_arrive_relaxed();
+    tc_fence_after();
+    tmem = *s_tmem;
+  }
+
+  if (warp == 1) {
     // ---------------------------------------- scale copies and MMAs ----
     // a k-tile's copies go out from the elected lane right before its MMAs
     // (the tensor core runs them in issue order), so no other warp hands
@@ -2021,49 +2071,64 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
     bool ok = true;
     const uint32_t idesc = idesc_fp4_swap(0, 0, kDecRows), idesc_c = idesc_bf16_swap(kDecRows);
     const uint32_t ring_s = smem_u32(ring), tok_s = smem_u32(tok), tsf_s = smem_u32(tsf), res_s = smem_u32(res);
-    const bool full_kt = (p.K & 255) == 0;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const bool first = t == (int)blockIdx.x;  // the token data barriers complete during the first tile
       if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_acc = tmem + 32u * (uint32_t)acc;
+      int grp_seen = -1;
       for (int i = 0; i < n_use; ++i) {
-        if (first && i < n_kt && !mbar_wait_warp(&xready[i], 0, kWaitXReady, s_abort)) { ok = false; break; }
-        if (first && i == n_kt && !mbar_wait_warp(rready, 0, kWaitRReady, s_abort)) { ok = false; break; }
+        const int kt0 = i * kDecSub;
+        if (first && i < n_st) {
+          const int kt_last = (kt0 + kDecSub < n_kt ? kt0 + kDecSub : n_kt) - 1;
+          for (int g = kt0 / C; g <= kt_last / C; ++g)
+            if (g > grp_seen) {
+              if (!mbar_wait_warp(&xready[g], 0, kWaitXReady, s_abort)) { ok = false; break; }
+              grp_seen = g;
+            }
+          if (!ok) break;
+        }
+        if (first && i == n_st && !mbar_wait_warp(rready, 0, kWaitRReady, s_abort)) { ok = false; break; }
         if (!mbar_wait_warp(&full[stage], phase, kWaitFull, s_abort)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
           const uint32_t sb = ring_s + (uint32_t)stage * (uint32_t)kDecStageBytes;
-          const uint64_t a0 = desc_sw128(sb);  // + 2 per 32 bytes of K
-          if (i < n_kt) {
-            const uint64_t b0 = desc_sw128(tok_s + (uint32_t)i * 2048u);
-            const uint64_t sfa0 = desc_sf(tsf_s + (uint32_t)i * 1024u);  // + 16 per 256-byte token chunk
-            const uint64_t sfb0 = desc_sf(sb + (uint32_t)kTileBytes);     // + 32 per 512-byte weight chunk
-            const uint32_t col_sf = tmem + kDecColSf + 32u * (uint32_t)stage;
-            const uint32_t acc0 = i > 0 ? 1u : 0u;
-            // the slot's previous MMAs completed before the producer refilled this stage
-            if (full_kt || i + 1 < n_kt) {
+          if (i < n_st) {
+            const uint32_t col_st = tmem + kDecColSf + 32u * kDecSub * (uint32_t)stage;
+            const uint64_t sfb0 = desc_sf(sb + (uint32_t)(kDecSub * kTileBytes));  // + 32 per 512-byte weight chunk
+            const int nsub = (n_kt - kt0) < kDecSub ? (n_kt - kt0) : kDecSub;
+            for (int s = 0; s < nsub; ++s) {
+              const int kt = kt0 + s;
+              const uint64_t a0 = desc_sw128(sb + (uint32_t)(s * kTileBytes));  // + 2 per 32 bytes of K
+              const uint64_t b0 = desc_sw128(tok_s + (uint32_t)kt * 2048u);
+              const uint64_t sfa0 = desc_sf(tsf_s + (uint32_t)kt * 1024u);  // + 16 per 256-byte token chunk
+              const uint32_t col_sf = col_st + 32u * (uint32_t)s;
+              const uint32_t acc0 = kt > 0 ? 1u : 0u;
+              // the slot's previous MMAs completed before the producer refilled this stage
+              const int nch = (int)((n_cg - (int64_t)kt * 4) < 4 ? (n_cg - (int64_t)kt * 4) : 4);
+              if (nch == 4) {
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
-                tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * c);
-              }
+                for (int c = 0; c < 4; ++c) {
+                  tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
+                  tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * (uint32_t)(4 * s + c));
+                }
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
-                            j > 0 ? 1u : acc0);
-            } else {
-              const int nch = (int)(n_cg - (int64_t)i * 4);  // the last, partial k-tile
-              for (int c = 0; c < nch; ++c) {
-                tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
-                tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * c);
+                for (int j = 0; j < 4; ++j)
+                  mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
+                              j > 0 ? 1u : acc0);
+              } else {
+                for (int c = 0; c < nch; ++c) {
+                  tmem_cp_32x128b_x4(col_sf + 4u * c, sfa0 + 16u * c);
+                  tmem_cp_32x128b_x4(col_sf + 16u + 4u * c, sfb0 + 32u * (uint32_t)(4 * s + c));
+                }
+                for (int j = 0; j < nch; ++j)
+                  mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
+                              j > 0 ? 1u : acc0);
               }
-              for (int j = 0; j < nch; ++j)
-                mma_nvf4_4x(d_acc, a0 + 2u * j, b0 + 2u * j, idesc, col_sf + 16u + 4u * j, col_sf + 4u * j,
-                            j > 0 ? 1u : acc0);
             }
           } else {
-            const int ct = i - n_kt;
+            const int ct = i - n_st;
+            const uint64_t a0 = desc_sw128(sb);
             const uint64_t r0 = desc_sw128(res_s + (uint32_t)ct * 2048u);
             const int krem = p.k - ct * 64;
             const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
@@ -2085,31 +2150,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     mbar_wait_warp(drain, 0, kWaitDrain, nullptr);
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------ token quantization ----
     // thread qt owns block (row m, 16-column block b) of the k-tiles r, r + C,
     // r + 2C, ... of this CTA's cluster rank r
-    const int qt = threadIdx.x - 64;
     const int qw = qt >> 5;
-    const int m = qt >> 4, b = qt & 15;
-    pdl_wait();  // X (and a static tensor scale) may come from the preceding kernel
     cluster_wait();  // every CTA of the cluster has its barriers set up
-    const bool row_ok = m < p.M;
-    const __nv_bfloat16* xrow = p.x + (int64_t)(row_ok ? m : 0) * p.ldx;
-    const int n_own = rank < n_kt ? (n_kt - rank + C - 1) / C : 0;
-    const int n_groups = (n_own + kDecGroup - 1) / kDecGroup;
-    uint4 v[kDecGroup][2];
-    auto load_group = [&](int g) {
-#pragma unroll
-      for (int i = 0; i < kDecGroup; ++i) {
-        const int j = g * kDecGroup + i;
-        const int64_t col = (int64_t)(rank + j * C) * 256 + b * 16;
-        v[i][0] = make_uint4(0, 0, 0, 0);
-        v[i][1] = make_uint4(0, 0, 0, 0);
-        if (row_ok && j < n_own && col < p.K) ldg_stream32(xrow + col, v[i][0], v[i][1]);
-      }
-    };
-    if (n_groups > 0) load_group(0);
     float g;
     if (p.g_in != nullptr) {
       g = *p.g_in;
@@ -2185,10 +2231,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
         fence_proxy_async_smem();
         named_bar_sync(1, 32 * kDecQuantWarps);
         if (qt == 0) {
-          mbar_arrive(&xready[kt]);
+          const int grp = kt / C;
+          mbar_arrive(&xready[grp]);
           for (int c = 0; c < C; ++c) {
             if (c == rank) continue;
-            const uint32_t bar = cluster_addr(&xready[kt], (uint32_t)c);
+            const uint32_t bar = cluster_addr(&xready[grp], (uint32_t)c);
             bulk_copy_to_cta(cluster_addr(tok + kt * 2048, (uint32_t)c), tok + kt * 2048, 2048u, bar);
             bulk_copy_to_cta(cluster_addr(tsf + kt * 1024, (uint32_t)c), tsf + kt * 1024, 1024u, bar);
           }
@@ -2247,7 +2294,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) w4a4_decode_kernel(const __gri
     if (warp == 6 && lane == 0) {
       // every copy into this CTA has landed (so every copy this cluster issued
       // has completed once all its CTAs pass the closing cluster barrier)
-      for (int i = 0; i < n_kt; ++i) mbar_wait(&xready[i], 0, kWaitXReady, s_abort);
+      for (int i = 0; i < n_grp; ++i) mbar_wait(&xready[i], 0, kWaitXReady, s_abort);
       if (n_ct > 0) mbar_wait(rready, 0, kWaitRReady, s_abort);
       if (p.g_in == nullptr) mbar_wait(amax_bar, 0, kWaitXReady, s_abort);
     }

@@ -355,6 +355,11 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* d
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_caddr), "r"(x), "r"(y)
       : "memory");
 }
+// Arrival on named barrier `id` without waiting (the barrier completes when
+// `n` threads have arrived or synced on it).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Barrier `id` (1..15) over the first `n` threads that reach it (whole warps).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
