@@ -13,27 +13,27 @@
 // FourSight (arXiv 2611.04887) abstract -- the compensated channels stay in
 // BF16 alongside native NVFP4.
 //
-// Design (one persistent CTA per SM, 224 threads):
-//   warp 0      TMA producer: A/B code tiles (128 x 128 B, 128-byte swizzle)
-//               and their block-scale tiles (2 KB bulk copies) into a ring of
-//               smem stages; after the FP4 k-tiles of an output tile it
-//               streams the compensation operands R_S / W_S through the same
-//               ring as 128 x 64 bf16 tiles.
-//   warp 1      allocates TMEM and issues the MMAs from one thread;
-//               completion is signalled with tcgen05.commit on mbarriers.
-//   warp 2      copies each stage's block scales smem -> TMEM (tcgen05.cp)
-//               into that stage's own TMEM slot.  Measured on GB300, a
-//               32x128b.warpx4 copy costs about as much as a 128x128x64 FP4
-//               MMA and copies from a second warp overlap the MMAs, while
-//               copies issued by the MMA thread serialize with them.
-//   warps 3..6  epilogue: tcgen05.ld of the accumulators, the scale-and-add,
-//               bf16 conversion and stores; warp w reads TMEM lanes
-//               32*(w%4) .. 32*(w%4)+31.
-// TMEM (512 columns): two 128-column FP4 accumulators (so the epilogue of
-// one tile overlaps the main loop of the next), one 128-column compensation
-// accumulator, and one 32-column scale-factor slot (A 16 + B 16) per stage.
-// Every mbarrier wait is bounded; a wait that gives up latches an error for
-// nvfp4_check_status and the CTA winds down.
+// Four kernels share one warp-specialized design: persistent CTAs (one per
+// SM), a TMA producer warp filling a ring of shared-memory stages, one
+// elected lane issuing the tcgen05 MMAs with accumulators in TMEM, the block
+// scales copied smem -> TMEM with tcgen05.cp, epilogue warps reading TMEM
+// with tcgen05.ld (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31), and
+// completion signalled with tcgen05.commit on mbarriers.
+//   w4a4_gemm_kernel       128 x 128 tiles, 320 threads (warp 0 TMA, 1 MMA,
+//                          2..5 scale copies, 6..9 epilogue); up to 64 rows it
+//                          swaps the operands (weight rows in the MMA's M
+//                          slot) and may split K across CTAs
+//   w4a4_gemm_wide_kernel  128 x 256 tiles, 384 threads: the grouped (MoE)
+//                          GEMM and its fused SwiGLU-quantize / combine
+//                          epilogues
+//   w4a4_gemm_pair_kernel  256 x 256 tiles on a CTA pair (cta_group::2), 384
+//                          threads: dense GEMMs with more than 256 rows
+//   w4a4_decode_kernel     the whole layer for at most 16 tokens (the token
+//                          quantization in the same launch), 320 threads
+// After the FP4 k-tiles of an output tile the producer streams the
+// compensation operands R_S / W_S through the same ring as 128 x 64 bf16
+// tiles.  Every mbarrier wait is bounded; a wait that gives up latches an
+// error for nvfp4_check_status and the CTA winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -234,12 +234,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// ------------------------------------------------ CTA pairs (cta_group::2) --
+// ------------------------------------- clusters: CTA pairs, shared data --
 // Two CTAs of a 2-CTA cluster run one tcgen05 MMA stream together: the even
 // rank (the leader) issues MMAs, scale copies and commits for both, each CTA
 // keeps its half of the operands in its own shared memory and its half of
-// the accumulator in its own TMEM.  Shared-memory addresses of either CTA are
-// reached through the cluster window (mapa).
+// the accumulator in its own TMEM.  The decode layer's 4-CTA clusters share
+// the quantized tokens with CTA-to-CTA bulk copies.  Shared-memory addresses
+// of any CTA of the cluster are reached through the cluster window (mapa).
 __device__ __forceinline__ uint32_t cta_rank_in_cluster() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -249,36 +250,6 @@ __device__ __forceinline__ uint32_t cta_rank_in_cluster() {
 __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
-  return out;
-}
-__device__ __forceinline__ uint32_t cluster_num_ctas() {
-  uint32_t n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-// Stores into the shared memory of any CTA of the cluster (cluster address).
-__device__ __forceinline__ void st_cluster_u16(uint32_t caddr, uint16_t v) {
-  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(caddr), "h"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v2(uint32_t caddr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(caddr), "r"(a), "r"(b) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-// This thread's generic-proxy writes to the shared memory of any CTA of the
-// cluster become visible to later async-proxy (tensor core) accesses.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-// The same location as cluster address `caddr_own` (this CTA's) in CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr_of(uint32_t caddr_own, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(caddr_own), "r"(rank));
   return out;
 }
 // Bulk copy (async proxy) of `bytes` (a multiple of 16, both addresses 16-byte
@@ -291,12 +262,9 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_caddr, const void*
                "r"(smem_u32(src)), "r"(bytes), "r"(bar_caddr)
                : "memory");
 }
-// The two halves of cluster_barrier, for threads that have work to do
-// between announcing they are here and needing everyone else to be.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-// Arrival with no memory ordering: enough after fence_mbar_init when the
+// The two halves of a cluster barrier, for threads that have work to do
+// between announcing they are here and needing everyone else to be.  The
+// arrival has no memory ordering: enough after fence_mbar_init when the
 // barriers' initialization is all the other CTAs need to see.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
