@@ -1783,7 +1783,9 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_l);  // accumulator free: the next tile's MMAs may start
+      // accumulator free: the next tile's MMAs may start (a cluster-scope
+      // release here would first wait for the previous tile's Y stores)
+      if (lane == 0) mbar_arrive_cluster_cta(acc_empty_l);
       const int64_t row = (mt * 2 + rank) * BM + r;
       const int64_t col0 = nt * BNP + h * 128;
       if (row < p.M && col0 < p.N) {

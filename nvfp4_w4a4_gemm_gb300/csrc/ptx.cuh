@@ -278,6 +278,13 @@ __device__ __forceinline__ void cluster_barrier() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+// The same arrival with release at CTA scope only: it does not wait for the
+// thread's earlier global stores to become visible to the cluster.  Enough
+// when what the arrival hands over is TMEM this thread has finished reading
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync).
+__device__ __forceinline__ void mbar_arrive_cluster_cta(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
 // try_wait with acquire at cluster scope: for barriers that other CTAs of
 // the cluster arrive on (their writes before the arrival become visible).
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
