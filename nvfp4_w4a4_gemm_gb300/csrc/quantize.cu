@@ -293,6 +293,7 @@ struct QTables {
   const int32_t* off;    // grouped: offsets [E+1]
   const int32_t* pbase;  // grouped: first padded scale row of each expert [E]
   const uint16_t* pref;  // per-expert prefix counts of the channel bitmaps [E][n_words]
+  __nv_bfloat16* unit;   // this warp's 1024-column shared slice (the unit's elements for its residual slots)
   int n_words;
 };
 
@@ -311,8 +312,9 @@ __device__ __forceinline__ void load_unit_t(const QuantArgs& a, uint32_t r, uint
 
 // Quantize the two blocks of unit (r, gi) held in v, then the unit's
 // compensation residuals: the slots [rb, re) of the row's sorted channel list
-// that fall in the unit's columns, one slot per lane (the element is re-read,
-// from L2, and its block's scale byte fetched from the owning lane).
+// that fall in the unit's columns, one slot per lane (the element is read
+// back from the warp's shared slice, where the lanes put the unit's elements
+// first, and its block's scale byte fetched from the owning lane).
 template <bool kGrouped, bool kFull>
 __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v)[4], uint32_t r, uint32_t gi,
                                              int lane, const ScaleCtx& sc, const QTables& t, int64_t n_cg) {
@@ -362,7 +364,17 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
       re += __popc(__ballot_sync(0xffffffffu, v < (int32_t)(col0 + cols)));
     }
   }
-  const __nv_bfloat16* xrow = a.x + (int64_t)r * a.ldx;
+  if (re <= rb) return;  // warp-uniform: no slot in this unit
+  __nv_bfloat16* u = t.unit;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (kFull || h * 512 + lane * 16 < cols) {
+      uint4* dst = reinterpret_cast<uint4*>(u + h * 512 + lane * 16);
+      dst[0] = v[2 * h];
+      dst[1] = v[2 * h + 1];
+    }
+  }
+  __syncwarp();
   __nv_bfloat16* rrow = a.resid + (int64_t)r * a.k;
   for (int base = rb; base < re; base += 32) {  // warp-uniform
     const int i = base + lane;
@@ -376,11 +388,12 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
       __nv_bfloat16 val = __float2bfloat16_rn(0.f);
       if (in) {
         const float2 dr = sc.dr[blk >= 32 ? s1 : s0];
-        val = element_residual(__bfloat162float(xrow[j]), dr.x, dr.y, sc.rs);
+        val = element_residual(__bfloat162float(u[j - col0]), dr.x, dr.y, sc.rs);
       }
       rrow[i] = val;
     }
   }
+  __syncwarp();  // the slice is read before the warp's next unit overwrites it
 }
 
 template <bool kGrouped, bool kFused, bool kFull>
@@ -388,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
   extern __shared__ __align__(16) int32_t smem_i32[];
   __shared__ float2 s_dr[256];
+  __shared__ __align__(16) __nv_bfloat16 s_unit[kThreads / 32][1024];
   // offsets [E+1] | padded bases [E] | dense only: bitmap words [n_words] |
   // prefix counts [n_words] (uint16)
   const int n_words = (int)((a.K + 31) / 32);
@@ -539,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   const int64_t n_cg = (a.K / 16 + 3) / 4;
   QTables t;
   t.off = s_off; t.pbase = s_pbase; t.pref = s_pref;
+  t.unit = s_unit[threadIdx.x >> 5];
   t.n_words = n_words;
   const uint32_t n = walk.n_units;
   while (wa.u < n) {
@@ -1137,7 +1152,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
       {{(const void*)nvfp4_quant_kernel<true, false, false>, (const void*)nvfp4_quant_kernel<true, false, true>},
        {(const void*)nvfp4_quant_kernel<true, true, false>, (const void*)nvfp4_quant_kernel<true, true, true>}}};
   const void* kern = kerns[offsets != nullptr][fused][full];
-  if (smem > 48 * 1024) {
+  if (smem > 24 * 1024) {  // with the 18 KB of static unit slices, above the default 48 KB per block
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
