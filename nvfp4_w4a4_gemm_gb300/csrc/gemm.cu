@@ -769,29 +769,41 @@ __device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile
   }
   const uint32_t t_g = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(64 * hh);
   uint32_t scale_word = 0;
+  // the projection's bf16 outputs, packed two per register as they come out
+  // of TMEM (16 gate and 16 up columns per round), so that the accumulator is
+  // released before any of the SwiGLU and quantize arithmetic
+  uint32_t pg[4][8], pu[4][8];  // [16-column block][pair]
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t vg[16], vu[16];
+    tmem_ld_32x32b_x16(t_g + (uint32_t)(16 * c), vg);
+    tmem_ld_32x32b_x16(t_g + 128u + (uint32_t)(16 * c), vu);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162 g2 = __floats2bfloat162_rn(alpha * __uint_as_float(vg[2 * i]),
+                                                      alpha * __uint_as_float(vg[2 * i + 1]));
+      const __nv_bfloat162 u2 = __floats2bfloat162_rn(alpha * __uint_as_float(vu[2 * i]),
+                                                      alpha * __uint_as_float(vu[2 * i + 1]));
+      pg[c][i] = *reinterpret_cast<const uint32_t*>(&g2);
+      pu[c][i] = *reinterpret_cast<const uint32_t*>(&u2);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(acc_empty);  // accumulator free: the next tile's MMAs may start
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
-    uint32_t vg[2][16], vu[2][16];
-    tmem_ld_32x32b_x16(t_g + (uint32_t)(32 * b), vg[0]);
-    tmem_ld_32x32b_x16(t_g + (uint32_t)(32 * b + 16), vg[1]);
-    tmem_ld_32x32b_x16(t_g + 128u + (uint32_t)(32 * b), vu[0]);
-    tmem_ld_32x32b_x16(t_g + 128u + (uint32_t)(32 * b + 16), vu[1]);
-    tmem_ld_wait();
-    if (b == 1) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);  // accumulator free: the next tile's MMAs may start
-    }
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
+      const int c = 2 * b + blk;
       float hv[16];
       float am = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        // the projection's bf16 outputs, then h rounded to bf16
-        const float2 yg = bf16r2(alpha * __uint_as_float(vg[blk][i]), alpha * __uint_as_float(vg[blk][i + 1]));
-        const float2 yu = bf16r2(alpha * __uint_as_float(vu[blk][i]), alpha * __uint_as_float(vu[blk][i + 1]));
-        const float2 hh2 = bf16r2(swiglu_f32(yg.x, yu.x), swiglu_f32(yg.y, yu.y));
+        const uint32_t wg = pg[c][i / 2], wu = pu[c][i / 2];
+        const float2 hh2 = bf16r2(swiglu_f32(__uint_as_float(wg << 16), __uint_as_float(wu << 16)),
+                                  swiglu_f32(__uint_as_float(wg & 0xFFFF0000u), __uint_as_float(wu & 0xFFFF0000u)));
         hv[i] = hh2.x;
         hv[i + 1] = hh2.y;
         am = fmaxf(am, fmaxf(fabsf(hh2.x), fabsf(hh2.y)));
