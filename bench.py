@@ -502,9 +502,13 @@ def other_workloads(nv, pk, steps=10):
     E = s.experts
     res = {}
     tot_ms, tot_flops, tot_bytes = 0.0, 0.0, 0
+    tok_rows = dm["token_of_row"].to(torch.int32).to(dev)
     for which, xk, wk in (("gate_up", "x_gate_up", "wt_gate_up"), ("down", "x_down", "wt_down")):
         xg = dm[xk].to(dev)
         K = xg.shape[1]
+        # gate/up reads its routed rows straight from the token rows; the
+        # down input is per routed row already
+        x_in = dm["x_tokens"].to(dev) if which == "gate_up" else xg
         # per-expert channel sets by residual variance on the calibration
         # batch's rows routed to each expert
         chan = nv.nvfp4_calibrate_channels(dc[xk].to(dev), s.k, offsets=dc["offsets"].to(dev))
@@ -518,24 +522,29 @@ def other_workloads(nv, pk, steps=10):
         w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan, E=E)
         yg = torch.empty((xg.shape[0], N), dtype=torch.bfloat16, device=dev)
 
+        def quantize_x():
+            if which == "gate_up":
+                return nv.nvfp4_quantize_grouped_gather(x_in, tok_rows, offs, chan, resid_scaled=True)
+            return nv.nvfp4_quantize_grouped(xg, offs, chan, resid_scaled=True)
+
         def moe():
-            qx = nv.nvfp4_quantize_grouped(xg, offs, chan, resid_scaled=True)
+            qx = quantize_x()
             nv.w4a4_grouped_gemm_comp(qx, offs, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel, y=yg,
                                       weights_ready=True)
         ms = _time_steps(moe, steps, flush)
-        qfix = nv.nvfp4_quantize_grouped(xg, offs, chan, resid_scaled=True)
+        qfix = quantize_x()
 
         def moe_gemm():
             nv.w4a4_grouped_gemm_comp(qfix, offs, b_codes, b_scales, g_b, N, resid=qfix["resid"], w_sel=w_sel,
                                       y=yg, weights_ready=True)
         ms_g = _time_steps(moe_gemm, steps, flush)
         flops = 2.0 * xg.shape[0] * N * K
-        byts = (b_codes.numel() + b_scales.numel() + w_sel.numel() * 2 + xg.numel() * 2 + yg.numel() * 2)
+        byts = (b_codes.numel() + b_scales.numel() + w_sel.numel() * 2 + x_in.numel() * 2 + yg.numel() * 2)
         res[which] = {"ms_per_step": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
                       "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "gemm_alone_ms": round(ms_g, 4),
                       "quantize_ms": round(ms - ms_g, 4)}
         tot_ms += ms; tot_flops += flops; tot_bytes += byts
-        del xg, b_codes, b_scales, g_b, w_sel, yg
+        del xg, x_in, b_codes, b_scales, g_b, w_sel, yg
     out["moe"] = {"shape": "4096 tokens x top-8 of 128 experts, hidden 2048, gate/up 1536, down 2048, k=32/expert",
                   "ms_per_step": round(tot_ms, 4), "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 1),
                   "frac_fp4_peak": round(tot_flops / (tot_ms * 1e-3) / 1e12 / fp4_peak, 4),
@@ -547,9 +556,10 @@ def other_workloads(nv, pk, steps=10):
                   "attainable_tflops": round(min(fp4_peak, tot_flops / tot_bytes * pk["hbm_gbs"] / 1e3), 1),
                   "frac_attainable": round((tot_flops / (tot_ms * 1e-3) / 1e12)
                                            / min(fp4_peak, tot_flops / tot_bytes * pk["hbm_gbs"] / 1e3), 4),
-                  "note": "each projection: grouped dynamic-scale quantize + grouped GEMM with compensation; "
-                          "channel sets calibrated per expert (residual variance on the calibration batch's "
-                          "rows routed to that expert)"}
+                  "note": "each projection: grouped dynamic-scale quantize + grouped GEMM with compensation "
+                          "(gate/up quantizes its routed rows straight from the 4096 token rows through the "
+                          "routing table, so x bytes = the token rows); channel sets calibrated per expert "
+                          "(residual variance on the calibration batch's rows routed to that expert)"}
     out["moe"]["fused_layer"] = moe_fused_layer(nv, pk, flush, steps)
     del dm
 
@@ -620,7 +630,8 @@ def moe_fused_layer(nv, pk, flush, steps):
     dc = W.moe_inputs(calibration=True, with_weights=False)
     E, inter, hidden = s.experts, s.inter, s.hidden
     offs = d["offsets"].to(dev)
-    x = d["x_gate_up"].to(dev)
+    x = d["x_tokens"].to(dev)
+    rows = d["x_gate_up"].shape[0]
     chan = nv.nvfp4_calibrate_channels(dc["x_gate_up"].to(dev), s.k, offsets=dc["offsets"].to(dev))
     h_chan = nv.nvfp4_calibrate_channels(dc["x_down"].to(dev), s.k, offsets=dc["offsets"].to(dev))
 
@@ -643,7 +654,7 @@ def moe_fused_layer(nv, pk, flush, steps):
     out = torch.empty((s.tokens, hidden), dtype=torch.float32, device=dev)
 
     def layer():
-        qx = nv.nvfp4_quantize_grouped(x, offs, chan, resid_scaled=True)
+        qx = nv.nvfp4_quantize_grouped_gather(x, tok, offs, chan, resid_scaled=True)
         qh = nv.w4a4_grouped_gemm_swiglu_quant(qx, offs, gu_codes, gu_scales, gu_g, 2 * inter, g_h, h_chan,
                                                resid=qx["resid"], w_sel=gu_sel, h_resid_scaled=True,
                                                weights_ready=True)
@@ -651,7 +662,6 @@ def moe_fused_layer(nv, pk, flush, steps):
         nv.w4a4_grouped_gemm_combine(qh, offs, dn_codes, dn_scales, dn_g, hidden, tok, w_row, s.tokens,
                                      resid=qh["resid"], w_sel=dn_sel, out=out, weights_ready=True)
     ms = _time_steps(layer, steps, flush)
-    rows = x.shape[0]
     flops = 2.0 * rows * (2 * inter) * hidden + 2.0 * rows * hidden * inter
     byts = (gu_codes.numel() + gu_scales.numel() + gu_sel.numel() * 2 + dn_codes.numel() + dn_scales.numel()
             + dn_sel.numel() * 2 + x.numel() * 2 + out.numel() * 4)
@@ -661,7 +671,8 @@ def moe_fused_layer(nv, pk, flush, steps):
     return {"ms_per_step": round(ms, 4), "tflops": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4),
             "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "bytes_per_step": byts,
             "attainable_tflops": round(att, 1), "frac_attainable": round(tf / att, 4),
-            "note": "one step = the whole FFN on 32768 routed rows: grouped dynamic-scale quantize of x; gate/up "
+            "note": "one step = the whole FFN on 32768 routed rows: grouped dynamic-scale quantize of the routed "
+                    "rows read from the 4096 token rows x through the routing table; gate/up "
                     "GEMM with SwiGLU + static-scale NVFP4 quantize of h (with its residual slice) in the "
                     "epilogue; zeroing of the fp32 output; down GEMM with the routing-weighted combine into "
                     "token rows in the epilogue (fp32 vector atomics). Bytes = weights + compensation columns + x "

@@ -169,6 +169,28 @@ int nvfp4_quantize_grouped_ex(const uint16_t* x, int64_t M_total, int64_t K, int
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * nvfp4_quantize_grouped_gather -- nvfp4_quantize_grouped_ex of the routed
+ * operand x[token_of_row[r], :] (r < M_total), read straight from the token
+ * rows: the expert-sorted copy of the tokens (top_k times their bytes) is
+ * never written.  Results are bit-identical to nvfp4_quantize_grouped_ex on
+ * the gathered rows: the dynamic tensor scale is the amax over the routed
+ * rows, codes / scales / resid are indexed by routed row r.
+ * Source: as nvfp4_quantize_grouped; the gather is this library's operand
+ * form (an MoE layer's expert inputs are its tokens, each routed to top_k
+ * experts).
+ * x             device bf16 [T, K], row stride ldx (16-byte aligned)
+ * token_of_row  device int32 [M_total], each in [0, T); an index outside
+ *               reads token row 0 and latches NVFP4_ERR_INVALID_ARG for
+ *               nvfp4_check_status
+ * Other arguments and errors as nvfp4_quantize_grouped_ex; T <= 2^31 - 1,
+ * T >= 1 when M_total > 0.
+ */
+int nvfp4_quantize_grouped_gather(const uint16_t* x, int64_t T, const int32_t* token_of_row, int64_t M_total,
+                                  int64_t K, int64_t ldx, int32_t E, const int32_t* offsets, const float* g_in,
+                                  float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k,
+                                  uint16_t* resid, int flags, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * nvfp4_quantize_noalloc -- nvfp4_quantize with the dynamic tensor scale,
  * for callers that cannot allocate device memory: code running where
  * cudaMalloc is off limits (an engine that owns all device memory through

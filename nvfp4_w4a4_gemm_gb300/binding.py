@@ -45,6 +45,8 @@ _SIGS = {
                           ctypes.c_int),
     "nvfp4_quantize_grouped_ex": ([_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, ctypes.c_int, _P,
                                    _SZ, _P], ctypes.c_int),
+    "nvfp4_quantize_grouped_gather": ([_P, _I64, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _I32, _P,
+                                       ctypes.c_int, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
     "mxfp4_decompose_elements": ([_P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
@@ -253,6 +255,35 @@ def nvfp4_quantize_grouped(x, offsets, chan, g=None, g_out=None, resid_scaled=Fa
                                        _ptr(resid) if k else None, QUANT_RESID_SCALED if resid_scaled else 0,
                                        _ptr(ws), ws.numel(), _stream())
     _check("nvfp4_quantize_grouped_ex", st)
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
+
+
+def nvfp4_quantize_grouped_gather(x_tokens, token_of_row, offsets, chan, g=None, g_out=None, resid_scaled=False):
+    """The routed operand x_tokens[token_of_row] (expert-sorted rows, offsets
+    int32 [E+1], chan int32 [E, k]) quantized straight from the token rows
+    x_tokens [T, K]; same result as nvfp4_quantize_grouped on the gathered rows."""
+    lib = load()
+    _need(x_tokens, torch.bfloat16, "x_tokens")
+    _need(token_of_row, torch.int32, "token_of_row")
+    _need(offsets, torch.int32, "offsets")
+    _need(chan, torch.int32, "chan")
+    T, K = x_tokens.shape
+    M = token_of_row.numel()
+    E = offsets.numel() - 1
+    k = chan.shape[1] if chan.dim() == 2 else 0
+    dev = x_tokens.device
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(lib.nvfp4_grouped_scale_bytes(M, K, E), dtype=torch.uint8, device=dev)
+    resid = torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    if g_out is None:
+        g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    st = lib.nvfp4_quantize_grouped_gather(_ptr(x_tokens), T, _ptr(token_of_row), M, K, x_tokens.stride(0), E,
+                                           _ptr(offsets), _ptr(g), _ptr(g_out), _ptr(codes), _ptr(scales),
+                                           _ptr(chan) if k else None, k, _ptr(resid) if k else None,
+                                           QUANT_RESID_SCALED if resid_scaled else 0, _ptr(ws), ws.numel(),
+                                           _stream())
+    _check("nvfp4_quantize_grouped_gather", st)
     return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
 
 

@@ -81,6 +81,27 @@ int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8
   return NVFP4_OK;
 }
 
+// Expert-grouped quantize of M_total operand rows; with a routing gather
+// (token_of_row != nullptr) row r is x's token row token_of_row[r] of T.
+int quantize_grouped(const uint16_t* x, int64_t T, const int32_t* token_of_row, int64_t M_total, int64_t K,
+                     int64_t ldx, int32_t E, const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
+                     uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  int st = check_quant_args(x, M_total, K, ldx, codes, scales, chan, k, resid, 16);
+  if (st != NVFP4_OK) return st;
+  if ((flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || E > 4096 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
+  if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
+    return NVFP4_ERR_WORKSPACE;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
+  return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
+                                              bf(resid), offsets, E, static_cast<float*>(workspace),
+                                              quant_barrier(workspace), d->num_sms, as_stream(stream),
+                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0, token_of_row, T));
+}
+
 }  // namespace
 
 extern "C" {
@@ -150,19 +171,18 @@ int nvfp4_quantize_grouped_ex(const uint16_t* x, int64_t M_total, int64_t K, int
                               const int32_t* offsets, const float* g_in, float* g_out, uint8_t* codes,
                               uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
                               void* workspace, size_t ws_bytes, void* stream) {
-  int st = check_quant_args(x, M_total, K, ldx, codes, scales, chan, k, resid, 16);
-  if (st != NVFP4_OK) return st;
-  if ((flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
-  if (E <= 0 || E > 4096 || offsets == nullptr || !aligned(offsets, 4)) return NVFP4_ERR_INVALID_ARG;
-  if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
-    return NVFP4_ERR_WORKSPACE;
-  const DeviceInfo* d = nullptr;
-  if ((st = current_device(&d)) != NVFP4_OK) return st;
-  if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
-  return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
-                                              bf(resid), offsets, E, static_cast<float*>(workspace),
-                                              quant_barrier(workspace), d->num_sms, as_stream(stream),
-                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0));
+  return quantize_grouped(x, 0, nullptr, M_total, K, ldx, E, offsets, g_in, g_out, codes, scales, chan, k, resid,
+                          flags, workspace, ws_bytes, stream);
+}
+
+int nvfp4_quantize_grouped_gather(const uint16_t* x, int64_t T, const int32_t* token_of_row, int64_t M_total,
+                                  int64_t K, int64_t ldx, int32_t E, const int32_t* offsets, const float* g_in,
+                                  float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k,
+                                  uint16_t* resid, int flags, void* workspace, size_t ws_bytes, void* stream) {
+  if (T < 0 || T > ((int64_t)1 << 31) - 1) return NVFP4_ERR_INVALID_ARG;
+  if (M_total > 0 && (T == 0 || token_of_row == nullptr || !aligned(token_of_row, 4))) return NVFP4_ERR_INVALID_ARG;
+  return quantize_grouped(x, T, token_of_row, M_total, K, ldx, E, offsets, g_in, g_out, codes, scales, chan, k,
+                          resid, flags, workspace, ws_bytes, stream);
 }
 
 int nvfp4_quantize_grouped(const uint16_t* x, int64_t M_total, int64_t K, int64_t ldx, int32_t E,

@@ -17,7 +17,8 @@ int amax_partials_count(int64_t M, int64_t K, int num_sms);
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled = 0);
+                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled = 0,
+                                  const int32_t* gather = nullptr, int64_t T = 0);
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);

@@ -144,6 +144,8 @@ struct QuantArgs {
   int use_map;              // channel bitmaps + prefix counts in shared memory
   int vec32;                // rows start on 32-byte boundaries: 256-bit loads
   int resid_scaled;         // residual written divided by g (times RN(1/g))
+  const int32_t* gather;    // routing gather: row r is x's row gather[r] (of T rows), else nullptr
+  int64_t T;
 };
 
 // Per-thread constants of the block-scale step.
@@ -235,9 +237,26 @@ struct UnitWalk {
   }
 };
 
+// First element of operand row r: x's row r, or with a routing gather
+// (kGather) the token row gather[r] (an index outside [0, T) is reported and
+// row 0 read).
+template <bool kGather>
+__device__ __forceinline__ const __nv_bfloat16* src_row(const QuantArgs& a, uint32_t r) {
+  int64_t s = r;
+  if (kGather) {
+    s = __ldg(a.gather + r);
+    if ((uint64_t)s >= (uint64_t)a.T) {
+      report_error(kDevErrInvalidArg, 0x210u);
+      s = 0;
+    }
+  }
+  return a.x + s * a.ldx;
+}
+
 // Load this lane's 32 bf16 of unit (r, gi): 2 blocks of 16 (zero past K).
+template <bool kGather = false>
 __device__ __forceinline__ void load_unit(const QuantArgs& a, uint32_t r, uint32_t gi, int lane, uint4 (&v)[4]) {
-  const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx + (int64_t)gi * 1024 + lane * 16;
+  const __nv_bfloat16* row = src_row<kGather>(a, r) + (int64_t)gi * 1024 + lane * 16;
   const int cols = (int)((a.K - (int64_t)gi * 1024) < 1024 ? (a.K - (int64_t)gi * 1024) : 1024);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -257,6 +276,7 @@ __device__ __forceinline__ void load_unit(const QuantArgs& a, uint32_t r, uint32
 // Largest |x| over the units of this warp, visited last to first (so the
 // units the quantize pass visits first are the ones read most recently),
 // two units' loads in flight at a time.
+template <bool kGather = false>
 __device__ float warp_units_amax(const QuantArgs& a, UnitWalk w, int lane) {
   uint32_t m2 = 0u;
   if (w.u < w.n_units) {
@@ -266,9 +286,9 @@ __device__ float warp_units_amax(const QuantArgs& a, UnitWalk w, int lane) {
     w.gi = w.u - w.r * w.gpr;
     for (; left >= 2; left -= 2) {
       uint4 v[4], v2[4];
-      load_unit(a, w.r, w.gi, lane, v);
+      load_unit<kGather>(a, w.r, w.gi, lane, v);
       w.prev();
-      load_unit(a, w.r, w.gi, lane, v2);
+      load_unit<kGather>(a, w.r, w.gi, lane, v2);
       w.prev();
 #pragma unroll
       for (int i = 0; i < 4; ++i) m2 = absmax8(m2, v[i]);
@@ -277,7 +297,7 @@ __device__ float warp_units_amax(const QuantArgs& a, UnitWalk w, int lane) {
     }
     if (left == 1) {
       uint4 v[4];
-      load_unit(a, w.r, w.gi, lane, v);
+      load_unit<kGather>(a, w.r, w.gi, lane, v);
 #pragma unroll
       for (int i = 0; i < 4; ++i) m2 = absmax8(m2, v[i]);
     }
@@ -299,14 +319,14 @@ struct QTables {
 
 // Loads of unit (r, gi); kFull: K % 1024 == 0 and 32-byte aligned rows, so
 // every lane's two blocks are inside the row.
-template <bool kFull>
+template <bool kFull, bool kGather = false>
 __device__ __forceinline__ void load_unit_t(const QuantArgs& a, uint32_t r, uint32_t gi, int lane, uint4 (&v)[4]) {
   if (kFull) {
-    const __nv_bfloat16* row = a.x + (int64_t)r * a.ldx + (int64_t)gi * 1024 + lane * 16;
+    const __nv_bfloat16* row = src_row<kGather>(a, r) + (int64_t)gi * 1024 + lane * 16;
     ldg_stream32(row, v[0], v[1]);
     ldg_stream32(row + 512, v[2], v[3]);
   } else {
-    load_unit(a, r, gi, lane, v);
+    load_unit<kGather>(a, r, gi, lane, v);
   }
 }
 
@@ -396,7 +416,7 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
   __syncwarp();  // the slice is read before the warp's next unit overwrites it
 }
 
-template <bool kGrouped, bool kFused, bool kFull>
+template <bool kGrouped, bool kFused, bool kFull, bool kGather>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
   extern __shared__ __align__(16) int32_t smem_i32[];
@@ -425,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   // depend on g, so they are built before that barrier
   uint4 va[4], vb[4];
   UnitWalk wa = walk;
-  if (!kFused && wa.u < walk.n_units) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+  if (!kFused && wa.u < walk.n_units) load_unit_t<kFull, kGather>(a, wa.r, wa.gi, lane, va);
   if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
   if (a.use_map) {
@@ -515,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
     // every CTA reduces all of them (the quantize pass below re-reads X,
     // mostly from L2)
     __shared__ float red[kThreads / 32];
-    const float m = warp_units_amax(a, walk, lane);
+    const float m = warp_units_amax<kGather>(a, walk, lane);
     if (lane == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -525,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
     }
     if (!grid_barrier(a.bar)) return;
     // this warp's first unit (mostly in L2) is in flight while g is reduced
-    if (wa.u < walk.n_units) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+    if (wa.u < walk.n_units) load_unit_t<kFull, kGather>(a, wa.r, wa.gi, lane, va);
     g = tensor_scale_from_partials(a.partials, (int)gridDim.x);
   }
 
@@ -559,12 +579,12 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   while (wa.u < n) {
     UnitWalk wb = wa;
     wb.next();
-    if (wb.u < n) load_unit_t<kFull>(a, wb.r, wb.gi, lane, vb);
+    if (wb.u < n) load_unit_t<kFull, kGather>(a, wb.r, wb.gi, lane, vb);
     process_unit<kGrouped, kFull>(a, va, wa.r, wa.gi, lane, sc, t, n_cg);
     if (wb.u >= n) break;
     wa = wb;
     wa.next();
-    if (wa.u < n) load_unit_t<kFull>(a, wa.r, wa.gi, lane, va);
+    if (wa.u < n) load_unit_t<kFull, kGather>(a, wa.r, wa.gi, lane, va);
     process_unit<kGrouped, kFull>(a, vb, wb.r, wb.gi, lane, sc, t, n_cg);
   }
 }
@@ -1119,9 +1139,14 @@ int amax_partials_count(int64_t M, int64_t K, int num_sms) {
 cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
-                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled) {
+                                  unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled,
+                                  const int32_t* gather, int64_t T) {
   if (M == 0) { k = 0; chan = nullptr; resid = nullptr; }
+  // the separate amax pre-pass reads x's rows in order: a gathered operand
+  // takes a static scale or the fused grid-barrier form
+  if (gather != nullptr && g_in == nullptr && bar == nullptr) return cudaErrorInvalidValue;
   QuantArgs a{};
+  a.gather = gather; a.T = T;
   a.x = x; a.M = M; a.K = K; a.ldx = ldx;
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
@@ -1147,11 +1172,20 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   if (a.use_map) smem += (size_t)a.E * (size_t)((K + 31) / 32) * (sizeof(uint32_t) + sizeof(uint16_t));
   const bool full = a.vec32 && (K % 1024) == 0;
   const void* kerns[2][2][2] = {
-      {{(const void*)nvfp4_quant_kernel<false, false, false>, (const void*)nvfp4_quant_kernel<false, false, true>},
-       {(const void*)nvfp4_quant_kernel<false, true, false>, (const void*)nvfp4_quant_kernel<false, true, true>}},
-      {{(const void*)nvfp4_quant_kernel<true, false, false>, (const void*)nvfp4_quant_kernel<true, false, true>},
-       {(const void*)nvfp4_quant_kernel<true, true, false>, (const void*)nvfp4_quant_kernel<true, true, true>}}};
-  const void* kern = kerns[offsets != nullptr][fused][full];
+      {{(const void*)nvfp4_quant_kernel<false, false, false, false>,
+        (const void*)nvfp4_quant_kernel<false, false, true, false>},
+       {(const void*)nvfp4_quant_kernel<false, true, false, false>,
+        (const void*)nvfp4_quant_kernel<false, true, true, false>}},
+      {{(const void*)nvfp4_quant_kernel<true, false, false, false>,
+        (const void*)nvfp4_quant_kernel<true, false, true, false>},
+       {(const void*)nvfp4_quant_kernel<true, true, false, false>,
+        (const void*)nvfp4_quant_kernel<true, true, true, false>}}};
+  // the routing gather exists for grouped operands only
+  const void* kerns_gather[2][2] = {
+      {(const void*)nvfp4_quant_kernel<true, false, false, true>, (const void*)nvfp4_quant_kernel<true, false, true, true>},
+      {(const void*)nvfp4_quant_kernel<true, true, false, true>, (const void*)nvfp4_quant_kernel<true, true, true, true>}};
+  if (gather != nullptr && offsets == nullptr) return cudaErrorInvalidValue;
+  const void* kern = gather != nullptr ? kerns_gather[fused][full] : kerns[offsets != nullptr][fused][full];
   if (smem > 24 * 1024) {  // with the 18 KB of static unit slices, above the default 48 KB per block
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

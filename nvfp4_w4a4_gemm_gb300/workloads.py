@@ -160,7 +160,8 @@ def dense_inputs(name, calibration=False, with_weights=True):
 
 
 def moe_inputs(calibration=False, with_weights=True, which=("gate_up", "down")):
-    """MoE workload inputs (CPU).  Keys: x_gate_up [T*top, hidden] (sorted
+    """MoE workload inputs (CPU).  Keys: x_tokens [T, hidden] (the token
+    rows), x_gate_up [T*top, hidden] (x_tokens[token_of_row]: the sorted
     rows), x_down [T*top, inter], offsets, token_of_row, route_weight (per
     sorted row), and the weights
     wt_gate_up [E, 2*inter, hidden], wt_down [E, hidden, inter]."""
@@ -170,6 +171,7 @@ def moe_inputs(calibration=False, with_weights=True, which=("gate_up", "down")):
     out = dict(spec=s, offsets=offsets, token_of_row=tok, route_weight=w_rows)
     if "gate_up" in which:
         xt = activations(s.tokens, s.hidden, _n_outliers(s.hidden), "t3x20", s.seed, vs)
+        out["x_tokens"] = xt
         out["x_gate_up"] = xt[tok].contiguous()
     if "down" in which:
         rows = s.tokens * s.top

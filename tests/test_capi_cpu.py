@@ -128,6 +128,16 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 2, None, 0, None) == 1
     assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 4, None,
                                          0, None) == 1
+    # routed gather: token rows and a row table are required; flags and workspace as the grouped quantizer
+    gat = lambda T, tok, flags=0, g=fake, ws=fake, wsb=1 << 16: lib.nvfp4_quantize_grouped_gather(
+        fake, T, tok, 8, 32, 32, 1, fake, g, None, fake, fake, None, 0, None, flags, ws, wsb, None)
+    assert gat(0, fake) == 1
+    assert gat(-1, fake) == 1
+    assert gat(4, None) == 1
+    assert gat(4, P((1 << 20) + 2)) == 1
+    assert gat(1 << 31, fake) == 1
+    assert gat(4, fake, flags=2) == 1
+    assert gat(4, fake, g=None, ws=None, wsb=0) == 5
     # QDQ: K % 16, strides, misaligned buffers, codes without scales, dynamic scale without workspace
     g = fake
     assert lib.nvfp4_qdq(fake, 4, 24, 24, g, None, fake, 24, None, None, None, 0, None) == 1

@@ -10,6 +10,8 @@ that runs out, and routing offsets that do not partition the rows.
 * Grouped launches given offsets that are not a partition of the rows
   latch NVFP4_ERR_INVALID_ARG and write nothing instead of indexing past
   the buffers.
+* The routed quantizer given a token index outside [0, T) latches
+  NVFP4_ERR_INVALID_ARG and reads token row 0 for that row instead.
 
 Nothing here faults, traps or hangs a GPU: every wait is bounded and every
 rejected launch returns before touching its outputs.
@@ -134,3 +136,26 @@ def test_grouped_offsets_not_a_partition_are_rejected(nv, bad):
     nv.w4a4_grouped_gemm_comp(qa, good, b_codes, b_scales, g_b, N, resid=qa["resid"], w_sel=w_sel, y=y)
     assert nv.check_status()[0] == 0
     assert not bool((y == 5.0).all())
+
+
+@pytest.mark.parametrize("bad", [-1, 37, 1 << 30])
+def test_gather_index_out_of_range_reported(nv, bad):
+    T, K, E, k = 37, 256, 3, 8
+    offs = torch.tensor([0, 10, 10, 25], dtype=torch.int32).cuda()
+    tok = torch.arange(25, dtype=torch.int32) % T
+    tok[7] = bad
+    xt = W.activations(T, K, 3, "t3x20", 41, 42)
+    chan = torch.stack([torch.arange(0, K, K // k, dtype=torch.int32)] * E).cuda()
+    g = torch.ones(1, device="cuda")
+    q = nv.nvfp4_quantize_grouped_gather(xt.cuda(), tok.cuda(), offs, chan, g=g)
+    st, where = nv.check_status()
+    assert st == nv.ERR_INVALID_ARG and where == 0x210, (st, where)
+    # the bad row was read as token row 0; every other row is its token's
+    good = tok.clone()
+    good[7] = 0
+    ref = nv.nvfp4_quantize_grouped(xt[good.long()].cuda(), offs, chan, g=g)
+    assert nv.check_status()[0] == 0
+    for key in ("codes", "resid"):
+        assert torch.equal(q[key], ref[key]), key
+    tiles = onv.grouped_scale_tile_offsets(offs.cpu().numpy(), K // 16)
+    assert np.array_equal(gather_scales(q["scales"], tiles), gather_scales(ref["scales"], tiles))

@@ -95,6 +95,15 @@ def test_moe_full_size(nv, which):
     chan = chan_t.cpu().numpy().astype(np.int32)
     offs_t = torch.from_numpy(offs).cuda()
     qx = nv.nvfp4_quantize_grouped(x.cuda(), offs_t, chan_t, resid_scaled=True)
+    if which == "gate_up":
+        # the bench's form: read through the routing table from the token rows
+        qg = nv.nvfp4_quantize_grouped_gather(d["x_tokens"].cuda(), d["token_of_row"].to(torch.int32).cuda(),
+                                              offs_t, chan_t, resid_scaled=True)
+        for key in ("g", "codes", "resid"):
+            assert torch.equal(qg[key], qx[key]), key
+        tiles = onv.grouped_scale_tile_offsets(offs, K // 16)
+        assert np.array_equal(gather_scales(qg["scales"], tiles), gather_scales(qx["scales"], tiles))
+        del qg
     codes, scales, gs = [], [], []
     for e in range(E):
         q = nv.nvfp4_quantize(wt[e].cuda())

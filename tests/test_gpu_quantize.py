@@ -235,6 +235,63 @@ def test_grouped_quantize(nv):
     assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(ref["resid"]))
 
 
+def _check_gather(nv, xt, tok, offs, chan, g=None, resid_scaled=False):
+    """The routed quantize read through the row table against the oracle on
+    the gathered rows (the test gathers them on the CPU)."""
+    K = xt.shape[1]
+    gt = None if g is None else torch.tensor([g], dtype=torch.float32).cuda()
+    q = nv.nvfp4_quantize_grouped_gather(xt.cuda(), torch.from_numpy(tok).cuda(), torch.from_numpy(offs).cuda(),
+                                         torch.from_numpy(chan).cuda(), g=gt, resid_scaled=resid_scaled)
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    ref = onv.quantize_grouped(f32(xt)[tok], offs, chan, g=g)
+    assert f32(q["g"])[0] == ref["g"]
+    assert np.array_equal(u8(q["codes"]), ref["packed"]), "codes differ"
+    sc = gather_scales(q["scales"], onv.grouped_scale_tile_offsets(offs, K // 16))
+    assert np.array_equal(sc, ref["sigma"]), "scale bytes differ"
+    want = ref["resid_scaled"] if resid_scaled else ref["resid"]
+    assert np.array_equal(bf16_bits_of(q["resid"]), F.bf16_bits(want)), "residual differs"
+    return q
+
+
+@pytest.mark.parametrize("resid_scaled", [False, True])
+def test_grouped_gather_quantize(nv, resid_scaled):
+    # the MoE workload's routing on its first experts, read from all 4096 token rows
+    d = W.moe_inputs(with_weights=False, which=("gate_up",))
+    offs = d["offsets"].numpy()
+    E = int(np.searchsorted(offs, 2500, side="right")) - 1
+    offs_c = offs[: E + 1].astype(np.int32)
+    tok = d["token_of_row"].numpy()[: int(offs_c[-1])].astype(np.int32)
+    rng = np.random.default_rng(5)
+    chan = np.stack([np.sort(rng.choice(2048, 32, replace=False)) for _ in range(E)]).astype(np.int32)
+    q = _check_gather(nv, d["x_tokens"], tok, offs_c, chan, resid_scaled=resid_scaled)
+    # bit-identical to the grouped quantizer on the materialized rows
+    qm = nv.nvfp4_quantize_grouped(d["x_tokens"][tok].cuda(), torch.from_numpy(offs_c).cuda(),
+                                   torch.from_numpy(chan).cuda(), resid_scaled=resid_scaled)
+    for key in ("g", "codes", "resid"):
+        assert torch.equal(q[key], qm[key]), key
+    # the scale bytes of the rows (the padding rows between experts are not written)
+    tiles = onv.grouped_scale_tile_offsets(offs_c, 2048 // 16)
+    assert np.array_equal(gather_scales(q["scales"], tiles), gather_scales(qm["scales"], tiles))
+
+
+@pytest.mark.parametrize("K,static", [(160, False), (1056, True), (3072, False)])
+def test_grouped_gather_ragged(nv, K, static):
+    # rows past the last full 1024-column group, repeated and unused tokens,
+    # empty experts, experts of one row, a static tensor scale
+    rng = np.random.default_rng(K)
+    T, E, k = 37, 7, 8
+    sizes = np.array([5, 0, 1, 130, 0, 19, 3])
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    tok = rng.integers(0, T - 3, int(offs[-1])).astype(np.int32)  # the last three tokens never routed
+    tok[:4] = 0
+    xt = W.activations(T, K, 3, "t3x20", K + 1, K + 2)
+    xt[T - 1, 5] = 1000.0  # an unrouted outlier must not enter the dynamic scale
+    chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
+    g = 0.75 * onv.tensor_scale(f32(xt)[tok]) if static else None
+    _check_gather(nv, xt, tok, offs, chan, g=g, resid_scaled=static)
+
+
 @pytest.mark.parametrize("M,K", [(64, 256), (33, 160), (256, 5120)])
 def test_mxfp4_quantize_and_decomposition(nv, M, K):
     x = W.activations(M, K, max(1, K // 100), "t3x20", K, M + 3)
