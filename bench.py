@@ -388,8 +388,8 @@ def prefill_components(nv, pk, s, chan, sets, steps=20):
             it[0] += 1
             nv.nvfp4_quantize(sets[it[0] % N_SETS]["x"], g=g, chan=chan, out=out, g_out=g_out, resid_scaled=True)
         return f
-    ms_dyn = _time_steps(quant(None), steps, flush)
-    ms_st = _time_steps(quant(g_static), steps, flush)
+    ms_dyn = _time_steps(quant(None), steps, flush, "prefill_quantize_dynamic")
+    ms_st = _time_steps(quant(g_static), steps, flush, "prefill_quantize_static")
     qs = [nv.nvfp4_quantize(st["x"], chan=chan, resid_scaled=True) for st in sets]
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
@@ -398,7 +398,7 @@ def prefill_components(nv, pk, s, chan, sets, steps=20):
         i = it[0] % N_SETS
         nv.w4a4_gemm_comp(qs[i], sets[i]["qw"], N, resid=qs[i]["resid"], w_sel=sets[i]["w_sel"], y=y,
                           weights_ready=True)
-    ms_g = _time_steps(gemm, steps, flush)
+    ms_g = _time_steps(gemm, steps, flush, "prefill_gemm")
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     tf = 2.0 * M * N * K / (ms_g * 1e-3) / 1e12
     return {"alone_clean_l2": {
@@ -414,12 +414,21 @@ def prefill_components(nv, pk, s, chan, sets, steps=20):
 
 
 # ------------------------------------------- the other four workloads ----
-def _time_steps(fn, steps, flush):
+def _time_steps(fn, steps, flush, name=None):
     """Mean device time (ms) of `fn` over `steps` runs.  Between runs, outside
     the timed window, a buffer larger than the L2 is written and then read
     back: the write flushes the L2, the read writes its dirty lines back to
     HBM, so a step does not start behind 129 MB of pending write-backs.
-    flush=None: no flush (the step's own inputs are larger than the L2)."""
+    flush=None: no flush (the step's own inputs are larger than the L2).
+    `name` labels the warm-up and timed runs with an NVTX range, so a
+    profiler can select one workload's launches (ncu --nvtx --nvtx-include
+    "<name>/")."""
+    if name is not None:
+        torch.cuda.nvtx.range_push(name)
+        try:
+            return _time_steps(fn, steps, flush)
+        finally:
+            torch.cuda.nvtx.range_pop()
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
@@ -477,9 +486,9 @@ def other_workloads(nv, pk, steps=10):
         qw, ws = layer()
         qx = nv.nvfp4_quantize(x, chan=chan, resid_scaled=True)
         nv.w4a4_gemm_comp(qx, qw, s.N, resid=qx["resid"], w_sel=ws, y=y, weights_ready=True)
-    ms = _time_steps(dec, steps, None)
-    ms_two = _time_steps(dec_two, steps, None)
-    ms_flush = _time_steps(dec, steps, flush)
+    ms = _time_steps(dec, steps, None, "decode_layer")
+    ms_two = _time_steps(dec_two, steps, None, "decode_two_launch")
+    ms_flush = _time_steps(dec, steps, flush, "decode_layer_flushed")
     qw, ws = layers[0]
     byts = qw["codes"].numel() + qw["scales"].numel() + ws.numel() * 2 + x.numel() * 2 + y.numel() * 2
     out["decode"] = {"shape": "X[16,4096] x W[4096,14336], k=64", "ms_per_step": round(ms, 4),
@@ -531,13 +540,13 @@ def other_workloads(nv, pk, steps=10):
             qx = quantize_x()
             nv.w4a4_grouped_gemm_comp(qx, offs, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel, y=yg,
                                       weights_ready=True)
-        ms = _time_steps(moe, steps, flush)
+        ms = _time_steps(moe, steps, flush, "moe_" + which)
         qfix = quantize_x()
 
         def moe_gemm():
             nv.w4a4_grouped_gemm_comp(qfix, offs, b_codes, b_scales, g_b, N, resid=qfix["resid"], w_sel=w_sel,
                                       y=yg, weights_ready=True)
-        ms_g = _time_steps(moe_gemm, steps, flush)
+        ms_g = _time_steps(moe_gemm, steps, flush, "moe_" + which + "_gemm")
         flops = 2.0 * xg.shape[0] * N * K
         byts = (b_codes.numel() + b_scales.numel() + w_sel.numel() * 2 + x_in.numel() * 2 + yg.numel() * 2)
         res[which] = {"ms_per_step": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
@@ -577,15 +586,15 @@ def other_workloads(nv, pk, steps=10):
         box["q"] = qx
         nv.w4a4_gemm_comp(dict(codes=qx["codes"], scales=qx["scales"]), dict(codes=qw["codes"], scales=qw["scales"]),
                           s.N, fmt=nv.FMT_MXFP4, y=y, weights_ready=True)
-    ms = _time_steps(mx, steps, flush)
-    ms_q = _time_steps(lambda: nv.mxfp4_quantize(x, stats=True), steps, flush)
+    ms = _time_steps(mx, steps, flush, "mxfp4_step")
+    ms_q = _time_steps(lambda: nv.mxfp4_quantize(x, stats=True), steps, flush, "mxfp4_quantize")
     qfix = nv.mxfp4_quantize(x)
 
     def mx_gemm():
         nv.w4a4_gemm_comp(dict(codes=qfix["codes"], scales=qfix["scales"]),
                           dict(codes=qw["codes"], scales=qw["scales"]), s.N, fmt=nv.FMT_MXFP4, y=y,
                           weights_ready=True)
-    ms_g = _time_steps(mx_gemm, steps, flush)
+    ms_g = _time_steps(mx_gemm, steps, flush, "mxfp4_gemm")
     n_el, n_blk = s.M * s.K, s.M * s.K // 32
     q_bytes = n_el * 2 + n_el // 2 + nv.mx_scale_bytes(s.M, s.K) + n_blk * 17   # X + codes + E8M0 + stats/dead
     gf = 2.0 * s.M * s.N * s.K
@@ -607,7 +616,7 @@ def other_workloads(nv, pk, steps=10):
 
     def qdq():
         nv.nvfp4_qdq(wq, with_codes=True, out=w_out)
-    ms = _time_steps(qdq, steps, flush)
+    ms = _time_steps(qdq, steps, flush, "qdq")
     n_el = wq.numel()
     byts = n_el * 2 + n_el * 2 + n_el // 2 + nv.load().nvfp4_scale_bytes(s.N, s.K)
     out["qdq"] = {"shape": "W^T[14336,4096] bf16 -> bf16 QDQ + NVFP4 codes/scales, dynamic tensor scale",
@@ -661,7 +670,7 @@ def moe_fused_layer(nv, pk, flush, steps):
         out.zero_()
         nv.w4a4_grouped_gemm_combine(qh, offs, dn_codes, dn_scales, dn_g, hidden, tok, w_row, s.tokens,
                                      resid=qh["resid"], w_sel=dn_sel, out=out, weights_ready=True)
-    ms = _time_steps(layer, steps, flush)
+    ms = _time_steps(layer, steps, flush, "moe_fused_layer")
     flops = 2.0 * rows * (2 * inter) * hidden + 2.0 * rows * hidden * inter
     byts = (gu_codes.numel() + gu_scales.numel() + gu_sel.numel() * 2 + dn_codes.numel() + dn_scales.numel()
             + dn_sel.numel() * 2 + x.numel() * 2 + out.numel() * 4)

@@ -424,6 +424,39 @@ __device__ __forceinline__ uint32_t bf16x8_mul_e2m1(const uint4& w, uint64_t s2)
 #undef NV4_E2M1_PAIR
   return out;
 }
+// Packed pairs of fp32 (low word = first element) and their element-wise
+// IEEE round-to-nearest arithmetic (f32x2 instructions: one issue for two
+// results, each rounded exactly as the scalar instruction would).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // Per-half max of magnitudes of two bf16 pairs (max.xorsign.abs: the result's
 // sign bits carry no meaning, its magnitudes are max(|a|, |b|)).
 __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
