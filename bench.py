@@ -489,6 +489,14 @@ def other_workloads(nv, pk, steps=10):
     ms = _time_steps(dec, steps, None, "decode_layer")
     ms_two = _time_steps(dec_two, steps, None, "decode_two_launch")
     ms_flush = _time_steps(dec, steps, flush, "decode_layer_flushed")
+
+    def dec_seq():
+        for _ in range(len(layers)):
+            dec()
+    # the six layers back to back, as a model runs them: each launch still
+    # waits for the previous one to finish before it reads X (programmatic
+    # dependent launch), only its prologue overlaps the previous layer's tail
+    ms_seq = _time_steps(dec_seq, steps, None, "decode_layer_sequence") / len(layers)
     qw, ws = layers[0]
     byts = qw["codes"].numel() + qw["scales"].numel() + ws.numel() * 2 + x.numel() * 2 + y.numel() * 2
     out["decode"] = {"shape": "X[16,4096] x W[4096,14336], k=64", "ms_per_step": round(ms, 4),
@@ -496,11 +504,14 @@ def other_workloads(nv, pk, steps=10):
                      "gbs": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                      "bytes_per_step": byts, "bound": "hbm",
                      "two_launch_ms": round(ms_two, 4), "after_l2_flush_ms": round(ms_flush, 4),
+                     "per_layer_in_sequence_ms": round(ms_seq, 4),
                      "note": "one launch (w4a4_decode_linear): clusters of 4 CTAs quantize X (dynamic scale) "
                              "into shared memory, the swapped-operand GEMM with compensation streams the weights; "
                              "weights of 6 layers used in turn (> L2); two_launch_ms = quantize kernel + GEMM "
                              "kernel on the same rotation; after_l2_flush_ms = the one launch after a 256 MB "
-                             "L2 flush (code and X also cold)"}
+                             "L2 flush (code and X also cold); per_layer_in_sequence_ms = the six layers launched "
+                             "back to back between one event pair, divided by six (each layer waits for the "
+                             "previous one before reading X; only launch and prologue overlap)"}
     del layers, x, y
 
     # MoE: 4096 tokens top-8 of 128 experts; gate/up [2048->1536] and down [768->2048], k=32 per expert
