@@ -851,41 +851,50 @@ __device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile
                                  (uint64_t)(prow & 31) * 16u + (uint64_t)((prow >> 5) & 3) * 4u) = scale_word;
 }
 
-// kEpiCombine epilogue: row q*32+lane of the tile, 128 columns of half hh,
-// out[token] += w * alpha * acc in fp32 (vector atomic adds); releases the
-// accumulator once its last columns are in registers.
+// kEpiCombine epilogue: rows q*32 .. q*32+31 of the tile, 128 columns of
+// half hh: out[token] += w * alpha * acc in fp32.  The accumulator is read in
+// the 16x256b shape, so four lanes hold 8 consecutive columns of one row and
+// each warp-wide vector atomic covers eight whole 32-byte sectors (eight rows)
+// instead of 32 half sectors (32 rows).  Releases the accumulator once its
+// last columns are in registers.
 __device__ __forceinline__ void epi_combine(const GemmParams& p, const Tile& tl, int q, int hh, int lane,
                                             uint32_t tmem, float alpha, uint64_t* acc_empty) {
-  const int r = q * 32 + lane;
-  const bool row_ok = r < tl.rows;
-  const int64_t row = tl.row0 + r;
   const int64_t col0 = tl.n0 + hh * 128;
-  float* dst = nullptr;
-  float w = 0.f;
-  if (row_ok && col0 < p.N) {
-    dst = p.out_f32 + (int64_t)p.token_of_row[row] * p.N + col0;
-    w = alpha * p.w_row[row];
-  }
-  const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hh * 128);
+  const int cq = 2 * (lane & 3);  // this lane's column pair within each group of 8
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    uint32_t v[4][16];
+  for (int rh = 0; rh < 2; ++rh) {
+    // this lane's two rows of the 16-row half: r and r + 8
+    float* dst[2] = {nullptr, nullptr};
+    float w[2] = {0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x16(t_acc + (uint32_t)(b * 64 + c * 16), v[c]);
-    tmem_ld_wait();
-    if (b == 1) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const int r = q * 32 + rh * 16 + s2 * 8 + (lane >> 2);
+      if (r < tl.rows && col0 < p.N) {
+        const int64_t row = tl.row0 + r;
+        dst[s2] = p.out_f32 + (int64_t)p.token_of_row[row] * p.N + col0 + cq;
+        w[s2] = alpha * p.w_row[row];
+      }
     }
-    if (dst != nullptr) {
+    const uint32_t t_acc = tmem + ((uint32_t)(q * 32 + rh * 16) << 16) + (uint32_t)(hh * 128);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+    for (int b = 0; b < 2; ++b) {
+      uint32_t v[32];
+      tmem_ld_16x256b_x8(t_acc + (uint32_t)(b * 64), v);
+      tmem_ld_wait();
+      if (rh == 1 && b == 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+      }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          atomicAdd(reinterpret_cast<float4*>(dst + b * 64 + c * 16 + 4 * i),
-                    make_float4(w * __uint_as_float(v[c][4 * i]), w * __uint_as_float(v[c][4 * i + 1]),
-                                w * __uint_as_float(v[c][4 * i + 2]), w * __uint_as_float(v[c][4 * i + 3])));
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (dst[s2] == nullptr) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          atomicAdd(reinterpret_cast<float2*>(dst[s2] + b * 64 + 8 * j),
+                    make_float2(w[s2] * __uint_as_float(v[4 * j + 2 * s2]),
+                                w[s2] * __uint_as_float(v[4 * j + 2 * s2 + 1])));
+      }
     }
   }
 }
