@@ -81,6 +81,7 @@ struct GemmParams {
   const uint8_t* a_sf;
   const uint8_t* b_sf;
   uint64_t b_sf_expert_stride;
+  int64_t b_sf_expert_tiles;  // 128-row scale tiles per expert (pair kernel, grouped)
   const float* g_a;
   const float* g_b;
   __nv_bfloat16* y;
@@ -1358,6 +1359,12 @@ __global__ void __launch_bounds__(kWThreads, 1) w4a4_gemm_wide_kernel(const __gr
 // operand bytes of a 128 x 256 single-SM tile.  Both CTAs also load the block
 // scales of all 256 B rows (each CTA's MMA half reads them from its own TMEM).
 //
+// Grouped (MoE) problems take the same tiles per expert: an expert's rows
+// form ceil(M_e / 256) pair tiles (rows past the expert's end are computed
+// from whatever A holds there and never stored), its weights and W_S come
+// from the expert's slice of the stacked [E, N, .] operands, its A scales
+// from the expert's 128-row tiles of the grouped scale layout.
+//
 // Scale factors travel in a ring of their own, ahead of the operands.  The
 // tensor pipe runs MMAs and scale copies (tcgen05.cp) in issue order, so a
 // k-tile's copies must be queued before the MMAs of the k-tile ahead of it
@@ -1399,6 +1406,45 @@ static_assert(kPColSf + 48 * kPStages <= kTmemCols, "TMEM budget");
 static_assert(kPStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStageBytes + (size_t)kPSfStages * kPSfStageBytes + 512;
 
+// One pair tile: expert, first row of its 256, rows that exist (<= 256; the
+// rest belong to the next expert or lie past M), first 128-row tile of the A
+// scale layout, and the 256-column tile index.
+struct PairTile {
+  int e;
+  int64_t row0;
+  int rows;
+  int64_t sf_rt;
+  int64_t nt;
+};
+
+__device__ __forceinline__ void pair_tile_of(const GemmParams& p, const SchedSmem& s, int64_t t, int n_tiles_n,
+                                             PairTile& o) {
+  if (!p.grouped) {
+    const int64_t mt = t / n_tiles_n;
+    o.e = 0;
+    o.nt = t - mt * n_tiles_n;
+    o.row0 = mt * BMP;
+    const int64_t rem = p.M - o.row0;
+    o.rows = rem < BMP ? (int)rem : BMP;
+    o.sf_rt = 2 * mt;
+    return;
+  }
+  // expert e: last with tile_start[e] <= t
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int64_t local = t - s.tile_start[lo];
+  const int64_t mt = local / n_tiles_n;
+  o.e = lo;
+  o.nt = local - mt * n_tiles_n;
+  o.row0 = (int64_t)s.off[lo] + mt * BMP;
+  const int64_t rem = (int64_t)s.off[lo + 1] - o.row0;
+  o.rows = rem < BMP ? (int)rem : BMP;
+  o.sf_rt = (int64_t)(s.pbase[lo] >> 7) + 2 * mt;
+}
+
 __device__ __forceinline__ uint32_t idesc_fp4_pair(int fmt, uint32_t sf_id) {
   uint32_t d = (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
   if (fmt == 1) d |= (1u << 23) | (sf_id << 29) | (sf_id << 4);
@@ -1427,6 +1473,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   uint64_t* sf_drain = drain + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_tmem + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1436,6 +1483,28 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   // launched as a programmatic dependent: without the early-weights promise
   // nothing touches global memory before the preceding kernel has finished
   if (!p.early_w) pdl_wait();
+  const int n_tiles_n = (int)((p.N + BNP - 1) / BNP);
+  SchedSmem sched{};
+  if (p.grouped) {
+    // both CTAs of a pair read the same offsets, so on a bad table both
+    // return here, before any barrier, TMEM or cluster step
+    sched.off = s_sched;
+    sched.tile_start = s_sched + (p.E + 1);
+    sched.pbase = s_sched + 2 * (p.E + 1);
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sched.off[i] = p.offsets[i];
+    if (!offsets_valid(p, sched.off)) return;
+    if (threadIdx.x == 0) {
+      int32_t ts = 0, pb = 0;
+      for (int e = 0; e < p.E; ++e) {
+        const int32_t rows = sched.off[e + 1] - sched.off[e];
+        sched.tile_start[e] = ts;
+        sched.pbase[e] = pb;
+        ts += (rows + BMP - 1) / BMP * n_tiles_n;
+        pb += (rows + BM - 1) / BM * BM;  // the quantizer's grouped scale layout: 128-row tiles per expert
+      }
+      sched.tile_start[p.E] = ts;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&full[i], 1);
@@ -1464,8 +1533,8 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   cluster_barrier();  // both CTAs' barriers exist before any remote arrival or TMA completion
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int n_tiles_n = (int)((p.N + BNP - 1) / BNP);
-  const int64_t num_tiles = ((p.M + BMP - 1) / BMP) * (int64_t)n_tiles_n;
+  const int64_t num_tiles =
+      p.grouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BMP - 1) / BMP) * (int64_t)n_tiles_n;
   const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int cpk = p.fmt == 1 ? 2 : 4;                     // 512-byte scale chunks per 256-element k-tile
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
@@ -1490,23 +1559,28 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     __syncwarp();
     const uint32_t full0 = cluster_addr(full, 0);  // the leader's full[0]; full[i] is 8 bytes further
     constexpr uint32_t kTx = 2u * (uint32_t)(kPTileA + kPTileB);
-    auto issue_b = [&](int stg, int64_t nt, int kt) {
-      tma_load_2d_pair(stages + stg * kPStageBytes + kPTileA, &p.tm_b, full0 + 8u * (uint32_t)stg, kt * BKB,
-                       (int32_t)(nt * BNP + BM * rank));
+    auto issue_b = [&](int stg, const PairTile& tl, int kt) {
+      uint8_t* dst = stages + stg * kPStageBytes + kPTileA;
+      const uint32_t fb = full0 + 8u * (uint32_t)stg;
+      const int32_t n = (int32_t)(tl.nt * BNP + BM * rank);
+      if (p.grouped) tma_load_3d_pair(dst, &p.tm_b, fb, kt * BKB, n, tl.e);
+      else tma_load_2d_pair(dst, &p.tm_b, fb, kt * BKB, n);
     };
-    auto issue_a = [&](int stg, int64_t mt, int kt) {
+    auto issue_a = [&](int stg, const PairTile& tl, int kt) {
       tma_load_2d_pair(stages + stg * kPStageBytes, &p.tm_a, full0 + 8u * (uint32_t)stg, kt * BKB,
-                       (int32_t)((mt * 2 + rank) * BM));
+                       (int32_t)(tl.row0 + BM * rank));
     };
     // early weights: the B halves of this pair's first k-tiles go out before
     // the wait for the preceding kernel (the ring starts empty)
     int pre = 0;
     if (p.early_w && pair < num_tiles) {
+      PairTile tl;
+      pair_tile_of(p, sched, pair, n_tiles_n, tl);
       pre = n_kt < kPStages ? n_kt : kPStages;
       if (elect_one()) {
         for (int i = 0; i < pre; ++i) {
           if (leader) mbar_arrive_expect_tx(&full[i], kTx);
-          issue_b(i, pair % n_tiles_n, i);
+          issue_b(i, tl, i);
         }
       }
       __syncwarp();
@@ -1517,14 +1591,15 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     uint32_t phase = 0;
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
-      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
+      PairTile tl;
+      pair_tile_of(p, sched, t, n_tiles_n, tl);
       for (int kt = 0; kt < n_kt && ok; ++kt) {
         const bool early = issued++ < pre;  // B half already in flight, stage known empty
         if (!early && !mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
         if (elect_one()) {
           if (!early && leader) mbar_arrive_expect_tx(&full[stage], kTx);
-          issue_a(stage, mt, kt);
-          if (!early) issue_b(stage, nt, kt);
+          issue_a(stage, tl, kt);
+          if (!early) issue_b(stage, tl, kt);
         }
         __syncwarp();
         if (++stage == kPStages) { stage = 0; phase ^= 1u; }
@@ -1534,9 +1609,11 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
         if (elect_one()) {
           uint8_t* sa = stages + stage * kPStageBytes;
           const uint32_t fb = full0 + 8u * (uint32_t)stage;
+          const int32_t n = (int32_t)(tl.nt * BNP + BM * rank);
           if (leader) mbar_arrive_expect_tx(&full[stage], kTx);
-          tma_load_2d_pair(sa, &p.tm_r, fb, ct * 64, (int32_t)((mt * 2 + rank) * BM));
-          tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, (int32_t)(nt * BNP + BM * rank));
+          tma_load_2d_pair(sa, &p.tm_r, fb, ct * 64, (int32_t)(tl.row0 + BM * rank));
+          if (p.grouped) tma_load_3d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n, tl.e);
+          else tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n);
         }
         __syncwarp();
         if (++stage == kPStages) { stage = 0; phase ^= 1u; }
@@ -1658,8 +1735,10 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     uint32_t sphase = 0;
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
-      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
-      const int64_t at = mt * 2 + rank, bt = nt * 2;
+      PairTile tl;
+      pair_tile_of(p, sched, t, n_tiles_n, tl);
+      // 128-row scale tiles (of the expert's slice of the stacked B scales)
+      const int64_t at = tl.sf_rt + rank, bt = (int64_t)tl.e * p.b_sf_expert_tiles + tl.nt * 2;
       for (int kt = 0; kt < n_kt && ok; ++kt) {
         if (!mbar_wait_warp(&sfl_empty[slot], sphase ^ 1u, kWaitSfDrain, s_abort)) { ok = false; break; }
         if (elect_one()) {
@@ -1751,17 +1830,23 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     int stage = 0;
     uint32_t ct_phase = 0;  // bit s: parity of ct_landed[s]'s next phase
     const float ga = p.g_a ? *p.g_a : 1.f;
-    const float gb = p.g_b ? *p.g_b : 1.f;
-    float c = 1.f;
-    if (p.resid_scaled) {
-      if (p.flags == 1) c = __fdiv_rn(1.0f, gb);
-    } else {
-      c = p.flags == 1 ? __fdiv_rn(1.0f, ga * gb) : __fdiv_rn(1.0f, ga);
-    }
     const uint32_t comp_ready_l0 = cluster_addr(comp_ready, 0);
     const uint32_t acc_empty_l = cluster_addr(acc_empty, 0);
+    int e_prev = -1;
+    float gb = 1.f, c = 1.f;
     for (int64_t t = pair; t < num_tiles; t += n_pairs) {
-      const int64_t mt = t / n_tiles_n, nt = t - mt * n_tiles_n;
+      PairTile tl;
+      pair_tile_of(p, sched, t, n_tiles_n, tl);
+      if (tl.e != e_prev) {  // the expert's weight scale and the residual factor it sets
+        e_prev = tl.e;
+        gb = p.g_b ? p.g_b[tl.e] : 1.f;
+        c = 1.f;
+        if (p.resid_scaled) {
+          if (p.flags == 1) c = __fdiv_rn(1.0f, gb);
+        } else {
+          c = p.flags == 1 ? __fdiv_rn(1.0f, ga * gb) : __fdiv_rn(1.0f, ga);
+        }
+      }
       if (scale_r) {
         stage = (stage + n_kt) % kPStages;
         bool okc = true;
@@ -1807,9 +1892,9 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       // accumulator free: the next tile's MMAs may start (a cluster-scope
       // release here would first wait for the previous tile's Y stores)
       if (lane == 0) mbar_arrive_cluster_cta(acc_empty_l);
-      const int64_t row = (mt * 2 + rank) * BM + r;
-      const int64_t col0 = nt * BNP + h * 128;
-      if (row < p.M && col0 < p.N) {
+      const int64_t row = tl.row0 + rank * BM + r;
+      const int64_t col0 = tl.nt * BNP + h * 128;
+      if ((int)(rank * BM) + r < tl.rows && col0 < p.N) {
         __nv_bfloat16* dst = p.y + row * p.N + col0;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
@@ -2759,31 +2844,44 @@ int pair_clusters(int num_sms) {
   return cached[dev];
 }
 
-cudaError_t launch_pair(const GemmProblem& pr, int clusters_max, cudaStream_t stream) {
+// Dynamic shared memory of the pair kernel: the rings, the barriers and, when
+// grouped, the schedule tables (offsets, tile starts, scale bases: 3 (E + 1)
+// ints).
+size_t pair_smem_bytes(int E) { return kPSmemBytes + (E > 0 ? sizeof(int32_t) * 3 * ((size_t)E + 1) : 0); }
+
+cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
+  const int E = grouped ? pr.E : 1;
   const uint64_t kb = (uint64_t)(pr.K / 2);
   {
     const uint64_t d[2] = {kb, (uint64_t)pr.M};
     if (!make_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
   }
-  {
+  if (grouped) {
+    const uint64_t d[3] = {kb, (uint64_t)pr.N, (uint64_t)E};
+    if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 3, d, BKB, BM)) return cudaErrorInvalidValue;
+  } else {
     const uint64_t d[2] = {kb, (uint64_t)pr.N};
     if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BM)) return cudaErrorInvalidValue;
   }
   // tiled scales viewed as rows of 256 bytes; one box = one k-tile's chunks
-  // of one 128-row scale tile (4 x 512 B NVFP4, 2 x 512 B MXFP4)
+  // of one 128-row scale tile (4 x 512 B NVFP4, 2 x 512 B MXFP4).  Grouped:
+  // A's scales in the grouped layout (each expert from a 128-row tile, at
+  // most ceil(M / 128) + E tiles), B's the E experts' buffers back to back.
   const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
   const uint32_t sf_rows = pr.fmt == 1 ? 4u : 8u;
+  const int64_t b_tiles = (pr.N + 127) / 128;
   {
-    const uint64_t bytes = (uint64_t)((pr.M + 127) / 128) * 128u * (uint64_t)n_sf_cols;
+    const uint64_t tiles = (uint64_t)((pr.M + 127) / 128) + (grouped ? (uint64_t)E : 0u);
+    const uint64_t bytes = tiles * 128u * (uint64_t)n_sf_cols;
     const uint64_t d[2] = {256, bytes / 256};
     if (!make_map(&p.tm_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.a_scales, 2, d, 256, sf_rows,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t bytes = (uint64_t)((pr.N + 127) / 128) * 128u * (uint64_t)n_sf_cols;
+    const uint64_t bytes = (uint64_t)E * (uint64_t)b_tiles * 128u * (uint64_t)n_sf_cols;
     const uint64_t d[2] = {256, bytes / 256};
     if (!make_map(&p.tm_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_scales, 2, d, 256, sf_rows,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -2792,9 +2890,17 @@ cudaError_t launch_pair(const GemmProblem& pr, int clusters_max, cudaStream_t st
   if (pr.k > 0) {
     const uint64_t dr[2] = {(uint64_t)pr.k, (uint64_t)pr.M};
     if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
-    const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
-    if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BM)) return cudaErrorInvalidValue;
+    if (grouped) {
+      const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BM))
+        return cudaErrorInvalidValue;
+    } else {
+      const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
+      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BM))
+        return cudaErrorInvalidValue;
+    }
   }
+  p.b_sf_expert_tiles = b_tiles;
   p.g_a = pr.g_a;
   p.g_b = pr.g_b;
   p.y = pr.y;
@@ -2806,17 +2912,21 @@ cudaError_t launch_pair(const GemmProblem& pr, int clusters_max, cudaStream_t st
   p.early_w = (pr.flags & kGemmWeightsReady) ? 1 : 0;
   p.resid_scaled = (pr.flags & kGemmResidScaled) ? 1 : 0;
   p.fmt = pr.fmt;
-  p.E = 1;
+  p.E = E;
+  p.offsets = pr.offsets;
+  p.grouped = grouped ? 1 : 0;
   p.y_vec32 = ((reinterpret_cast<uintptr_t>(pr.y) & 31u) == 0 && (pr.N % 16) == 0) ? 1 : 0;
-  const int64_t tiles = ((pr.M + BMP - 1) / BMP) * ((pr.N + BNP - 1) / BNP);
+  const int64_t n_tiles_n = (pr.N + BNP - 1) / BNP;
+  const int64_t tiles = ((pr.M + BMP - 1) / BMP + (grouped ? E : 0)) * n_tiles_n;  // grouped: an upper bound
   const int64_t clusters = tiles < clusters_max ? tiles : clusters_max;
+  const size_t smem = pair_smem_bytes(grouped ? E : 0);
   cudaError_t err =
-      cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+      cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(2 * clusters));
   cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -2832,14 +2942,23 @@ cudaError_t launch_pair(const GemmProblem& pr, int clusters_max, cudaStream_t st
   return cudaGetLastError();
 }
 
+// Grouped problems whose experts average at least this many rows take the
+// pair kernel's 256-row tiles: per useful row it is about twice as fast as
+// the 128 x 256 single-SM tile (half the B bytes per SM), which outweighs
+// the padding rows of an expert's last 256-row tile from here on.
+constexpr int64_t kPairGroupedMinRows = 192;
+
 cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   // few rows: 128 x 128 tiles keep more SMs busy; dense layers with more
-  // rows: 256 x 256 tiles on CTA pairs; grouped: 128 x 256 tiles (one expert
-  // per tile, so the pair tile's 256 rows would mostly be padding)
+  // rows: 256 x 256 tiles on CTA pairs; grouped: 256 x 256 pair tiles per
+  // expert when the experts are large enough, else 128 x 256 tiles (one
+  // expert per tile); the fused MoE epilogues run on the 128 x 256 kernel
   if (!grouped && pr.M <= 2 * BM) return launch_narrow(pr, grouped, num_sms, stream);
-  if (!grouped) {
+  const bool pair_ok = !grouped || (pr.epi == kEpiStore && pr.M >= kPairGroupedMinRows * pr.E &&
+                                    pair_smem_bytes(pr.E) <= 227 * 1024);
+  if (pair_ok) {
     const int clusters = pair_clusters(num_sms);
-    if (clusters > 0) return launch_pair(pr, clusters, stream);
+    if (clusters > 0) return launch_pair(pr, grouped, clusters, stream);
   }
   return launch_wide(pr, grouped, num_sms, stream);
 }

@@ -343,6 +343,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* d
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_caddr), "r"(x), "r"(y)
       : "memory");
 }
+// The 3D form (per-expert stacked weights of a grouped GEMM).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* desc, uint32_t bar_caddr, int32_t x,
+                                                 int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_caddr), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 // Arrival on named barrier `id` without waiting (the barrier completes when
 // `n` threads have arrived or synced on it).
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {

@@ -138,6 +138,42 @@ def test_grouped_offsets_not_a_partition_are_rejected(nv, bad):
     assert not bool((y == 5.0).all())
 
 
+@pytest.mark.parametrize("bad", ["decreasing", "last_long"])
+def test_grouped_pair_tiles_reject_bad_offsets(nv, bad):
+    # experts large enough for the 256-row pair tiles: the pair kernel checks
+    # the table before any copy, and both CTAs of every pair return
+    E, K, N = 3, 256, 256
+    counts = [300, 260, 250]
+    M = sum(counts)
+    good = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    offs = good.copy()
+    if bad == "decreasing":
+        offs[2] = offs[1] - 7
+    else:
+        offs[-1] = M + 256
+    x = W.activations(M, K, 3, "t3x20", 51, 52).cuda()
+    chan = torch.stack([torch.arange(0, 256, 16, dtype=torch.int32)] * E).cuda()
+    qa = nv.nvfp4_quantize_grouped(x, torch.from_numpy(good).cuda(), chan)
+    wt = torch.stack([W.weights_t(N, K, 60 + e) for e in range(E)]).cuda()
+    qs = [nv.nvfp4_quantize(wt[e]) for e in range(E)]
+    b_codes = torch.stack([s["codes"] for s in qs])
+    b_scales = torch.cat([s["scales"] for s in qs])
+    g_b = torch.cat([s["g"] for s in qs])
+    w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan, E=E)
+    assert nv.check_status()[0] == 0
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.w4a4_grouped_gemm_comp(qa, torch.from_numpy(offs).cuda(), b_codes, b_scales, g_b, N, resid=qa["resid"],
+                              w_sel=w_sel, y=y)
+    st, where = nv.check_status()
+    assert st == nv.ERR_INVALID_ARG and where == 0x300, (st, where)
+    assert bool(torch.isnan(y).all())
+    # the good table writes every row
+    nv.w4a4_grouped_gemm_comp(qa, torch.from_numpy(good).cuda(), b_codes, b_scales, g_b, N, resid=qa["resid"],
+                              w_sel=w_sel, y=y)
+    assert nv.check_status()[0] == 0
+    assert not bool(torch.isnan(y).any())
+
+
 @pytest.mark.parametrize("bad", [-1, 37, 1 << 30])
 def test_gather_index_out_of_range_reported(nv, bad):
     T, K, E, k = 37, 256, 3, 8

@@ -148,6 +148,53 @@ def test_grouped_gemm_small(nv, resid_scaled):
     _assert_close(f32(y), y_ref)
 
 
+@pytest.mark.parametrize("bf16_w,resid_scaled", [(False, False), (False, True), (True, False), (True, True)])
+def test_grouped_gemm_pair_tiles(nv, bf16_w, resid_scaled):
+    # experts averaging >= 192 rows take 256-row tiles on CTA pairs: empty,
+    # one-row, exactly-one-tile and one-past-a-tile experts, a ragged last
+    # 256-column tile (N % 256 = 128), a partial last k-tile (K % 256 = 64),
+    # a partial compensation tile (k = 72), per-expert weight scales
+    counts = [300, 0, 128, 257, 1, 513, 255, 129]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, K, N, k = int(offs[-1]), 576, 384, 72
+    E = len(counts)
+    assert M >= 192 * E
+    x = W.activations(M, K, 5, "t3x20", 13, 14)
+    wt = W.weights_t(N, K, 15, experts=E)
+    rng = np.random.default_rng(11)
+    chan = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(E)]).astype(np.int32)
+    offs_t = torch.from_numpy(offs).cuda()
+    chan_t = torch.from_numpy(chan).cuda()
+    qs = [nv.nvfp4_quantize(wt[e].cuda()) for e in range(E)]
+    b_codes = torch.stack([q["codes"] for q in qs])
+    b_scales = torch.cat([q["scales"] for q in qs])
+    g_b = torch.cat([q["g"] for q in qs])
+    if bf16_w:
+        w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan_t, flags=nv.COMP_W_BF16, wt=wt.cuda(), E=E)
+        flags = nv.COMP_W_BF16
+    else:
+        w_sel = nv.nvfp4_prepare_comp_weights(b_codes, b_scales, chan_t, E=E)
+        flags = nv.COMP_W_DEQ
+    xd = x.cuda()
+    torch.cuda.synchronize()
+    ys = []
+    for ready in (False, True):
+        qx = nv.nvfp4_quantize_grouped(xd, offs_t, chan_t, resid_scaled=resid_scaled)
+        ys.append(nv.w4a4_grouped_gemm_comp(qx, offs_t, b_codes, b_scales, g_b, N, resid=qx["resid"], w_sel=w_sel,
+                                            flags=flags, weights_ready=ready))
+    torch.cuda.synchronize()
+    st, _ = nv.check_status()
+    assert st == 0
+    assert torch.equal(ys[0], ys[1])
+    rq = onv.quantize_grouped(f32(x), offs, chan)
+    a = onv.dequantize(rq["codes"], rq["sigma"], rq["g"])
+    bq = [onv.quantize(f32(wt[e])) for e in range(E)]
+    b = np.stack([onv.dequantize(q["codes"], q["sigma"], q["g"]) for q in bq])
+    ws = np.stack([og.comp_weight_rows(bq[e], chan[e], f32(wt[e]) if bf16_w else None) for e in range(E)])
+    y_ref = og.grouped_reference(a, offs, b, rq["resid"], ws)
+    _assert_close(f32(ys[0]), y_ref)
+
+
 @pytest.mark.parametrize("M,N,K,k", [(16, 1024, 4096, 64), (200, 384, 1024, 32), (600, 512, 2048, 128)])
 def test_weights_ready_overlap_is_bit_identical(nv, M, N, K, k):
     """The GEMM starts while the activation quantizer before it still runs
