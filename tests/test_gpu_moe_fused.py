@@ -86,8 +86,9 @@ def test_swiglu_quant_epilogue(nv, counts, K, inter, k, h_k, scaled):
     assert np.array_equal(bf16_bits_of(fz["resid"]), F.bf16_bits(want)), "residual"
 
 
-def test_combine_epilogue(nv):
-    T, E, top, K, N, k = 96, 12, 4, 512, 384, 32
+@pytest.mark.parametrize("T,E,top", [(96, 12, 4), (512, 4, 2)])  # small experts: 128-row tiles; large: pair tiles
+def test_combine_epilogue(nv, T, E, top):
+    K, N, k = 512, 384, 32
     tok, offs, w_rows, logits = W.route(T, E, top, 31, with_weights=True)
     ex, w = omoe.route_weights(logits.numpy(), top)
     w_oracle = omoe.row_weights(ex, w, tok.numpy(), offs.numpy())
