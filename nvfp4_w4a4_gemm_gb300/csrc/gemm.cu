@@ -1417,9 +1417,10 @@ struct PairTile {
   int64_t nt;
 };
 
+template <bool kGrouped>
 __device__ __forceinline__ void pair_tile_of(const GemmParams& p, const SchedSmem& s, int64_t t, int n_tiles_n,
                                              PairTile& o) {
-  if (!p.grouped) {
+  if (!kGrouped) {
     const int64_t mt = t / n_tiles_n;
     o.e = 0;
     o.nt = t - mt * n_tiles_n;
@@ -1454,6 +1455,7 @@ __device__ __forceinline__ uint32_t idesc_bf16_pair() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1485,7 +1487,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   if (!p.early_w) pdl_wait();
   const int n_tiles_n = (int)((p.N + BNP - 1) / BNP);
   SchedSmem sched{};
-  if (p.grouped) {
+  if (kGrouped) {
     // both CTAs of a pair read the same offsets, so on a bad table both
     // return here, before any barrier, TMEM or cluster step
     sched.off = s_sched;
@@ -1534,7 +1536,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int64_t num_tiles =
-      p.grouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BMP - 1) / BMP) * (int64_t)n_tiles_n;
+      kGrouped ? (int64_t)sched.tile_start[p.E] : ((p.M + BMP - 1) / BMP) * (int64_t)n_tiles_n;
   const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int cpk = p.fmt == 1 ? 2 : 4;                     // 512-byte scale chunks per 256-element k-tile
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
@@ -1563,7 +1565,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       uint8_t* dst = stages + stg * kPStageBytes + kPTileA;
       const uint32_t fb = full0 + 8u * (uint32_t)stg;
       const int32_t n = (int32_t)(tl.nt * BNP + BM * rank);
-      if (p.grouped) tma_load_3d_pair(dst, &p.tm_b, fb, kt * BKB, n, tl.e);
+      if (kGrouped) tma_load_3d_pair(dst, &p.tm_b, fb, kt * BKB, n, tl.e);
       else tma_load_2d_pair(dst, &p.tm_b, fb, kt * BKB, n);
     };
     auto issue_a = [&](int stg, const PairTile& tl, int kt) {
@@ -1575,7 +1577,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     int pre = 0;
     if (p.early_w && pair < num_tiles) {
       PairTile tl;
-      pair_tile_of(p, sched, pair, n_tiles_n, tl);
+      pair_tile_of<kGrouped>(p, sched, pair, n_tiles_n, tl);
       pre = n_kt < kPStages ? n_kt : kPStages;
       if (elect_one()) {
         for (int i = 0; i < pre; ++i) {
@@ -1592,7 +1594,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
       PairTile tl;
-      pair_tile_of(p, sched, t, n_tiles_n, tl);
+      pair_tile_of<kGrouped>(p, sched, t, n_tiles_n, tl);
       for (int kt = 0; kt < n_kt && ok; ++kt) {
         const bool early = issued++ < pre;  // B half already in flight, stage known empty
         if (!early && !mbar_wait_warp(&empty[stage], phase ^ 1u, kWaitEmpty, s_abort)) { ok = false; break; }
@@ -1612,7 +1614,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
           const int32_t n = (int32_t)(tl.nt * BNP + BM * rank);
           if (leader) mbar_arrive_expect_tx(&full[stage], kTx);
           tma_load_2d_pair(sa, &p.tm_r, fb, ct * 64, (int32_t)(tl.row0 + BM * rank));
-          if (p.grouped) tma_load_3d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n, tl.e);
+          if (kGrouped) tma_load_3d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n, tl.e);
           else tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n);
         }
         __syncwarp();
@@ -1736,7 +1738,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     bool ok = true;
     for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
       PairTile tl;
-      pair_tile_of(p, sched, t, n_tiles_n, tl);
+      pair_tile_of<kGrouped>(p, sched, t, n_tiles_n, tl);
       // 128-row scale tiles (of the expert's slice of the stacked B scales)
       const int64_t at = tl.sf_rt + rank, bt = (int64_t)tl.e * p.b_sf_expert_tiles + tl.nt * 2;
       for (int kt = 0; kt < n_kt && ok; ++kt) {
@@ -1832,20 +1834,22 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
     const float ga = p.g_a ? *p.g_a : 1.f;
     const uint32_t comp_ready_l0 = cluster_addr(comp_ready, 0);
     const uint32_t acc_empty_l = cluster_addr(acc_empty, 0);
-    int e_prev = -1;
-    float gb = 1.f, c = 1.f;
+    // the weight scale and the residual factor it sets: the expert's, per
+    // tile when grouped
+    auto residual_factor = [&](float g) {
+      if (p.resid_scaled) return p.flags == 1 ? __fdiv_rn(1.0f, g) : 1.f;
+      return p.flags == 1 ? __fdiv_rn(1.0f, ga * g) : __fdiv_rn(1.0f, ga);
+    };
+    int e_prev = 0;
+    float gb = p.g_b ? *p.g_b : 1.f;
+    float c = residual_factor(gb);
     for (int64_t t = pair; t < num_tiles; t += n_pairs) {
       PairTile tl;
-      pair_tile_of(p, sched, t, n_tiles_n, tl);
-      if (tl.e != e_prev) {  // the expert's weight scale and the residual factor it sets
+      pair_tile_of<kGrouped>(p, sched, t, n_tiles_n, tl);
+      if (kGrouped && tl.e != e_prev) {
         e_prev = tl.e;
         gb = p.g_b ? p.g_b[tl.e] : 1.f;
-        c = 1.f;
-        if (p.resid_scaled) {
-          if (p.flags == 1) c = __fdiv_rn(1.0f, gb);
-        } else {
-          c = p.flags == 1 ? __fdiv_rn(1.0f, ga * gb) : __fdiv_rn(1.0f, ga);
-        }
+        c = residual_factor(gb);
       }
       if (scale_r) {
         stage = (stage + n_kt) % kPStages;
@@ -2823,7 +2827,7 @@ int pair_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::call_once(once[dev], [dev, num_sms] {
     int n = 0;
-    if (cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(w4a4_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPSmemBytes) == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
       cfg.gridDim = dim3((unsigned)(num_sms & ~1));
@@ -2836,7 +2840,7 @@ int pair_clusters(int num_sms) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, w4a4_gemm_pair_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, w4a4_gemm_pair_kernel<false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     cached[dev] = n;
@@ -2920,8 +2924,8 @@ cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, c
   const int64_t tiles = ((pr.M + BMP - 1) / BMP + (grouped ? E : 0)) * n_tiles_n;  // grouped: an upper bound
   const int64_t clusters = tiles < clusters_max ? tiles : clusters_max;
   const size_t smem = pair_smem_bytes(grouped ? E : 0);
-  cudaError_t err =
-      cudaFuncSetAttribute(w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = grouped ? w4a4_gemm_pair_kernel<true> : w4a4_gemm_pair_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(2 * clusters));
@@ -2937,7 +2941,7 @@ cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  err = cudaLaunchKernelEx(&cfg, w4a4_gemm_pair_kernel, p);
+  err = cudaLaunchKernelEx(&cfg, kern, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
