@@ -24,10 +24,11 @@
 //                          swaps the operands (weight rows in the MMA's M
 //                          slot) and may split K across CTAs
 //   w4a4_gemm_wide_kernel  128 x 256 tiles, 384 threads: the grouped (MoE)
-//                          GEMM and its fused SwiGLU-quantize / combine
-//                          epilogues
+//                          GEMM of small experts and the fused SwiGLU-quantize
+//                          / combine epilogues
 //   w4a4_gemm_pair_kernel  256 x 256 tiles on a CTA pair (cta_group::2), 384
-//                          threads: dense GEMMs with more than 256 rows
+//                          threads: dense GEMMs with more than 256 rows, and
+//                          grouped ones whose experts average >= 192 rows
 //   w4a4_decode_kernel     the whole layer for at most 16 tokens (the token
 //                          quantization in the same launch), 320 threads
 // After the FP4 k-tiles of an output tile the producer streams the
