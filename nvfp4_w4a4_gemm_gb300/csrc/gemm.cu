@@ -758,17 +758,6 @@ __device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile
   const int64_t hcol0 = (int64_t)(tl.n0 / 2) + 64 * hh;
   const int64_t n_cg_h = (p.h_cols / 16 + 3) / 4;
   const int32_t* S = p.h_chan + (int64_t)tl.e * p.h_k;
-  // slots [s_lo, s_hi) of the expert's sorted channel list that fall in this
-  // warp's 64 columns (binary searches, the same for the whole warp)
-  int s_lo = 0, s_hi = p.h_k;
-  {
-    int lo = 0, hi = p.h_k;
-    while (lo < hi) { const int mid = (lo + hi) >> 1; if (S[mid] < hcol0) lo = mid + 1; else hi = mid; }
-    s_lo = lo;
-    hi = p.h_k;
-    while (lo < hi) { const int mid = (lo + hi) >> 1; if (S[mid] < hcol0 + 64) lo = mid + 1; else hi = mid; }
-    s_hi = lo;
-  }
   const uint32_t t_g = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(64 * hh);
   uint32_t scale_word = 0;
   // the projection's bf16 outputs, packed two per register as they come out
@@ -794,56 +783,71 @@ __device__ __forceinline__ void epi_swiglu_quant(const GemmParams& p, const Tile
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(acc_empty);  // accumulator free: the next tile's MMAs may start
+  // slots [s_lo, s_hi) of the expert's sorted channel list that fall in this
+  // warp's 64 columns: the entries below each bound, counted 32 at a time
+  // across the warp (independent loads, no chain of dependent ones)
+  int s_lo = 0, s_hi = 0;
+  for (int b0 = 0; b0 < p.h_k; b0 += 32) {  // warp-uniform trip count
+    const int i = b0 + lane;
+    const int32_t v = i < p.h_k ? S[i] : 0x7FFFFFFF;
+    s_lo += __popc(__ballot_sync(0xffffffffu, v < hcol0));
+    s_hi += __popc(__ballot_sync(0xffffffffu, v < hcol0 + 64));
+  }
+  // the four 16-column blocks in a loop that is not unrolled (one copy of
+  // the block's code: unrolled four times it no longer fit the instruction
+  // cache), each block's packed values moved to the front of a register
+  // window so that every index stays constant
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float hv[16];
+    float am = 0.f;
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {
+    for (int i = 0; i < 16; i += 2) {
+      const uint32_t wg = pg[0][i / 2], wu = pu[0][i / 2];
+      const float2 hh2 = bf16r2(swiglu_f32(__uint_as_float(wg << 16), __uint_as_float(wu << 16)),
+                                swiglu_f32(__uint_as_float(wg & 0xFFFF0000u), __uint_as_float(wu & 0xFFFF0000u)));
+      hv[i] = hh2.x;
+      hv[i + 1] = hh2.y;
+      am = fmaxf(am, fmaxf(fabsf(hh2.x), fabsf(hh2.y)));
+    }
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      const int c = 2 * b + blk;
-      float hv[16];
-      float am = 0.f;
+    for (int i = 0; i < 8; ++i) {
+      pg[0][i] = pg[1][i]; pg[1][i] = pg[2][i]; pg[2][i] = pg[3][i];
+      pu[0][i] = pu[1][i]; pu[1][i] = pu[2][i]; pu[2][i] = pu[3][i];
+    }
+    const uint32_t sig = block_scale_byte(am, g_h, yg_h, fast_h);
+    const float2 dr = s_dr[sig];
+    uint32_t w0 = 0, w1 = 0;
+    if (dr.x != 0.f) {
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const uint32_t wg = pg[c][i / 2], wu = pu[c][i / 2];
-        const float2 hh2 = bf16r2(swiglu_f32(__uint_as_float(wg << 16), __uint_as_float(wu << 16)),
-                                  swiglu_f32(__uint_as_float(wg & 0xFFFF0000u), __uint_as_float(wu & 0xFFFF0000u)));
-        hv[i] = hh2.x;
-        hv[i + 1] = hh2.y;
-        am = fmaxf(am, fmaxf(fabsf(hh2.x), fabsf(hh2.y)));
+      for (int i = 0; i < 4; ++i) {
+        w0 |= cvt_e2m1x2(__fmul_rn(hv[2 * i], dr.y), __fmul_rn(hv[2 * i + 1], dr.y)) << (8 * i);
+        w1 |= cvt_e2m1x2(__fmul_rn(hv[8 + 2 * i], dr.y), __fmul_rn(hv[8 + 2 * i + 1], dr.y)) << (8 * i);
       }
-      const uint32_t sig = block_scale_byte(am, g_h, yg_h, fast_h);
-      const float2 dr = s_dr[sig];
-      uint32_t w0 = 0, w1 = 0;
-      if (dr.x != 0.f) {
+    }
+    scale_word |= sig << (8 * c);
+    const int64_t c0 = hcol0 + 16 * c;  // first column of this block
+    if (row_ok) {
+      *reinterpret_cast<uint2*>(p.h_codes + row * (p.h_cols / 2) + c0 / 2) = make_uint2(w0, w1);
+      if (p.h_out != nullptr) {
+        uint32_t hb[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          w0 |= cvt_e2m1x2(__fmul_rn(hv[2 * i], dr.y), __fmul_rn(hv[2 * i + 1], dr.y)) << (8 * i);
-          w1 |= cvt_e2m1x2(__fmul_rn(hv[8 + 2 * i], dr.y), __fmul_rn(hv[8 + 2 * i + 1], dr.y)) << (8 * i);
+        for (int i = 0; i < 8; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * i], hv[2 * i + 1]);
+          hb[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
+        uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.h_cols + c0);
+        dst[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+        dst[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
       }
-      scale_word |= sig << (8 * (2 * b + blk));
-      const int64_t c0 = hcol0 + 32 * b + 16 * blk;  // first column of this block
-      if (row_ok) {
-        *reinterpret_cast<uint2*>(p.h_codes + row * (p.h_cols / 2) + c0 / 2) = make_uint2(w0, w1);
-        if (p.h_out != nullptr) {
-          uint32_t hb[8];
+      // residual slots of the expert's channel set that fall in this block
+      for (int i = s_lo; i < s_hi; ++i) {
+        const int32_t j = S[i];
+        if (j >= c0 && j < c0 + 16) {
+          float x = 0.f;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * i], hv[2 * i + 1]);
-            hb[i] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.h_cols + c0);
-          dst[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-          dst[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
-        }
-        // residual slots of the expert's channel set that fall in this block
-        for (int i = s_lo; i < s_hi; ++i) {
-          const int32_t j = S[i];
-          if (j >= c0 && j < c0 + 16) {
-            float x = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x = (j - c0 == e) ? hv[e] : x;
-            p.h_resid[row * p.h_k + i] = element_residual(x, dr.x, dr.y, rs_h);
-          }
+          for (int e = 0; e < 16; ++e) x = (j - c0 == e) ? hv[e] : x;
+          p.h_resid[row * p.h_k + i] = element_residual(x, dr.x, dr.y, rs_h);
         }
       }
     }
@@ -863,8 +867,8 @@ __device__ __forceinline__ void epi_combine(const GemmParams& p, const Tile& tl,
                                             uint32_t tmem, float alpha, uint64_t* acc_empty) {
   const int64_t col0 = tl.n0 + hh * 128;
   const int cq = 2 * (lane & 3);  // this lane's column pair within each group of 8
-#pragma unroll
-  for (int rh = 0; rh < 2; ++rh) {
+#pragma unroll 1
+  for (int rh = 0; rh < 2; ++rh) {  // not unrolled: one copy of the code stays in the instruction cache
     // this lane's two rows of the 16-row half: r and r + 8
     float* dst[2] = {nullptr, nullptr};
     float w[2] = {0.f, 0.f};
