@@ -1984,7 +1984,7 @@ constexpr int kDecStageBytes = kDecSub * (kTileBytes + kSfBytes);  // 36 KB: 2 c
 constexpr int kDecMaxStages = 7;  // TMEM: 64 + 64 * 7 = 512 columns
 constexpr int kDecQuantWarps = 8;
 constexpr int kDecCluster = 4;   // CTAs sharing the token quantization
-constexpr int kDecGroup = 8;     // owned k-tiles whose blocks a thread holds in registers at once
+constexpr int kDecGroup = 4;     // owned k-tiles whose blocks a thread holds in registers at once (the loop over them is unrolled: 8 made the code too large for the instruction cache)
 constexpr uint32_t kDecColSf = 64;
 static_assert(kDecColSf + 32u * kDecSub * kDecMaxStages <= kTmemCols, "TMEM budget");
 static_assert(2 + kDecQuantWarps == kDecThreads / 32, "warp roles");
