@@ -626,23 +626,65 @@ __device__ __forceinline__ float e2m1_mag(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-// x / s* rounded to fp32 for the code at the ideal scale s*: x * RN(1/s*)
-// is within 2 fp32 ulps of RN(x / s*), so it rounds to the same E2M1 code
-// unless it lies within a few ulps of an E2M1 rounding midpoint (0.25, 0.75,
-// 1.25, 1.75, 2.5, 3.5, 5: fp32 patterns whose low 21 bits are zero); those
-// elements, and blocks with a tiny or huge s*, take the IEEE division.
-__device__ __forceinline__ float ideal_quotient_of(float x, float y, float ss, bool fast) {
-  const uint32_t m = (__float_as_uint(y) + 8u) & 0x1FFFFFu;
-  return (!fast || m <= 16u) ? __fdiv_rn(x, ss) : y;
-}
-__device__ __forceinline__ float ideal_quotient(float x, float ss, float rss, bool fast) {
-  return ideal_quotient_of(x, __fmul_rn(x, rss), ss, fast);
-}
-
 // Two E2M1 codes (one byte, low nibble first) -> their two values.
 __device__ __forceinline__ float2 e2m1x2_vals(uint32_t byte) {
   const uint32_t h2 = cvt_e2m1x2_to_f16x2(byte);
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// Decomposition energies {|B|^2, |D|^2, |G|^2, |E|^2} and the deadzone count
+// of one 32-element block (v: its bf16 elements, cw: its codes at the E8M0
+// scale 2^e), through the ideal scale ss = RN(a / 6):
+//   B = Q_s - Q*,  D / G = Q* - x on zero / non-zero codes at ss,  E = Q_s - x
+// with Q* = E2M1(RN(x / ss)) ss.  Each element pair goes through f32x2
+// arithmetic: the per-element products and differences are the fp32
+// operations of the definition; the energies are summed over even and odd
+// elements separately and the two partial sums added at the end.
+// kFast (ss in [2^-100, 2^100]): RN(x / ss) from the product with the rounded
+// reciprocal and two fma corrections (y0 = RN(x RN(1/ss)), r = x - y ss
+// exact by an fma, y1 = RN(y0 + r0 RN(1/ss)), q = RN(y1 + r1 RN(1/ss));
+// Markstein's division refinement, the correctly rounded quotient when no
+// step underflows, which the range guarantees wherever the code can change);
+// otherwise the IEEE division of every element.
+template <bool kFast>
+__device__ __forceinline__ float4 mx_block_stats(const uint4 (&v)[4], const uint4& cw, int e, float ss, uint32_t& nd) {
+  const float rss = __frcp_rn(ss);
+  const float sc = pow2f(e);
+  const uint64_t rss2 = f2_pack(rss, rss), nss2 = f2_pack(-ss, -ss), sc2 = f2_pack(sc, sc), ss2 = f2_pack(ss, ss);
+  uint64_t EE = 0, EB = 0, ED = 0, EG = 0;  // {even, odd} sums (+0.0f pairs)
+  const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                           v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+  const uint32_t cq4[4] = {cw.x, cw.y, cw.z, cw.w};
+  nd = 0;
+#pragma unroll
+  for (int pr = 0; pr < 16; ++pr) {
+    const uint32_t word = wv[pr];
+    const float x0 = __uint_as_float(word << 16), x1 = __uint_as_float(word & 0xFFFF0000u);
+    const uint64_t X = f2_pack(x0, x1);
+    float2 q;
+    if (kFast) {
+      const uint64_t Y0 = f2_mul(X, rss2);
+      const uint64_t Y1 = f2_fma(f2_fma(Y0, nss2, X), rss2, Y0);
+      q = f2_unpack(f2_fma(f2_fma(Y1, nss2, X), rss2, Y1));
+    } else {
+      q = make_float2(__fdiv_rn(x0, ss), __fdiv_rn(x1, ss));
+    }
+    const uint32_t cqb = (cq4[pr >> 2] >> (8 * (pr & 3))) & 0xFFu;
+    const uint32_t csb = cvt_e2m1x2(q.x, q.y);
+    const float2 vq = e2m1x2_vals(cqb), vs = e2m1x2_vals(csb);
+    const uint64_t QS = f2_mul(f2_pack(vq.x, vq.y), sc2);
+    const uint64_t QST = f2_mul(f2_pack(vs.x, vs.y), ss2);
+    const uint64_t Ev = f2_sub(QS, X), Bv = f2_sub(QS, QST), Rv = f2_sub(QST, X);
+    EE = f2_fma(Ev, Ev, EE);
+    EB = f2_fma(Bv, Bv, EB);
+    const float2 r2 = f2_unpack(f2_mul(Rv, Rv));
+    const bool dz0 = (csb & 7u) == 0u, dz1 = ((csb >> 4) & 7u) == 0u;
+    ED = f2_add(ED, f2_pack(dz0 ? r2.x : 0.f, dz1 ? r2.y : 0.f));
+    EG = f2_add(EG, f2_pack(dz0 ? 0.f : r2.x, dz1 ? 0.f : r2.y));
+    nd += ((dz0 && x0 != 0.f) ? 1u : 0u) + ((dz1 && x1 != 0.f) ? 1u : 0u);
+  }
+  const float2 e2 = f2_unpack(EE), b2 = f2_unpack(EB), d2 = f2_unpack(ED), g2 = f2_unpack(EG);
+  return make_float4(b2.x + b2.y, d2.x + d2.y, g2.x + g2.y, e2.x + e2.y);
 }
 
 // One warp per unit of 1024 columns of a row; each lane owns one 32-element
@@ -697,52 +739,16 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
       *reinterpret_cast<uint32_t*>(a.scales + tile_group_offset(r, (gi * 32 + lane) / 4, n_cg)) =
           sb | (s1 << 8) | (s2b << 16) | (s3 << 24);
     if (kStats && valid) {
-      // decomposition through the ideal scale s* = a / 6 (fp32):
-      //   B = Q_s - Q*,  D / G = Q* - x on zero / non-zero codes at s*,  E = Q_s - x
-      // Each element pair (2pr, 2pr + 1) goes through f32x2 arithmetic: the
-      // per-element products and differences are the fp32 operations of the
-      // definition; the four energies are summed over even and odd elements
-      // separately and the two partial sums added at the end.
-      float eb = 0.f, ed = 0.f, eg = 0.f, ee = 0.f;
+      // decomposition through the ideal scale s* = RN(a / 6)
+      float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
       uint32_t nd = 0;
       if (am > 0.f) {
         const float ss = div6_rn(am);
-        const float rss = __frcp_rn(ss);
-        const bool fast = ss >= 0x1p-120f && ss <= 0x1p120f;
-        const float sc = pow2f(e);
-        const uint64_t rss2 = f2_pack(rss, rss), sc2 = f2_pack(sc, sc), ss2 = f2_pack(ss, ss);
-        uint64_t EE = 0, EB = 0, ED = 0, EG = 0;  // {even, odd} sums (+0.0f pairs)
-        const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
-                                 v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-        const uint32_t cq4[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int pr = 0; pr < 16; ++pr) {
-          const uint32_t word = wv[pr];
-          const float x0 = __uint_as_float(word << 16), x1 = __uint_as_float(word & 0xFFFF0000u);
-          const uint64_t X = f2_pack(x0, x1);
-          const float2 y = f2_unpack(f2_mul(X, rss2));
-          const uint32_t cqb = (cq4[pr >> 2] >> (8 * (pr & 3))) & 0xFFu;
-          const uint32_t csb = cvt_e2m1x2(ideal_quotient_of(x0, y.x, ss, fast), ideal_quotient_of(x1, y.y, ss, fast));
-          const float2 vq = e2m1x2_vals(cqb), vs = e2m1x2_vals(csb);
-          const uint64_t QS = f2_mul(f2_pack(vq.x, vq.y), sc2);
-          const uint64_t QST = f2_mul(f2_pack(vs.x, vs.y), ss2);
-          const uint64_t Ev = f2_sub(QS, X), Bv = f2_sub(QS, QST), Rv = f2_sub(QST, X);
-          EE = f2_fma(Ev, Ev, EE);
-          EB = f2_fma(Bv, Bv, EB);
-          const float2 r2 = f2_unpack(f2_mul(Rv, Rv));
-          const bool dz0 = (csb & 7u) == 0u, dz1 = ((csb >> 4) & 7u) == 0u;
-          ED = f2_add(ED, f2_pack(dz0 ? r2.x : 0.f, dz1 ? r2.y : 0.f));
-          EG = f2_add(EG, f2_pack(dz0 ? 0.f : r2.x, dz1 ? 0.f : r2.y));
-          nd += ((dz0 && x0 != 0.f) ? 1u : 0u) + ((dz1 && x1 != 0.f) ? 1u : 0u);
-        }
-        const float2 e2 = f2_unpack(EE), b2 = f2_unpack(EB), d2 = f2_unpack(ED), g2 = f2_unpack(EG);
-        ee = e2.x + e2.y;
-        eb = b2.x + b2.y;
-        ed = d2.x + d2.y;
-        eg = g2.x + g2.y;
+        if (ss >= 0x1p-100f && ss <= 0x1p100f) st = mx_block_stats<true>(v, cw, e, ss, nd);
+        else st = mx_block_stats<false>(v, cw, e, ss, nd);
       }
       const int64_t bidx = r * nblk + gi * 32 + lane;
-      if (a.stats != nullptr) *reinterpret_cast<float4*>(a.stats + bidx * 4) = make_float4(eb, ed, eg, ee);
+      if (a.stats != nullptr) *reinterpret_cast<float4*>(a.stats + bidx * 4) = st;
       if (a.dead != nullptr) a.dead[bidx] = (uint8_t)nd;
     }
   }
