@@ -81,6 +81,13 @@ int check_quant_args(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8
   return NVFP4_OK;
 }
 
+// No rows and a static tensor scale: nothing to launch, but g_out still
+// receives the scale used (one device copy on the caller's stream).
+int static_scale_of_no_rows(const float* g_in, float* g_out, void* stream) {
+  if (g_out == nullptr) return NVFP4_OK;
+  return from_cuda(cudaMemcpyAsync(g_out, g_in, sizeof(float), cudaMemcpyDeviceToDevice, as_stream(stream)));
+}
+
 // Expert-grouped quantize of M_total operand rows; with a routing gather
 // (token_of_row != nullptr) row r is x's token row token_of_row[r] of T.
 int quantize_grouped(const uint16_t* x, int64_t T, const int32_t* token_of_row, int64_t M_total, int64_t K,
@@ -95,7 +102,7 @@ int quantize_grouped(const uint16_t* x, int64_t T, const int32_t* token_of_row, 
     return NVFP4_ERR_WORKSPACE;
   const DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
-  if (M_total == 0 && g_in != nullptr) return NVFP4_OK;
+  if (M_total == 0 && g_in != nullptr) return static_scale_of_no_rows(g_in, g_out, stream);
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M_total, K, ldx, g_in, g_out, codes, scales, chan, k,
                                               bf(resid), offsets, E, static_cast<float*>(workspace),
                                               quant_barrier(workspace), d->num_sms, as_stream(stream),
@@ -154,7 +161,7 @@ int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, cons
     return NVFP4_ERR_WORKSPACE;
   const DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
-  if (M == 0 && g_in != nullptr) return NVFP4_OK;
+  if (M == 0 && g_in != nullptr) return static_scale_of_no_rows(g_in, g_out, stream);
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M, K, ldx, g_in, g_out, codes, scales, chan, k, bf(resid),
                                               nullptr, 1, static_cast<float*>(workspace), quant_barrier(workspace),
                                               d->num_sms, as_stream(stream),
@@ -229,7 +236,7 @@ int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float*
   const DeviceInfo* d = nullptr;
   int st;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
-  if (M == 0 && g_in != nullptr) return NVFP4_OK;
+  if (M == 0 && g_in != nullptr) return static_scale_of_no_rows(g_in, g_out, stream);
   return from_cuda(nv4::launch_nvfp4_qdq(bf(w), M, K, ldw, g_in, g_out, bf(w_qdq), ld_out, codes, scales,
                                          static_cast<float*>(workspace),
                                          g_in == nullptr ? quant_barrier(workspace) : nullptr, d->num_sms,
