@@ -95,6 +95,26 @@ def e4m3_encode(v):
     return _nearest_even(E4M3_VALUES, v).astype(np.uint8)
 
 
+def e4m3_encode_signed(v):
+    """Round finite values to E4M3FN bytes with the sign in bit 7 (the
+    element type of the FP8 compensation operands): the magnitude as
+    :func:`e4m3_encode` (nearest, ties to even, saturating at 448), the sign
+    bit = signbit(v), so a negative value that rounds to zero gives 0x80."""
+    v = np.asarray(v, dtype=np.float64)
+    if np.any(~np.isfinite(v)):
+        raise ValueError("e4m3_encode_signed: inputs must be finite")
+    mag = _nearest_even(E4M3_VALUES, np.abs(v)).astype(np.uint8)
+    return (mag | (np.signbit(v).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def e4m3_value(byte):
+    """Decode E4M3FN bytes with a sign bit (0x7F and 0xFF, the NaNs,
+    excluded) to float64."""
+    b = np.asarray(byte, dtype=np.uint8)
+    mag = e4m3_decode(b & 0x7F)
+    return np.where(b & 0x80, -mag, mag)
+
+
 # ---------------------------------------------------------------- E8M0 ----
 
 def e8m0_value(byte):

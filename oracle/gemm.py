@@ -16,11 +16,22 @@ columns S of W^T: deq(q(W^T))[:, S] by default (so the correction uses the
 same quantized weights as the rollout GEMM), or the original bf16 W^T[:, S]
 under the BF16-weight flag.  Everything is formed in fp64, where the
 dequantized operands are exact.
+
+Quantized-residual variant (the explainer's "second-pass quantization" of
+the high-residual channels, section 2.2 B, read as FP8 E4M3 operands for
+the compensation product):
+
+    Y = deq(q(X)) . deq(q(W^T))^T  +  2^3 g_a g_w  R8 . W8^T
+
+with R8 [M, k] the E4M3 residual of the residual pre-scaled by 1/g_a
+(nvfp4.quantize's resid_fp8) and W8 [N, k] the E4M3 weight rows
+E2M1 * sigma * 2^-3 (nvfp4.comp_weights_fp8), both decoded exactly in fp64.
 """
 
 import numpy as np
 
 from . import nvfp4
+from .formats import e4m3_value
 
 
 def reference(a_deq, b_deq, resid=None, w_sel=None):
@@ -73,6 +84,30 @@ def linear_comp(x, wt, chan, g_x=None, bf16_weights=False):
     else:
         y = reference(a, b)
     return y, qx, qw
+
+
+def comp_term_fp8(resid_fp8, w_fp8, g_a, g_w):
+    """The quantized-residual compensation term 2^3 g_a g_w R8 . W8^T in
+    fp64, R8 [M, k] and W8 [N, k] E4M3 bytes."""
+    r = e4m3_value(resid_fp8)
+    w = e4m3_value(w_fp8)
+    f = np.float64(2.0 ** nvfp4.COMP_FP8_SHIFT) * np.float64(g_a) * np.float64(g_w)
+    return f * (r @ w.T)
+
+
+def linear_comp_fp8(x, wt, chan, g_x=None):
+    """Whole dense layer with the quantized-residual compensation: quantize X
+    (dynamic scale unless g_x given) and W^T (dynamic scale), then
+    deq . deq^T + comp_term_fp8.  Returns (Y fp64, qx, qw, w_fp8)."""
+    qx = nvfp4.quantize(x, g=g_x, chan=chan)
+    qw = nvfp4.quantize(wt)
+    a = nvfp4.dequantize(qx["codes"], qx["sigma"], qx["g"])
+    b = nvfp4.dequantize(qw["codes"], qw["sigma"], qw["g"])
+    y = reference(a, b)
+    w8 = nvfp4.comp_weights_fp8(qw["codes"], qw["sigma"], chan)
+    if len(chan):
+        y = y + comp_term_fp8(qx["resid_fp8"], w8, qx["g"], qw["g"])
+    return y, qx, qw, w8
 
 
 def grouped_reference(a_deq, offsets, b_deq, resid=None, w_sel=None):

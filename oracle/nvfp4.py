@@ -29,6 +29,14 @@ Readings (the pages name NVFP4 but do not define its arithmetic):
   reciprocal of the tensor scale, fp32 multiply), rounded once to bf16.  The
   GEMM multiplies the compensation product by g again, so R_S . W_S is
   unchanged up to that rounding.
+* Quantized residual (the explainer's "second-pass quantization" of the
+  high-residual channels, section 2.2 B; the spec's residual stays BF16):
+  the pre-scaled fp32 residual R_i * fp32(1 / g) rounded once to FP8 E4M3
+  (RNE, satfinite, sign kept).  |R_i / g| is at most about the block's E4M3
+  scale, so the value lands in E4M3's range without a scale of its own.  The
+  matching weight rows are E4M3(E2M1(code) * sigma * 2^-3): the largest
+  product 6 * 448 = 2688 times 2^-3 is 336 <= 448; the GEMM multiplies the
+  FP8 product by 2^3 again.
 * Trainer-side fake quantization (QDQ, asymmetric W4A16 QAT): the same
   codes and scales, and per element bf16_rn(deq_i), deq_i as above (the
   fp32 product rounded once more to bf16, the trainer's weight dtype).
@@ -43,7 +51,7 @@ Readings (the pages name NVFP4 but do not define its arithmetic):
 import numpy as np
 
 from .formats import (bf16_round, e2m1_encode, e2m1_value, e4m3_decode,
-                      e4m3_encode)
+                      e4m3_encode, e4m3_encode_signed)
 
 BLOCK = 16
 AMAX_TO_G = np.float32(2688.0)  # 6 * 448
@@ -94,6 +102,8 @@ def quantize(x, g=None, chan=None):
       resid_f32 [M, K]  float32 residual x - deq (before bf16 rounding)
       resid   [M, k]    float32 bf16-rounded residual on S (if chan given)
       resid_scaled [M, k] float32 bf16(resid_f32 * fp32(1/g)) on S (if chan given)
+      resid_fp8 [M, k]  uint8  E4M3 bytes of fp32(resid_f32 * fp32(1/g)) on S
+                               (the quantized residual; if chan given)
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     M, K = x.shape
@@ -111,7 +121,9 @@ def quantize(x, g=None, chan=None):
     if chan is not None:
         chan = np.asarray(chan, dtype=np.int64)
         out["resid"] = bf16_round(resid_f32[:, chan])
-        out["resid_scaled"] = bf16_round((resid_f32[:, chan] * reciprocal(g)).astype(np.float32))
+        pre = (resid_f32[:, chan] * reciprocal(g)).astype(np.float32)
+        out["resid_scaled"] = bf16_round(pre)
+        out["resid_fp8"] = e4m3_encode_signed(pre)
     return out
 
 
@@ -260,3 +272,14 @@ def comp_weights(codes_w, sigma_w, chan):
     v = e2m1_value(codes_w[:, chan])
     s = e4m3_decode(sigma_w[:, chan // BLOCK])
     return v * s
+
+
+#: power-of-two factor of the FP8 compensation weight rows (2688 * 2^-3 <= 448)
+COMP_FP8_SHIFT = 3
+
+
+def comp_weights_fp8(codes_w, sigma_w, chan):
+    """FP8 compensation weight rows: E4M3 bytes (sign in bit 7) of
+    :func:`comp_weights` times 2^-3, shape [N, k].  The product with 2^-3 is
+    exact in fp64; the one rounding is to E4M3 (RNE, satfinite)."""
+    return e4m3_encode_signed(comp_weights(codes_w, sigma_w, chan) * 2.0 ** -COMP_FP8_SHIFT)
