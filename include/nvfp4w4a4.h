@@ -64,11 +64,12 @@ enum { NVFP4_FMT_NVFP4 = 0, NVFP4_FMT_MXFP4 = 1 };
 /* Compensation weight rows: the dequantized NVFP4 weight columns (default;
  * the correction then uses the same weights as the W4A4 product), or the
  * original bf16 weight columns. */
-enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1 };
+enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1, NVFP4_COMP_W_DEQ_FP8 = 2 };
 /* GEMM flag bits, OR-ed with the compensation mode (see w4a4_gemm_comp). */
-enum { NVFP4_GEMM_WEIGHTS_READY = 0x100, NVFP4_GEMM_RESID_SCALED = 0x200 };
-/* Quantizer flag bit (nvfp4_quantize_ex / nvfp4_quantize_grouped_ex). */
-enum { NVFP4_QUANT_RESID_SCALED = 1 };
+enum { NVFP4_GEMM_WEIGHTS_READY = 0x100, NVFP4_GEMM_RESID_SCALED = 0x200, NVFP4_GEMM_COMP_FP8 = 0x400 };
+/* Quantizer flag bits (nvfp4_quantize_ex; nvfp4_quantize_grouped_ex takes
+ * NVFP4_QUANT_RESID_SCALED only). */
+enum { NVFP4_QUANT_RESID_SCALED = 1, NVFP4_QUANT_RESID_FP8 = 2 };
 
 /* Library version (major*10000 + minor*100 + patch). */
 int nvfp4_version(void);
@@ -139,8 +140,17 @@ int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const f
  * NVFP4_GEMM_RESID_SCALED.  Codes, scales and g are those of nvfp4_quantize.
  * Source: as nvfp4_quantize (the residual term R_S of Residual Activation
  * Compensation); the division by g is this library's operand form.
- * flags  0 (exactly nvfp4_quantize) or NVFP4_QUANT_RESID_SCALED; other bits
- *        give NVFP4_ERR_INVALID_ARG
+ * NVFP4_QUANT_RESID_SCALED | NVFP4_QUANT_RESID_FP8 writes the same pre-scaled
+ * fp32 value rounded to FP8 E4M3 instead (RNE, satfinite, sign in bit 7):
+ *   resid[m, i] = E4M3(fp32(x - E2M1(code) * d) * fp32(1 / g))   (bytes)
+ * so resid then points to M * k bytes.  |R / g| is at most about the block's
+ * E4M3 scale (<= 448), so the value needs no scale of its own.  This is the
+ * quantized-residual compensation (gist.science explainer of QUADS,
+ * Technisches Resuemee 2.2 B: a second-pass quantization of the
+ * high-residual channels); pass it to w4a4_gemm_comp with
+ * NVFP4_GEMM_COMP_FP8.
+ * flags  0 (exactly nvfp4_quantize), NVFP4_QUANT_RESID_SCALED, or both bits;
+ *        NVFP4_QUANT_RESID_FP8 alone or other bits give NVFP4_ERR_INVALID_ARG
  */
 int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
                       uint8_t* codes, uint8_t* scales, const int32_t* chan, int32_t k, uint16_t* resid, int flags,
@@ -283,8 +293,13 @@ int mxfp4_decompose_elements(const uint16_t* x, int64_t M, int64_t K, int64_t ld
  *         sigma[e, n, S_i/16] (exact in bf16; the tensor scale g_w is applied
  *         in the GEMM epilogue);  b_codes/b_scales required, wt_bf16 ignored.
  * flags = NVFP4_COMP_W_BF16: w_sel[e, n, i] = wt_bf16[e, n, S_i].
+ * flags = NVFP4_COMP_W_DEQ_FP8: w_sel[e, n, i] = E4M3(E2M1(code) * sigma *
+ *         2^-3) as bytes (RNE, satfinite; the largest product 6 * 448 times
+ *         2^-3 is 336), the weight rows of the FP8 compensation
+ *         (w4a4_gemm_comp with NVFP4_GEMM_COMP_FP8 multiplies by 2^3 again);
+ *         w_sel then points to E * N * k bytes.
  * b_codes [E, N, K/2]; b_scales E consecutive nvfp4_scale_bytes(N, K) tiles;
- * wt_bf16 [E, N, K]; chan [E, k]; w_sel [E, N, k] bf16.
+ * wt_bf16 [E, N, K]; chan [E, k]; w_sel [E, N, k] bf16 (or E4M3 bytes).
  * A channel index outside [0, K) writes 0 and latches NVFP4_ERR_INVALID_ARG
  * for nvfp4_check_status.
  */
@@ -327,7 +342,8 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  * b_codes [N, K/2] (= W^T), b_scales tiled [N, K]
  * g_a, g_b device floats (NVFP4), or NULL for 1
  * resid [M, k] bf16, w_sel [N, k] bf16 (k % 8 == 0 so rows are 16-byte
- *         aligned for the tensor copies, 0 <= k <= K; NULL if k == 0)
+ *         aligned for the tensor copies, 0 <= k <= K; NULL if k == 0), or
+ *         E4M3 bytes with NVFP4_GEMM_COMP_FP8
  * y [M, N] bf16 (16-byte aligned)
  * workspace / ws_bytes: >= w4a4_gemm_workspace_bytes(M, N, K) (may be 0)
  * flags   NVFP4_COMP_W_DEQ or NVFP4_COMP_W_BF16 (the mode w_sel was prepared
@@ -337,6 +353,16 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  *         y = bf16_rn(ga*gb*acc + c*accc) with c = ga*gb (COMP_W_DEQ) or ga
  *         (COMP_W_BF16).  Dense GEMMs with more than 256 rows then feed the
  *         compensation tiles to the tensor core with no rescaling pass.
+ *         NVFP4_GEMM_COMP_FP8 (dense GEMMs only; with NVFP4_COMP_W_DEQ and
+ *         NVFP4_GEMM_RESID_SCALED, else NVFP4_ERR_INVALID_ARG; k % 16 == 0,
+ *         else NVFP4_ERR_UNSUPPORTED): resid [M, k] and w_sel [N, k] are the
+ *         E4M3 bytes of nvfp4_quantize_ex(... NVFP4_QUANT_RESID_FP8) and
+ *         nvfp4_prepare_comp_weights(NVFP4_COMP_W_DEQ_FP8); the term is the
+ *         FP8 product (fp32 accumulate) times 2^3:
+ *           y = bf16_rn(ga*gb*(acc + 2^3 * sum_i r8[m,i] w8[n,i]))
+ *         (the quantized-residual compensation, gist.science explainer of
+ *         QUADS 2.2 B: second-pass quantization of the high-residual
+ *         channels).
  * The kernel is a programmatic dependent launch: it may start while the
  * preceding kernel of the stream is still running (the library's quantizers
  * let it).  By default it waits for that kernel before touching global
@@ -362,6 +388,8 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
  * g_a      device float [1];  g_b device float [E]
  * b_codes [E, N, K/2]; b_scales E consecutive nvfp4_scale_bytes(N, K) tiles
  * resid [M_total, k]; w_sel [E, N, k]; y [M_total, N]
+ * NVFP4_GEMM_COMP_FP8 gives NVFP4_ERR_UNSUPPORTED here and in the fused MoE
+ * GEMMs below (the FP8 compensation is built for dense GEMMs).
  */
 size_t w4a4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K);
 int w4a4_grouped_gemm_comp(int fmt, int32_t E, const int32_t* offsets, int64_t M_total, int64_t N, int64_t K,

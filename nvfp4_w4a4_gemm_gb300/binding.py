@@ -18,10 +18,12 @@ LIB_PATH = os.path.join(_HERE, "libnvfp4w4a4.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
 FMT_NVFP4, FMT_MXFP4 = 0, 1
-COMP_W_DEQ, COMP_W_BF16 = 0, 1
+COMP_W_DEQ, COMP_W_BF16, COMP_W_DEQ_FP8 = 0, 1, 2
 GEMM_WEIGHTS_READY = 0x100  # flag bit: the weights are not written by work still pending on the stream
 GEMM_RESID_SCALED = 0x200   # flag bit: resid is the pre-scaled residual of nvfp4_quantize(..., resid_scaled=True)
-QUANT_RESID_SCALED = 1
+GEMM_COMP_FP8 = 0x400       # flag bit: resid / w_sel are E4M3 bytes (nvfp4_quantize(..., resid_fp8=True),
+                            # nvfp4_prepare_comp_weights(..., flags=COMP_W_DEQ_FP8))
+QUANT_RESID_SCALED, QUANT_RESID_FP8 = 1, 2
 
 _lib = None
 
@@ -133,11 +135,14 @@ def grouped_scale_bytes(M_total, K, E):
     return load().nvfp4_grouped_scale_bytes(M_total, K, E)
 
 
-def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None, resid_scaled=False):
+def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None, resid_scaled=False, resid_fp8=False):
     """x bf16 [M, K] -> dict(codes u8 [M, K/2], scales u8 tiled, g f32 [1],
     resid bf16 [M, k]).  g: None (dynamic) or device float32 [1].
     resid_scaled: the residual comes divided by g (the GEMM's pre-scaled
-    compensation operand; pass resid_scaled=True to the GEMM too)."""
+    compensation operand; pass resid_scaled=True to the GEMM too).
+    resid_fp8: the pre-scaled residual as E4M3 bytes (u8 [M, k]; implies
+    resid_scaled), the operand of the FP8 compensation."""
+    resid_scaled = resid_scaled or resid_fp8
     lib = load()
     _need(x, torch.bfloat16, "x")
     M, K = x.shape
@@ -151,18 +156,22 @@ def nvfp4_quantize(x, g=None, chan=None, out=None, g_out=None, resid_scaled=Fals
     codes = o.get("codes") if o.get("codes") is not None else torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
     scales = o.get("scales") if o.get("scales") is not None else torch.empty(
         lib.nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
-    resid = o.get("resid") if o.get("resid") is not None else torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    rdt = torch.uint8 if resid_fp8 else torch.bfloat16
+    resid = o.get("resid") if o.get("resid") is not None else torch.empty((M, k), dtype=rdt, device=dev)
+    if k:
+        _need(resid, rdt, "resid")
     if g_out is None:
         g_out = torch.empty(1, dtype=torch.float32, device=dev)
     ws = o.get("ws")
     if ws is None and g is None:
         ws = torch.empty(lib.nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    flags = (QUANT_RESID_SCALED if resid_scaled else 0) | (QUANT_RESID_FP8 if resid_fp8 else 0)
     st = lib.nvfp4_quantize_ex(_ptr(x), M, K, x.stride(0), _ptr(g), _ptr(g_out), _ptr(codes), _ptr(scales),
-                               _ptr(chan) if k else None, k, _ptr(resid) if k else None,
-                               QUANT_RESID_SCALED if resid_scaled else 0, _ptr(ws),
+                               _ptr(chan) if k else None, k, _ptr(resid) if k else None, flags, _ptr(ws),
                                0 if ws is None else ws.numel(), _stream())
     _check("nvfp4_quantize_ex", st)
-    return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
+    return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled),
+                resid_fp8=bool(resid_fp8))
 
 
 def _need_rows(t, dtype, name):
@@ -303,7 +312,8 @@ def mxfp4_quantize(x, stats=False):
 
 
 def nvfp4_prepare_comp_weights(b_codes, b_scales, chan, flags=COMP_W_DEQ, wt=None, E=1):
-    """Compensation weight columns w_sel [E, N, k] (or [N, k] when E == 1)."""
+    """Compensation weight columns w_sel [E, N, k] (or [N, k] when E == 1):
+    bf16, or E4M3 bytes for flags=COMP_W_DEQ_FP8."""
     lib = load()
     _need(chan, torch.int32, "chan")
     k = chan.shape[-1]
@@ -313,7 +323,7 @@ def nvfp4_prepare_comp_weights(b_codes, b_scales, chan, flags=COMP_W_DEQ, wt=Non
         E, N, Kh = b_codes.shape
     K = Kh * 2
     dev = b_codes.device
-    w_sel = torch.empty((E, N, k), dtype=torch.bfloat16, device=dev)
+    w_sel = torch.empty((E, N, k), dtype=torch.uint8 if flags == COMP_W_DEQ_FP8 else torch.bfloat16, device=dev)
     st = lib.nvfp4_prepare_comp_weights(E, N, K, _ptr(b_codes), _ptr(b_scales), _ptr(wt), _ptr(chan), k, flags,
                                         _ptr(w_sel), _stream())
     _check("nvfp4_prepare_comp_weights", st)
@@ -344,6 +354,8 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
         flags |= GEMM_WEIGHTS_READY
     if resid is not None and qa.get("resid_scaled"):
         flags |= GEMM_RESID_SCALED
+    if resid is not None and qa.get("resid_fp8"):
+        flags |= GEMM_COMP_FP8  # w_sel must then come from COMP_W_DEQ_FP8
     lib = load()
     a_codes, b_codes = qa["codes"], qb["codes"]
     M, Kh = a_codes.shape
@@ -398,6 +410,8 @@ def w4a4_grouped_gemm_comp(qa, offsets, b_codes, b_scales, g_b, N, resid=None, w
         flags |= GEMM_WEIGHTS_READY
     if resid is not None and qa.get("resid_scaled"):
         flags |= GEMM_RESID_SCALED
+    if resid is not None and qa.get("resid_fp8"):
+        flags |= GEMM_COMP_FP8  # not built for grouped GEMMs: the library refuses it
     lib = load()
     a_codes = qa["codes"]
     M, Kh = a_codes.shape
@@ -425,6 +439,8 @@ def w4a4_grouped_gemm_swiglu_quant(qa, offsets, b_codes, b_scales, g_b, N, g_h, 
         flags |= GEMM_WEIGHTS_READY
     if resid is not None and qa.get("resid_scaled"):
         flags |= GEMM_RESID_SCALED
+    if resid is not None and qa.get("resid_fp8"):
+        flags |= GEMM_COMP_FP8  # not built for grouped GEMMs: the library refuses it
     lib = load()
     a_codes = qa["codes"]
     M, Kh = a_codes.shape
@@ -459,6 +475,8 @@ def w4a4_grouped_gemm_combine(qa, offsets, b_codes, b_scales, g_b, N, token_of_r
         flags |= GEMM_WEIGHTS_READY
     if resid is not None and qa.get("resid_scaled"):
         flags |= GEMM_RESID_SCALED
+    if resid is not None and qa.get("resid_fp8"):
+        flags |= GEMM_COMP_FP8  # not built for grouped GEMMs: the library refuses it
     lib = load()
     a_codes = qa["codes"]
     M, Kh = a_codes.shape

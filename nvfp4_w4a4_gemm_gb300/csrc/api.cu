@@ -156,7 +156,9 @@ int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, cons
                       void* workspace, size_t ws_bytes, void* stream) {
   int st = check_quant_args(x, M, K, ldx, codes, scales, chan, k, resid, 16);
   if (st != NVFP4_OK) return st;
-  if ((flags & ~NVFP4_QUANT_RESID_SCALED) != 0) return NVFP4_ERR_INVALID_ARG;
+  if ((flags & ~(NVFP4_QUANT_RESID_SCALED | NVFP4_QUANT_RESID_FP8)) != 0) return NVFP4_ERR_INVALID_ARG;
+  // the E4M3 residual is the pre-scaled one (its range is then that of E4M3)
+  if ((flags & NVFP4_QUANT_RESID_FP8) && !(flags & NVFP4_QUANT_RESID_SCALED)) return NVFP4_ERR_INVALID_ARG;
   if (g_in == nullptr && (workspace == nullptr || ws_bytes < kQuantWs || !aligned(workspace, 16)))
     return NVFP4_ERR_WORKSPACE;
   const DeviceInfo* d = nullptr;
@@ -165,7 +167,8 @@ int nvfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, cons
   return from_cuda(nv4::launch_nvfp4_quantize(bf(x), M, K, ldx, g_in, g_out, codes, scales, chan, k, bf(resid),
                                               nullptr, 1, static_cast<float*>(workspace), quant_barrier(workspace),
                                               d->num_sms, as_stream(stream),
-                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0));
+                                              (flags & NVFP4_QUANT_RESID_SCALED) ? 1 : 0, nullptr, 0,
+                                              (flags & NVFP4_QUANT_RESID_FP8) ? 1 : 0));
 }
 
 int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* g_in, float* g_out,
@@ -258,17 +261,18 @@ int nvfp4_prepare_comp_weights(int32_t E, int64_t N, int64_t K, const uint8_t* b
                                const uint16_t* wt_bf16, const int32_t* chan, int32_t k, int flags,
                                uint16_t* w_sel, void* stream) {
   if (E <= 0 || N < 0 || K <= 0 || K % 16 != 0 || k < 0 || k > K) return NVFP4_ERR_INVALID_ARG;
-  if (flags != NVFP4_COMP_W_DEQ && flags != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
+  if (flags != NVFP4_COMP_W_DEQ && flags != NVFP4_COMP_W_BF16 && flags != NVFP4_COMP_W_DEQ_FP8)
+    return NVFP4_ERR_INVALID_ARG;
   if (k == 0 || N == 0) return NVFP4_OK;
   if (!chan || !w_sel) return NVFP4_ERR_INVALID_ARG;
-  if (flags == NVFP4_COMP_W_DEQ && (!b_codes || !b_scales)) return NVFP4_ERR_INVALID_ARG;
+  if (flags != NVFP4_COMP_W_BF16 && (!b_codes || !b_scales)) return NVFP4_ERR_INVALID_ARG;
   if (flags == NVFP4_COMP_W_BF16 && !wt_bf16) return NVFP4_ERR_INVALID_ARG;
   const DeviceInfo* d = nullptr;
   int st;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   return from_cuda(nv4::launch_comp_weights(b_codes, b_scales, flags == NVFP4_COMP_W_BF16 ? bf(wt_bf16) : nullptr,
                                             N, K, chan, k, E, nvfp4_scale_bytes(N, K), bf(w_sel), d->num_sms,
-                                            as_stream(stream)));
+                                            as_stream(stream), flags == NVFP4_COMP_W_DEQ_FP8 ? 1 : 0));
 }
 
 size_t nvfp4_calibrate_workspace_bytes(int64_t K, int32_t E) {
@@ -312,11 +316,19 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
 
 static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
                              const uint8_t* a_scales, const uint8_t* b_codes, const uint8_t* b_scales,
-                             const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y) {
+                             const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
+                             bool dense = false) {
   if (fmt != NVFP4_FMT_NVFP4 && fmt != NVFP4_FMT_MXFP4) return NVFP4_ERR_INVALID_ARG;
-  const int mode = flags & ~(NVFP4_GEMM_WEIGHTS_READY | NVFP4_GEMM_RESID_SCALED);
+  const int mode = flags & ~(NVFP4_GEMM_WEIGHTS_READY | NVFP4_GEMM_RESID_SCALED | NVFP4_GEMM_COMP_FP8);
   if (mode != NVFP4_COMP_W_DEQ && mode != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
   if (M < 0 || N <= 0 || K <= 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
+  if (flags & NVFP4_GEMM_COMP_FP8) {
+    // E4M3 operands: the pre-scaled residual and weight rows from the codes
+    // (NVFP4_COMP_W_DEQ_FP8), so the term shares the FP4 product's factor
+    if (fmt != NVFP4_FMT_NVFP4 || mode != NVFP4_COMP_W_DEQ || !(flags & NVFP4_GEMM_RESID_SCALED))
+      return NVFP4_ERR_INVALID_ARG;
+    if (!dense || k % 16 != 0) return NVFP4_ERR_UNSUPPORTED;  // dense GEMMs; rows of 16-byte multiples
+  }
   if (N % 128 != 0 || K % (fmt == NVFP4_FMT_MXFP4 ? 128 : 64) != 0) return NVFP4_ERR_UNSUPPORTED;
   if (M > ((int64_t)1 << 31) - 256 || N > ((int64_t)1 << 31) - 256 || K > ((int64_t)1 << 30)) return NVFP4_ERR_UNSUPPORTED;
   if (fmt == NVFP4_FMT_MXFP4 && k != 0) return NVFP4_ERR_UNSUPPORTED;
@@ -340,7 +352,7 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
                    const float* g_a, const uint8_t* b_codes, const uint8_t* b_scales, const float* g_b,
                    const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
                    void* workspace, size_t ws_bytes, void* stream) {
-  int st = check_gemm_common(fmt, M, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k, flags, y);
+  int st = check_gemm_common(fmt, M, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k, flags, y, true);
   if (st != NVFP4_OK || M == 0) return st;
   const DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
@@ -350,7 +362,8 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
   p.fmt = fmt; p.M = M; p.N = N; p.K = K;
   p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
   p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
-  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.flags = flags; p.y = bf(y);
+  p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.y = bf(y);
+  p.flags = (flags & ~NVFP4_GEMM_COMP_FP8) | ((flags & NVFP4_GEMM_COMP_FP8) ? nv4::kGemmCompFp8 : 0);
   p.ws = workspace; p.ws_bytes = ws_bytes;
   return from_cuda(nv4::launch_gemm(p, d->num_sms, as_stream(stream)));
 }

@@ -101,6 +101,8 @@ struct GemmParams {
                     // for the preceding kernel (programmatic dependent launch)
   int swap;         // narrow kernel, M <= 64: weight rows take the MMA's M = 128 slot, tokens its N slot
   int resid_scaled; // the residual was divided by g_a in the quantizer
+  int comp_fp8;     // R_S / W_S are E4M3 bytes (W_S carries 2^-3): 128 channels per
+                    // compensation tile, FP8 MMAs, the term times 2^3
   uint32_t n_mma;   // swap: MMA N = M rounded up to 16
   // wide kernel, grouped: what the epilogue makes of the accumulator
   int epi;                    // kEpiStore, kEpiSwigluQuant or kEpiCombine
@@ -220,6 +222,18 @@ __device__ __forceinline__ uint32_t idesc_bf16() {
   // D f32 (=1) at bit 4, A/B bf16 (=1) at bits 7 / 10, K-major both.
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+__device__ __forceinline__ uint32_t idesc_f8(uint32_t n) {
+  // kind::f8f6f4: D f32 (=1) at bit 4, A/B E4M3 (=0) at bits 7 / 10, K-major both.
+  return (1u << 4) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+// Compensation tile geometry: 128-byte rows of 64 bf16 or 128 E4M3 channels;
+// MMAs per tile for the channels left (K = 16 bf16 or 32 E4M3 per issue, 32
+// bytes of the row either way).
+__device__ __forceinline__ int comp_tile_cols(const GemmParams& p) { return p.comp_fp8 ? 128 : 64; }
+__device__ __forceinline__ int comp_mmas(const GemmParams& p, int krem) {
+  const int per = p.comp_fp8 ? 32 : 16;
+  return krem >= 4 * per ? 4 : (krem + per - 1) / per;
+}
 // the same two forms with MMA N = n (swap: the token count rounded up to 16)
 __device__ __forceinline__ uint32_t idesc_fp4_swap(int fmt, uint32_t sf_id, uint32_t n) {
   uint32_t d = (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -324,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
   const int sf_chunks_per_kt = p.fmt == 1 ? 2 : 4;  // 512-byte chunks per 256-element k-tile
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
   const int n_kt = (int)((p.K + 255) / 256);
-  const int n_ct = (p.k + 63) / 64;
+  const int ct_cols = comp_tile_cols(p);
+  const int n_ct = (p.k + ct_cols - 1) / ct_cols;
   auto kt_lo = [&](int64_t u) { return (int)((u % split) * n_kt / split); };
   auto kt_hi = [&](int64_t u) { return (int)((u % split + 1) * n_kt / split); };
   auto ct_of = [&](int64_t u) { return (u % split) == 0 ? n_ct : 0; };
@@ -409,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           uint8_t* sa = stages + stage * kStageB;
           uint8_t* sb = sa + kAB;
           mbar_arrive_expect_tx(&full[stage], p.a_rows * BKB + kTileBytes);
-          tma_load_2d(sa, &p.tm_r, &full[stage], ct * 64, (int32_t)tl.row0);
-          if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0, tl.e);
-          else tma_load_2d(sb, &p.tm_w, &full[stage], ct * 64, tl.n0);
+          tma_load_2d(sa, &p.tm_r, &full[stage], ct * ct_cols, (int32_t)tl.row0);
+          if (p.grouped) tma_load_3d(sb, &p.tm_w, &full[stage], ct * ct_cols, tl.n0, tl.e);
+          else tma_load_2d(sb, &p.tm_w, &full[stage], ct * ct_cols, tl.n0);
         }
         __syncwarp();
         ++armed;
@@ -477,15 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           if (elect_one()) {
             const uint32_t sa = smem_u32(stages + stage * kStageB);
             const uint32_t sb = sa + kAB;
-            const int krem = p.k - ct * 64;
-            const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
+            const int n_mma = comp_mmas(p, p.k - ct * ct_cols);
             for (int j = 0; j < n_mma; ++j) {
-              if (p.swap)
-                mma_bf16(tmem + kComp, desc_sw128(sb + 32u * j), desc_sw128(sa + 32u * j),
-                         idesc_bf16_swap(p.n_mma), (ct > 0 || j > 0) ? 1u : 0u);
-              else
-                mma_bf16(tmem + kComp, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16(),
-                         (ct > 0 || j > 0) ? 1u : 0u);
+              const uint32_t accum = (ct > 0 || j > 0) ? 1u : 0u;
+              const uint64_t rd = desc_sw128(sa + 32u * j), wd = desc_sw128(sb + 32u * j);
+              if (p.comp_fp8) {
+                if (p.swap) mma_f8(tmem + kComp, wd, rd, idesc_f8(p.n_mma), accum);
+                else mma_f8(tmem + kComp, rd, wd, idesc_f8(BN), accum);
+              } else {
+                if (p.swap) mma_bf16(tmem + kComp, wd, rd, idesc_bf16_swap(p.n_mma), accum);
+                else mma_bf16(tmem + kComp, rd, wd, idesc_bf16(), accum);
+              }
             }
             tc_commit(&empty[stage]);
           }
@@ -556,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         alpha = ga * gb;
         beta = (p.flags == 1) ? 1.f : gb;
         if (p.resid_scaled) beta *= ga;  // the residual came divided by g_a
+        if (p.comp_fp8) beta *= 8.f;     // the FP8 weight rows carry 2^-3
       }
       const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kAcc1 : kAcc0);
       const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kComp;
@@ -1407,9 +1425,16 @@ constexpr int kPSfA = 2048, kPSfB = 4096; // this CTA's A rows, all 256 B rows
 constexpr int kPSfStageBytes = kPSfA + kPSfB;
 constexpr int kPThreads = 384;
 constexpr uint32_t kPColSf = 256;         // TMEM: accumulator [0, 256), 48-column scale slots after it
-static_assert(kPColSf + 48 * kPStages <= kTmemCols, "TMEM budget");
+// FP8 compensation: constant UE8M0 block scales for its MMAs, 2^0 for the
+// residual rows (4 columns) and 2^3 for the weight rows (8 columns, and the
+// 4 after them, so every column up to the end of the allocation holds a
+// scale), copied once from two 512-byte chunks of shared memory
+constexpr uint32_t kPColSfConst = kPColSf + 48 * kPStages;
+constexpr int kPSfConstBytes = 1024;
+static_assert(kPColSfConst + 16 == kTmemCols, "TMEM budget");
 static_assert(kPStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-constexpr size_t kPSmemBytes = 1024 + (size_t)kPStages * kPStageBytes + (size_t)kPSfStages * kPSfStageBytes + 512;
+constexpr size_t kPSmemBytes =
+    1024 + (size_t)kPStages * kPStageBytes + (size_t)kPSfStages * kPSfStageBytes + kPSfConstBytes + 512;
 
 // One pair tile: expert, first row of its 256, rows that exist (<= 256; the
 // rest belong to the next expert or lie past M), first 128-row tile of the A
@@ -1459,6 +1484,11 @@ __device__ __forceinline__ uint32_t idesc_fp4_pair(int fmt, uint32_t sf_id) {
 __device__ __forceinline__ uint32_t idesc_bf16_pair() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
 }
+// kind::mxf8f6f4: A/B E4M3 (=0) at bits 7 / 10, UE8M0 scales (bit 23 = 1),
+// scale-factor ids 0.
+__device__ __forceinline__ uint32_t idesc_mxf8_pair() {
+  return ((uint32_t)(BNP >> 3) << 17) | (1u << 23) | ((uint32_t)(BMP >> 4) << 24);
+}
 
 template <bool kGrouped>
 __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
@@ -1466,7 +1496,8 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   uint8_t* sf_ring = smem + kPStages * kPStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_ring + kPSfStages * kPSfStageBytes);
+  uint8_t* sf_const = sf_ring + kPSfStages * kPSfStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_const + kPSfConstBytes);
   uint64_t* full = bars;                        // leader: 1 arrival + both CTAs' operand bytes
   uint64_t* empty = full + kPStages;            // each CTA: the leader's MMA commit
   uint64_t* sf_full = empty + kPStages;         // leader: warp 3 (copy commit / plain arrive)
@@ -1512,6 +1543,13 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       sched.tile_start[p.E] = ts;
     }
   }
+  if (p.comp_fp8) {
+    // the constant scale chunks (every byte of a chunk the same, so the copy's
+    // lane layout does not matter): 2^0 = 0x7F, then 2^3 = 0x82
+    uint32_t* w = reinterpret_cast<uint32_t*>(sf_const);
+    for (int i = threadIdx.x; i < kPSfConstBytes / 4; i += blockDim.x) w[i] = i < 128 ? 0x7F7F7F7Fu : 0x82828282u;
+    fence_proxy_async_smem();  // visible to the tensor core's copies after the barrier below
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&full[i], 1);
@@ -1546,7 +1584,8 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
   const int cpk = p.fmt == 1 ? 2 : 4;                     // 512-byte scale chunks per 256-element k-tile
   const int64_t n_cg = p.fmt == 1 ? p.K / 128 : p.K / 64;  // chunks per 128-row scale tile row
   const int n_kt = (int)((p.K + 255) / 256);
-  const int n_ct = (p.k + 63) / 64;
+  const int ct_cols = comp_tile_cols(p);
+  const int n_ct = (p.k + ct_cols - 1) / ct_cols;
   const int n_uses_tile = n_kt + n_ct;
   const int64_t my_tiles = pair < num_tiles ? (num_tiles - 1 - pair) / n_pairs + 1 : 0;
   // compensation residual scaling in shared memory by the epilogue warps,
@@ -1618,9 +1657,9 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
           const uint32_t fb = full0 + 8u * (uint32_t)stage;
           const int32_t n = (int32_t)(tl.nt * BNP + BM * rank);
           if (leader) mbar_arrive_expect_tx(&full[stage], kTx);
-          tma_load_2d_pair(sa, &p.tm_r, fb, ct * 64, (int32_t)(tl.row0 + BM * rank));
-          if (kGrouped) tma_load_3d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n, tl.e);
-          else tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * 64, n);
+          tma_load_2d_pair(sa, &p.tm_r, fb, ct * ct_cols, (int32_t)(tl.row0 + BM * rank));
+          if (kGrouped) tma_load_3d_pair(sa + kPTileA, &p.tm_w, fb, ct * ct_cols, n, tl.e);
+          else tma_load_2d_pair(sa + kPTileA, &p.tm_w, fb, ct * ct_cols, n);
         }
         __syncwarp();
         if (++stage == kPStages) { stage = 0; phase ^= 1u; }
@@ -1645,6 +1684,17 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       bool ok = true;
       const uint32_t empty_own0 = smem_u32(empty), empty_peer0 = cluster_addr(empty, peer);
       const uint32_t idesc_main = idesc_fp4_pair(p.fmt, 0);
+      const uint32_t t_sfc = tmem + kPColSfConst;  // FP8 compensation: residual scales, weight scales at +4
+      if (p.comp_fp8 && n_ct > 0) {
+        // issued before any MMA by this thread, so every MMA sees the scales
+        if (elect_one()) {
+          tmem_cp_32x128b_x4_pair(t_sfc, desc_sf(smem_u32(sf_const)));
+          tmem_cp_32x128b_x4_pair(t_sfc + 4u, desc_sf(smem_u32(sf_const + 512)));
+          tmem_cp_32x128b_x4_pair(t_sfc + 8u, desc_sf(smem_u32(sf_const + 512)));
+          tmem_cp_32x128b_x4_pair(t_sfc + 12u, desc_sf(smem_u32(sf_const + 512)));
+        }
+        __syncwarp();
+      }
       int64_t done_tiles = 0;
       for (int64_t t = pair; t < num_tiles && ok; t += n_pairs) {
         if (!mbar_wait_cl_warp(acc_empty, acc_phase ^ 1u, kWaitAccEmpty, s_abort)) { ok = false; break; }
@@ -1702,10 +1752,14 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
           if (elect_one()) {
             const uint32_t sa = smem_u32(stages + stage * kPStageBytes);
             const uint32_t sb = sa + kPTileA;
-            const int krem = p.k - ct * 64;
-            const int n_mma = krem >= 64 ? 4 : (krem + 15) / 16;
-            for (int j = 0; j < n_mma; ++j)
-              mma_bf16_pair(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16_pair(), 1u);
+            const int n_mma = comp_mmas(p, p.k - ct * ct_cols);
+            for (int j = 0; j < n_mma; ++j) {
+              if (p.comp_fp8)
+                mma_mxf8_1x_pair(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_mxf8_pair(), t_sfc,
+                                 t_sfc + 4u, 1u);
+              else
+                mma_bf16_pair(tmem, desc_sw128(sa + 32u * j), desc_sw128(sb + 32u * j), idesc_bf16_pair(), 1u);
+            }
             tc_commit_pair(empty_own0 + 8u * (uint32_t)stage);
             tc_commit_pair(empty_peer0 + 8u * (uint32_t)stage);
           }
@@ -2540,6 +2594,23 @@ cudaError_t launch_dependent(Kern kern, int grid, int threads, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Tensor maps of the compensation operands: bf16 tiles of 64 channels, or
+// E4M3 tiles of 128 (128-byte rows either way).
+struct CompMap {
+  CUtensorMapDataType dtype;
+  int elem;
+  uint32_t box;
+};
+CompMap comp_map(bool fp8) {
+  return fp8 ? CompMap{CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128u} : CompMap{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64u};
+}
+// The FP8 term needs what lets it share the FP4 accumulator's factor g_a g_b:
+// the residual pre-scaled by 1/g_a and weight rows from the NVFP4 codes; its
+// rows must start on 16-byte boundaries for the tensor copies.
+bool comp_fp8_ok(const GemmProblem& pr) {
+  return pr.fmt == 0 && (pr.flags & kGemmResidScaled) && !(pr.flags & kGemmCompBf16) && pr.k % 16 == 0;
+}
+
 cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_t stream) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -2565,20 +2636,21 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
     const uint64_t d[2] = {kb, (uint64_t)pr.N};
     if (!make_map(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.b_codes, 2, d, BKB, BN)) return cudaErrorInvalidValue;
   }
+  const bool fp8 = (pr.flags & kGemmCompFp8) != 0;
+  if (fp8 && (grouped || !comp_fp8_ok(pr))) return cudaErrorInvalidValue;
   if (pr.k > 0) {
+    const CompMap cm = comp_map(fp8);
     const uint64_t dr[2] = {(uint64_t)pr.k, rows};
-    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, p.a_rows))
-      return cudaErrorInvalidValue;
+    if (!make_map(&p.tm_r, cm.dtype, cm.elem, pr.resid, 2, dr, cm.box, p.a_rows)) return cudaErrorInvalidValue;
     if (grouped) {
       const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
-      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BN))
-        return cudaErrorInvalidValue;
+      if (!make_map(&p.tm_w, cm.dtype, cm.elem, pr.w_sel, 3, dw, cm.box, BN)) return cudaErrorInvalidValue;
     } else {
       const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
-      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BN))
-        return cudaErrorInvalidValue;
+      if (!make_map(&p.tm_w, cm.dtype, cm.elem, pr.w_sel, 2, dw, cm.box, BN)) return cudaErrorInvalidValue;
     }
   }
+  p.comp_fp8 = fp8 ? 1 : 0;
   p.a_sf = pr.a_scales;
   p.b_sf = pr.b_scales;
   const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
@@ -2896,19 +2968,21 @@ cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, c
                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
+  const bool fp8 = (pr.flags & kGemmCompFp8) != 0;
+  if (fp8 && (grouped || !comp_fp8_ok(pr))) return cudaErrorInvalidValue;
   if (pr.k > 0) {
+    const CompMap cm = comp_map(fp8);
     const uint64_t dr[2] = {(uint64_t)pr.k, (uint64_t)pr.M};
-    if (!make_map(&p.tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.resid, 2, dr, 64, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tm_r, cm.dtype, cm.elem, pr.resid, 2, dr, cm.box, BM)) return cudaErrorInvalidValue;
     if (grouped) {
       const uint64_t dw[3] = {(uint64_t)pr.k, (uint64_t)pr.N, (uint64_t)E};
-      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 3, dw, 64, BM))
-        return cudaErrorInvalidValue;
+      if (!make_map(&p.tm_w, cm.dtype, cm.elem, pr.w_sel, 3, dw, cm.box, BM)) return cudaErrorInvalidValue;
     } else {
       const uint64_t dw[2] = {(uint64_t)pr.k, (uint64_t)pr.N};
-      if (!make_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.w_sel, 2, dw, 64, BM))
-        return cudaErrorInvalidValue;
+      if (!make_map(&p.tm_w, cm.dtype, cm.elem, pr.w_sel, 2, dw, cm.box, BM)) return cudaErrorInvalidValue;
     }
   }
+  p.comp_fp8 = fp8 ? 1 : 0;
   p.b_sf_expert_tiles = b_tiles;
   p.g_a = pr.g_a;
   p.g_b = pr.g_b;
@@ -2969,6 +3043,8 @@ cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_
     const int clusters = pair_clusters(num_sms);
     if (clusters > 0) return launch_pair(pr, grouped, clusters, stream);
   }
+  // the FP8 compensation exists on the narrow and the pair kernels only
+  if (pr.flags & kGemmCompFp8) return cudaErrorInvalidValue;
   return launch_wide(pr, grouped, num_sms, stream);
 }
 

@@ -18,7 +18,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
                                   unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled = 0,
-                                  const int32_t* gather = nullptr, int64_t T = 0);
+                                  const int32_t* gather = nullptr, int64_t T = 0, int resid_fp8 = 0);
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                   uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
@@ -37,7 +37,7 @@ cudaError_t launch_mxfp4_decompose(const __nv_bfloat16* x, int64_t M, int64_t K,
 
 cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
                                 int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
-                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream);
+                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream, int fp8 = 0);
 
 cudaError_t launch_channel_stats(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g,
                                  const int32_t* offsets, int E, double* sum, double* sumsq, int num_sms,
@@ -68,6 +68,7 @@ cudaError_t launch_nvfp4_quantize_noalloc(const __nv_bfloat16* x, int64_t M, int
 constexpr int kGemmCompBf16 = 1;          // compensation columns are the BF16 weights
 constexpr int kGemmWeightsReady = 0x100;  // weights may be read before the preceding kernel ends
 constexpr int kGemmResidScaled = 0x200;   // the residual was divided by g_a (nvfp4_quantize_for_gemm)
+constexpr int kGemmCompFp8 = 0x400;       // resid / w_sel are E4M3 bytes (w_sel carries 2^-3)
 struct GemmProblem {
   int fmt = 0;  // 0 NVFP4, 1 MXFP4
   int64_t M = 0, N = 0, K = 0;
@@ -77,8 +78,8 @@ struct GemmProblem {
   const uint8_t* b_codes = nullptr;
   const uint8_t* b_scales = nullptr;
   const float* g_b = nullptr;
-  const __nv_bfloat16* resid = nullptr;
-  const __nv_bfloat16* w_sel = nullptr;
+  const __nv_bfloat16* resid = nullptr;  // bf16, or E4M3 bytes with kGemmCompFp8
+  const __nv_bfloat16* w_sel = nullptr;  // bf16, or E4M3 bytes with kGemmCompFp8
   int k = 0;
   int flags = 0;
   __nv_bfloat16* y = nullptr;

@@ -56,16 +56,20 @@ __device__ __forceinline__ uint32_t block_scale_byte(float am, float g, float yg
 
 // Compensation residual of one element: x - E2M1(RN(x * rcp)) * d in fp32,
 // times rs (1, or RN(1/g) for the pre-scaled residual; a product with 1 is
-// exact), rounded to bf16 (0-scale blocks have code 0).  The code is the one
+// exact), before (element_residual_f32) and after the rounding to bf16
+// (0-scale blocks have code 0).  The code is the one
 // the block quantizer wrote for this element: the same fp32 product and
 // conversion.
-__device__ __forceinline__ __nv_bfloat16 element_residual(float x, float d, float rcp, float rs) {
+__device__ __forceinline__ float element_residual_f32(float x, float d, float rcp, float rs) {
   float dq = 0.f;
   if (d != 0.f) {
     const uint32_t h2 = cvt_e2m1x2_to_f16x2(cvt_e2m1x2(__fmul_rn(x, rcp), 0.f));
     dq = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), d);
   }
-  return __float2bfloat16_rn(__fmul_rn(__fsub_rn(x, dq), rs));
+  return __fmul_rn(__fsub_rn(x, dq), rs);
+}
+__device__ __forceinline__ __nv_bfloat16 element_residual(float x, float d, float rcp, float rs) {
+  return __float2bfloat16_rn(element_residual_f32(x, d, rcp, rs));
 }
 
 }  // namespace

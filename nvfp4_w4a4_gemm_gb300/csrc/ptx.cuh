@@ -205,6 +205,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// FP8 MMA (kind::f8f6f4, element types from the instruction descriptor),
+// K = 32 per issue, fp32 accumulate, no block scales.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Copy a 128-row x 16-byte scale tile from shared memory (described by an
 // smem matrix descriptor) into 4 TMEM columns, replicated to all 4 lane
 // quarters (32 lanes x 128 bits, warpx4).
@@ -412,6 +422,17 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled FP8 MMA on a CTA pair (kind::mxf8f6f4, one UE8M0 scale per
+// row per 32 elements), K = 32 per issue, fp32 accumulate.
+__device__ __forceinline__ void mma_mxf8_1x_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Scale-tile copy in both CTAs of the pair: each CTA's shared memory at the
 // descriptor's address into its own TMEM at taddr (replicated to all 4 lane
 // quarters, as tmem_cp_32x128b_x4).
@@ -504,7 +525,7 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte) {
   asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(byte));
   return out;
 }
-// fp32 -> E4M3 byte, RNE + satfinite (the value is >= 0 here).
+// fp32 -> E4M3 byte (sign in bit 7), RNE + satfinite.
 __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   uint32_t out;
   asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"

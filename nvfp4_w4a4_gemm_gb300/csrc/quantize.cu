@@ -138,12 +138,13 @@ struct QuantArgs {
   uint8_t* scales;          // tiled
   const int32_t* chan;      // [E, k] sorted per expert (E = 1 for dense)
   int k;
-  __nv_bfloat16* resid;     // [M, k]
+  __nv_bfloat16* resid;     // [M, k] bf16, or [M, k] E4M3 bytes when resid_fp8
   const int32_t* offsets;   // grouped: [E+1] device, else nullptr
   int E;
   int use_map;              // channel bitmaps + prefix counts in shared memory
   int vec32;                // rows start on 32-byte boundaries: 256-bit loads
   int resid_scaled;         // residual written divided by g (times RN(1/g))
+  int resid_fp8;            // residual rounded to E4M3 (RNE, satfinite) instead of bf16
   const int32_t* gather;    // routing gather: row r is x's row gather[r] (of T rows), else nullptr
   int64_t T;
 };
@@ -395,7 +396,7 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
     }
   }
   __syncwarp();
-  __nv_bfloat16* rrow = a.resid + (int64_t)r * a.k;
+  const int64_t rrow = (int64_t)r * a.k;
   for (int base = rb; base < re; base += 32) {  // warp-uniform
     const int i = base + lane;
     const bool act = i < re;
@@ -405,12 +406,13 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
     const uint32_t s0 = __shfl_sync(0xffffffffu, sig[0], blk & 31);
     const uint32_t s1 = __shfl_sync(0xffffffffu, sig[1], blk & 31);
     if (act) {
-      __nv_bfloat16 val = __float2bfloat16_rn(0.f);
+      float val = 0.f;
       if (in) {
         const float2 dr = sc.dr[blk >= 32 ? s1 : s0];
-        val = element_residual(__bfloat162float(u[j - col0]), dr.x, dr.y, sc.rs);
+        val = element_residual_f32(__bfloat162float(u[j - col0]), dr.x, dr.y, sc.rs);
       }
-      rrow[i] = val;
+      if (a.resid_fp8) reinterpret_cast<uint8_t*>(a.resid)[rrow + i] = (uint8_t)cvt_e4m3(val);
+      else a.resid[rrow + i] = __float2bfloat16_rn(val);
     }
   }
   __syncwarp();  // the slice is read before the warp's next unit overwrites it
@@ -928,11 +930,14 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_qdq_kernel(QdqArgs q) {
 
 // ------------------------------------------------ compensation weights -----
 // w_sel[e][n][i] = E2M1(code[e][n][S_e[i]]) * sigma[e][n][S_e[i]/16] (exact in
-// bf16), or the original bf16 W^T[e][n][S_e[i]] when `wt` is given.
+// bf16), or the original bf16 W^T[e][n][S_e[i]] when `wt` is given.  fp8:
+// the same product times 2^-3 (exact in fp32) as one E4M3 byte (RNE,
+// satfinite; 6 * 448 / 8 = 336 fits), the FP8 compensation operand.
 __global__ void comp_weights_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                     const __nv_bfloat16* __restrict__ wt, int64_t N, int64_t K,
                                     const int32_t* __restrict__ chan, int k, int E, uint64_t scale_stride,
-                                    __nv_bfloat16* __restrict__ w_sel) {
+                                    __nv_bfloat16* __restrict__ w_sel, int fp8) {
+  uint8_t* w8 = reinterpret_cast<uint8_t*>(w_sel);
   const int64_t total = (int64_t)E * N * k;
   const int64_t n_cg = (K / 16 + 3) / 4;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
@@ -942,7 +947,8 @@ __global__ void comp_weights_kernel(const uint8_t* __restrict__ codes, const uin
     const int64_t j = chan[(int64_t)e * k + i];
     if (j < 0 || j >= K) {
       report_error(kDevErrInvalidArg, 0x100u);
-      w_sel[t] = __float2bfloat16_rn(0.f);
+      if (fp8) w8[t] = 0;
+      else w_sel[t] = __float2bfloat16_rn(0.f);
       continue;
     }
     if (wt != nullptr) {
@@ -955,7 +961,8 @@ __global__ void comp_weights_kernel(const uint8_t* __restrict__ codes, const uin
     const uint8_t sig = scales[(uint64_t)e * scale_stride + tile_group_offset(n, blk / 4, n_cg) + (blk & 3)];
     float v = __fmul_rn(e2m1_mag(code), e4m3_to_f32(sig));
     if (code & 8u) v = -v;
-    w_sel[t] = __float2bfloat16_rn(v);
+    if (fp8) w8[t] = (uint8_t)cvt_e4m3(__fmul_rn(v, 0.125f));
+    else w_sel[t] = __float2bfloat16_rn(v);
   }
 }
 
@@ -1155,7 +1162,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
                                   float* g_out, uint8_t* codes, uint8_t* scales, const int32_t* chan, int k,
                                   __nv_bfloat16* resid, const int32_t* offsets, int E, float* partials,
                                   unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled,
-                                  const int32_t* gather, int64_t T) {
+                                  const int32_t* gather, int64_t T, int resid_fp8) {
   if (M == 0) { k = 0; chan = nullptr; resid = nullptr; }
   // the separate amax pre-pass reads x's rows in order: a gathered operand
   // takes a static scale or the fused grid-barrier form
@@ -1166,6 +1173,7 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   a.g_in = g_in; a.g_out = g_out; a.codes = codes; a.scales = scales;
   a.chan = chan; a.k = k; a.resid = resid; a.offsets = offsets; a.E = E > 0 ? E : 1;
   a.resid_scaled = resid_scaled;
+  a.resid_fp8 = resid_fp8;
   {
     const size_t words = (size_t)((K + 31) / 32);
     const size_t tab = (size_t)a.E * words * (sizeof(uint32_t) + sizeof(uint16_t));
@@ -1293,12 +1301,14 @@ cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64
 
 cudaError_t launch_comp_weights(const uint8_t* codes, const uint8_t* scales, const __nv_bfloat16* wt, int64_t N,
                                 int64_t K, const int32_t* chan, int k, int E, uint64_t scale_stride,
-                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream) {
+                                __nv_bfloat16* w_sel, int num_sms, cudaStream_t stream, int fp8) {
   const int64_t total = (int64_t)E * N * k;
   if (total == 0) return cudaSuccess;
+  if (fp8 && wt != nullptr) return cudaErrorInvalidValue;  // FP8 rows come from the codes
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
-  comp_weights_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, wt, N, K, chan, k, E, scale_stride, w_sel);
+  comp_weights_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, wt, N, K, chan, k, E, scale_stride, w_sel,
+                                                             fp8);
   return cudaGetLastError();
 }
 

@@ -95,9 +95,10 @@ def test_invalid_arguments_rejected_on_host(lib):
                                       0, 0, fake, None, 0, None) == 1
     # dynamic tensor scale without workspace
     assert lib.nvfp4_quantize(fake, 4, 32, 32, None, None, fake, fake, None, 0, None, None, 0, None) == 5
-    # GEMM flag bits: only the compensation mode, the weights-ready and the
-    # pre-scaled-residual bits exist
-    for bad in (2, 0x400, 0x101 | 0x400, 0x800 | 0x200):
+    # GEMM flag bits: the compensation mode, the weights-ready, the
+    # pre-scaled-residual and the FP8-compensation bits; FP8 needs the
+    # pre-scaled residual and the dequantized-weight mode
+    for bad in (2, 0x400, 0x101 | 0x400, 0x800 | 0x200, 0x601):
         assert lib.w4a4_gemm_comp(0, 4, 128, 64, fake, fake, None, fake, fake, None, None, None, 0, bad, fake,
                                   None, 0, None) == 1
     assert lib.w4a4_grouped_gemm_comp(0, 4, fake, 8, 128, 64, fake, fake, None, fake, fake, None, None, None,
@@ -124,10 +125,27 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert dec(4, 128, 256, 200, 0, 0) == 1
     assert dec(4, 128, 256, 256, 0, 0x200) == 1
     assert dec(4, 128, 256, 256, 8, 0, chan=None) == 1
-    # quantizer flags: only the pre-scaled-residual bit exists
+    # FP8 compensation: NVFP4 only, k % 16, dense GEMMs only
+    gf8 = 0x400 | 0x200
+    assert lib.w4a4_gemm_comp(1, 4, 128, 128, fake, fake, None, fake, fake, None, None, None, 0, gf8, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_gemm_comp(0, 4, 128, 64, fake, fake, None, fake, fake, None, fake, fake, 24, gf8, fake,
+                              None, 0, None) == 2
+    assert lib.w4a4_grouped_gemm_comp(0, 4, fake, 8, 128, 64, fake, fake, None, fake, fake, None, fake, fake,
+                                      16, gf8, fake, None, 0, None) == 2
+    assert lib.w4a4_grouped_gemm_combine(4, fake, 8, 512, 64, fake, fake, None, fake, fake, None, fake, fake, 16,
+                                         gf8, fake, fake, 2, fake, None) == 2
+    # quantizer flags: the pre-scaled-residual bit, and the E4M3-residual bit
+    # with it (dense only)
     assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 2, None, 0, None) == 1
+    assert lib.nvfp4_quantize_ex(fake, 4, 32, 32, fake, None, fake, fake, None, 0, None, 4, None, 0, None) == 1
     assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 4, None,
                                          0, None) == 1
+    assert lib.nvfp4_quantize_grouped_ex(fake, 4, 32, 32, 1, fake, fake, None, fake, fake, None, 0, None, 3, None,
+                                         0, None) == 1
+    # compensation weight modes 0, 1, 2 (FP8 rows come from the codes)
+    assert lib.nvfp4_prepare_comp_weights(1, 128, 64, fake, fake, None, fake, 8, 3, fake, None) == 1
+    assert lib.nvfp4_prepare_comp_weights(1, 128, 64, None, None, fake, fake, 8, 2, fake, None) == 1
     # routed gather: token rows and a row table are required; flags and workspace as the grouped quantizer
     gat = lambda T, tok, flags=0, g=fake, ws=fake, wsb=1 << 16: lib.nvfp4_quantize_grouped_gather(
         fake, T, tok, 8, 32, 32, 1, fake, g, None, fake, fake, None, 0, None, flags, ws, wsb, None)
