@@ -401,7 +401,9 @@ def prefill_components(nv, pk, s, chan, sets, steps=20):
     ms_g = _time_steps(gemm, steps, flush, "prefill_gemm")
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     tf = 2.0 * M * N * K / (ms_g * 1e-3) / 1e12
-    return {"alone_clean_l2": {
+    comp8 = comp_fp8_components(nv, pk, s, chan, sets, qs, flush, steps)
+    comp8["comp_overhead_bf16"] = round(ms_g / comp8["gemm_k0_ms"] - 1.0, 4)
+    return {"comp_fp8": comp8, "alone_clean_l2": {
         "quantize_dynamic_ms": round(ms_dyn, 4),
         "quantize_dynamic_gbs": round(q_bytes / (ms_dyn * 1e-3) / 1e9, 1),
         "quantize_dynamic_frac_hbm": round(q_bytes / (ms_dyn * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
@@ -411,6 +413,74 @@ def prefill_components(nv, pk, s, chan, sets, steps=20):
         "gemm_ms": round(ms_g, 4), "gemm_tflops": round(tf, 1), "gemm_frac_fp4_peak": round(tf / fp4_peak, 4),
         "note": "each kernel alone after an L2 flush (write + read of 256 MB); static scale = the dynamic "
                 "scale of a previous batch passed in (one read of X, no grid barrier)"}}
+
+
+def comp_fp8_components(nv, pk, s, chan, sets, qs, flush, steps):
+    """The quantized-residual (FP8 E4M3) compensation on the prefill
+    workload: the dynamic-scale quantizer writing the E4M3 residual, the GEMM
+    with the FP8 term, the same GEMM without compensation (k = 0, the
+    baseline of both terms' overhead), each alone after an L2 flush; and the
+    whole step (quantize + GEMM, inputs rotating, no flush) with the BF16 and
+    with the FP8 term, timed the same way."""
+    dev = torch.device("cuda")
+    M, K, N, k = s.M, s.K, s.N, s.k
+    w8 = [nv.nvfp4_prepare_comp_weights(st["qw"]["codes"], st["qw"]["scales"], chan, flags=nv.COMP_W_DEQ_FP8)
+          for st in sets]
+    out8 = dict(codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                scales=torch.empty(nv.scale_bytes(M, K), dtype=torch.uint8, device=dev),
+                resid=torch.empty((M, k), dtype=torch.uint8, device=dev),
+                ws=torch.empty(nv.load().nvfp4_quantize_workspace_bytes(), dtype=torch.uint8, device=dev))
+    out16 = dict(out8, resid=torch.empty((M, k), dtype=torch.bfloat16, device=dev))
+    g_out = torch.empty(1, dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    it = [0]
+
+    def quant8():
+        it[0] += 1
+        nv.nvfp4_quantize(sets[it[0] % N_SETS]["x"], chan=chan, out=out8, g_out=g_out, resid_fp8=True)
+    ms_q8 = _time_steps(quant8, steps, flush, "prefill_quantize_dynamic_fp8")
+    q8 = [nv.nvfp4_quantize(st["x"], chan=chan, resid_fp8=True) for st in sets]
+
+    def gemm8():
+        it[0] += 1
+        i = it[0] % N_SETS
+        nv.w4a4_gemm_comp(q8[i], sets[i]["qw"], N, resid=q8[i]["resid"], w_sel=w8[i], y=y, weights_ready=True)
+    ms_g8 = _time_steps(gemm8, steps, flush, "prefill_gemm_fp8")
+
+    def gemm0():
+        it[0] += 1
+        i = it[0] % N_SETS
+        nv.w4a4_gemm_comp(qs[i], sets[i]["qw"], N, y=y, weights_ready=True)
+    ms_g0 = _time_steps(gemm0, steps, flush, "prefill_gemm_k0")
+
+    def step_with(fp8):
+        def f():
+            it[0] += 1
+            i = it[0] % N_SETS
+            qx = nv.nvfp4_quantize(sets[i]["x"], chan=chan, out=out8 if fp8 else out16, g_out=g_out,
+                                   resid_scaled=True, resid_fp8=fp8)
+            nv.w4a4_gemm_comp(qx, sets[i]["qw"], N, resid=qx["resid"], w_sel=w8[i] if fp8 else sets[i]["w_sel"],
+                              y=y, weights_ready=True)
+        return f
+    ms_s16 = _time_steps(step_with(False), steps, None, "prefill_step_bf16_comp")
+    ms_s8 = _time_steps(step_with(True), steps, None, "prefill_step_fp8_comp")
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    flops = 2.0 * M * N * K
+    return {
+        "quantize_dynamic_fp8_ms": round(ms_q8, 4),
+        "gemm_fp8_ms": round(ms_g8, 4),
+        "gemm_fp8_tflops": round(flops / (ms_g8 * 1e-3) / 1e12, 1),
+        "gemm_fp8_frac_fp4_peak": round(flops / (ms_g8 * 1e-3) / 1e12 / fp4_peak, 4),
+        "gemm_k0_ms": round(ms_g0, 4),
+        "comp_overhead_fp8": round(ms_g8 / ms_g0 - 1.0, 4),
+        "step_bf16_comp_ms": round(ms_s16, 4),
+        "step_fp8_comp_ms": round(ms_s8, 4),
+        "step_fp8_comp_tflops": round(flops / (ms_s8 * 1e-3) / 1e12, 1),
+        "note": "quantized-residual compensation: E4M3 residual (pre-scaled by 1/g_a) and E4M3 weight rows "
+                "(x 2^-3), 128-channel tiles on the FP8 tensor-core kinds; GEMMs and the quantizer alone after an "
+                "L2 flush; the two steps (quantize + GEMM) on rotating inputs without a flush, timed the same way; "
+                "overheads against the same GEMM with k = 0",
+    }
 
 
 # ------------------------------------------- the other four workloads ----
