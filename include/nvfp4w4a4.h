@@ -66,10 +66,15 @@ enum { NVFP4_FMT_NVFP4 = 0, NVFP4_FMT_MXFP4 = 1 };
  * original bf16 weight columns. */
 enum { NVFP4_COMP_W_DEQ = 0, NVFP4_COMP_W_BF16 = 1, NVFP4_COMP_W_DEQ_FP8 = 2 };
 /* GEMM flag bits, OR-ed with the compensation mode (see w4a4_gemm_comp). */
-enum { NVFP4_GEMM_WEIGHTS_READY = 0x100, NVFP4_GEMM_RESID_SCALED = 0x200, NVFP4_GEMM_COMP_FP8 = 0x400 };
+enum {
+  NVFP4_GEMM_WEIGHTS_READY = 0x100,
+  NVFP4_GEMM_RESID_SCALED = 0x200,
+  NVFP4_GEMM_COMP_FP8 = 0x400,
+  NVFP4_GEMM_MX_ROW_SCALES = 0x800
+};
 /* Quantizer flag bits (nvfp4_quantize_ex; nvfp4_quantize_grouped_ex takes
- * NVFP4_QUANT_RESID_SCALED only). */
-enum { NVFP4_QUANT_RESID_SCALED = 1, NVFP4_QUANT_RESID_FP8 = 2 };
+ * NVFP4_QUANT_RESID_SCALED only; mxfp4_quantize_ex takes MXFP4_QUANT_MACRO). */
+enum { NVFP4_QUANT_RESID_SCALED = 1, NVFP4_QUANT_RESID_FP8 = 2, MXFP4_QUANT_MACRO = 1 };
 
 /* Library version (major*10000 + minor*100 + patch). */
 int nvfp4_version(void);
@@ -276,6 +281,37 @@ int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t
                    float* stats, uint8_t* deadzone, void* stream);
 
 /*
+ * mxfp4_quantize_ex -- mxfp4_quantize with the two corrections the MXFP4
+ * decomposition paper names ("Decomposing MXFP4 quantization error ..."
+ * (arXiv 2605.20402v2), abstract: macro-block scaling reduces the scale
+ * bias; Outlier Fallback recovers deadzone entries and partly reduces the
+ * scale-bias error).  The abstract defines neither; this library's readings:
+ *   Outlier Fallback (k > 0): the channels chan[0..k) (sorted, unique, in
+ *     [0, K)) leave the FP4 operand: they are set to 0 before the row scale,
+ *     the block scales and the codes, and their values go to fb.
+ *   Macro-block scaling (flags & MXFP4_QUANT_MACRO): a macro-block is one
+ *     row; t = RN(max|x'| / 6) over the row without the fallback channels,
+ *     m = significand of t in [1, 2) (1 when t == 0 or t < 2^-126) ->
+ *     row_scale[r]; the row is scaled by rho = RN(1 / m).  Without the flag
+ *     rho = 1 and row_scale is not written.
+ *   Per block of the scaled operand x'' = RN(x' * rho): e = floor(log2
+ *   max|x''|) - 2 (clamped), codes = E2M1_rn_sat(RN(x'' * 2^-e)); values
+ *   m * 2^e * E2M1(code).  fb[r, i] = bf16(RN(x[r, chan[i]] * rho)).
+ *   stats / deadzone: the decomposition of mxfp4_quantize applied to x''
+ *   (energies in units of m^2).
+ * A GEMM of two such operands (w4a4_gemm_comp, NVFP4_FMT_MXFP4) takes the
+ * row scales as g_a / g_b (NVFP4_GEMM_MX_ROW_SCALES) and the two fb arrays
+ * as resid / w_sel.
+ * chan   device int32 [k] or NULL (k == 0); fb [M, k] bf16 (NULL if k == 0)
+ * row_scale device float [M] (needed with MXFP4_QUANT_MACRO)
+ * other arguments as mxfp4_quantize; K <= 524288 when k > 0
+ * flags  0 or MXFP4_QUANT_MACRO; other bits give NVFP4_ERR_INVALID_ARG
+ */
+int mxfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int32_t* chan, int32_t k, int flags,
+                      float* row_scale, uint16_t* fb, uint8_t* codes, uint8_t* scales, float* stats, uint8_t* deadzone,
+                      void* stream);
+
+/*
  * mxfp4_decompose_elements -- the decomposition of mxfp4_quantize per
  * element instead of per block, a checking aid for small shapes: the same
  * fp32 arithmetic, E = B + D + G for every element.
@@ -336,7 +372,15 @@ int nvfp4_calibrate_channels(const uint16_t* x_cal, int64_t M, int64_t K, int64_
  *   y    = bf16_rn(ga*gb*acc + c*accc),  c = gb (COMP_W_DEQ) or 1 (COMP_W_BF16)
  *
  * fmt     NVFP4_FMT_NVFP4 (E4M3 scales, 16-blocks) or NVFP4_FMT_MXFP4 (E8M0
- *         scales, 32-blocks; ga, gb ignored, k must be 0)
+ *         scales, 32-blocks; ga, gb ignored unless NVFP4_GEMM_MX_ROW_SCALES)
+ * MXFP4 corrections (mxfp4_quantize_ex operands of both sides, dense GEMMs,
+ *         mode NVFP4_COMP_W_DEQ; other combinations NVFP4_ERR_INVALID_ARG):
+ *         NVFP4_GEMM_MX_ROW_SCALES: g_a [M] and g_b [N] (16-byte aligned) are
+ *         the row macro-block scales; k > 0: resid [M, k] and w_sel [N, k]
+ *         are the two operands' bf16 fallback values (the same channels);
+ *           y = bf16_rn(g_a[m] g_b[n] (acc + sum_i resid[m,i] w_sel[n,i]))
+ *         (the row-scale product rounded to fp32 first; without row scales
+ *         g_a[m] g_b[n] = 1)
  * M >= 0, N % 128 == 0, K % 64 == 0 (K % 128 for MXFP4)
  * a_codes [M, K/2], a_scales tiled [M, K] (16-byte aligned)
  * b_codes [N, K/2] (= W^T), b_scales tiled [N, K]

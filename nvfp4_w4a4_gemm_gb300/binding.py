@@ -24,6 +24,8 @@ GEMM_RESID_SCALED = 0x200   # flag bit: resid is the pre-scaled residual of nvfp
 GEMM_COMP_FP8 = 0x400       # flag bit: resid / w_sel are E4M3 bytes (nvfp4_quantize(..., resid_fp8=True),
                             # nvfp4_prepare_comp_weights(..., flags=COMP_W_DEQ_FP8))
 QUANT_RESID_SCALED, QUANT_RESID_FP8 = 1, 2
+MXFP4_QUANT_MACRO = 1
+GEMM_MX_ROW_SCALES = 0x800  # flag bit: MXFP4 operands carry row macro-block scales (g_a [M], g_b [N])
 
 _lib = None
 
@@ -51,6 +53,8 @@ _SIGS = {
                                        ctypes.c_int, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_quantize_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _I32, _P, _P], ctypes.c_int),
     "mxfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "mxfp4_quantize_ex": ([_P, _I64, _I64, _I64, _P, _I32, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P],
+                          ctypes.c_int),
     "mxfp4_decompose_elements": ([_P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "nvfp4_qdq": ([_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "nvfp4_prepare_comp_weights": ([_I32, _I64, _I64, _P, _P, _P, _P, _I32, ctypes.c_int, _P, _P], ctypes.c_int),
@@ -296,8 +300,11 @@ def nvfp4_quantize_grouped_gather(x_tokens, token_of_row, offsets, chan, g=None,
     return dict(codes=codes, scales=scales, g=g_out, resid=resid, resid_scaled=bool(resid_scaled))
 
 
-def mxfp4_quantize(x, stats=False):
-    """x bf16 [M, K] (K % 32 == 0) -> dict(codes, scales, stats f32 [M*K/32, 4], dead u8 [M*K/32])."""
+def mxfp4_quantize(x, stats=False, chan=None, macro=False):
+    """x bf16 [M, K] (K % 32 == 0) -> dict(codes, scales, stats f32 [M*K/32, 4], dead u8 [M*K/32]).
+    chan (int32 [k], sorted) / macro: the corrected quantizer (Outlier
+    Fallback on those channels, row macro-block scales); the dict then also
+    holds fb bf16 [M, k] and m f32 [M] (None without macro)."""
     lib = load()
     _need(x, torch.bfloat16, "x")
     M, K = x.shape
@@ -306,9 +313,21 @@ def mxfp4_quantize(x, stats=False):
     scales = torch.empty(lib.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device=dev)
     st_t = torch.empty((M * K // 32, 4), dtype=torch.float32, device=dev) if stats else None
     dead = torch.empty(M * K // 32, dtype=torch.uint8, device=dev) if stats else None
-    st = lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales), _ptr(st_t), _ptr(dead), _stream())
-    _check("mxfp4_quantize", st)
-    return dict(codes=codes, scales=scales, stats=st_t, dead=dead)
+    if chan is None and not macro:
+        st = lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales), _ptr(st_t), _ptr(dead),
+                                _stream())
+        _check("mxfp4_quantize", st)
+        return dict(codes=codes, scales=scales, stats=st_t, dead=dead)
+    k = 0 if chan is None else int(chan.numel())
+    if k:
+        _need(chan, torch.int32, "chan")
+    fb = torch.empty((M, k), dtype=torch.bfloat16, device=dev)
+    m = torch.empty(M, dtype=torch.float32, device=dev) if macro else None
+    st = lib.mxfp4_quantize_ex(_ptr(x), M, K, x.stride(0), _ptr(chan) if k else None, k,
+                               MXFP4_QUANT_MACRO if macro else 0, _ptr(m), _ptr(fb) if k else None, _ptr(codes),
+                               _ptr(scales), _ptr(st_t), _ptr(dead), _stream())
+    _check("mxfp4_quantize_ex", st)
+    return dict(codes=codes, scales=scales, stats=st_t, dead=dead, fb=fb, m=m)
 
 
 def nvfp4_prepare_comp_weights(b_codes, b_scales, chan, flags=COMP_W_DEQ, wt=None, E=1):
@@ -356,6 +375,11 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
         flags |= GEMM_RESID_SCALED
     if resid is not None and qa.get("resid_fp8"):
         flags |= GEMM_COMP_FP8  # w_sel must then come from COMP_W_DEQ_FP8
+    g_a, g_b = qa.get("g"), qb.get("g")
+    if fmt == FMT_MXFP4 and (qa.get("m") is not None or qb.get("m") is not None):
+        # corrected MXFP4 operands: both sides carry row macro-block scales
+        flags |= GEMM_MX_ROW_SCALES
+        g_a, g_b = qa["m"], qb["m"]
     lib = load()
     a_codes, b_codes = qa["codes"], qb["codes"]
     M, Kh = a_codes.shape
@@ -366,8 +390,8 @@ def w4a4_gemm_comp(qa, qb, N, resid=None, w_sel=None, flags=COMP_W_DEQ, fmt=FMT_
     need = lib.w4a4_gemm_workspace_bytes(M, N, K)
     if need and ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device=a_codes.device)
-    st = lib.w4a4_gemm_comp(fmt, M, N, K, _ptr(a_codes), _ptr(qa["scales"]), _ptr(qa.get("g")),
-                            _ptr(b_codes), _ptr(qb["scales"]), _ptr(qb.get("g")),
+    st = lib.w4a4_gemm_comp(fmt, M, N, K, _ptr(a_codes), _ptr(qa["scales"]), _ptr(g_a),
+                            _ptr(b_codes), _ptr(qb["scales"]), _ptr(g_b),
                             _ptr(resid) if k else None, _ptr(w_sel) if k else None, k, flags, _ptr(y),
                             _ptr(ws), 0 if ws is None else ws.numel(), _stream())
     _check("w4a4_gemm_comp", st)

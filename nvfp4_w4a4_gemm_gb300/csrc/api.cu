@@ -226,6 +226,22 @@ int mxfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t
                                               as_stream(stream)));
 }
 
+int mxfp4_quantize_ex(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int32_t* chan, int32_t k, int flags,
+                      float* row_scale, uint16_t* fb, uint8_t* codes, uint8_t* scales, float* stats, uint8_t* deadzone,
+                      void* stream) {
+  int st = check_quant_args(x, M, K, ldx, codes, scales, chan, k, fb, 32);
+  if (st != NVFP4_OK) return st;
+  if ((flags & ~MXFP4_QUANT_MACRO) != 0) return NVFP4_ERR_INVALID_ARG;
+  const bool macro = (flags & MXFP4_QUANT_MACRO) != 0;
+  if (M > 0 && macro && (row_scale == nullptr || !aligned(row_scale, 4))) return NVFP4_ERR_INVALID_ARG;
+  if (stats != nullptr && !aligned(stats, 16)) return NVFP4_ERR_INVALID_ARG;
+  if (k > 0 && K > 524288) return NVFP4_ERR_UNSUPPORTED;  // the fallback tables live in shared memory
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  return from_cuda(nv4::launch_mxfp4_quantize(bf(x), M, K, ldx, codes, scales, stats, deadzone, d->num_sms,
+                                              as_stream(stream), chan, k, macro ? row_scale : nullptr, bf(fb)));
+}
+
 int nvfp4_qdq(const uint16_t* w, int64_t M, int64_t K, int64_t ldw, const float* g_in, float* g_out, uint16_t* w_qdq,
               int64_t ld_out, uint8_t* codes, uint8_t* scales, void* workspace, size_t ws_bytes, void* stream) {
   if (M < 0 || K <= 0 || K % 16 != 0 || ldw < K || ldw % 8 != 0 || ld_out < K || ld_out % 8 != 0)
@@ -319,9 +335,18 @@ static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uin
                              const uint16_t* resid, const uint16_t* w_sel, int32_t k, int flags, uint16_t* y,
                              bool dense = false) {
   if (fmt != NVFP4_FMT_NVFP4 && fmt != NVFP4_FMT_MXFP4) return NVFP4_ERR_INVALID_ARG;
-  const int mode = flags & ~(NVFP4_GEMM_WEIGHTS_READY | NVFP4_GEMM_RESID_SCALED | NVFP4_GEMM_COMP_FP8);
+  const int mode =
+      flags & ~(NVFP4_GEMM_WEIGHTS_READY | NVFP4_GEMM_RESID_SCALED | NVFP4_GEMM_COMP_FP8 | NVFP4_GEMM_MX_ROW_SCALES);
   if (mode != NVFP4_COMP_W_DEQ && mode != NVFP4_COMP_W_BF16) return NVFP4_ERR_INVALID_ARG;
   if (M < 0 || N <= 0 || K <= 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
+  if (fmt == NVFP4_FMT_MXFP4 && ((flags & NVFP4_GEMM_MX_ROW_SCALES) || k != 0)) {
+    // the corrected MXFP4 GEMM: row macro-block scales and the Outlier
+    // Fallback term, whose bf16 operands carry every factor but the row scales
+    if (mode != NVFP4_COMP_W_DEQ || (flags & (NVFP4_GEMM_RESID_SCALED | NVFP4_GEMM_COMP_FP8)))
+      return NVFP4_ERR_INVALID_ARG;
+    if (!dense) return NVFP4_ERR_UNSUPPORTED;
+  }
+  if (fmt == NVFP4_FMT_NVFP4 && (flags & NVFP4_GEMM_MX_ROW_SCALES)) return NVFP4_ERR_INVALID_ARG;
   if (flags & NVFP4_GEMM_COMP_FP8) {
     // E4M3 operands: the pre-scaled residual and weight rows from the codes
     // (NVFP4_COMP_W_DEQ_FP8), so the term shares the FP4 product's factor
@@ -331,7 +356,6 @@ static int check_gemm_common(int fmt, int64_t M, int64_t N, int64_t K, const uin
   }
   if (N % 128 != 0 || K % (fmt == NVFP4_FMT_MXFP4 ? 128 : 64) != 0) return NVFP4_ERR_UNSUPPORTED;
   if (M > ((int64_t)1 << 31) - 256 || N > ((int64_t)1 << 31) - 256 || K > ((int64_t)1 << 30)) return NVFP4_ERR_UNSUPPORTED;
-  if (fmt == NVFP4_FMT_MXFP4 && k != 0) return NVFP4_ERR_UNSUPPORTED;
   if (k % 8 != 0 || k > K) return NVFP4_ERR_UNSUPPORTED;
   if (M == 0) return NVFP4_OK;
   if (!a_codes || !a_scales || !b_codes || !b_scales || !y) return NVFP4_ERR_INVALID_ARG;
@@ -354,6 +378,8 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
                    void* workspace, size_t ws_bytes, void* stream) {
   int st = check_gemm_common(fmt, M, N, K, a_codes, a_scales, b_codes, b_scales, resid, w_sel, k, flags, y, true);
   if (st != NVFP4_OK || M == 0) return st;
+  if ((flags & NVFP4_GEMM_MX_ROW_SCALES) && (!g_a || !g_b || !aligned(g_a, 4) || !aligned(g_b, 16)))
+    return NVFP4_ERR_INVALID_ARG;
   const DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
   const size_t need = nv4::gemm_workspace_bytes(M, N, K, d->num_sms);
@@ -363,7 +389,8 @@ int w4a4_gemm_comp(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* a_co
   p.a_codes = a_codes; p.a_scales = a_scales; p.g_a = g_a;
   p.b_codes = b_codes; p.b_scales = b_scales; p.g_b = g_b;
   p.resid = bf(resid); p.w_sel = bf(w_sel); p.k = k; p.y = bf(y);
-  p.flags = (flags & ~NVFP4_GEMM_COMP_FP8) | ((flags & NVFP4_GEMM_COMP_FP8) ? nv4::kGemmCompFp8 : 0);
+  p.flags = flags;  // the C ABI's GEMM flag values are the launcher's
+  if (fmt == NVFP4_FMT_MXFP4 && k > 0) p.flags |= nv4::kGemmResidScaled;  // fallback operands go to the MMA as they are
   p.ws = workspace; p.ws_bytes = ws_bytes;
   return from_cuda(nv4::launch_gemm(p, d->num_sms, as_stream(stream)));
 }

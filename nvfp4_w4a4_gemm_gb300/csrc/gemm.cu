@@ -103,6 +103,7 @@ struct GemmParams {
   int resid_scaled; // the residual was divided by g_a in the quantizer
   int comp_fp8;     // R_S / W_S are E4M3 bytes (W_S carries 2^-3): 128 channels per
                     // compensation tile, FP8 MMAs, the term times 2^3
+  int mx_rows;      // MXFP4 with row macro-block scales: g_a [M], g_b [N], y = g_a[m] g_b[n] (acc + accc)
   uint32_t n_mma;   // swap: MMA N = M rounded up to 16
   // wide kernel, grouped: what the epilogue makes of the accumulator
   int epi;                    // kEpiStore, kEpiSwigluQuant or kEpiCombine
@@ -222,6 +223,23 @@ __device__ __forceinline__ uint32_t idesc_bf16() {
   // D f32 (=1) at bit 4, A/B bf16 (=1) at bits 7 / 10, K-major both.
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+// MXFP4 with row macro-block scales: 16 outputs of row `row` from column
+// col0 times g_a[row] g_b[col] (each factor product rounded to fp32, then
+// the output's product; g_b is 16-byte aligned and col0 a multiple of 16).
+__device__ __forceinline__ void mx_row_factors(const GemmParams& p, bool row_ok, int64_t row, int64_t col0,
+                                               float (&yv)[16]) {
+  const float fa = row_ok ? __ldg(p.g_a + row) : 0.f;
+  const float4* gb = reinterpret_cast<const float4*>(p.g_b + col0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 f = __ldg(gb + q);
+    yv[4 * q] = __fmul_rn(yv[4 * q], __fmul_rn(fa, f.x));
+    yv[4 * q + 1] = __fmul_rn(yv[4 * q + 1], __fmul_rn(fa, f.y));
+    yv[4 * q + 2] = __fmul_rn(yv[4 * q + 2], __fmul_rn(fa, f.z));
+    yv[4 * q + 3] = __fmul_rn(yv[4 * q + 3], __fmul_rn(fa, f.w));
+  }
+}
+
 __device__ __forceinline__ uint32_t idesc_f8(uint32_t n) {
   // kind::f8f6f4: D f32 (=1) at bit 4, A/B E4M3 (=0) at bits 7 / 10, K-major both.
   return (1u << 4) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -574,6 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
         beta = (p.flags == 1) ? 1.f : gb;
         if (p.resid_scaled) beta *= ga;  // the residual came divided by g_a
         if (p.comp_fp8) beta *= 8.f;     // the FP8 weight rows carry 2^-3
+      } else {
+        beta = 1.f;  // MXFP4 fallback term: its operands carry every factor but the row scales
       }
       const uint32_t t_acc = tmem + ((uint32_t)(q * 32) << 16) + (acc ? kAcc1 : kAcc0);
       const uint32_t t_cmp = tmem + ((uint32_t)(q * 32) << 16) + kComp;
@@ -591,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
             if (n_ct_u > 0) yv = fmaf(beta, __uint_as_float(w[i]), yv);
             const int m = c + i;
             if (m < tl.rows) {
+              if (p.mx_rows) yv = __fmul_rn(yv, __fmul_rn(p.g_a[tl.row0 + m], p.g_b[tl.n0 + r]));
               const int64_t off = (tl.row0 + m) * p.N + tl.n0 + r;
               if (split > 1) p.partial[(u % split) * p.M * p.N + off] = yv;
               else p.y[off] = __float2bfloat16_rn(yv);
@@ -621,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_kernel(const __grid_con
           yv[i] = alpha * __uint_as_float(v[i]);
           if (n_ct_u > 0) yv[i] = fmaf(beta, __uint_as_float(w[i]), yv[i]);
         }
+        if (p.mx_rows) mx_row_factors(p, row_ok, tl.row0 + r, tl.n0 + c, yv);
         if (split > 1) {  // fp32 partial sums, reduced in split order by the finalize kernel
           if (row_ok) {
             float4* dst = reinterpret_cast<float4*>(p.partial + ((u % split) * p.M + tl.row0 + r) * p.N + tl.n0 + c);
@@ -1959,6 +1981,18 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       const int64_t col0 = tl.nt * BNP + h * 128;
       if ((int)(rank * BM) + r < tl.rows && col0 < p.N) {
         __nv_bfloat16* dst = p.y + row * p.N + col0;
+        if (p.mx_rows) {
+          // MXFP4 with row macro-block scales: each output times g_a[row] g_b[col]
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            float yv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yv[i] = __uint_as_float(v[cc][i]);
+            mx_row_factors(p, true, row, col0 + 16 * cc, yv);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[cc][i] = __float_as_uint(yv[i]);
+          }
+        }
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           uint32_t w[8];
@@ -2651,6 +2685,7 @@ cudaError_t launch_narrow(const GemmProblem& pr, bool grouped, int num_sms, cuda
     }
   }
   p.comp_fp8 = fp8 ? 1 : 0;
+  p.mx_rows = (pr.flags & kGemmMxRowScales) ? 1 : 0;
   p.a_sf = pr.a_scales;
   p.b_sf = pr.b_scales;
   const int64_t n_sf_cols = pr.fmt == 1 ? ((pr.K / 32 + 3) / 4) * 4 : ((pr.K / 16 + 3) / 4) * 4;
@@ -2983,6 +3018,7 @@ cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, c
     }
   }
   p.comp_fp8 = fp8 ? 1 : 0;
+  p.mx_rows = (pr.flags & kGemmMxRowScales) ? 1 : 0;
   p.b_sf_expert_tiles = b_tiles;
   p.g_a = pr.g_a;
   p.g_b = pr.g_b;
@@ -3043,8 +3079,9 @@ cudaError_t launch(const GemmProblem& pr, bool grouped, int num_sms, cudaStream_
     const int clusters = pair_clusters(num_sms);
     if (clusters > 0) return launch_pair(pr, grouped, clusters, stream);
   }
-  // the FP8 compensation exists on the narrow and the pair kernels only
-  if (pr.flags & kGemmCompFp8) return cudaErrorInvalidValue;
+  // the FP8 compensation and the MXFP4 row scales exist on the narrow and
+  // the pair kernels only
+  if ((pr.flags & (kGemmCompFp8 | kGemmMxRowScales)) || (pr.fmt == 1 && pr.k > 0)) return cudaErrorInvalidValue;
   return launch_wide(pr, grouped, num_sms, stream);
 }
 

@@ -20,8 +20,13 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
                                   unsigned int* bar, int num_sms, cudaStream_t stream, int resid_scaled = 0,
                                   const int32_t* gather = nullptr, int64_t T = 0, int resid_fp8 = 0);
 
+// The corrected form (fallback channels chan[k] with their values fb [M, k],
+// and/or row macro-block scales written to row_scale [M]) when k > 0 or
+// row_scale != nullptr.
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream);
+                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream,
+                                  const int32_t* chan = nullptr, int k = 0, float* row_scale = nullptr,
+                                  __nv_bfloat16* fb = nullptr);
 
 // Weight fake quantization: y = bf16(E2M1(code) * d) per element, optionally
 // the codes and tiled scales of the same quantization (dynamic scale: one
@@ -69,6 +74,7 @@ constexpr int kGemmCompBf16 = 1;          // compensation columns are the BF16 w
 constexpr int kGemmWeightsReady = 0x100;  // weights may be read before the preceding kernel ends
 constexpr int kGemmResidScaled = 0x200;   // the residual was divided by g_a (nvfp4_quantize_for_gemm)
 constexpr int kGemmCompFp8 = 0x400;       // resid / w_sel are E4M3 bytes (w_sel carries 2^-3)
+constexpr int kGemmMxRowScales = 0x800;   // MXFP4: g_a [M] / g_b [N] are row macro-block scales
 struct GemmProblem {
   int fmt = 0;  // 0 NVFP4, 1 MXFP4
   int64_t M = 0, N = 0, K = 0;

@@ -467,6 +467,22 @@ __device__ __forceinline__ uint32_t bf16x8_mul_e2m1(const uint4& w, uint64_t s2)
 #undef NV4_E2M1_PAIR
   return out;
 }
+// The same with two products per element, each rounded to nearest fp32:
+// E2M1(RN(RN(x * r) * s)) (r2 = {r, r}, s2 = {s, s}).
+__device__ __forceinline__ uint32_t bf16x8_mul2_e2m1(const uint4& w, uint64_t r2, uint64_t s2) {
+  uint32_t out;
+#define NV4_E2M1_PAIR2(W, T)                                                                       \
+  "shl.b32 lo, " W ", 16;\n\tand.b32 hi, " W ", 0xFFFF0000;\n\t"                                  \
+  "mov.b64 x, {lo, hi};\n\tmul.rn.f32x2 p, x, %5;\n\tmul.rn.f32x2 p, p, %6;\n\tmov.b64 {lo, hi}, p;\n\t" \
+  "cvt.rn.satfinite.e2m1x2.f32 " T ", hi, lo;\n\t"
+  asm("{\n\t.reg .b64 x, p;\n\t.reg .b32 lo, hi;\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      NV4_E2M1_PAIR2("%1", "t0") NV4_E2M1_PAIR2("%2", "t1") NV4_E2M1_PAIR2("%3", "t2") NV4_E2M1_PAIR2("%4", "t3")
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(out)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "l"(r2), "l"(s2));
+#undef NV4_E2M1_PAIR2
+  return out;
+}
 // Packed pairs of fp32 (low word = first element) and their element-wise
 // IEEE round-to-nearest arithmetic (f32x2 instructions: one issue for two
 // results, each rounded exactly as the scalar instruction would).

@@ -37,6 +37,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr size_t kMaxTableBytes = 64 * 1024;  // channel bitmaps + prefixes kept in shared memory up to this size
+constexpr size_t kMaxMxTableBytes = 96 * 1024;  // MXFP4 fallback tables (K <= 524288)
 constexpr float kAmaxToScale = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -418,6 +419,48 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
   __syncwarp();  // the slice is read before the warp's next unit overwrites it
 }
 
+// Channel bitmaps of E channel lists chan[e*k .. e*k+k) over K columns (bit
+// j%32 of word e*n_words + j/32 set for every j of list e inside [0, K)) and
+// their exclusive prefix counts per word, in shared memory: cleared, then set
+// from every channel entry at once (independent loads), then one warp per list
+// turns them into prefix counts.  Called by every thread of the block; the
+// caller synchronizes before reading the tables.
+__device__ void build_channel_tables(const int32_t* chan, int E, int k, int64_t K, int n_words, uint32_t* s_bits,
+                                     uint16_t* s_pref) {
+  for (int i = threadIdx.x; i < E * n_words; i += blockDim.x) s_bits[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < E * k; i += blockDim.x) {
+    const int32_t j = chan[i];
+    const int e = i / k;
+    if (j >= 0 && j < K) atomicOr(&s_bits[e * n_words + (j >> 5)], 1u << (j & 31));
+  }
+  __syncthreads();
+  const int warp_id = threadIdx.x >> 5, ln = threadIdx.x & 31, n_wp = blockDim.x >> 5;
+  const int per = (n_words + 31) / 32;
+  for (int e = warp_id; e < E; e += n_wp) {
+    const uint32_t* bits = s_bits + e * n_words;
+    uint32_t cnt = 0;
+    for (int q = 0; q < per; ++q) {
+      const int w = ln * per + q;
+      if (w < n_words) cnt += __popc(bits[w]);
+    }
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (ln >= o) incl += v;
+    }
+    uint32_t run = incl - cnt;
+    for (int q = 0; q < per; ++q) {
+      const int w = ln * per + q;
+      if (w < n_words) {
+        s_pref[e * n_words + w] = (uint16_t)run;
+        run += __popc(bits[w]);
+      }
+    }
+  }
+}
+
 template <bool kGrouped, bool kFused, bool kFull, bool kGather>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
@@ -450,43 +493,7 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   if (!kFused && wa.u < walk.n_units) load_unit_t<kFull, kGather>(a, wa.r, wa.gi, lane, va);
   if (kGrouped)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
-  if (a.use_map) {
-    // channel bitmaps of all experts (bit j%32 of word j/32 set for j in S_e):
-    // cleared, then set from every channel entry at once (independent loads),
-    // then one warp per expert turns them into prefix counts (shared memory only)
-    for (int i = threadIdx.x; i < a.E * n_words; i += blockDim.x) s_bits[i] = 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < a.E * a.k; i += blockDim.x) {
-      const int32_t j = a.chan[i];
-      const int e = i / a.k;
-      if (j >= 0 && j < a.K) atomicOr(&s_bits[e * n_words + (j >> 5)], 1u << (j & 31));
-    }
-    __syncthreads();
-    const int warp_id = threadIdx.x >> 5, ln = threadIdx.x & 31, n_wp = blockDim.x >> 5;
-    const int per = (n_words + 31) / 32;
-    for (int e = warp_id; e < a.E; e += n_wp) {
-      const uint32_t* bits = s_bits + e * n_words;
-      uint32_t cnt = 0;
-      for (int q = 0; q < per; ++q) {
-        const int w = ln * per + q;
-        if (w < n_words) cnt += __popc(bits[w]);
-      }
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (ln >= o) incl += v;
-      }
-      uint32_t run = incl - cnt;
-      for (int q = 0; q < per; ++q) {
-        const int w = ln * per + q;
-        if (w < n_words) {
-          s_pref[e * n_words + w] = (uint16_t)run;
-          run += __popc(bits[w]);
-        }
-      }
-    }
-  }
+  if (a.use_map) build_channel_tables(a.chan, a.E, a.k, a.K, n_words, s_bits, s_pref);
   __syncthreads();
   if (kGrouped) {
     // the routing offsets must be a partition of the rows (offsets[0] = 0,
@@ -600,6 +607,12 @@ struct MxArgs {
   float* stats;        // [M*K/32][4] or nullptr
   uint8_t* dead;       // [M*K/32] or nullptr
   int vec32;           // rows start on 32-byte boundaries: 256-bit loads
+  // corrections (kCorr): fallback channels leave the FP4 operand, rows are
+  // scaled by RN(1 / m) before the block scales
+  const int32_t* chan;     // fallback channels [k], sorted, or nullptr (k == 0)
+  int k;
+  const float* row_scale;  // macro-block (row) scales m [M], or nullptr (m = 1)
+  __nv_bfloat16* fb;       // fallback values bf16(RN(x * RN(1 / m))) [M, k]
 };
 
 // floor(log2 a) - 2 clamped to [-127, 127], from the fp32 bit pattern.
@@ -648,8 +661,11 @@ __device__ __forceinline__ float2 e2m1x2_vals(uint32_t byte) {
 // Markstein's division refinement, the correctly rounded quotient when no
 // step underflows, which the range guarantees wherever the code can change);
 // otherwise the IEEE division of every element.
-template <bool kFast>
-__device__ __forceinline__ float4 mx_block_stats(const uint4 (&v)[4], const uint4& cw, int e, float ss, uint32_t& nd) {
+// kScaled: the block's elements are those of the scaled operand RN(x * rho)
+// (the corrected quantizer's), formed here in fp32 from the bf16 x.
+template <bool kFast, bool kScaled = false>
+__device__ __forceinline__ float4 mx_block_stats(const uint4 (&v)[4], const uint4& cw, int e, float ss, uint32_t& nd,
+                                                 float rho = 1.f) {
   const float rss = __frcp_rn(ss);
   const float sc = pow2f(e);
   const uint64_t rss2 = f2_pack(rss, rss), nss2 = f2_pack(-ss, -ss), sc2 = f2_pack(sc, sc), ss2 = f2_pack(ss, ss);
@@ -661,8 +677,14 @@ __device__ __forceinline__ float4 mx_block_stats(const uint4 (&v)[4], const uint
 #pragma unroll
   for (int pr = 0; pr < 16; ++pr) {
     const uint32_t word = wv[pr];
-    const float x0 = __uint_as_float(word << 16), x1 = __uint_as_float(word & 0xFFFF0000u);
-    const uint64_t X = f2_pack(x0, x1);
+    float x0 = __uint_as_float(word << 16), x1 = __uint_as_float(word & 0xFFFF0000u);
+    uint64_t X = f2_pack(x0, x1);
+    if (kScaled) {
+      X = f2_mul(X, f2_pack(rho, rho));
+      const float2 xs = f2_unpack(X);
+      x0 = xs.x;
+      x1 = xs.y;
+    }
     float2 q;
     if (kFast) {
       const uint64_t Y0 = f2_mul(X, rss2);
@@ -689,14 +711,48 @@ __device__ __forceinline__ float4 mx_block_stats(const uint4 (&v)[4], const uint
   return make_float4(b2.x + b2.y, d2.x + d2.y, g2.x + g2.y, e2.x + e2.y);
 }
 
+// Fallback values of one lane's block: the elements on channels of its
+// bitmap word `mask` go to their slots fb[row*k + base + rank in the word] as
+// bf16(RN(x * rho)), then leave the block (set to +0).
+__device__ __forceinline__ void mx_fallback(const MxArgs& a, uint4 (&v)[4], uint32_t mask, int base, int64_t r,
+                                            float rho) {
+  uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                     v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+  __nv_bfloat16* dst = a.fb + r * a.k + base;
+#pragma unroll
+  for (int pr = 0; pr < 16; ++pr) {
+    const uint32_t two = (mask >> (2 * pr)) & 3u;
+    if (two != 0u) {
+      int slot = __popc(mask & ((1u << (2 * pr)) - 1u));
+      if (two & 1u) dst[slot++] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(wv[pr] << 16), rho));
+      if (two & 2u) dst[slot] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(wv[pr] & 0xFFFF0000u), rho));
+      wv[pr] &= ~(((two & 1u) ? 0x0000FFFFu : 0u) | ((two & 2u) ? 0xFFFF0000u : 0u));
+    }
+  }
+  v[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  v[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+  v[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+  v[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+}
+
 // One warp per unit of 1024 columns of a row; each lane owns one 32-element
-// block (64 bytes: two sector-aligned 32-byte loads).
-template <bool kStats>
+// block (64 bytes: two sector-aligned 32-byte loads).  kCorr: the corrected
+// quantizer (fallback channels and row scales, see MxArgs): the block's
+// fallback elements leave it first, its exponent comes from the block max of
+// the scaled operand RN(max |x| * rho) and its codes from RN(RN(x * rho) 2^-e).
+template <bool kStats, bool kCorr>
 __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
   pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
+  extern __shared__ __align__(16) uint32_t mx_tables[];  // kCorr, k > 0: bitmap [K/32], then prefix counts (u16)
   const int lane = threadIdx.x & 31;
   const int64_t nblk = a.K / 32;
   const int64_t n_cg = (nblk + 3) / 4;
+  const bool fallback = kCorr && a.k > 0;
+  uint16_t* s_pref = reinterpret_cast<uint16_t*>(mx_tables + nblk);
+  if (fallback) {
+    build_channel_tables(a.chan, 1, a.k, a.K, (int)nblk, mx_tables, s_pref);
+    __syncthreads();
+  }
   UnitWalk w;
   w.gpr = (uint32_t)((a.K + 1023) / 1024);
   w.n_units = (uint32_t)(a.M * w.gpr);
@@ -721,16 +777,33 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
         for (int i = 0; i < 4; ++i) v[i] = ldg_stream(src + 8 * i);
       }
     }
+    float rho = 1.f;
+    if (kCorr) {
+      if (a.row_scale != nullptr) rho = __frcp_rn(__ldg(a.row_scale + r));
+      if (fallback && valid) {
+        const uint32_t mask = mx_tables[col >> 5];
+        if (mask != 0u) mx_fallback(a, v, mask, s_pref[col >> 5], r, rho);
+      }
+    }
     // block absmax, E8M0 scale 2^e with e = floor(log2 a) - 2
-    const float am = absmax_of(absmax8(absmax8(absmax8(absmax8(v[0].x, v[0]), v[1]), v[2]), v[3]));
+    float am = absmax_of(absmax8(absmax8(absmax8(absmax8(v[0].x, v[0]), v[1]), v[2]), v[3]));
+    if (kCorr) am = __fmul_rn(am, rho);  // the scaled operand's block max (rounding is monotonic)
     const int e = mx_exponent(am);
     const float inv = pow2f(-e);
     const uint64_t s2 = ((uint64_t)__float_as_uint(inv) << 32) | __float_as_uint(inv);
     uint4 cw;
-    cw.x = bf16x8_mul_e2m1(v[0], s2);
-    cw.y = bf16x8_mul_e2m1(v[1], s2);
-    cw.z = bf16x8_mul_e2m1(v[2], s2);
-    cw.w = bf16x8_mul_e2m1(v[3], s2);
+    if (kCorr) {
+      const uint64_t r2 = f2_pack(rho, rho);
+      cw.x = bf16x8_mul2_e2m1(v[0], r2, s2);
+      cw.y = bf16x8_mul2_e2m1(v[1], r2, s2);
+      cw.z = bf16x8_mul2_e2m1(v[2], r2, s2);
+      cw.w = bf16x8_mul2_e2m1(v[3], r2, s2);
+    } else {
+      cw.x = bf16x8_mul_e2m1(v[0], s2);
+      cw.y = bf16x8_mul_e2m1(v[1], s2);
+      cw.z = bf16x8_mul_e2m1(v[2], s2);
+      cw.w = bf16x8_mul_e2m1(v[3], s2);
+    }
     if (valid) *reinterpret_cast<uint4*>(a.codes + r * (a.K / 2) + col / 2) = cw;
     // 4 blocks of a 128-element group -> one 32-bit store in the tile layout
     const uint32_t sb = valid ? (uint32_t)(e + 127) : 0u;
@@ -745,13 +818,55 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
       float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
       uint32_t nd = 0;
       if (am > 0.f) {
-        const float ss = div6_rn(am);
-        if (ss >= 0x1p-100f && ss <= 0x1p100f) st = mx_block_stats<true>(v, cw, e, ss, nd);
-        else st = mx_block_stats<false>(v, cw, e, ss, nd);
+        const float ss = am >= 0x1p-100f ? div6_rn(am) : __fdiv_rn(am, 6.0f);
+        if (ss >= 0x1p-100f && ss <= 0x1p100f) st = mx_block_stats<true, kCorr>(v, cw, e, ss, nd, rho);
+        else st = mx_block_stats<false, kCorr>(v, cw, e, ss, nd, rho);
       }
       const int64_t bidx = r * nblk + gi * 32 + lane;
       if (a.stats != nullptr) *reinterpret_cast<float4*>(a.stats + bidx * 4) = st;
       if (a.dead != nullptr) a.dead[bidx] = (uint8_t)nd;
+    }
+  }
+}
+
+// Macro-block (row) scales of the corrected MXFP4 quantizer: per row the
+// largest |x| outside the fallback channels A, t = RN(A / 6), m = the
+// significand of t in [1, 2) (m = 1 when t == 0 or t < 2^-126).  One warp
+// per row, rows strided over the grid, 16-byte loads.
+__global__ void __launch_bounds__(kThreads) mx_row_scale_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
+                                                                int64_t K, int64_t ldx,
+                                                                const int32_t* __restrict__ chan, int k,
+                                                                float* __restrict__ m_out) {
+  extern __shared__ __align__(16) uint32_t mx_tables[];
+  const int n_words = (int)(K / 32);
+  if (k > 0) {
+    build_channel_tables(chan, 1, k, K, n_words, mx_tables, reinterpret_cast<uint16_t*>(mx_tables + n_words));
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < M; r += n_warps) {
+    uint32_t m2 = 0u;
+    for (int64_t c = lane * 8; c < K; c += 256) {
+      uint4 v = ldg_stream(x + r * ldx + c);
+      if (k > 0) {
+        const uint32_t bits = (mx_tables[c >> 5] >> (c & 31)) & 0xFFu;  // the 8 columns' fallback bits
+        if (bits != 0u) {
+          uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wv[i] &= ~((((bits >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((bits >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u));
+          v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+      m2 = absmax8(m2, v);
+    }
+    float A = absmax_of(m2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, o));
+    if (lane == 0) {
+      const float t = A >= 0x1p-100f ? div6_rn(A) : __fdiv_rn(A, 6.0f);
+      m_out[r] = t >= 0x1p-126f ? __uint_as_float((__float_as_uint(t) & 0x7FFFFFu) | 0x3F800000u) : 1.0f;
     }
   }
 }
@@ -1244,21 +1359,46 @@ cudaError_t launch_mxfp4_decompose(const __nv_bfloat16* x, int64_t M, int64_t K,
 }
 
 cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream) {
+                                  uint8_t* scales, float* stats, uint8_t* dead, int num_sms, cudaStream_t stream,
+                                  const int32_t* chan, int k, float* row_scale, __nv_bfloat16* fb) {
   if (M == 0) return cudaSuccess;
-  MxArgs a{x, M, K, ldx, codes, scales, stats, dead, 0};
+  MxArgs a{};
+  a.x = x; a.M = M; a.K = K; a.ldx = ldx; a.codes = codes; a.scales = scales; a.stats = stats; a.dead = dead;
   a.vec32 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ldx & 15) == 0) ? 1 : 0;
+  a.chan = k > 0 ? chan : nullptr; a.k = k; a.row_scale = row_scale; a.fb = fb;
+  const bool corr = k > 0 || row_scale != nullptr;
+  // fallback tables: a bitmap word and a prefix count per 32-column block
+  const size_t tab = k > 0 ? (size_t)(K / 32) * (sizeof(uint32_t) + sizeof(uint16_t)) : 0;
+  if (tab > kMaxMxTableBytes) return cudaErrorInvalidValue;
+  if (row_scale != nullptr) {
+    int64_t blocks = (M + (kThreads / 32) - 1) / (kThreads / 32);
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    if (tab > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(mx_row_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab);
+      if (e != cudaSuccess) return e;
+    }
+    mx_row_scale_kernel<<<(unsigned)blocks, kThreads, tab, stream>>>(x, M, K, ldx, a.chan, k, row_scale);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const bool st = stats != nullptr || dead != nullptr;
-  const void* kern = st ? (const void*)mxfp4_quant_kernel<true> : (const void*)mxfp4_quant_kernel<false>;
+  const void* kerns[2][2] = {{(const void*)mxfp4_quant_kernel<false, false>, (const void*)mxfp4_quant_kernel<false, true>},
+                             {(const void*)mxfp4_quant_kernel<true, false>, (const void*)mxfp4_quant_kernel<true, true>}};
+  const void* kern = kerns[st][corr];
+  if (tab > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t n_units = M * ((K + 1023) / 1024);
   int64_t blocks = (n_units + (kThreads / 32) - 1) / (kThreads / 32);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, tab) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
   const int64_t cap = (int64_t)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void* args[] = {&a};
-  return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, 0, stream);
+  return cudaLaunchKernel(kern, dim3((unsigned)blocks), dim3(kThreads), args, tab, stream);
 }
 
 cudaError_t launch_nvfp4_qdq(const __nv_bfloat16* x, int64_t M, int64_t K, int64_t ldx, const float* g_in,

@@ -87,9 +87,22 @@ def test_invalid_arguments_rejected_on_host(lib):
                               None, 0, None) == 1
     assert lib.w4a4_gemm_comp(0, 4, 100, 64, fake, fake, None, fake, fake, None, None, None, 0, 0, fake,
                               None, 0, None) == 2
-    # MXFP4 with compensation is not part of the method
-    assert lib.w4a4_gemm_comp(1, 4, 128, 128, fake, fake, None, fake, fake, None, fake, fake, 16, 0, fake,
-                              None, 0, None) == 2
+    # MXFP4: the fallback term takes the plain mode only, dense GEMMs only;
+    # row scales are MXFP4's
+    assert lib.w4a4_gemm_comp(1, 4, 128, 128, fake, fake, None, fake, fake, None, fake, fake, 16, 0x200, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_gemm_comp(1, 4, 128, 128, fake, fake, None, fake, fake, None, fake, fake, 16, 1, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_gemm_comp(0, 4, 128, 128, fake, fake, None, fake, fake, None, None, None, 0, 0x800, fake,
+                              None, 0, None) == 1
+    assert lib.w4a4_grouped_gemm_comp(1, 4, fake, 8, 128, 128, fake, fake, None, fake, fake, None, fake, fake,
+                                      16, 0, fake, None, 0, None) == 2
+    # corrected MXFP4 quantize: flag bits, row scales with the macro flag, the fallback list
+    mxq = lambda flags, rs=fake, chan=None, k=0, fb=None: lib.mxfp4_quantize_ex(
+        fake, 4, 64, 64, chan, k, flags, rs, fb, fake, fake, None, None, None)
+    assert mxq(2) == 1
+    assert mxq(1, rs=None) == 1
+    assert mxq(0, k=8) == 1
     # grouped: missing offsets
     assert lib.w4a4_grouped_gemm_comp(0, 4, None, 8, 128, 64, fake, fake, None, fake, fake, None, None, None,
                                       0, 0, fake, None, 0, None) == 1

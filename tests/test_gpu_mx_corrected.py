@@ -1,0 +1,111 @@
+"""GPU parity of the corrected MXFP4 path (Outlier Fallback and row
+macro-block scaling) against the oracle: codes, E8M0 bytes, row scales,
+fallback values and deadzone counts bit-exact, block energies within 1e-5 of
+the block's error energy, the GEMM within the GEMM tolerance
+|y - y_ref| <= 4e-3 |y_ref| + 1e-3 rms(y_ref) on the 128-row (and swapped)
+and the 256-row pair kernels, and the full-size MXFP4 workload on sampled
+outputs."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mxfp4 as omx, nvfp4 as onv
+from nvfp4_w4a4_gemm_gb300 import workloads as W
+from tests.helpers import bf16_bits_of, f32, gather_scales, gemm_within_tol, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_w4a4_gemm_gb300 import binding
+    binding.load()
+    assert binding.check_status()[0] == 0
+    return binding
+
+
+def _fallback(K, k, n_out, seed):
+    """k sorted channels: the workload's outlier channels first, the rest drawn."""
+    if k == 0:
+        return np.zeros(0, np.int32)
+    c = list(dict.fromkeys(int(v) for v in W.outlier_channels(K, n_out, seed)))[:k]
+    rest = [int(v) for v in np.random.default_rng(seed + 1).permutation(K) if int(v) not in set(c)]
+    return np.sort(np.array(c + rest[:k - len(c)], np.int32))
+
+
+def _check_quant(q, ref, M, K, rows=None):
+    rows = np.arange(M) if rows is None else rows
+    nb = K // 32
+    assert np.array_equal(u8(q["codes"])[rows], ref["packed"])
+    assert np.array_equal(gather_scales(q["scales"], onv.scale_tile_offsets(M, nb)[rows]), ref["scale"])
+    if q["m"] is not None:
+        assert np.array_equal(f32(q["m"])[rows], ref["m"])
+    assert np.array_equal(bf16_bits_of(q["fb"])[rows], bf16_bits_of(torch.from_numpy(ref["fb"]).bfloat16()))
+    if q["dead"] is not None:
+        assert np.array_equal(u8(q["dead"]).reshape(M, nb)[rows], ref["dead"])
+        st = ref["stats"]
+        g = f32(q["stats"]).reshape(M, nb, 4)[rows].astype(np.float64)
+        assert np.all(np.abs(g - st) <= 1e-5 * (st[..., 3:4] + st.sum(-1, keepdims=True)) + 1e-30)
+
+
+@pytest.mark.parametrize("M,K,k,macro", [(64, 1024, 16, True), (37, 2080, 0, True), (100, 512, 32, False),
+                                         (300, 4096, 48, True), (5, 64, 8, True), (33, 256, 256, True)])
+def test_corrected_quantize_bit_exact(nv, M, K, k, macro):
+    n_out = max(2, K // 128)
+    x = W.activations(M, K, n_out, "t3x20", K + 1, M + 9)
+    S = _fallback(K, k, n_out, K + 1)
+    q = nv.mxfp4_quantize(x.cuda(), stats=True, chan=torch.from_numpy(S).cuda() if k else None, macro=macro)
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    ref = omx.quantize_corrected(f32(x), macro=macro, fallback=S if k else None)
+    _check_quant(q, ref, M, K)
+
+
+@pytest.mark.parametrize("M,N,K,k,macro", [(1, 128, 256, 16, True), (40, 256, 1024, 32, True),
+                                           (200, 128, 512, 0, True), (300, 384, 1024, 64, True),
+                                           (777, 256, 2048, 48, False), (513, 128, 1024, 16, True)])
+def test_corrected_gemm(nv, M, N, K, k, macro):
+    n_out = max(2, K // 128)
+    x = W.activations(M, K, n_out, "t3x20", K + 5, M + 1)
+    wt = W.weights_t(N, K, N + K + 3)
+    S = _fallback(K, k, n_out, K + 5)
+    ch = torch.from_numpy(S).cuda() if k else None
+    qa = nv.mxfp4_quantize(x.cuda(), chan=ch, macro=macro)
+    qb = nv.mxfp4_quantize(wt.cuda(), chan=ch, macro=macro)
+    y = nv.w4a4_gemm_comp(qa, qb, N, resid=qa["fb"] if k else None, w_sel=qb["fb"] if k else None,
+                          fmt=nv.FMT_MXFP4)
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    ra = omx.quantize_corrected(f32(x), macro=macro, fallback=S if k else None)
+    rb = omx.quantize_corrected(f32(wt), macro=macro, fallback=S if k else None)
+    y_ref = omx.gemm_corrected(ra, rb)
+    ok, ratio, rms = gemm_within_tol(f32(y), y_ref)
+    assert ok, f"max err/allowance {ratio:.3f} (rms {rms:.4g})"
+    # the corrections do what they are for: closer to the bf16 product than plain MXFP4
+    exact = f32(x).astype(np.float64) @ f32(wt).astype(np.float64).T
+    plain = omx.gemm_corrected(omx.quantize_corrected(f32(x)), omx.quantize_corrected(f32(wt)))
+    assert np.linalg.norm(f32(y) - exact) < np.linalg.norm(plain - exact)
+
+
+def test_corrected_full_size(nv):
+    s = W.SPECS["mxfp4"]
+    d = W.dense_inputs("mxfp4")
+    x, wt = d["x"], d["wt"]
+    k = 64
+    S = _fallback(s.K, k, s.n_out, s.seed)
+    ch = torch.from_numpy(S).cuda()
+    qa = nv.mxfp4_quantize(x.cuda(), stats=True, chan=ch, macro=True)
+    qb = nv.mxfp4_quantize(wt.cuda(), chan=ch, macro=True)
+    y = nv.w4a4_gemm_comp(qa, qb, s.N, resid=qa["fb"], w_sel=qb["fb"], fmt=nv.FMT_MXFP4)
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    rng = np.random.default_rng(8)
+    rows = np.sort(rng.choice(s.M, 256, replace=False))
+    cols = np.sort(rng.choice(s.N, 384, replace=False))
+    ra = omx.quantize_corrected(f32(x)[rows], macro=True, fallback=S)
+    rb = omx.quantize_corrected(f32(wt)[cols], macro=True, fallback=S)
+    _check_quant(qa, ra, s.M, s.K, rows)
+    assert np.array_equal(u8(qb["codes"])[cols], rb["packed"]) and np.array_equal(f32(qb["m"])[cols], rb["m"])
+    ok, ratio, rms = gemm_within_tol(f32(y)[np.ix_(rows, cols)], omx.gemm_corrected(ra, rb))
+    assert ok, f"max err/allowance {ratio:.3f} (rms {rms:.4g})"
