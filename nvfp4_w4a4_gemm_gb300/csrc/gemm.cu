@@ -1512,7 +1512,9 @@ __device__ __forceinline__ uint32_t idesc_mxf8_pair() {
   return ((uint32_t)(BNP >> 3) << 17) | (1u << 23) | ((uint32_t)(BMP >> 4) << 24);
 }
 
-template <bool kGrouped>
+// kMxRows: MXFP4 with row macro-block scales (dense only; p.mx_rows), its
+// own instantiation so that the other forms keep their epilogue code.
+template <bool kGrouped, bool kMxRows = false>
 __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1981,25 +1983,29 @@ __global__ void __launch_bounds__(kPThreads, 1) w4a4_gemm_pair_kernel(const __gr
       const int64_t col0 = tl.nt * BNP + h * 128;
       if ((int)(rank * BM) + r < tl.rows && col0 < p.N) {
         __nv_bfloat16* dst = p.y + row * p.N + col0;
-        if (p.mx_rows) {
-          // MXFP4 with row macro-block scales: each output times g_a[row] g_b[col]
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            float yv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) yv[i] = __uint_as_float(v[cc][i]);
-            mx_row_factors(p, true, row, col0 + 16 * cc, yv);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[cc][i] = __float_as_uint(yv[i]);
-          }
-        }
+        // MXFP4 with row macro-block scales: each output times RN(g_a[row] g_b[col])
+        const float fa = kMxRows ? __ldg(p.g_a + row) : 0.f;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
+          float f[16];
+          if (kMxRows) {
+            const float4* gb = reinterpret_cast<const float4*>(p.g_b + col0 + 16 * cc);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const float4 t = __ldg(gb + qq);
+              f[4 * qq] = __fmul_rn(fa, t.x);
+              f[4 * qq + 1] = __fmul_rn(fa, t.y);
+              f[4 * qq + 2] = __fmul_rn(fa, t.z);
+              f[4 * qq + 3] = __fmul_rn(fa, t.w);
+            }
+          }
           uint32_t w[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(alpha * __uint_as_float(v[cc][2 * i]),
-                                                            alpha * __uint_as_float(v[cc][2 * i + 1]));
+            const float y0 = __uint_as_float(v[cc][2 * i]), y1 = __uint_as_float(v[cc][2 * i + 1]);
+            const __nv_bfloat162 b2 =
+                kMxRows ? __floats2bfloat162_rn(__fmul_rn(y0, f[2 * i]), __fmul_rn(y1, f[2 * i + 1]))
+                        : __floats2bfloat162_rn(alpha * y0, alpha * y1);
             w[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           if (p.y_vec32) {
@@ -3039,7 +3045,8 @@ cudaError_t launch_pair(const GemmProblem& pr, bool grouped, int clusters_max, c
   const int64_t tiles = ((pr.M + BMP - 1) / BMP + (grouped ? E : 0)) * n_tiles_n;  // grouped: an upper bound
   const int64_t clusters = tiles < clusters_max ? tiles : clusters_max;
   const size_t smem = pair_smem_bytes(grouped ? E : 0);
-  auto kern = grouped ? w4a4_gemm_pair_kernel<true> : w4a4_gemm_pair_kernel<false>;
+  auto kern = grouped ? w4a4_gemm_pair_kernel<true> : p.mx_rows ? w4a4_gemm_pair_kernel<false, true>
+                                                               : w4a4_gemm_pair_kernel<false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};

@@ -337,7 +337,7 @@ __device__ __forceinline__ void load_unit_t(const QuantArgs& a, uint32_t r, uint
 // that fall in the unit's columns, one slot per lane (the element is read
 // back from the warp's shared slice, where the lanes put the unit's elements
 // first, and its block's scale byte fetched from the owning lane).
-template <bool kGrouped, bool kFull>
+template <bool kGrouped, bool kFull, bool kResid8>
 __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v)[4], uint32_t r, uint32_t gi,
                                              int lane, const ScaleCtx& sc, const QTables& t, int64_t n_cg) {
   int64_t srow = r;
@@ -412,7 +412,7 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
         const float2 dr = sc.dr[blk >= 32 ? s1 : s0];
         val = element_residual_f32(__bfloat162float(u[j - col0]), dr.x, dr.y, sc.rs);
       }
-      if (a.resid_fp8) reinterpret_cast<uint8_t*>(a.resid)[rrow + i] = (uint8_t)cvt_e4m3(val);
+      if (kResid8) reinterpret_cast<uint8_t*>(a.resid)[rrow + i] = (uint8_t)cvt_e4m3(val);
       else a.resid[rrow + i] = __float2bfloat16_rn(val);
     }
   }
@@ -425,8 +425,8 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
 // from every channel entry at once (independent loads), then one warp per list
 // turns them into prefix counts.  Called by every thread of the block; the
 // caller synchronizes before reading the tables.
-__device__ void build_channel_tables(const int32_t* chan, int E, int k, int64_t K, int n_words, uint32_t* s_bits,
-                                     uint16_t* s_pref) {
+__device__ __forceinline__ void build_channel_tables(const int32_t* chan, int E, int k, int64_t K, int n_words, uint32_t* s_bits,
+                                                     uint16_t* s_pref) {
   for (int i = threadIdx.x; i < E * n_words; i += blockDim.x) s_bits[i] = 0u;
   __syncthreads();
   for (int i = threadIdx.x; i < E * k; i += blockDim.x) {
@@ -461,7 +461,8 @@ __device__ void build_channel_tables(const int32_t* chan, int E, int k, int64_t 
   }
 }
 
-template <bool kGrouped, bool kFused, bool kFull, bool kGather>
+// kResid8: the residual as E4M3 bytes (a.resid_fp8; dense operands).
+template <bool kGrouped, bool kFused, bool kFull, bool kGather, bool kResid8 = false>
 __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
   pdl_launch_dependents();  // a GEMM launched after this kernel may start its prologue now
   extern __shared__ __align__(16) int32_t smem_i32[];
@@ -589,12 +590,12 @@ __global__ void __launch_bounds__(kThreads, 3) nvfp4_quant_kernel(QuantArgs a) {
     UnitWalk wb = wa;
     wb.next();
     if (wb.u < n) load_unit_t<kFull, kGather>(a, wb.r, wb.gi, lane, vb);
-    process_unit<kGrouped, kFull>(a, va, wa.r, wa.gi, lane, sc, t, n_cg);
+    process_unit<kGrouped, kFull, kResid8>(a, va, wa.r, wa.gi, lane, sc, t, n_cg);
     if (wb.u >= n) break;
     wa = wb;
     wa.next();
     if (wa.u < n) load_unit_t<kFull, kGather>(a, wa.r, wa.gi, lane, va);
-    process_unit<kGrouped, kFull>(a, vb, wb.r, wb.gi, lane, sc, t, n_cg);
+    process_unit<kGrouped, kFull, kResid8>(a, vb, wb.r, wb.gi, lane, sc, t, n_cg);
   }
 }
 
@@ -1322,8 +1323,17 @@ cudaError_t launch_nvfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   const void* kerns_gather[2][2] = {
       {(const void*)nvfp4_quant_kernel<true, false, false, true>, (const void*)nvfp4_quant_kernel<true, false, true, true>},
       {(const void*)nvfp4_quant_kernel<true, true, false, true>, (const void*)nvfp4_quant_kernel<true, true, true, true>}};
+  // the E4M3 residual exists for dense operands
+  const void* kerns_resid8[2][2] = {
+      {(const void*)nvfp4_quant_kernel<false, false, false, false, true>,
+       (const void*)nvfp4_quant_kernel<false, false, true, false, true>},
+      {(const void*)nvfp4_quant_kernel<false, true, false, false, true>,
+       (const void*)nvfp4_quant_kernel<false, true, true, false, true>}};
   if (gather != nullptr && offsets == nullptr) return cudaErrorInvalidValue;
-  const void* kern = gather != nullptr ? kerns_gather[fused][full] : kerns[offsets != nullptr][fused][full];
+  if (resid_fp8 && (offsets != nullptr || gather != nullptr)) return cudaErrorInvalidValue;
+  const void* kern = gather != nullptr ? kerns_gather[fused][full]
+                     : resid_fp8       ? kerns_resid8[fused][full]
+                                       : kerns[offsets != nullptr][fused][full];
   if (smem > 24 * 1024) {  // with the 18 KB of static unit slices, above the default 48 KB per block
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
