@@ -830,37 +830,48 @@ __global__ void __launch_bounds__(kThreads, 3) mxfp4_quant_kernel(MxArgs a) {
   }
 }
 
+// 8 bf16 of a row without its fallback channels: `bits` holds the 8
+// columns' bits of the channel bitmap (element j -> bit j).
+__device__ __forceinline__ uint4 mx_drop_fallback(uint4 v, uint32_t bits) {
+  uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    wv[i] &= ~((((bits >> (2 * i)) & 1u) * 0x0000FFFFu) | (((bits >> (2 * i + 1)) & 1u) * 0xFFFF0000u));
+  return make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
 // Macro-block (row) scales of the corrected MXFP4 quantizer: per row the
 // largest |x| outside the fallback channels A, t = RN(A / 6), m = the
 // significand of t in [1, 2) (m = 1 when t == 0 or t < 2^-126).  One warp
-// per row, rows strided over the grid, 16-byte loads.
+// per row, rows strided over the grid; 16-byte loads, four in flight per lane.
+template <bool kFallback>
 __global__ void __launch_bounds__(kThreads) mx_row_scale_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
                                                                 int64_t K, int64_t ldx,
                                                                 const int32_t* __restrict__ chan, int k,
                                                                 float* __restrict__ m_out) {
   extern __shared__ __align__(16) uint32_t mx_tables[];
   const int n_words = (int)(K / 32);
-  if (k > 0) {
+  if (kFallback) {
     build_channel_tables(chan, 1, k, K, n_words, mx_tables, reinterpret_cast<uint16_t*>(mx_tables + n_words));
     __syncthreads();
   }
+  auto bits_of = [&](int64_t c) { return (mx_tables[c >> 5] >> (c & 31)) & 0xFFu; };
   const int lane = threadIdx.x & 31;
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < M; r += n_warps) {
+    const __nv_bfloat16* row = x + r * ldx;
     uint32_t m2 = 0u;
-    for (int64_t c = lane * 8; c < K; c += 256) {
-      uint4 v = ldg_stream(x + r * ldx + c);
-      if (k > 0) {
-        const uint32_t bits = (mx_tables[c >> 5] >> (c & 31)) & 0xFFu;  // the 8 columns' fallback bits
-        if (bits != 0u) {
-          uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    int64_t c = lane * 8;
+    for (; c + 768 < K; c += 1024) {
+      uint4 v[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            wv[i] &= ~((((bits >> (2 * i)) & 1u) ? 0x0000FFFFu : 0u) | (((bits >> (2 * i + 1)) & 1u) ? 0xFFFF0000u : 0u));
-          v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-      }
-      m2 = absmax8(m2, v);
+      for (int i = 0; i < 4; ++i) v[i] = ldg_stream(row + c + 256 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m2 = absmax8(m2, kFallback ? mx_drop_fallback(v[i], bits_of(c + 256 * i)) : v[i]);
+    }
+    for (; c < K; c += 256) {
+      const uint4 v = ldg_stream(row + c);
+      m2 = absmax8(m2, kFallback ? mx_drop_fallback(v, bits_of(c)) : v);
     }
     float A = absmax_of(m2);
 #pragma unroll
@@ -871,6 +882,7 @@ __global__ void __launch_bounds__(kThreads) mx_row_scale_kernel(const __nv_bfloa
     }
   }
 }
+
 
 // Per-element MXFP4 decomposition (a checking aid for small shapes): one
 // warp per 32-element block, lane = element, the fp32 arithmetic of the
@@ -1383,11 +1395,12 @@ cudaError_t launch_mxfp4_quantize(const __nv_bfloat16* x, int64_t M, int64_t K, 
   if (row_scale != nullptr) {
     int64_t blocks = (M + (kThreads / 32) - 1) / (kThreads / 32);
     if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    auto rk = k > 0 ? mx_row_scale_kernel<true> : mx_row_scale_kernel<false>;
     if (tab > 48 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(mx_row_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab);
+      const cudaError_t e = cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab);
       if (e != cudaSuccess) return e;
     }
-    mx_row_scale_kernel<<<(unsigned)blocks, kThreads, tab, stream>>>(x, M, K, ldx, a.chan, k, row_scale);
+    rk<<<(unsigned)blocks, kThreads, tab, stream>>>(x, M, K, ldx, a.chan, k, row_scale);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
