@@ -159,29 +159,27 @@ struct ScaleCtx {
 };
 
 // Quantize one 16-element block owned by this thread (`valid` = the block
-// lies inside the row): its 8 code bytes go to `code_ptr`, and the 4 scale
-// bytes of a 64-element group are gathered into one 32-bit store at
-// `scale_ptr` by lane % 4 == 0 (blocks past the row end contribute 0).
-// Returns the block's scale byte.
-__device__ __forceinline__ uint32_t quant_block(const uint4& raw0, const uint4& raw1, bool valid, int lane,
-                                                const ScaleCtx& sc, uint8_t* code_ptr, uint8_t* scale_ptr) {
+// lies inside the row, `group_valid` = its 64-element scale group starts
+// inside the row): its 8 code bytes go to `code_ptr`, its scale byte to byte
+// lane % 4 of the group's 4 bytes at `scale_ptr` (0 for a block past the
+// row end).  Returns the block's scale byte.
+__device__ __forceinline__ uint32_t quant_block(const uint4& raw0, const uint4& raw1, bool valid, bool group_valid,
+                                                int lane, const ScaleCtx& sc, uint8_t* code_ptr, uint8_t* scale_ptr) {
   // block absmax (exact: a max of bf16 magnitudes)
   const float am = absmax_of(absmax8(absmax8(raw0.x, raw0), raw1));
   uint32_t sig = block_scale_byte(am, sc.g, sc.yg, sc.fast);
   sig = valid ? sig : 0u;
   const float2 dr = sc.dr[sig];
-  uint32_t lo = 0, hi = 0;
-  if (dr.x != 0.f) {
-    const uint64_t s2 = ((uint64_t)__float_as_uint(dr.y) << 32) | __float_as_uint(dr.y);
-    lo = bf16x8_mul_e2m1(raw0, s2);
-    hi = bf16x8_mul_e2m1(raw1, s2);
-  }
+  // a zero-scale block (d == 0, 1/d stored as 0) codes every element +0: the
+  // products are computed anyway and masked, no branch
+  const uint64_t s2 = ((uint64_t)__float_as_uint(dr.y) << 32) | __float_as_uint(dr.y);
+  const uint32_t keep = dr.x != 0.f ? 0xFFFFFFFFu : 0u;
+  const uint32_t lo = bf16x8_mul_e2m1(raw0, s2) & keep;
+  const uint32_t hi = bf16x8_mul_e2m1(raw1, s2) & keep;
   if (valid) *reinterpret_cast<uint2*>(code_ptr) = make_uint2(lo, hi);
-  const uint32_t s1 = __shfl_down_sync(0xffffffffu, sig, 1);
-  const uint32_t s2 = __shfl_down_sync(0xffffffffu, sig, 2);
-  const uint32_t s3 = __shfl_down_sync(0xffffffffu, sig, 3);
-  if ((lane & 3) == 0 && valid)
-    *reinterpret_cast<uint32_t*>(scale_ptr) = sig | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  // each lane stores its own scale byte (blocks past the row end of a
+  // 4-block group that starts inside the row write 0)
+  if (group_valid) scale_ptr[lane & 3] = (uint8_t)sig;
   return sig;
 }
 
@@ -362,7 +360,8 @@ __device__ __forceinline__ void process_unit(const QuantArgs& a, const uint4 (&v
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     if (!kFull && h * 512 >= cols) break;  // warp-uniform
-    sig[h] = quant_block(v[2 * h], v[2 * h + 1], kFull || h * 512 + lane * 16 < cols, lane, sc, code_ptr + h * 256,
+    sig[h] = quant_block(v[2 * h], v[2 * h + 1], kFull || h * 512 + lane * 16 < cols,
+                         kFull || h * 512 + (lane & ~3) * 16 < cols, lane, sc, code_ptr + h * 256,
                          scale_ptr + h * 8 * 512);
   }
   if (a.k == 0) return;
