@@ -156,3 +156,23 @@ def test_fp8_flag_combinations_rejected(nv):
         nv.w4a4_gemm_comp(qx, qw, N, resid=qx["resid"][:, :24].contiguous(), w_sel=w8[:, :24].contiguous())
     torch.cuda.synchronize()
     assert nv.check_status()[0] == 0
+
+
+@pytest.mark.parametrize("M", [40, 200, 700])
+def test_fp8_weights_ready_overlap_is_bit_identical(nv, M):
+    # the GEMM with the FP8 term started as a programmatic dependent of the
+    # quantizer before it, with and without streaming weights before its wait
+    N, K, k = 384, 1024, 64
+    x = W.activations(M, K, 8, "t3x20", 41, 42).cuda()
+    wt = W.weights_t(N, K, 43).cuda()
+    ch = torch.arange(0, K, K // k, dtype=torch.int32, device="cuda")
+    qw = nv.nvfp4_quantize(wt)
+    w8 = nv.nvfp4_prepare_comp_weights(qw["codes"], qw["scales"], ch, flags=nv.COMP_W_DEQ_FP8)
+    torch.cuda.synchronize()
+    ys = []
+    for ready in (False, True, True):
+        qx = nv.nvfp4_quantize(x, chan=ch, resid_fp8=True)
+        ys.append(nv.w4a4_gemm_comp(qx, qw, N, resid=qx["resid"], w_sel=w8, weights_ready=ready))
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])

@@ -109,3 +109,20 @@ def test_corrected_full_size(nv):
     assert np.array_equal(u8(qb["codes"])[cols], rb["packed"]) and np.array_equal(f32(qb["m"])[cols], rb["m"])
     ok, ratio, rms = gemm_within_tol(f32(y)[np.ix_(rows, cols)], omx.gemm_corrected(ra, rb))
     assert ok, f"max err/allowance {ratio:.3f} (rms {rms:.4g})"
+
+
+@pytest.mark.parametrize("M", [48, 600])
+def test_corrected_weights_ready_overlap_is_bit_identical(nv, M):
+    N, K, k = 256, 1024, 32
+    x = W.activations(M, K, 8, "t3x20", 51, 52).cuda()
+    S = _fallback(K, k, 8, 51)
+    ch = torch.from_numpy(S).cuda()
+    qb = nv.mxfp4_quantize(W.weights_t(N, K, 53).cuda(), chan=ch, macro=True)
+    torch.cuda.synchronize()
+    ys = []
+    for ready in (False, True, True):
+        qa = nv.mxfp4_quantize(x, chan=ch, macro=True)
+        ys.append(nv.w4a4_gemm_comp(qa, qb, N, resid=qa["fb"], w_sel=qb["fb"], fmt=nv.FMT_MXFP4, weights_ready=ready))
+    torch.cuda.synchronize()
+    assert nv.check_status()[0] == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
